@@ -1,0 +1,67 @@
+"""Layout swap of Ulysses sequence parallelism, written as its index formula.
+
+TEST INFRASTRUCTURE ONLY.
+
+Before attention every rank holds a contiguous chunk of S = T/sp tokens with
+all H heads; after the first all-to-all it holds all T tokens for H/sp heads,
+and the second all-to-all undoes that (HF Transformers "Ulysses sequence
+parallelism" guide, opening paragraph and its layout figure; congresoia365
+article, "Cómo Funciona Ulysses", steps 1, 3 and 5). With the sp simulated
+ranks stored as shards of one buffer:
+
+    seq-sharded  x[r_s][s][h][d]     token t = r_s*S + s, all heads
+    head-sharded y[r][hl][t][d]      head  h = r*Hl + hl, all tokens
+
+    y[r][hl][t][d] = x[t // S][t % S][r*Hl + hl][d]
+
+Arrays hold raw 16-bit patterns: the swap moves bits and never does arithmetic
+on them.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def _check(T: int, H: int, sp: int):
+    if sp <= 0 or T % sp != 0:
+        raise ValueError("total tokens must be a multiple of sp_size")
+    if H % sp != 0:
+        raise ValueError("head count must be divisible by sp_size")
+
+
+def seq_to_head(x: np.ndarray, sp: int) -> np.ndarray:
+    """x: [sp][S][H][D] (or [T][H][D]) -> y: [sp][H/sp][T][D]."""
+    H, D = x.shape[-2], x.shape[-1]
+    T = x.size // (H * D)
+    _check(T, H, sp)
+    S, Hl = T // sp, H // sp
+    xs = x.reshape(sp, S, H, D)
+    y = np.empty((sp, Hl, T, D), dtype=x.dtype)
+    t = np.arange(T)
+    for r in range(sp):
+        for hl in range(Hl):
+            y[r, hl, t, :] = xs[t // S, t % S, r * Hl + hl, :]
+    return y
+
+
+def head_to_seq(y: np.ndarray, sp: int) -> np.ndarray:
+    """y: [sp][H/sp][T][D] (or [H][T][D]) -> x: [sp][S][H][D]."""
+    T, D = y.shape[-2], y.shape[-1]
+    H = y.size // (T * D)
+    _check(T, H, sp)
+    S, Hl = T // sp, H // sp
+    ys = y.reshape(sp, Hl, T, D)
+    x = np.empty((sp, S, H, D), dtype=y.dtype)
+    t = np.arange(T)
+    for r in range(sp):
+        for hl in range(Hl):
+            x[t // S, t % S, r * Hl + hl, :] = ys[r, hl, t, :]
+    return x
+
+
+def seq_to_head_elem(x: np.ndarray, sp: int, r: int, hl: int, t: int, d: int):
+    """One element of the head-sharded view, straight from the formula (for sampled checks)."""
+    H, D = x.shape[-2], x.shape[-1]
+    T = x.size // (H * D)
+    S, Hl = T // sp, H // sp
+    return x.reshape(sp, S, H, D)[t // S, t % S, r * Hl + hl, d]
