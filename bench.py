@@ -1,0 +1,345 @@
+"""Benchmark of the Ulysses sequence-parallel hot path on GB300.
+
+One step = the whole per-layer attention path for all sp simulated ranks of one
+GPU: seq->head re-layout of Q, K, V; causal packed attention forward; head->seq of
+O; seq->head of dO; attention backward; head->seq of dQ, dK, dV. The metric is
+algorithmic attention TFLOP/s (4*D FLOPs per allowed (query, key) pair per query
+head forward, 10*D backward), plus re-layout GB/s against HBM.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl usp|reference]
+       [--workload llama|tiny|packed|gqa|long]
+Under torchrun (N > 1) every rank runs the same per-GPU workload on its own GPU
+(weak scaling, no data-path collective); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "local attn fwd+bwd TFLOP/s & % GB300 bf16 peak; re-layout GB/s vs HBM peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload_desc(w):
+    kind = "packed" if w.num_seqs > 1 else "single sequence"
+    return (f"{w.name}: {w.total_tokens} tokens ({kind}, {w.num_seqs} samples), sp={w.sp}, hq={w.hq}, "
+            f"hkv={w.hkv}, D={w.head_dim}, causal, bf16 N(0,1), fwd+bwd, all sp ranks' heads in one launch")
+
+
+def attention_flops(w):
+    pairs = w.allowed_pairs()
+    return 4.0 * w.head_dim * pairs * w.hq, 10.0 * w.head_dim * pairs * w.hq
+
+
+class ClockSampler:
+    """nvidia-smi SM clocks and throttle reasons sampled during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [l.strip().split(", ") for l in self.file.read().splitlines() if l.strip()]
+        self.file.close()
+        os.unlink(self.file.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, r[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def oracle_sample_step(w, tokens: int):
+    """The oracle's fwd+bwd on one head over the first `tokens` tokens of the workload's
+    first sample; returns (seconds, algorithmic FLOPs credited, threads)."""
+    import numpy as np
+
+    import oracle
+    from ulysses_sequence_seq_gb300.synth import head_bits
+    L = min(tokens, w.lengths[0])
+    q = head_bits(w, "q", 0)[None, :L]
+    k = head_bits(w, "k", 0)[None, :L]
+    v = head_bits(w, "v", 0)[None, :L]
+    do = head_bits(w, "do", 0)[None, :L]
+    cu = np.array([0, L], dtype=np.int32)
+    t0 = time.perf_counter()
+    oracle.attn_fwd(q, k, v, cu)
+    oracle.attn_bwd(q, k, v, do, cu)
+    dt = time.perf_counter() - t0
+    pairs = L * (L + 1) // 2
+    return dt, 14.0 * w.head_dim * pairs, oracle.num_threads(), L
+
+
+def run_reference(args, w):
+    """The CPU oracle as the reference arm (rank 0 only)."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from oracle.build import build_oracle
+    build_oracle()
+    tokens = args.ref_tokens
+    for _ in range(args.warmup):
+        oracle_sample_step(w, min(tokens, 256))
+    times, flops = [], 0.0
+    for _ in range(args.steps):
+        dt, fl, threads, L = oracle_sample_step(w, tokens)
+        times.append(dt)
+        flops = fl
+    mean = sum(times) / len(times)
+    value = flops / mean / 1e12
+    sample = (f"one query head, causal fwd+bwd over the first {L} tokens of sample 0 of the {w.name} "
+              f"workload per step (float64 C oracle)")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": workload_desc(w), "sample": sample},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_usp(args, w):
+    import numpy as np
+    import torch
+
+    import ulysses_sequence_seq_gb300 as usp
+    from ulysses_sequence_seq_gb300.synth import seq_sharded_bits
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+
+    usp.load()
+    dev = torch.device("cuda", local_rank)
+    T, H, HKV, D, sp = w.total_tokens, w.hq, w.hkv, w.head_dim, w.sp
+
+    def to_host_pinned(bits):
+        t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+        return t.pin_memory()
+
+    hq_, hk_, hv_, hdo_ = (to_host_pinned(seq_sharded_bits(w, t)) for t in ("q", "k", "v", "do"))
+    xq, xk, xv, xdo = (t.to(dev) for t in (hq_, hk_, hv_, hdo_))
+    cu = torch.from_numpy(w.cu_seqlens()).to(dev)
+    layer = usp.UlyssesAttention(T, w.num_seqs, H, HKV, D, sp, causal=True, device=dev)
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)   # > L2 (129 MB)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev is None:
+            layer.forward(xq, xk, xv, cu)
+            layer.backward(xdo, cu)
+            return
+        ev[0].record(stream)
+        usp.seq_to_head(xq, layer.q_h, sp)
+        usp.seq_to_head(xk, layer.k_h, sp)
+        usp.seq_to_head(xv, layer.v_h, sp)
+        ev[1].record(stream)
+        usp.attn_fwd_varlen(layer.q_h, layer.k_h, layer.v_h, layer.o_h, layer.lse, cu, layer.B, T, H, HKV, D,
+                            layer.scale, True, layer.ws, layer.ws_bytes)
+        ev[2].record(stream)
+        usp.head_to_seq(layer.o_h, layer.o_seq, sp)
+        usp.seq_to_head(xdo, layer.do_h, sp)
+        ev[3].record(stream)
+        usp.attn_bwd_varlen(layer.q_h, layer.k_h, layer.v_h, layer.o_h, layer.lse, layer.do_h, layer.dq_h,
+                            layer.dk_h, layer.dv_h, usp.USP_BF16, cu, layer.B, T, H, HKV, D, layer.scale, True,
+                            layer.ws, layer.ws_bytes)
+        ev[4].record(stream)
+        usp.head_to_seq(layer.dq_h, layer.dq_seq, sp)
+        usp.head_to_seq(layer.dk_h, layer.dk_seq, sp)
+        usp.head_to_seq(layer.dv_h, layer.dv_seq, sp)
+        ev[5].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if layer.device_status() != usp.USP_OK:
+        raise RuntimeError(f"device status {usp.status_string(layer.device_status())} after warm-up")
+
+    clocks = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.zero_()                          # evict L2 between timed steps (outside the events)
+        step(evs[i])
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    ck = clocks.stop() if clocks else None
+    if layer.device_status() != usp.USP_OK:
+        raise RuntimeError(f"device status {usp.status_string(layer.device_status())} after timing")
+
+    step_ms = [e[0].elapsed_time(e[5]) for e in evs]
+    fwd_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    bwd_ms = [e[3].elapsed_time(e[4]) for e in evs]
+    rel_ms = [e[0].elapsed_time(e[1]) + e[2].elapsed_time(e[3]) + e[4].elapsed_time(e[5]) for e in evs]
+    total_ms = sum(step_ms)
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    fwd_fl, bwd_fl = attention_flops(w)
+    value = (fwd_fl + bwd_fl) * world / (ms_per_step * 1e-3) / 1e12
+
+    # ---- end to end through the public API: pinned host inputs in, results back to host
+    out_host = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                for t in (layer.o_seq, layer.dq_seq, layer.dk_seq, layer.dv_seq)]
+    h2d = sum(t.numel() * t.element_size() for t in (hq_, hk_, hv_, hdo_))
+    d2h = sum(t.numel() * t.element_size() for t in out_host)
+
+    def e2e_step():
+        dq_, dk_, dv_, ddo_ = (t.to(dev, non_blocking=True) for t in (hq_, hk_, hv_, hdo_))
+        o = layer.forward(dq_, dk_, dv_, cu)
+        g = layer.backward(ddo_, cu)
+        for dst, src in zip(out_host, (o,) + tuple(g)):
+            dst.copy_(src, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_ms = []
+    for _ in range(args.steps):
+        flush.zero_()
+        e0.record(stream)
+        e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms.append(e0.elapsed_time(e1))
+    e2e_value = (fwd_fl + bwd_fl) * world / (statistics.mean(e2e_ms) * 1e-3) / 1e12
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+
+    peaks, peak_src = load_peaks()
+    bwd_mean = statistics.mean(bwd_ms)
+    fwd_mean = statistics.mean(fwd_ms)
+    bwd_tflops = bwd_fl / (bwd_mean * 1e-3) / 1e12
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    # eight tensor swaps per step (Q, K, V, O, dO, dQ, dK, dV), each read once and written once
+    relayout_bytes = 2 * 2 * T * D * (H + HKV + HKV + H + H + H + HKV + HKV)
+    rel_gbs = relayout_bytes / (statistics.mean(rel_ms) * 1e-3) / 1e9
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        from oracle.build import build_oracle
+        build_oracle()
+        dt, fl, threads, L = oracle_sample_step(w, args.cpu_tokens)
+        cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+               "sample": f"one query head, causal fwd+bwd over the first {L} tokens of sample 0 "
+                         f"({dt:.1f} s of float64 C oracle work)"}
+    launches_per_step = 3 + 1 + 1 + 1 + 1 + 1 + 1 + 1 + 1 + 3
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": workload_desc(w), "seq_len": T, "heads": H, "kv_heads": HKV, "head_dim": D,
+                   "sp": sp, "parallelism": f"replicas x{world} (sp={sp} simulated per GPU)",
+                   "l2": "flushed between timed steps (512 MB write outside the events)",
+                   "fwd_ms": fwd_mean, "bwd_ms": bwd_mean, "relayout_ms": statistics.mean(rel_ms),
+                   "fwd_tflops": fwd_fl / (fwd_mean * 1e-3) / 1e12, "bwd_tflops": bwd_tflops},
+        "roofline": {"bound": "tensor", "kernel": "usp_attn_bwd_varlen (attn_bwd_kernel + prep + convert)",
+                     "achieved": bwd_tflops, "peak": peak, "unit": "TFLOP/s", "frac": bwd_tflops / peak,
+                     "peak_source": f"{peak_src} bf16 burst", "traffic": None},
+        "relayout": {"achieved_gbs": rel_gbs, "peak_gbs": hbm, "frac": rel_gbs / hbm,
+                     "peak_source": f"{peak_src} hbm copy", "bytes_per_step": relayout_bytes},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": ck,
+    }
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="usp", choices=["usp", "reference"])
+    ap.add_argument("--workload", default="llama", choices=["tiny", "llama", "packed", "gqa", "long"])
+    ap.add_argument("--ref-tokens", type=int, default=2048)
+    ap.add_argument("--cpu-tokens", type=int, default=4096)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    from ulysses_sequence_seq_gb300.synth import WORKLOADS
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_usp(args, w)
+
+
+if __name__ == "__main__":
+    main()

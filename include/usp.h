@@ -1,0 +1,172 @@
+/*
+ * usp.h -- C ABI of libusp: the data-parallel hot path of Ulysses sequence
+ * parallelism on one GB300 (sm_103a).
+ *
+ * Ulysses sequence parallelism splits a long sequence of T tokens over sp
+ * ranks. Before attention each rank holds T/sp consecutive tokens with all H
+ * heads; an all-to-all swaps the sharded dimension from sequence to heads, each
+ * rank then computes ordinary attention over the full sequence for its H/sp
+ * heads, and a second all-to-all swaps back (HF Transformers "Ulysses sequence
+ * parallelism" guide, opening paragraph and layout figure; congresoia365
+ * article "Nuevo método Ulysses...", section "Cómo Funciona Ulysses", steps
+ * 1-5). Heads are independent, so the per-rank step is plain attention on a
+ * subset of heads (same article, closing paragraph of that section).
+ *
+ * On one GPU the sp ranks are simulated as shards of one device buffer:
+ *
+ *   seq-sharded   [sp][T/sp][H][D]   (token-major; identical bytes to [T][H][D])
+ *   head-sharded  [sp][H/sp][T][D]   (head-major;  identical bytes to [H][T][D])
+ *
+ * and the two all-to-alls become device-local permutations. No collective is
+ * issued by this library.
+ *
+ * Conventions shared by every call:
+ *   - The caller owns every buffer; the library never allocates device memory.
+ *     Attention calls take a caller-provided workspace whose size is returned by
+ *     usp_attn_workspace_size().
+ *   - Pointers are device pointers, 16-byte aligned. `stream` is a cudaStream_t
+ *     (NULL = legacy default stream). Calls are asynchronous on `stream`; the
+ *     return value reports host-side validation and launch errors only.
+ *     Errors found on the device (malformed cu_seqlens, a wait that timed out)
+ *     are written to the workspace status word; read it with
+ *     usp_get_device_status().
+ *   - No exception crosses the ABI. Calls are thread-safe as long as concurrent
+ *     calls use distinct workspaces.
+ */
+#ifndef USP_H_
+#define USP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    USP_OK = 0,
+    USP_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad size, divisibility violated, overlap */
+    USP_ERR_UNSUPPORTED = 2,  /* valid request this build does not implement (e.g. head_dim) */
+    USP_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed (launch, tensor map, attribute) */
+    USP_ERR_WORKSPACE = 4,    /* workspace missing or smaller than usp_attn_workspace_size() */
+    USP_ERR_TIMEOUT = 5,      /* device: a bounded wait inside a kernel expired; the kernel bailed out */
+    USP_ERR_DEVICE_CHECK = 6  /* device: cu_seqlens malformed (cu[0] != 0, decreasing, cu[B] != T) */
+} usp_status;
+
+typedef enum { USP_BF16 = 0, USP_FP16 = 1, USP_FP32 = 2 } usp_dtype;
+
+/*
+ * usp_seq_to_head -- the first all-to-all of Ulysses (sequence -> heads), as a
+ * device-local permutation over sp simulated ranks.
+ *   Passage: HF Transformers "Ulysses sequence parallelism" guide, opening
+ *   paragraph (the all-to-all moves the sharded dimension from sequence to
+ *   attention heads) and its two-GPU layout figure; congresoia365 article,
+ *   "Cómo Funciona Ulysses", step 3.
+ *   out[r][hl][t][d] = in[t / S][t % S][r*Hl + hl][d],  S = T/sp, Hl = heads/sp.
+ *   in   : [sp][S][heads][head_dim] elements of `dt` (read only)
+ *   out  : [sp][Hl][T][head_dim]   elements of `dt` (written)
+ *   The copy moves bits; `dt` only fixes the element size (2 or 4 bytes).
+ * Errors: USP_ERR_INVALID_ARG if a pointer is NULL or not 16-byte aligned, the
+ *   buffers overlap, sp < 1, total_tokens < 0, heads < 1, head_dim < 1,
+ *   heads % sp != 0 (the head count must be divisible by sp_size: guide,
+ *   "Configurar"), or total_tokens % sp != 0 (sequences are padded to a multiple
+ *   of sp_size: same section). USP_ERR_UNSUPPORTED if a row (head_dim elements)
+ *   is not a multiple of 16 bytes. total_tokens == 0 is a no-op (the buffers may
+ *   then be NULL); the divisibility rules are still checked.
+ */
+usp_status usp_seq_to_head(const void* in, void* out, int sp, int64_t total_tokens, int heads,
+                           int head_dim, usp_dtype dt, void* stream);
+
+/*
+ * usp_head_to_seq -- the second all-to-all (heads -> sequence), the inverse
+ * permutation of usp_seq_to_head.
+ *   Passage: guide, opening paragraph ("returns to the sequence-sharded
+ *   layout") and the last row of its layout figure; congresoia365 article,
+ *   step 5.
+ *   out[t / S][t % S][r*Hl + hl][d] = in[r][hl][t][d].
+ *   in : [sp][Hl][T][head_dim], out : [sp][S][heads][head_dim]. Same errors.
+ */
+usp_status usp_head_to_seq(const void* in, void* out, int sp, int64_t total_tokens, int heads,
+                           int head_dim, usp_dtype dt, void* stream);
+
+/*
+ * usp_attn_workspace_size -- bytes of workspace the attention calls need for
+ * these sizes (bwd != 0: for usp_attn_bwd_varlen, which also needs per-row
+ * Delta and, for bf16 gradients, an fp32 dQ accumulator). The workspace holds
+ * a status word, the varlen work list and those buffers; it may be reused
+ * across calls on the same stream.
+ */
+size_t usp_attn_workspace_size(int64_t total_tokens, int num_seqs, int hq, int hkv, int head_dim, int bwd);
+
+/*
+ * usp_attn_fwd_varlen -- local attention of one or more Ulysses ranks: causal,
+ * sample-boundary-masked softmax attention over the full (packed) sequence
+ * for the heads given.
+ *   Passages: congresoia365 article, "Cómo Funciona Ulysses", step 4 (standard
+ *   attention for the assigned heads over all positions) and "El Desafío..."
+ *   (FlashAttention-style computation keeps memory O(n) without materialising
+ *   the score matrix); HF guide, "Configurar" (packed samples must not attend
+ *   across their boundaries; no dense 4-D mask).
+ *   s_ij = scale * q_i . k_j; allowed(i,j) = same sample and (!causal or j <= i);
+ *   lse_i = log sum_{allowed j} exp(s_ij);  o_i = sum_j exp(s_ij - lse_i) v_j.
+ *   q   : bf16 [hq][T][head_dim]        k, v : bf16 [hkv][T][head_dim]
+ *   o   : bf16 [hq][T][head_dim]        lse  : fp32 [hq][T] (natural log, includes scale)
+ *   cu_seqlens : device int32 [num_seqs + 1], cu[0] = 0, non-decreasing, cu[num_seqs] = T.
+ *   Query head h reads key/value head h / (hq / hkv).
+ *   softmax_scale <= 0 selects 1/sqrt(head_dim).
+ *   The heads may be one rank's H/sp heads or all ranks' heads in one call.
+ * Errors: USP_ERR_INVALID_ARG (NULL/misaligned pointer, T < 0, num_seqs < 1 when
+ *   T > 0, hq or hkv < 1, hq % hkv != 0); USP_ERR_UNSUPPORTED (head_dim not 64
+ *   or 128); USP_ERR_WORKSPACE (ws_bytes too small). Malformed cu_seqlens is
+ *   detected on the device: the status word becomes USP_ERR_DEVICE_CHECK and
+ *   no output is written. T == 0 is a no-op (the buffers may then be NULL).
+ */
+usp_status usp_attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                               const int32_t* cu_seqlens, int num_seqs, int64_t total_tokens, int hq,
+                               int hkv, int head_dim, float softmax_scale, int causal, void* workspace,
+                               size_t ws_bytes, void* stream);
+
+/*
+ * usp_attn_bwd_varlen -- gradient of usp_attn_fwd_varlen with respect to q, k
+ * and v, from the saved logsumexp (the backward of the local attention step
+ * each rank runs; the pages' training loops call it through backward()).
+ *   dP_ij = dO_i . v_j; Delta_i = sum_j P_ij dP_ij (= dO_i . o_i);
+ *   dS_ij = P_ij (dP_ij - Delta_i); dq_i = scale sum_j dS_ij k_j;
+ *   dk_j = scale sum_i dS_ij q_i; dv_j = sum_i P_ij dO_i, where dk and dv of a
+ *   key/value head sum over the hq/hkv query heads that read it.
+ *   q, k, v, o, d_o : bf16 as in the forward; lse : fp32 [hq][T] from the forward.
+ *   dq : [hq][T][head_dim], dk, dv : [hkv][T][head_dim] of grad_dt (USP_BF16 or USP_FP32).
+ * Errors: as usp_attn_fwd_varlen; USP_ERR_UNSUPPORTED for grad_dt = USP_FP16.
+ */
+usp_status usp_attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
+                               const float* lse, const void* d_o, void* dq, void* dk, void* dv,
+                               usp_dtype grad_dt, const int32_t* cu_seqlens, int num_seqs,
+                               int64_t total_tokens, int hq, int hkv, int head_dim, float softmax_scale,
+                               int causal, void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * usp_get_device_status -- synchronises `stream`, then returns the status word
+ * the last attention call on `workspace` left there (USP_OK,
+ * USP_ERR_DEVICE_CHECK or USP_ERR_TIMEOUT), or USP_ERR_CUDA if the stream
+ * reports an error. Does not clear the word; every attention call resets it.
+ */
+usp_status usp_get_device_status(const void* workspace, void* stream);
+
+/* Human-readable name of a status code (static string). */
+const char* usp_status_string(usp_status status);
+
+/*
+ * usp_debug_wait_timeout -- launches one kernel that waits on an mbarrier that
+ * nothing ever arrives on, with a wall-clock limit of `limit_ns`, and records
+ * USP_ERR_TIMEOUT in the workspace status word when the limit expires. The
+ * kernel then returns normally, so the CUDA context stays usable. Exists to
+ * test the bounded-wait error path of the attention kernels without faulting
+ * or hanging a GPU. limit_ns is clamped to [1e3, 5e9].
+ */
+usp_status usp_debug_wait_timeout(void* workspace, size_t ws_bytes, uint64_t limit_ns, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* USP_H_ */

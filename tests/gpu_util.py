@@ -1,0 +1,80 @@
+"""Helpers shared by the GPU tests: moving seeded bf16 bit patterns to the device,
+reading results back, and choosing sampled rows for large-size parity checks."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import ulysses_sequence_seq_gb300 as usp
+
+
+def needs_gpu():
+    if not torch.cuda.is_available():
+        import pytest
+        pytest.skip("no CUDA device")
+
+
+def dev_bf16(bits: np.ndarray) -> torch.Tensor:
+    """uint16 bf16 bit patterns -> CUDA bf16 tensor with exactly those bits."""
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16))
+    return t.view(torch.bfloat16).cuda()
+
+
+def host_bits(t: torch.Tensor) -> np.ndarray:
+    return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def f64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def sample_rows(cu, n_random: int, seed: int = 0, T: int | None = None):
+    """Rows worth checking: the first and last rows of every sample, rows around
+    128-row tile edges, plus random rows (sorted, unique)."""
+    cu = [int(x) for x in cu]
+    T = cu[-1] if T is None else T
+    rows = set()
+    for b in range(len(cu) - 1):
+        s, e = cu[b], cu[b + 1]
+        for r in (s, s + 1, s + 127, s + 128, s + 129, s + 255, s + 256, e - 129, e - 128, e - 2, e - 1):
+            if s <= r < e:
+                rows.add(r)
+    rng = np.random.default_rng(seed)
+    if T > 0:
+        rows.update(int(x) for x in rng.integers(0, T, size=n_random))
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+class Problem:
+    """Device buffers for one attention problem in the head-major layout."""
+
+    def __init__(self, q_bits, k_bits, v_bits, cu, causal=True, do_bits=None):
+        self.q, self.k, self.v = dev_bf16(q_bits), dev_bf16(k_bits), dev_bf16(v_bits)
+        self.do = dev_bf16(do_bits) if do_bits is not None else None
+        self.cu_host = np.asarray(cu, dtype=np.int32)
+        self.cu = torch.from_numpy(self.cu_host).cuda()
+        self.hq, self.T, self.D = q_bits.shape
+        self.hkv = k_bits.shape[0]
+        self.B = len(cu) - 1
+        self.causal = causal
+        self.ws_bytes = max(usp.attn_workspace_size(self.T, self.B, self.hq, self.hkv, self.D, False),
+                            usp.attn_workspace_size(self.T, self.B, self.hq, self.hkv, self.D, True))
+        self.ws = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8, device="cuda")
+
+    def forward(self):
+        o = torch.full((self.hq, self.T, self.D), float("nan"), dtype=torch.bfloat16, device="cuda")
+        lse = torch.full((self.hq, self.T), float("nan"), dtype=torch.float32, device="cuda")
+        usp.attn_fwd_varlen(self.q, self.k, self.v, o, lse, self.cu, self.B, self.T, self.hq, self.hkv, self.D,
+                            0.0, self.causal, self.ws, self.ws_bytes)
+        status = usp.get_device_status(self.ws)
+        return o, lse, status
+
+    def backward(self, o, lse, grad_dtype=torch.float32):
+        gd = usp.USP_FP32 if grad_dtype == torch.float32 else usp.USP_BF16
+        dq = torch.full((self.hq, self.T, self.D), float("nan"), dtype=grad_dtype, device="cuda")
+        dk = torch.full((self.hkv, self.T, self.D), float("nan"), dtype=grad_dtype, device="cuda")
+        dv = torch.full((self.hkv, self.T, self.D), float("nan"), dtype=grad_dtype, device="cuda")
+        usp.attn_bwd_varlen(self.q, self.k, self.v, o, lse, self.do, dq, dk, dv, gd, self.cu, self.B, self.T,
+                            self.hq, self.hkv, self.D, 0.0, self.causal, self.ws, self.ws_bytes)
+        status = usp.get_device_status(self.ws)
+        return dq, dk, dv, status

@@ -1,0 +1,117 @@
+"""GPU parity of the attention backward against the float64 oracle.
+
+The gate is on fp32 gradient outputs: dQ, dK, dV within max-abs 2e-2 of the float64
+result. bf16 gradient outputs additionally carry their own rounding (half an ulp
+of bf16, 2^-9 relative), which the bf16 check adds to the same bound.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests.gpu_util import Problem, f64, needs_gpu, sample_rows
+from ulysses_sequence_seq_gb300.synth import WORKLOADS, custom_workload, head_sharded_bits
+
+pytestmark = pytest.mark.gpu
+
+G_TOL = 2e-2
+
+
+def make(w, q_heads=None, kv_heads=None):
+    return (head_sharded_bits(w, "q", q_heads), head_sharded_bits(w, "k", kv_heads),
+            head_sharded_bits(w, "v", kv_heads), head_sharded_bits(w, "do", q_heads))
+
+
+def check_bwd(q, k, v, do, cu, causal, q_heads=None, q_rows=None, kv_heads=None, k_rows=None,
+              grad_dtype=torch.float32):
+    p = Problem(q, k, v, cu, causal, do_bits=do)
+    o, lse, st = p.forward()
+    assert st == 0
+    dq, dk, dv, st = p.backward(o, lse, grad_dtype)
+    assert st == 0
+    rq, rk, rv = oracle.attn_bwd(q, k, v, do, cu, causal=causal, q_heads=q_heads, q_rows=q_rows,
+                                 kv_heads=kv_heads, k_rows=k_rows)
+    qh = list(range(q.shape[0])) if q_heads is None else list(q_heads)
+    qr = np.arange(q.shape[1]) if q_rows is None else np.asarray(q_rows)
+    kh = list(range(k.shape[0])) if kv_heads is None else list(kv_heads)
+    kr = np.arange(k.shape[1]) if k_rows is None else np.asarray(k_rows)
+    got = [f64(dq)[qh][:, qr], f64(dk)[kh][:, kr], f64(dv)[kh][:, kr]]
+    for name, g, r in zip(("dQ", "dK", "dV"), got, (rq, rk, rv)):
+        tol = G_TOL if grad_dtype == torch.float32 else G_TOL + np.abs(r) * 2.0 ** -8
+        err = np.abs(g - r)
+        assert (err <= tol).all(), f"{name} max-abs error {err.max()} (max |ref| {np.abs(r).max()})"
+    return dq, dk, dv
+
+
+def test_bwd_tiny_full():
+    needs_gpu()
+    w = WORKLOADS["tiny"]
+    check_bwd(*make(w), w.cu_seqlens(), True)
+
+
+def test_bwd_tiny_bf16_grads():
+    needs_gpu()
+    w = WORKLOADS["tiny"]
+    check_bwd(*make(w), w.cu_seqlens(), True, grad_dtype=torch.bfloat16)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("D", [64, 128])
+def test_bwd_ragged_packed_edges_gqa(causal, D):
+    needs_gpu()
+    w = custom_workload("ragged", [1, 7, 129, 163, 1, 254], sp=1, hq=4, hkv=2, head_dim=D, causal=causal,
+                        index=11)
+    check_bwd(*make(w), w.cu_seqlens(), causal)
+
+
+def test_bwd_llama_all_heads_launch():
+    """All 32 heads in one launch; two query heads (and their key/value heads) checked in full."""
+    needs_gpu()
+    w = WORKLOADS["llama"]
+    check_bwd(*make(w), w.cu_seqlens(), True, q_heads=[0, 31], kv_heads=[5, 31])
+
+
+def test_bwd_packed_rank_slice_sampled():
+    needs_gpu()
+    w = WORKLOADS["packed"]
+    cu = w.cu_seqlens()
+    ends = [int(x) for x in cu[1:]]
+    k_rows = sorted({r for e in ends for r in (e - 1, e - 2, e - 128, e - 129)} | {0, 1, 127, 128})
+    check_bwd(*make(w, range(4), range(4)), cu, True, q_heads=[1], q_rows=sample_rows(cu, 64, seed=7),
+              kv_heads=[2], k_rows=k_rows)
+
+
+def test_bwd_gqa_rank_slice_sampled():
+    needs_gpu()
+    w = WORKLOADS["gqa"]
+    cu = w.cu_seqlens()
+    ends = [int(x) for x in cu[1:]]
+    k_rows = sorted({r for e in ends for r in (e - 1, e - 128, e - 129)})
+    check_bwd(*make(w, range(4), range(1)), cu, True, q_heads=[0, 3], q_rows=sample_rows(cu, 48, seed=9),
+              kv_heads=[0], k_rows=k_rows)
+
+
+def test_bwd_long_rank_slice_sampled():
+    needs_gpu()
+    w = WORKLOADS["long"]
+    cu = w.cu_seqlens()
+    T = w.total_tokens
+    q_rows = np.array([0, 1, 128, 70000, 262143], dtype=np.int64)
+    k_rows = np.array([T - 300, T - 129, T - 128, T - 2, T - 1], dtype=np.int64)
+    check_bwd(*make(w, range(4), range(4)), cu, True, q_heads=[2], q_rows=q_rows, kv_heads=[2], k_rows=k_rows)
+
+
+def test_bwd_key_gradients_sum_to_zero_per_sample():
+    """Each row of dS sums to zero, so the key gradients of every sample sum to zero (up to
+    the bf16 rounding of O inside Delta = dO . O, hence the loose bound)."""
+    needs_gpu()
+    w = custom_workload("sums", [513, 300, 211], sp=1, hq=4, hkv=1, head_dim=128, index=16)
+    q, k, v, do = make(w)
+    cu = w.cu_seqlens()
+    p = Problem(q, k, v, cu, True, do_bits=do)
+    o, lse, _ = p.forward()
+    _, dk, _, st = p.backward(o, lse)
+    assert st == 0
+    g = f64(dk)
+    for b in range(3):
+        assert np.abs(g[:, cu[b]:cu[b + 1]].sum(axis=1)).max() < 1e-1

@@ -1,0 +1,153 @@
+"""GPU parity of the attention forward against the float64 oracle.
+
+Tolerances (bf16 inputs, fp32 accumulation, bf16 output): O within max-abs 1e-2 of
+the unrounded float64 result; LSE (fp32 output) within 1e-3.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests.gpu_util import Problem, f64, host_bits, needs_gpu, sample_rows
+from ulysses_sequence_seq_gb300.synth import WORKLOADS, custom_workload, head_sharded_bits
+
+pytestmark = pytest.mark.gpu
+
+O_TOL = 1e-2
+LSE_TOL = 1e-3
+
+
+def make(w, q_heads=None, kv_heads=None, with_do=False):
+    q = head_sharded_bits(w, "q", q_heads)
+    k = head_sharded_bits(w, "k", kv_heads)
+    v = head_sharded_bits(w, "v", kv_heads)
+    do = head_sharded_bits(w, "do", q_heads) if with_do else None
+    return q, k, v, do
+
+
+def check_fwd(q, k, v, cu, causal, heads=None, rows=None):
+    p = Problem(q, k, v, cu, causal)
+    o, lse, status = p.forward()
+    assert status == 0
+    ro, rl = oracle.attn_fwd(q, k, v, cu, causal=causal, heads=heads, rows=rows)
+    hs = list(range(q.shape[0])) if heads is None else list(heads)
+    rs = np.arange(q.shape[1]) if rows is None else np.asarray(rows)
+    go = f64(o)[hs][:, rs]
+    gl = f64(lse)[hs][:, rs]
+    err_o = np.abs(go - ro).max()
+    err_l = np.abs(gl - rl).max()
+    assert err_o <= O_TOL, f"O max-abs error {err_o}"
+    assert err_l <= LSE_TOL, f"LSE max-abs error {err_l}"
+    return p, o, lse
+
+
+def test_fwd_tiny_full():
+    needs_gpu()
+    w = WORKLOADS["tiny"]
+    q, k, v, _ = make(w)
+    check_fwd(q, k, v, w.cu_seqlens(), True)
+
+
+def test_fwd_llama_all_heads_launch():
+    """All 32 heads of the 2 x 4096 batch in one launch; four heads checked in full."""
+    needs_gpu()
+    w = WORKLOADS["llama"]
+    q, k, v, _ = make(w)
+    check_fwd(q, k, v, w.cu_seqlens(), True, heads=[0, 9, 22, 31])
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("D", [64, 128])
+def test_fwd_ragged_packed_edges(causal, D):
+    """Samples of 1, 7, 129, 163, 1 and 254 tokens (T = 555 is no multiple of 128),
+    and GQA 4 query heads over 2 key/value heads."""
+    needs_gpu()
+    w = custom_workload("ragged", [1, 7, 129, 163, 1, 254], sp=1, hq=4, hkv=2, head_dim=D, causal=causal,
+                        index=11)
+    q, k, v, _ = make(w)
+    check_fwd(q, k, v, w.cu_seqlens(), causal)
+
+
+def test_fwd_empty_samples():
+    needs_gpu()
+    w = custom_workload("empty", [0, 100, 0, 0, 156, 0], sp=1, hq=2, hkv=2, head_dim=128, index=12)
+    q, k, v, _ = make(w)
+    check_fwd(q, k, v, w.cu_seqlens(), True)
+
+
+def test_fwd_zero_tokens_is_noop():
+    needs_gpu()
+    z = np.zeros((2, 0, 128), dtype=np.uint16)
+    p = Problem(z, z, z, [0], True)
+    o, lse, status = p.forward()
+    assert status == 0
+
+
+def test_fwd_bad_cu_seqlens_reports_device_check():
+    needs_gpu()
+    w = custom_workload("bad", [128, 128], sp=1, hq=2, hkv=2, head_dim=128, index=13)
+    q, k, v, _ = make(w)
+    p = Problem(q, k, v, [0, 200, 100], True)        # decreasing offsets
+    o, lse, status = p.forward()
+    assert status == 6                                 # USP_ERR_DEVICE_CHECK
+    assert torch.isnan(o.float()).all()                # nothing written
+
+
+def test_fwd_packed_rank_slice_sampled():
+    """65536 packed tokens (lognormal lengths), one rank's 4 heads, sampled rows."""
+    needs_gpu()
+    w = WORKLOADS["packed"]
+    q, k, v, _ = make(w, range(4), range(4))
+    cu = w.cu_seqlens()
+    check_fwd(q, k, v, cu, True, heads=[0, 3], rows=sample_rows(cu, 96, seed=3))
+
+
+def test_fwd_gqa_rank_slice_sampled():
+    """131072 packed tokens, 4 query heads sharing 1 key/value head (one rank of 32q/8kv)."""
+    needs_gpu()
+    w = WORKLOADS["gqa"]
+    q, k, v, _ = make(w, range(4), range(1))
+    cu = w.cu_seqlens()
+    check_fwd(q, k, v, cu, True, heads=[0, 2, 3], rows=sample_rows(cu, 64, seed=5))
+
+
+def test_fwd_long_rank_slice_sampled():
+    """One 262144-token causal sequence, one rank's 4 heads, sampled rows."""
+    needs_gpu()
+    w = WORKLOADS["long"]
+    q, k, v, _ = make(w, range(4), range(4))
+    cu = w.cu_seqlens()
+    rows = np.array([0, 1, 127, 128, 4095, 65536, 131071, 200003, 262016, 262143], dtype=np.int64)
+    check_fwd(q, k, v, cu, True, heads=[1], rows=rows)
+
+
+def test_fwd_deterministic_and_head_independent():
+    """Bitwise identical across runs, and one rank's heads computed alone equal the
+    same heads computed with every rank's heads in one launch."""
+    needs_gpu()
+    w = custom_workload("det", [300, 700, 24], sp=2, hq=8, hkv=4, head_dim=128, index=14)
+    q, k, v, _ = make(w)
+    cu = w.cu_seqlens()
+    p = Problem(q, k, v, cu, True)
+    o1, l1, _ = p.forward()
+    o2, l2, _ = p.forward()
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16)) and torch.equal(l1, l2)
+    p_r1 = Problem(q[4:], k[2:], v[2:], cu, True)      # rank 1 of sp = 2
+    o3, l3, _ = p_r1.forward()
+    assert np.array_equal(host_bits(o3), host_bits(o1)[4:]) and torch.equal(l3, l1[4:])
+
+
+def test_fwd_no_leakage_between_samples():
+    """Changing one sample's keys and values leaves every other sample's output bit-identical."""
+    needs_gpu()
+    w = custom_workload("leak", [200, 333, 91], sp=1, hq=2, hkv=2, head_dim=128, index=15)
+    q, k, v, _ = make(w)
+    cu = w.cu_seqlens()
+    o1, _, _ = Problem(q, k, v, cu, True).forward()
+    k2, v2 = k.copy(), v.copy()
+    k2[:, 200:533] ^= np.uint16(0x0040)
+    v2[:, 200:533] ^= np.uint16(0x0040)
+    o2, _, _ = Problem(q, k2, v2, cu, True).forward()
+    a, b = host_bits(o1), host_bits(o2)
+    assert np.array_equal(a[:, :200], b[:, :200]) and np.array_equal(a[:, 533:], b[:, 533:])
+    assert not np.array_equal(a[:, 200:533], b[:, 200:533])

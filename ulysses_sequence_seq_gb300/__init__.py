@@ -1,0 +1,90 @@
+"""GB300-native hot path of Ulysses sequence parallelism.
+
+The library (``libusp.so``, C ABI in ``include/usp.h``) implements the per-rank
+step of Ulysses sequence parallelism with sp ranks simulated as shards of one
+device buffer:
+
+* :func:`seq_to_head` / :func:`head_to_seq` -- the two all-to-alls as
+  device-local permutations [sp][T/sp][H][D] <-> [sp][H/sp][T][D];
+* :func:`attn_fwd_varlen` / :func:`attn_bwd_varlen` -- causal, packed-sample
+  (cu_seqlens) softmax attention forward and backward on tcgen05 tensor cores.
+
+:class:`UlyssesAttention` chains them into the layer-level step: the seq-sharded
+Q, K, V of all ranks in, the seq-sharded attention output out, and the same in
+reverse for the gradients. PyTorch only provides device memory and streams.
+"""
+from __future__ import annotations
+
+import math
+
+from ._lib import (USP_BF16, USP_FP16, USP_FP32, USP_OK, UspError, attn_bwd_varlen, attn_fwd_varlen,  # noqa: F401
+                   attn_workspace_size, debug_wait_timeout, get_device_status, head_to_seq, load, seq_to_head,
+                   status_string)
+
+__all__ = [
+    "seq_to_head", "head_to_seq", "attn_fwd_varlen", "attn_bwd_varlen", "attn_workspace_size",
+    "get_device_status", "status_string", "UspError", "UlyssesAttention", "load",
+]
+
+
+class UlyssesAttention:
+    """The attention step of one Ulysses layer for all sp simulated ranks of one GPU.
+
+    Buffers are allocated once for a fixed (T, num_seqs, hq, hkv, D, sp) and reused.
+    ``forward`` takes seq-sharded bf16 tensors ([sp][T/sp][H][D] or [T][H][D]) and
+    returns the seq-sharded output; ``backward`` takes the seq-sharded output
+    gradient and returns seq-sharded dQ, dK, dV.
+    """
+
+    def __init__(self, total_tokens: int, num_seqs: int, hq: int, hkv: int, head_dim: int, sp: int,
+                 causal: bool = True, softmax_scale: float = 0.0, device="cuda", grad_dtype=None):
+        import torch
+        self.T, self.B, self.hq, self.hkv, self.D, self.sp = total_tokens, num_seqs, hq, hkv, head_dim, sp
+        self.causal = causal
+        self.scale = softmax_scale if softmax_scale > 0 else 1.0 / math.sqrt(head_dim)
+        self.grad_dtype = grad_dtype or torch.bfloat16
+        bf = torch.bfloat16
+        T, D = total_tokens, head_dim
+        self.q_h = torch.empty(hq, T, D, dtype=bf, device=device)
+        self.k_h = torch.empty(hkv, T, D, dtype=bf, device=device)
+        self.v_h = torch.empty(hkv, T, D, dtype=bf, device=device)
+        self.o_h = torch.empty(hq, T, D, dtype=bf, device=device)
+        self.do_h = torch.empty(hq, T, D, dtype=bf, device=device)
+        self.lse = torch.empty(hq, T, dtype=torch.float32, device=device)
+        self.o_seq = torch.empty(T, hq, D, dtype=bf, device=device)
+        gd = self.grad_dtype
+        self.dq_h = torch.empty(hq, T, D, dtype=gd, device=device)
+        self.dk_h = torch.empty(hkv, T, D, dtype=gd, device=device)
+        self.dv_h = torch.empty(hkv, T, D, dtype=gd, device=device)
+        self.dq_seq = torch.empty(T, hq, D, dtype=gd, device=device)
+        self.dk_seq = torch.empty(T, hkv, D, dtype=gd, device=device)
+        self.dv_seq = torch.empty(T, hkv, D, dtype=gd, device=device)
+        self.ws_bytes = max(attn_workspace_size(T, num_seqs, hq, hkv, D, False),
+                            attn_workspace_size(T, num_seqs, hq, hkv, D, True))
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=device)
+
+    def forward(self, xq, xk, xv, cu_seqlens, stream=None):
+        sp = self.sp
+        seq_to_head(xq, self.q_h, sp, stream)
+        seq_to_head(xk, self.k_h, sp, stream)
+        seq_to_head(xv, self.v_h, sp, stream)
+        attn_fwd_varlen(self.q_h, self.k_h, self.v_h, self.o_h, self.lse, cu_seqlens, self.B, self.T, self.hq,
+                        self.hkv, self.D, self.scale, self.causal, self.ws, self.ws_bytes, stream)
+        head_to_seq(self.o_h, self.o_seq, sp, stream)
+        return self.o_seq
+
+    def backward(self, d_out, cu_seqlens, stream=None):
+        import torch
+        sp = self.sp
+        seq_to_head(d_out, self.do_h, sp, stream)
+        gdt = USP_FP32 if self.grad_dtype == torch.float32 else USP_BF16
+        attn_bwd_varlen(self.q_h, self.k_h, self.v_h, self.o_h, self.lse, self.do_h, self.dq_h, self.dk_h,
+                        self.dv_h, gdt, cu_seqlens, self.B, self.T, self.hq, self.hkv, self.D, self.scale,
+                        self.causal, self.ws, self.ws_bytes, stream)
+        head_to_seq(self.dq_h, self.dq_seq, sp, stream)
+        head_to_seq(self.dk_h, self.dk_seq, sp, stream)
+        head_to_seq(self.dv_h, self.dv_seq, sp, stream)
+        return self.dq_seq, self.dk_seq, self.dv_seq
+
+    def device_status(self, stream=None) -> int:
+        return get_device_status(self.ws, stream)

@@ -1,0 +1,165 @@
+"""ctypes binding of ``libusp.so`` (argument marshalling only).
+
+Every function takes torch CUDA tensors (or raw integer device pointers), passes
+their addresses, sizes and the current CUDA stream to the C ABI declared in
+``include/usp.h``, and raises :class:`UspError` on a non-OK status. All work
+runs in the library's CUDA kernels; there is no fallback of any kind: if the
+library is missing or cannot be loaded, import-time loading fails loudly.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build_lib
+
+USP_OK = 0
+USP_ERR_INVALID_ARG = 1
+USP_ERR_UNSUPPORTED = 2
+USP_ERR_CUDA = 3
+USP_ERR_WORKSPACE = 4
+USP_ERR_TIMEOUT = 5
+USP_ERR_DEVICE_CHECK = 6
+
+USP_BF16 = 0
+USP_FP16 = 1
+USP_FP32 = 2
+
+EXPORTED = (
+    "usp_seq_to_head",
+    "usp_head_to_seq",
+    "usp_attn_workspace_size",
+    "usp_attn_fwd_varlen",
+    "usp_attn_bwd_varlen",
+    "usp_get_device_status",
+    "usp_status_string",
+    "usp_debug_wait_timeout",
+)
+
+
+class UspError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        self.code = int(code)
+        super().__init__(f"{fn} failed: {status_string(code)} ({code})")
+
+
+_lib = None
+
+
+def lib_path() -> str:
+    return build_lib.LIB
+
+
+def load(build_if_missing: bool = True):
+    """Load libusp.so (building it first when absent or stale and nvcc exists)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = build_lib.LIB
+    if build_if_missing and not build_lib.up_to_date():
+        build_lib.build()
+    if not os.path.exists(path):
+        raise ImportError(f"libusp.so not found at {path}; run __graft_entry__.build()")
+    L = ctypes.CDLL(path)
+    P, I, I64, Z, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
+    L.usp_seq_to_head.argtypes = [P, P, I, I64, I, I, I, P]
+    L.usp_head_to_seq.argtypes = [P, P, I, I64, I, I, I, P]
+    L.usp_attn_workspace_size.argtypes = [I64, I, I, I, I, I]
+    L.usp_attn_workspace_size.restype = Z
+    L.usp_attn_fwd_varlen.argtypes = [P, P, P, P, P, P, I, I64, I, I, I, F, I, P, Z, P]
+    L.usp_attn_bwd_varlen.argtypes = [P, P, P, P, P, P, P, P, P, I, P, I, I64, I, I, I, F, I, P, Z, P]
+    L.usp_get_device_status.argtypes = [P, P]
+    L.usp_status_string.argtypes = [I]
+    L.usp_status_string.restype = ctypes.c_char_p
+    L.usp_debug_wait_timeout.argtypes = [P, Z, ctypes.c_uint64, P]
+    for name in ("usp_seq_to_head", "usp_head_to_seq", "usp_attn_fwd_varlen", "usp_attn_bwd_varlen",
+                 "usp_get_device_status", "usp_debug_wait_timeout"):
+        getattr(L, name).restype = I
+    _lib = L
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return load().usp_status_string(int(code)).decode()
+
+
+def _check(fn: str, code: int):
+    if code != USP_OK:
+        raise UspError(fn, code)
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return USP_BF16
+    if t.dtype == torch.float16:
+        return USP_FP16
+    if t.dtype == torch.float32:
+        return USP_FP32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def seq_to_head(x, out, sp: int, stream=None):
+    """x: [sp][T/sp][H][D] (any view with those bytes) -> out: [sp][H/sp][T][D]."""
+    H, D = x.shape[-2], x.shape[-1]
+    T = x.numel() // (H * D)
+    _check("usp_seq_to_head", load().usp_seq_to_head(_ptr(x), _ptr(out), int(sp), int(T), int(H), int(D),
+                                                     _dtype_code(x), _stream(stream)))
+    return out
+
+
+def head_to_seq(y, out, sp: int, stream=None):
+    """y: [sp][H/sp][T][D] -> out: [sp][T/sp][H][D]."""
+    T, D = y.shape[-2], y.shape[-1]
+    H = y.numel() // (T * D)
+    _check("usp_head_to_seq", load().usp_head_to_seq(_ptr(y), _ptr(out), int(sp), int(T), int(H), int(D),
+                                                     _dtype_code(y), _stream(stream)))
+    return out
+
+
+def attn_workspace_size(total_tokens: int, num_seqs: int, hq: int, hkv: int, head_dim: int, bwd: bool) -> int:
+    return int(load().usp_attn_workspace_size(int(total_tokens), int(num_seqs), int(hq), int(hkv),
+                                              int(head_dim), int(bool(bwd))))
+
+
+def attn_fwd_varlen(q, k, v, o, lse, cu_seqlens, num_seqs: int, total_tokens: int, hq: int, hkv: int,
+                    head_dim: int, softmax_scale: float, causal: bool, workspace, ws_bytes: int, stream=None):
+    _check("usp_attn_fwd_varlen", load().usp_attn_fwd_varlen(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(cu_seqlens), int(num_seqs), int(total_tokens),
+        int(hq), int(hkv), int(head_dim), float(softmax_scale), int(bool(causal)), _ptr(workspace),
+        int(ws_bytes), _stream(stream)))
+
+
+def attn_bwd_varlen(q, k, v, o, lse, d_o, dq, dk, dv, grad_dt: int, cu_seqlens, num_seqs: int,
+                    total_tokens: int, hq: int, hkv: int, head_dim: int, softmax_scale: float, causal: bool,
+                    workspace, ws_bytes: int, stream=None):
+    _check("usp_attn_bwd_varlen", load().usp_attn_bwd_varlen(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(d_o), _ptr(dq), _ptr(dk), _ptr(dv), int(grad_dt),
+        _ptr(cu_seqlens), int(num_seqs), int(total_tokens), int(hq), int(hkv), int(head_dim),
+        float(softmax_scale), int(bool(causal)), _ptr(workspace), int(ws_bytes), _stream(stream)))
+
+
+def get_device_status(workspace, stream=None) -> int:
+    return int(load().usp_get_device_status(_ptr(workspace), _stream(stream)))
+
+
+def debug_wait_timeout(workspace, ws_bytes: int, limit_ns: int, stream=None):
+    _check("usp_debug_wait_timeout", load().usp_debug_wait_timeout(_ptr(workspace), int(ws_bytes),
+                                                                   int(limit_ns), _stream(stream)))

@@ -1,0 +1,57 @@
+// Launch interfaces of the attention kernels (attn_fwd.cu, attn_bwd.cu).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace usp {
+
+struct FwdArgs {
+    const int32_t* cu;
+    const WorkItem* items;
+    WsHeader* hdr;
+    __nv_bfloat16* o;   // [hq][T][D]
+    float* lse;         // [hq][T], natural log
+    int64_t T;
+    int group;          // hq / hkv
+    int causal;
+    float scale_log2;   // softmax scale * log2(e)
+};
+
+cudaError_t launch_attn_fwd(int head_dim, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                            const FwdArgs& a, int grid, cudaStream_t s);
+
+struct BwdArgs {
+    const int32_t* cu;
+    const WorkItem* items;
+    WsHeader* hdr;
+    const float* lse;    // [hq][T]
+    const float* delta;  // [hq][T]
+    float* dq_acc;       // [hq][T][D] fp32 accumulator (atomic adds)
+    void* dk;            // [hkv][T][D]
+    void* dv;            // [hkv][T][D]
+    int grad_fp32;       // 1: dk/dv written as fp32, 0: bf16
+    int64_t T;
+    int group;
+    int causal;
+    float scale;         // softmax scale
+    float scale_log2;    // softmax scale * log2(e)
+};
+
+cudaError_t launch_attn_bwd(int head_dim, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                            const CUtensorMap& dout, const BwdArgs& a, int grid, cudaStream_t s);
+
+// Delta_i = dO_i . O_i (fp32) for every query row, and zeroes the dQ accumulator.
+cudaError_t launch_bwd_prep(const __nv_bfloat16* o, const __nv_bfloat16* dout, float* delta, float* dq_acc,
+                            int64_t rows, int head_dim, cudaStream_t s);
+
+// dq = dq_acc converted to bf16.
+cudaError_t launch_dq_convert(const float* dq_acc, __nv_bfloat16* dq, int64_t n, cudaStream_t s);
+
+// Records `code` in the status word after a kernel that waits on an mbarrier nothing arrives on.
+cudaError_t launch_debug_timeout(WsHeader* hdr, uint64_t limit_ns, cudaStream_t s);
+
+}  // namespace usp

@@ -1,0 +1,499 @@
+// Backward of the local attention step on sm_103a: dQ, dK, dV of causal,
+// sample-boundary-masked softmax attention from the saved logsumexp.
+//
+//   P_ij  = exp(s_ij - lse_i)           dP_ij = dO_i . v_j        Delta_i = dO_i . O_i
+//   dS_ij = scale * P_ij (dP_ij - Delta_i)
+//   dV_j  = sum_i P_ij dO_i     dK_j = sum_i dS_ij q_i     dQ_i = sum_j dS_ij k_j
+//
+// One CTA owns a 128-row key/value tile of one sample and one key/value head and
+// walks every query block that sees it (from the diagonal on when causal), for all
+// query heads of its GQA group, so dK and dV accumulate in tensor memory and are
+// written once. dQ partial tiles are added into an fp32 accumulator with vector
+// atomics. Everything is computed transposed (key rows on TMEM lanes) so that P^T
+// and dS^T feed the dV and dK MMAs straight from TMEM.
+//
+// Warp roles (320 threads):
+//   warps 0-3  compute group: thread = key row; P^T, dS^T; writes dK, dV at the end
+//   warps 4-7  dQ group: thread = query row; drains the dQ tile with atomics
+//   warp  8    TMA producer: K, V once, then Q / dO blocks into a 2-stage ring
+//   warp  9    MMA issuer and TMEM owner
+// Tensor memory: S^T/P^T [0,128), dP^T/dS^T then dQ [128,256), dV [256,256+D),
+// dK [384,384+D).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "attn.cuh"
+#include "common.cuh"
+#include "ptx.cuh"
+#include "tiles.cuh"
+
+namespace usp {
+namespace {
+
+using namespace ptx;
+
+constexpr int kBwdThreads = 320;
+
+template <int D>
+struct BwdSmem {
+    static constexpr int kPanels = D / 64;
+    static constexpr int kTileBytes = kTileM * D * 2;
+    static constexpr int kK = 0;
+    static constexpr int kV = kTileBytes;
+    static constexpr int kQ = 2 * kTileBytes;        // + stage * kTileBytes
+    static constexpr int kDO = 4 * kTileBytes;       // + stage * kTileBytes
+    static constexpr int kDS = 6 * kTileBytes;       // [128 key rows][128 query cols] bf16, two 64-col panels
+    static constexpr int kLse = kDS + kTileM * kBlockN * 2;  // fp32[128] (log2 units)
+    static constexpr int kDelta = kLse + 512;                // fp32[128]
+    static constexpr int kBars = kDelta + 512;
+    static constexpr int bKvFull = 0, bQFull = 1, bDoFull = 3, bQEmpty = 5, bSFull = 7, bDpFull = 8, bPFull = 9,
+                         bDsFull = 10, bDqFull = 11, bDqEmpty = 12, bAccFull = 13, bDrain = 14, kNumBars = 15;
+    static constexpr int kTmemSlot = kBars + 8 * kNumBars;
+    static constexpr int kAbort = kTmemSlot + 8;
+    static constexpr int kBytes = kAbort + 8;
+    static constexpr int kAlloc = kBytes + 1024;
+};
+static_assert(BwdSmem<128>::kAlloc <= 232448, "backward shared memory exceeds the per-CTA limit");
+
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                    const BwdArgs a) {
+    using L = BwdSmem<D>;
+    const int count = a.hdr->bwd_count;
+    if ((int)blockIdx.x >= count) return;
+    // once any CTA of this launch has timed out, the rest skip their work
+    if (*(volatile int*)&a.hdr->status != (int)USP_OK) return;
+    const WorkItem it = a.items[blockIdx.x];
+    const int g = it.head;  // key/value head
+    const int s = a.cu[it.seq], e = a.cu[it.seq + 1];
+    const int kv0 = s + it.tile * kBlockN;
+    const int i0 = first_query_block_for_kv_block(it.tile, a.causal);
+    const int nq = query_blocks_in_sample(s, e) - i0;  // query blocks per query head
+    const int G = a.group;
+    const int nsteps = nq * G;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint64_t* bars = (uint64_t*)(sm + L::kBars);
+    uint32_t* tmem_slot = (uint32_t*)(sm + L::kTmemSlot);
+    volatile int* abort_flag = (volatile int*)(sm + L::kAbort);
+    float* lse_s = (float*)(sm + L::kLse);
+    float* delta_s = (float*)(sm + L::kDelta);
+
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+
+    if (warp == 9) {
+        tmem_alloc(tmem_slot, 512);
+        tmem_relinquish();
+    }
+    if (threadIdx.x == 0) {
+        mbar_init(&bars[L::bKvFull], 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars[L::bQFull + i], 1);
+            mbar_init(&bars[L::bDoFull + i], 1);
+            mbar_init(&bars[L::bQEmpty + i], 1);
+        }
+        mbar_init(&bars[L::bSFull], 1);
+        mbar_init(&bars[L::bDpFull], 1);
+        mbar_init(&bars[L::bPFull], 4);
+        mbar_init(&bars[L::bDsFull], 4);
+        mbar_init(&bars[L::bDqFull], 1);
+        mbar_init(&bars[L::bDqEmpty], 4);
+        mbar_init(&bars[L::bAccFull], 1);
+        mbar_init(&bars[L::bDrain], 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tmem_slot;
+
+    if (warp == 8) {
+        // ------------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            prefetch_tmap(&tmQ);
+            prefetch_tmap(&tmK);
+            prefetch_tmap(&tmV);
+            prefetch_tmap(&tmDO);
+            mbar_arrive_expect_tx(&bars[L::bKvFull], 2 * L::kTileBytes);
+            for (int p = 0; p < L::kPanels; ++p) {
+                tma_load_3d(sm + L::kK + p * (kTileM * 128), &tmK, &bars[L::bKvFull], p * 64, kv0, g);
+                tma_load_3d(sm + L::kV + p * (kTileM * 128), &tmV, &bars[L::bKvFull], p * 64, kv0, g);
+            }
+            int issued = 0;
+            for (int k = 0; k < nsteps; ++k) {
+                const int st = k & 1;
+                if (k >= 2 && !mbar_wait(&bars[L::bQEmpty + st], ((k >> 1) - 1) & 1, abort_flag, kWaitLimitNs))
+                    break;
+                const int h = g * G + k / nq;
+                const int q0 = s + (i0 + k % nq) * kTileM;
+                mbar_arrive_expect_tx(&bars[L::bQFull + st], L::kTileBytes);
+                for (int p = 0; p < L::kPanels; ++p)
+                    tma_load_3d(sm + L::kQ + st * L::kTileBytes + p * (kTileM * 128), &tmQ, &bars[L::bQFull + st],
+                                p * 64, q0, h);
+                mbar_arrive_expect_tx(&bars[L::bDoFull + st], L::kTileBytes);
+                for (int p = 0; p < L::kPanels; ++p)
+                    tma_load_3d(sm + L::kDO + st * L::kTileBytes + p * (kTileM * 128), &tmDO,
+                                &bars[L::bDoFull + st], p * 64, q0, h);
+                issued = k + 1;
+            }
+            mbar_wait_drain(&bars[L::bKvFull], 0, kDrainLimitNs);
+            for (int k = issued - 2 < 0 ? 0 : issued - 2; k < issued; ++k) {
+                mbar_wait_drain(&bars[L::bQFull + (k & 1)], (k >> 1) & 1, kDrainLimitNs);
+                mbar_wait_drain(&bars[L::bDoFull + (k & 1)], (k >> 1) & 1, kDrainLimitNs);
+            }
+        }
+    } else if (warp == 9) {
+        // ------------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idT = idesc_bf16_f32(kBlockN, kTileM, false, false);  // S^T, dP^T
+            constexpr uint32_t idAcc = idesc_bf16_f32(kBlockN, D, false, true);     // dV, dK (B MN-major)
+            constexpr uint32_t idDq = idesc_bf16_f32(kTileM, D, true, true);        // dQ (A, B MN-major)
+            const uint32_t sK = smem_u32(sm + L::kK), sV = smem_u32(sm + L::kV);
+            const uint32_t sQ = smem_u32(sm + L::kQ), sDO = smem_u32(sm + L::kDO), sDS = smem_u32(sm + L::kDS);
+            const uint32_t tS = tbase, tDP = tbase + 128, tDV = tbase + 256, tDK = tbase + 384;
+            auto issue_t = [&](uint32_t d, uint32_t a_s, uint32_t b_s) {  // d = A . B^T, both K-major
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk / 4) * (kTileM * 128) + (kk % 4) * 32;
+                    mma_ss(d, sdesc_sw128(a_s + off, 0, 1024), sdesc_sw128(b_s + off, 0, 1024), idT, kk > 0);
+                }
+            };
+            bool ok = mbar_wait(&bars[L::bKvFull], 0, abort_flag, kWaitLimitNs);
+            if (ok) ok = mbar_wait(&bars[L::bQFull], 0, abort_flag, kWaitLimitNs);
+            if (ok) {
+                tc_fence_after();
+                issue_t(tS, sK, sQ);
+                mma_commit(&bars[L::bSFull]);
+                ok = mbar_wait(&bars[L::bDoFull], 0, abort_flag, kWaitLimitNs);
+                if (ok) {
+                    tc_fence_after();
+                    issue_t(tDP, sV, sDO);
+                    mma_commit(&bars[L::bDpFull]);
+                }
+            }
+            for (int k = 0; ok && k < nsteps; ++k) {
+                const int st = k & 1;
+                const uint32_t q_s = sQ + st * L::kTileBytes, do_s = sDO + st * L::kTileBytes;
+                if (!mbar_wait(&bars[L::bPFull], k & 1, abort_flag, kWaitLimitNs)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < kTileM / 16; ++kk)  // dV += P^T . dO
+                    mma_ts(tDV, tS + kk * 8, sdesc_sw128(do_s + kk * 2048, kTileM * 128, 1024), idAcc,
+                           (k > 0 || kk > 0) ? 1u : 0u);
+                if (!mbar_wait(&bars[L::bDsFull], k & 1, abort_flag, kWaitLimitNs)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < kTileM / 16; ++kk)  // dK += dS^T . Q
+                    mma_ts(tDK, tDP + kk * 8, sdesc_sw128(q_s + kk * 2048, kTileM * 128, 1024), idAcc,
+                           (k > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                for (int kk = 0; kk < kBlockN / 16; ++kk)  // dQ = dS . K  (into the dP^T columns)
+                    mma_ss(tDP, sdesc_sw128(sDS + kk * 2048, kBlockN * 128, 1024),
+                           sdesc_sw128(sK + kk * 2048, kTileM * 128, 1024), idDq, kk > 0 ? 1u : 0u);
+                mma_commit(&bars[L::bDqFull]);
+                mma_commit(&bars[L::bQEmpty + st]);
+                if (k + 1 < nsteps) {
+                    const int st1 = (k + 1) & 1;
+                    const int ph1 = ((k + 1) >> 1) & 1;
+                    if (!mbar_wait(&bars[L::bQFull + st1], ph1, abort_flag, kWaitLimitNs)) break;
+                    tc_fence_after();
+                    issue_t(tS, sK, sQ + st1 * L::kTileBytes);
+                    mma_commit(&bars[L::bSFull]);
+                    if (!mbar_wait(&bars[L::bDqEmpty], k & 1, abort_flag, kWaitLimitNs)) break;
+                    if (!mbar_wait(&bars[L::bDoFull + st1], ph1, abort_flag, kWaitLimitNs)) break;
+                    tc_fence_after();
+                    issue_t(tDP, sV, sDO + st1 * L::kTileBytes);
+                    mma_commit(&bars[L::bDpFull]);
+                }
+            }
+            mma_commit(&bars[L::bAccFull]);
+            mma_commit(&bars[L::bDrain]);
+            mbar_wait_drain(&bars[L::bDrain], 0, kDrainLimitNs);
+        }
+    } else if (warp < 4) {
+        // ------------------------------------------------------------------ compute group (key rows)
+        const int r = warp * 32 + lane;
+        const int kv = kv0 + r;
+        const bool kv_ok = kv < e;
+        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        const uint32_t tS = tbase + lane_off, tDP = tbase + lane_off + 128;
+        const float sl2 = a.scale_log2;
+        bool ok = true;
+        for (int k = 0; k < nsteps; ++k) {
+            const int h = g * G + k / nq;
+            const int q0 = s + (i0 + k % nq) * kTileM;
+            // this query block's logsumexp (log2 units) and Delta; rows outside the sample get
+            // lse = +inf, which makes their P exactly zero
+            named_bar_sync(1, 128);
+            {
+                const int q = q0 + r;
+                const bool q_ok = q < e;
+                lse_s[r] = q_ok ? __ldg(a.lse + (int64_t)h * a.T + q) * 1.4426950408889634f : INFINITY;
+                delta_s[r] = q_ok ? __ldg(a.delta + (int64_t)h * a.T + q) : 0.f;
+            }
+            named_bar_sync(1, 128);
+            const bool diag = a.causal && (q0 == kv0);
+            if (!mbar_wait(&bars[L::bSFull], k & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
+            tc_fence_after();
+            float p[128];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t sr[32];
+                tmem_ld32(tS + 32 * c, sr);
+                tmem_ld_wait(sr);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int col = 32 * c + j;
+                    float x = ex2_approx(fmaf(__uint_as_float(sr[j]), sl2, -lse_s[col]));
+                    if (!kv_ok || (diag && col < r)) x = 0.f;
+                    p[col] = x;
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(p[32 * c + 2 * j], p[32 * c + 2 * j + 1]);
+                tmem_st16(tS + 16 * c, pk);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[L::bPFull]);
+
+            if (!mbar_wait(&bars[L::bDpFull], k & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
+            tc_fence_after();
+            const float sc = a.scale;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t dr[32];
+                tmem_ld32(tDP + 32 * c, dr);
+                tmem_ld_wait(dr);
+                uint32_t pk[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int c0 = 32 * c + 2 * j;
+                    const float d0 = sc * p[c0] * (__uint_as_float(dr[2 * j]) - delta_s[c0]);
+                    const float d1 = sc * p[c0 + 1] * (__uint_as_float(dr[2 * j + 1]) - delta_s[c0 + 1]);
+                    pk[j] = pack_bf16x2(d0, d1);
+                }
+                tmem_st16(tDP + 16 * c, pk);
+                // the same values, as row r of the [key][query] operand of the dQ MMA
+                uint8_t* panel = sm + L::kDS + (c >> 1) * (kBlockN * 128);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t bytecol = (uint32_t)((c & 1) * 64 + j * 16);
+                    *(uint4*)(panel + sw128_offset(r, bytecol)) =
+                        make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                }
+            }
+            tmem_st_wait();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[L::bDsFull]);
+        }
+        if (ok && mbar_wait(&bars[L::bAccFull], 0, abort_flag, kWaitLimitNs)) {
+            tc_fence_after();
+            const int64_t row = (int64_t)g * a.T + kv;
+#pragma unroll 1
+            for (int which = 0; which < 2; ++which) {
+                const uint32_t src = tbase + lane_off + (which ? 384 : 256);
+                void* dst_base = which ? a.dk : a.dv;
+#pragma unroll 1
+                for (int c = 0; c < D; c += 32) {
+                    uint32_t o[32];
+                    tmem_ld32(src + c, o);
+                    tmem_ld_wait(o);
+                    if (!kv_ok) continue;
+                    if (a.grad_fp32) {
+                        float4* dst = (float4*)((float*)dst_base + row * D + c);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            dst[j] = make_float4(__uint_as_float(o[4 * j]), __uint_as_float(o[4 * j + 1]),
+                                                 __uint_as_float(o[4 * j + 2]), __uint_as_float(o[4 * j + 3]));
+                    } else {
+                        uint4* dst = (uint4*)((__nv_bfloat16*)dst_base + row * D + c);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            dst[j] = make_uint4(pack_bf16x2(__uint_as_float(o[8 * j]), __uint_as_float(o[8 * j + 1])),
+                                                pack_bf16x2(__uint_as_float(o[8 * j + 2]), __uint_as_float(o[8 * j + 3])),
+                                                pack_bf16x2(__uint_as_float(o[8 * j + 4]), __uint_as_float(o[8 * j + 5])),
+                                                pack_bf16x2(__uint_as_float(o[8 * j + 6]), __uint_as_float(o[8 * j + 7])));
+                    }
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------------------------------ dQ group (query rows)
+        const int w4 = warp - 4;
+        const int r = w4 * 32 + lane;
+        const uint32_t tDQ = tbase + ((uint32_t)(w4 * 32) << 16) + 128;
+        for (int k = 0; k < nsteps; ++k) {
+            const int h = g * G + k / nq;
+            const int q = s + (i0 + k % nq) * kTileM + r;
+            if (!mbar_wait(&bars[L::bDqFull], k & 1, abort_flag, kWaitLimitNs)) break;
+            tc_fence_after();
+            uint32_t d0[32], d1[32], d2[32], d3[32];
+            tmem_ld32(tDQ + 0, d0);
+            if (D > 32) tmem_ld32(tDQ + 32, d1);
+            if (D > 64) {
+                tmem_ld32(tDQ + 64, d2);
+                tmem_ld32(tDQ + 96, d3);
+            }
+            tmem_ld_wait();
+            reg_fence(d0);
+            reg_fence(d1);
+            reg_fence(d2);
+            reg_fence(d3);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[L::bDqEmpty]);
+            if (q < e) {
+                float4* dst = (float4*)(a.dq_acc + ((int64_t)h * a.T + q) * D);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    atomicAdd(dst + j, make_float4(__uint_as_float(d0[4 * j]), __uint_as_float(d0[4 * j + 1]),
+                                                   __uint_as_float(d0[4 * j + 2]), __uint_as_float(d0[4 * j + 3])));
+                    if (D > 32)
+                        atomicAdd(dst + 8 + j,
+                                  make_float4(__uint_as_float(d1[4 * j]), __uint_as_float(d1[4 * j + 1]),
+                                              __uint_as_float(d1[4 * j + 2]), __uint_as_float(d1[4 * j + 3])));
+                    if (D > 64) {
+                        atomicAdd(dst + 16 + j,
+                                  make_float4(__uint_as_float(d2[4 * j]), __uint_as_float(d2[4 * j + 1]),
+                                              __uint_as_float(d2[4 * j + 2]), __uint_as_float(d2[4 * j + 3])));
+                        atomicAdd(dst + 24 + j,
+                                  make_float4(__uint_as_float(d3[4 * j]), __uint_as_float(d3[4 * j + 1]),
+                                              __uint_as_float(d3[4 * j + 2]), __uint_as_float(d3[4 * j + 3])));
+                    }
+                }
+            }
+        }
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 9) tmem_dealloc(tbase, 512);
+    if (threadIdx.x == 0 && *abort_flag) atomicCAS(&a.hdr->status, (int)USP_OK, (int)USP_ERR_TIMEOUT);
+}
+
+// Delta_i = dO_i . O_i in fp32, and zero row i of the dQ accumulator. TPR threads per row,
+// each owning 8 consecutive elements (one 16-byte vector of bf16).
+template <int D>
+__global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __restrict__ o,
+                                                       const __nv_bfloat16* __restrict__ dout, float* __restrict__ delta,
+                                                       float* __restrict__ dq_acc, int64_t rows) {
+    constexpr int TPR = D / 8;
+    const int sub = threadIdx.x % TPR;
+    const int64_t rows_per_cta = 256 / TPR;
+    // the loop bound is uniform across the CTA so that every lane reaches the shuffles
+    for (int64_t base = (int64_t)blockIdx.x * rows_per_cta; base < rows; base += (int64_t)gridDim.x * rows_per_cta) {
+        const int64_t row = base + threadIdx.x / TPR;
+        const bool valid = row < rows;
+        float acc = 0.f;
+        if (valid) {
+            const uint4 ov = __ldg((const uint4*)(o + row * D) + sub);
+            const uint4 dv = __ldg((const uint4*)(dout + row * D) + sub);
+            const __nv_bfloat162* o2 = (const __nv_bfloat162*)&ov;
+            const __nv_bfloat162* d2 = (const __nv_bfloat162*)&dv;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float2 x = __bfloat1622float2(o2[j]);
+                const float2 y = __bfloat1622float2(d2[j]);
+                acc = fmaf(x.x, y.x, acc);
+                acc = fmaf(x.y, y.y, acc);
+            }
+        }
+#pragma unroll
+        for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (valid) {
+            if (sub == 0) delta[row] = acc;
+            float4* z = (float4*)(dq_acc + row * D) + 2 * sub;
+            z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+            z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+}
+
+__global__ void __launch_bounds__(256) dq_convert_kernel(const float4* __restrict__ src, uint2* __restrict__ dst,
+                                                         int64_t n4) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (int64_t)gridDim.x * blockDim.x) {
+        const float4 v = src[i];
+        dst[i] = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+    }
+}
+
+__global__ void debug_timeout_kernel(WsHeader* hdr, uint64_t limit_ns) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        // nothing ever arrives on `bar`: the bounded wait must give up and report it
+        if (!mbar_wait(&bar, 0, &abort_flag, limit_ns)) atomicCAS(&hdr->status, (int)USP_OK, (int)USP_ERR_TIMEOUT);
+    }
+}
+
+template <int D>
+cudaError_t launch_bwd_impl(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& dout,
+                            const BwdArgs& a, int grid, cudaStream_t s) {
+    using L = BwdSmem<D>;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    attn_bwd_kernel<D><<<grid, kBwdThreads, L::kAlloc, s>>>(q, k, v, dout, a);
+    return cudaGetLastError();
+}
+
+int grid_for(int64_t work_items, int per_cta) {
+    int64_t g = (work_items + per_cta - 1) / per_cta;
+    if (g > 152 * 16) g = 152 * 16;
+    if (g < 1) g = 1;
+    return (int)g;
+}
+
+}  // namespace
+
+cudaError_t launch_attn_bwd(int head_dim, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                            const CUtensorMap& dout, const BwdArgs& a, int grid, cudaStream_t s) {
+    if (head_dim == 128) return launch_bwd_impl<128>(q, k, v, dout, a, grid, s);
+    return launch_bwd_impl<64>(q, k, v, dout, a, grid, s);
+}
+
+cudaError_t launch_bwd_prep(const __nv_bfloat16* o, const __nv_bfloat16* dout, float* delta, float* dq_acc,
+                            int64_t rows, int head_dim, cudaStream_t s) {
+    if (head_dim == 128) {
+        bwd_prep_kernel<128><<<grid_for(rows, 256 / 16), 256, 0, s>>>(o, dout, delta, dq_acc, rows);
+    } else {
+        bwd_prep_kernel<64><<<grid_for(rows, 256 / 8), 256, 0, s>>>(o, dout, delta, dq_acc, rows);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dq_convert(const float* dq_acc, __nv_bfloat16* dq, int64_t n, cudaStream_t s) {
+    const int64_t n4 = n / 4;
+    dq_convert_kernel<<<grid_for(n4, 256), 256, 0, s>>>((const float4*)dq_acc, (uint2*)dq, n4);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_debug_timeout(WsHeader* hdr, uint64_t limit_ns, cudaStream_t s) {
+    debug_timeout_kernel<<<1, 32, 0, s>>>(hdr, limit_ns);
+    return cudaGetLastError();
+}
+
+}  // namespace usp

@@ -1,0 +1,343 @@
+// Forward of the local attention step of Ulysses sequence parallelism on sm_103a:
+// causal, sample-boundary-masked softmax attention over the full packed sequence for
+// the heads a rank owns, written FlashAttention-style (online softmax, O(n) memory,
+// no materialised score matrix; congresoia365 article, "El Desafío del
+// Entrenamiento de Secuencias Largas", and HF guide "Configurar" on packed samples).
+//
+// One CTA takes one work item: a query head and two 128-row query tiles of one
+// sample. Warp roles (320 threads):
+//   warps 0-3  softmax group for query tile 0 (thread = one query row = one TMEM lane)
+//   warps 4-7  softmax group for query tile 1
+//   warp  8    TMA producer: Q tiles once, then K/V blocks into a 2-stage ring
+//   warp  9    MMA issuer (one thread) and TMEM owner
+// Tensor memory (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [384,384+D).
+// P (bf16) overwrites the first 64 columns of its S tile and feeds the P.V MMA
+// straight from TMEM. The two tiles ping-pong: while one softmax group works on
+// its S, the tensor core runs the other tile's P.V and next Q.K^T.
+// The O rescale is lazy: the running max is only moved when a row's max grows by
+// more than 2^8, which is exact after the final division by the row sum.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "attn.cuh"
+#include "common.cuh"
+#include "ptx.cuh"
+#include "tiles.cuh"
+
+namespace usp {
+namespace {
+
+using namespace ptx;
+
+constexpr int kFwdThreads = 320;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+template <int D>
+struct FwdSmem {
+    static constexpr int kPanels = D / 64;
+    static constexpr int kTileBytes = kTileM * D * 2;  // one 128-row bf16 tile
+    static constexpr int kQ0 = 0;
+    static constexpr int kQ1 = kTileBytes;
+    static constexpr int kK = 2 * kTileBytes;          // + stage * kTileBytes
+    static constexpr int kV = 4 * kTileBytes;          // + stage * kTileBytes
+    static constexpr int kBars = 6 * kTileBytes;
+    // barrier indices
+    static constexpr int bQFull = 0, bKFull = 1, bVFull = 3, bKvEmpty = 5, bSFull = 7, bPFull = 9, bODone = 11,
+                         bDrain = 13, kNumBars = 14;
+    static constexpr int kTmemSlot = kBars + 8 * kNumBars;
+    static constexpr int kAbort = kTmemSlot + 8;
+    static constexpr int kBytes = kAbort + 8;
+    static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment of the base
+};
+
+template <int D>
+__global__ void __launch_bounds__(kFwdThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const FwdArgs a) {
+    using L = FwdSmem<D>;
+    const int count = a.hdr->fwd_count;
+    if ((int)blockIdx.x >= count) return;
+    // once any CTA of this launch has timed out, the rest skip their work
+    if (*(volatile int*)&a.hdr->status != (int)USP_OK) return;
+    const WorkItem it = a.items[blockIdx.x];
+    const int h = it.head;
+    const int s = a.cu[it.seq], e = a.cu[it.seq + 1];
+    const int q00 = s + it.tile * kFwdRowsPerItem, q01 = q00 + kTileM;
+    const int nb0 = kv_blocks_for_query_tile(q00, s, e, a.causal);
+    const int nb1 = kv_blocks_for_query_tile(q01, s, e, a.causal);
+    const int nmax = nb0 > nb1 ? nb0 : nb1;
+    const int kvh = h / a.group;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint64_t* bars = (uint64_t*)(sm + L::kBars);
+    uint32_t* tmem_slot = (uint32_t*)(sm + L::kTmemSlot);
+    volatile int* abort_flag = (volatile int*)(sm + L::kAbort);
+
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+
+    if (warp == 9) {
+        tmem_alloc(tmem_slot, 512);
+        tmem_relinquish();
+    }
+    if (threadIdx.x == 0) {
+        mbar_init(&bars[L::bQFull], 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars[L::bKFull + i], 1);
+            mbar_init(&bars[L::bVFull + i], 1);
+            mbar_init(&bars[L::bKvEmpty + i], 1);
+            mbar_init(&bars[L::bSFull + i], 1);
+            mbar_init(&bars[L::bPFull + i], 4);
+            mbar_init(&bars[L::bODone + i], 1);
+        }
+        mbar_init(&bars[L::bDrain], 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tmem_slot;
+
+    if (warp == 8) {
+        // ------------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            prefetch_tmap(&tmQ);
+            prefetch_tmap(&tmK);
+            prefetch_tmap(&tmV);
+            const int ntiles = nb1 > 0 ? 2 : 1;
+            mbar_arrive_expect_tx(&bars[L::bQFull], ntiles * L::kTileBytes);
+            for (int t = 0; t < ntiles; ++t)
+                for (int p = 0; p < L::kPanels; ++p)
+                    tma_load_3d(sm + (t ? L::kQ1 : L::kQ0) + p * (kTileM * 128), &tmQ, &bars[L::bQFull], p * 64,
+                                t ? q01 : q00, h);
+            int issued = 0;
+            for (int n = 0; n < nmax; ++n) {
+                const int st = n & 1;
+                if (n >= 2 && !mbar_wait(&bars[L::bKvEmpty + st], ((n >> 1) - 1) & 1, abort_flag, kWaitLimitNs))
+                    break;
+                const int row = s + n * kBlockN;
+                mbar_arrive_expect_tx(&bars[L::bKFull + st], L::kTileBytes);
+                for (int p = 0; p < L::kPanels; ++p)
+                    tma_load_3d(sm + L::kK + st * L::kTileBytes + p * (kTileM * 128), &tmK, &bars[L::bKFull + st],
+                                p * 64, row, kvh);
+                mbar_arrive_expect_tx(&bars[L::bVFull + st], L::kTileBytes);
+                for (int p = 0; p < L::kPanels; ++p)
+                    tma_load_3d(sm + L::kV + st * L::kTileBytes + p * (kTileM * 128), &tmV, &bars[L::bVFull + st],
+                                p * 64, row, kvh);
+                issued = n + 1;
+            }
+            // Before the CTA may exit, every copy it issued must have landed. The last
+            // use of each stage is its final phase, so waiting on it is always sound.
+            mbar_wait_drain(&bars[L::bQFull], 0, kDrainLimitNs);
+            for (int n = issued - 2 < 0 ? 0 : issued - 2; n < issued; ++n) {
+                mbar_wait_drain(&bars[L::bKFull + (n & 1)], (n >> 1) & 1, kDrainLimitNs);
+                mbar_wait_drain(&bars[L::bVFull + (n & 1)], (n >> 1) & 1, kDrainLimitNs);
+            }
+        }
+    } else if (warp == 9) {
+        // ------------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idS = idesc_bf16_f32(kTileM, kBlockN, false, false);  // Q.K^T: both K-major
+            constexpr uint32_t idO = idesc_bf16_f32(kTileM, D, false, true);         // P.V: V is MN-major
+            const uint32_t sQ[2] = {smem_u32(sm + L::kQ0), smem_u32(sm + L::kQ1)};
+            const uint32_t sK = smem_u32(sm + L::kK), sV = smem_u32(sm + L::kV);
+            bool ok = mbar_wait(&bars[L::bQFull], 0, abort_flag, kWaitLimitNs);
+            auto issue_s = [&](int t, int st) {
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t off = (k / 4) * (kTileM * 128) + (k % 4) * 32;
+                    const uint64_t ad = sdesc_sw128(sQ[t] + off, 0, 1024);
+                    const uint64_t bd = sdesc_sw128(sK + st * L::kTileBytes + off, 0, 1024);
+                    mma_ss(tbase + t * 128, ad, bd, idS, k > 0);
+                }
+                mma_commit(&bars[L::bSFull + t]);
+            };
+            auto issue_pv = [&](int t, int st, bool acc) {
+#pragma unroll
+                for (int k = 0; k < kBlockN / 16; ++k) {
+                    const uint64_t bd = sdesc_sw128(sV + st * L::kTileBytes + k * 2048, kTileM * 128, 1024);
+                    mma_ts(tbase + 256 + t * 128, tbase + t * 128 + k * 8, bd, idO, (acc || k > 0) ? 1u : 0u);
+                }
+            };
+            if (ok && nmax > 0) {
+                ok = mbar_wait(&bars[L::bKFull], 0, abort_flag, kWaitLimitNs);
+                if (ok) {
+                    tc_fence_after();
+                    if (nb0 > 0) issue_s(0, 0);
+                    if (nb1 > 0) issue_s(1, 0);
+                }
+            }
+            for (int n = 0; ok && n < nmax; ++n) {
+                const int st = n & 1;
+                if (!mbar_wait(&bars[L::bVFull + st], (n >> 1) & 1, abort_flag, kWaitLimitNs)) break;
+                bool next_k_ready = false;
+                for (int t = 0; t < 2 && ok; ++t) {
+                    const int nbt = t ? nb1 : nb0;
+                    if (n >= nbt) continue;
+                    if (!mbar_wait(&bars[L::bPFull + t], n & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
+                    tc_fence_after();
+                    issue_pv(t, st, n > 0);
+                    if (n == nbt - 1) {
+                        mma_commit(&bars[L::bODone + t]);
+                    } else {
+                        const int st1 = (n + 1) & 1;
+                        if (!next_k_ready) {
+                            if (!mbar_wait(&bars[L::bKFull + st1], ((n + 1) >> 1) & 1, abort_flag, kWaitLimitNs)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            next_k_ready = true;
+                        }
+                        issue_s(t, st1);
+                    }
+                }
+                mma_commit(&bars[L::bKvEmpty + st]);
+            }
+            // Drain: the tensor pipe must be idle before TMEM is released.
+            mma_commit(&bars[L::bDrain]);
+            mbar_wait_drain(&bars[L::bDrain], 0, kDrainLimitNs);
+        }
+    } else {
+        // ------------------------------------------------------------------ softmax groups
+        const int t = warp >> 2;
+        const int q0 = t ? q01 : q00;
+        const int nbt = t ? nb1 : nb0;
+        const int rq = (warp & 3) * 32 + lane;
+        const int i = q0 + rq;  // this thread's query row
+        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t tS = tbase + lane_off + t * 128;
+        const uint32_t tO = tbase + lane_off + 256 + t * 128;
+        const float sl2 = a.scale_log2;
+        float m = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int n = 0; n < nbt; ++n) {
+            if (!mbar_wait(&bars[L::bSFull + t], n & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
+            tc_fence_after();
+            uint32_t r0[32], r1[32], r2[32], r3[32];
+            tmem_ld32(tS + 0, r0);
+            tmem_ld32(tS + 32, r1);
+            tmem_ld32(tS + 64, r2);
+            tmem_ld32(tS + 96, r3);
+            tmem_ld_wait();
+            reg_fence(r0);
+            reg_fence(r1);
+            reg_fence(r2);
+            reg_fence(r3);
+            float sv[128];
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                sv[c] = __uint_as_float(r0[c]);
+                sv[32 + c] = __uint_as_float(r1[c]);
+                sv[64 + c] = __uint_as_float(r2[c]);
+                sv[96 + c] = __uint_as_float(r3[c]);
+            }
+            const int kv0 = s + n * kBlockN;
+            const bool need_mask = (a.causal && kv0 + kBlockN - 1 > q0) || (kv0 + kBlockN > e);
+            if (need_mask) {
+                int lim = e - 1 - kv0;  // last visible column of this block
+                if (a.causal && i - kv0 < lim) lim = i - kv0;
+#pragma unroll
+                for (int c = 0; c < 128; ++c)
+                    if (c > lim) sv[c] = -INFINITY;
+            }
+            float mx = sv[0];
+#pragma unroll
+            for (int c = 1; c < 128; ++c) mx = fmaxf(mx, sv[c]);
+            const float m_blk = mx * sl2;
+            if (n == 0) {
+                m = m_blk;
+            } else if (m_blk > m + kRescaleThreshold) {
+                const float f = ex2_approx(m - m_blk);
+                l *= f;
+#pragma unroll 1
+                for (int c = 0; c < D; c += 32) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + c, o);
+                    tmem_ld_wait(o);
+                    uint32_t lo[16], hi[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        lo[j] = __float_as_uint(__uint_as_float(o[j]) * f);
+                        hi[j] = __float_as_uint(__uint_as_float(o[16 + j]) * f);
+                    }
+                    tmem_st16(tO + c, lo);
+                    tmem_st16(tO + c + 16, hi);
+                }
+                m = m_blk;
+            }
+            const float mu = (m == -INFINITY) ? 0.f : m;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const float p0 = ex2_approx(fmaf(sv[32 * c + 2 * j], sl2, -mu));
+                    const float p1 = ex2_approx(fmaf(sv[32 * c + 2 * j + 1], sl2, -mu));
+                    l += p0 + p1;
+                    pk[j] = pack_bf16x2(p0, p1);
+                }
+                tmem_st16(tS + 16 * c, pk);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[L::bPFull + t]);
+        }
+        if (ok && nbt > 0 && mbar_wait(&bars[L::bODone + t], 0, abort_flag, kWaitLimitNs)) {
+            tc_fence_after();
+            const bool valid = i < e;
+            const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+            __nv_bfloat16* orow = a.o + ((int64_t)h * a.T + i) * D;
+#pragma unroll 1
+            for (int c = 0; c < D; c += 32) {
+                uint32_t o[32];
+                tmem_ld32(tO + c, o);
+                tmem_ld_wait(o);
+                uint32_t pk[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    pk[j] = pack_bf16x2(__uint_as_float(o[2 * j]) * inv_l, __uint_as_float(o[2 * j + 1]) * inv_l);
+                if (valid) {
+                    uint4* dst = (uint4*)(orow + c);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                }
+            }
+            if (valid) a.lse[(int64_t)h * a.T + i] = (m + __log2f(l)) * 0.69314718055994530942f;
+        }
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 9) tmem_dealloc(tbase, 512);
+    if (threadIdx.x == 0 && *abort_flag) atomicCAS(&a.hdr->status, (int)USP_OK, (int)USP_ERR_TIMEOUT);
+}
+
+template <int D>
+cudaError_t launch_fwd_impl(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const FwdArgs& a,
+                            int grid, cudaStream_t s) {
+    using L = FwdSmem<D>;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    attn_fwd_kernel<D><<<grid, kFwdThreads, L::kAlloc, s>>>(q, k, v, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_fwd(int head_dim, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                            const FwdArgs& a, int grid, cudaStream_t s) {
+    if (head_dim == 128) return launch_fwd_impl<128>(q, k, v, a, grid, s);
+    return launch_fwd_impl<64>(q, k, v, a, grid, s);
+}
+
+}  // namespace usp

@@ -1,0 +1,80 @@
+// Shared definitions of the library: workspace layout, work items, limits.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include "usp.h"
+
+namespace usp {
+
+// Rows of one attention tile (tensor-core M) and of one key/value block (N).
+constexpr int kTileM = 128;
+constexpr int kBlockN = 128;
+// The forward gives each CTA two query tiles (256 rows); the backward one key/value tile.
+constexpr int kFwdRowsPerItem = 2 * kTileM;
+constexpr int kBwdRowsPerItem = kTileM;
+
+// Wall-clock limit of every bounded wait inside the attention kernels, and of the
+// teardown waits for copies and MMAs already in flight.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr uint64_t kDrainLimitNs = 200000000ull;
+
+// A unit of work: (head, sample, tile index within the sample). `head` is a query
+// head for the forward and a key/value head for the backward.
+struct WorkItem {
+    int head;
+    int seq;
+    int tile;
+    int cost;
+};
+
+// Workspace layout (all offsets 256-byte aligned):
+//   [0, 256)         header: status word, forward item count, backward item count
+//   hist             int32[hist_len]   scheduler cost histogram / bucket cursors
+//   tiles_prefix     int32[num_seqs+1] tiles per sample, prefix-summed
+//   items            WorkItem[max_items]
+//   delta            fp32[hq][T]       backward only: Delta_i = dO_i . O_i
+//   dq_acc           fp32[hq][T][D]    backward only: dQ accumulator
+struct WsHeader {
+    int status;
+    int fwd_count;
+    int bwd_count;
+    int max_cost;
+};
+
+struct WsLayout {
+    size_t hist, prefix, items, delta, dq_acc, total;
+    int hist_len;
+    int max_items;
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+inline int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+inline WsLayout ws_layout(int64_t T, int num_seqs, int hq, int hkv, int D, int bwd) {
+    WsLayout w{};
+    const int64_t rows_per_item = bwd ? kBwdRowsPerItem : kFwdRowsPerItem;
+    const int64_t heads = bwd ? hkv : hq;
+    const int64_t tiles = ceil_div64(T, rows_per_item) + num_seqs;
+    // costs are counted in key/value blocks (x query heads per kv head for the backward)
+    const int64_t max_cost = 2 * (ceil_div64(T, kBlockN) + 2) * (bwd ? (hq / (hkv > 0 ? hkv : 1)) : 1) + 8;
+    w.hist_len = (int)max_cost;
+    w.max_items = (int)(tiles * heads);
+    size_t off = 256;
+    w.hist = off;
+    off = align256(off + sizeof(int) * (size_t)w.hist_len);
+    w.prefix = off;
+    off = align256(off + sizeof(int) * (size_t)(num_seqs + 1));
+    w.items = off;
+    off = align256(off + sizeof(WorkItem) * (size_t)w.max_items);
+    w.delta = off;
+    if (bwd) off = align256(off + sizeof(float) * (size_t)hq * (size_t)T);
+    w.dq_acc = off;
+    if (bwd) off = align256(off + sizeof(float) * (size_t)hq * (size_t)T * (size_t)D);
+    w.total = off;
+    return w;
+}
+
+}  // namespace usp

@@ -1,0 +1,240 @@
+// C ABI of the attention calls: argument validation, workspace carving, TMA tensor
+// maps and the launch sequence (scheduler -> attention kernels).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "attn.cuh"
+#include "common.cuh"
+#include "sched.cuh"
+
+namespace usp {
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (EncodeTiledFn)p;
+    });
+    return fn;
+}
+
+// Tensor map over a head-major bf16 activation [heads][T][D]: boxes of 64 columns x 128
+// rows of one head, 128-byte swizzled (the layout the tensor-core descriptors expect).
+bool make_head_major_map(CUtensorMap* map, const void* base, int64_t T, int heads, int D) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)T, (cuuint64_t)heads};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)T * D * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)kTileM, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }
+
+usp_status check_common(int64_t T, int num_seqs, int hq, int hkv, int D, const int32_t* cu) {
+    if (T < 0 || hq < 1 || hkv < 1 || hq % hkv != 0) return USP_ERR_INVALID_ARG;
+    if (T > 0 && (num_seqs < 1 || !cu)) return USP_ERR_INVALID_ARG;
+    if (T > (int64_t)INT_MAX - 2 * kFwdRowsPerItem || num_seqs > (1 << 24)) return USP_ERR_UNSUPPORTED;
+    if (D != 64 && D != 128) return USP_ERR_UNSUPPORTED;
+    if ((int64_t)hq * (T / kTileM + num_seqs + 1) > (int64_t)INT_MAX / 2) return USP_ERR_UNSUPPORTED;
+    return USP_OK;
+}
+
+// T == 0: nothing to compute and the data pointers may be NULL (empty tensors); the
+// status word of a workspace, if one is given, is reset to USP_OK.
+usp_status reset_status_if_any(void* workspace, size_t ws_bytes, cudaStream_t s) {
+    if (!workspace || ws_bytes < sizeof(WsHeader)) return USP_OK;
+    if (!aligned16(workspace)) return USP_ERR_INVALID_ARG;
+    return cudaMemsetAsync(workspace, 0, sizeof(WsHeader), s) == cudaSuccess ? USP_OK : USP_ERR_CUDA;
+}
+
+float resolve_scale(float softmax_scale, int D) {
+    return softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt((float)D);
+}
+
+}  // namespace
+}  // namespace usp
+
+using namespace usp;
+
+extern "C" size_t usp_attn_workspace_size(int64_t total_tokens, int num_seqs, int hq, int hkv, int head_dim,
+                                          int bwd) {
+    if (total_tokens < 0 || num_seqs < 0 || hq < 1 || hkv < 1 || head_dim < 1) return 0;
+    return ws_layout(total_tokens, num_seqs, hq, hkv, head_dim, bwd ? 1 : 0).total;
+}
+
+extern "C" usp_status usp_attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                                          const int32_t* cu_seqlens, int num_seqs, int64_t total_tokens, int hq,
+                                          int hkv, int head_dim, float softmax_scale, int causal, void* workspace,
+                                          size_t ws_bytes, void* stream) {
+    usp_status st = check_common(total_tokens, num_seqs, hq, hkv, head_dim, cu_seqlens);
+    if (st != USP_OK) return st;
+    if (total_tokens == 0) return reset_status_if_any(workspace, ws_bytes, (cudaStream_t)stream);
+    if (!q || !k || !v || !o || !lse || !workspace) return USP_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(workspace))
+        return USP_ERR_INVALID_ARG;
+    const WsLayout w = ws_layout(total_tokens, num_seqs, hq, hkv, head_dim, 0);
+    if (ws_bytes < w.total) return USP_ERR_WORKSPACE;
+    cudaStream_t s = (cudaStream_t)stream;
+    uint8_t* ws = (uint8_t*)workspace;
+    WsHeader* hdr = (WsHeader*)ws;
+    if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return USP_ERR_CUDA;
+
+    SchedArgs sa{};
+    sa.cu = cu_seqlens;
+    sa.num_seqs = num_seqs;
+    sa.T = total_tokens;
+    sa.heads = hq;
+    sa.bwd = 0;
+    sa.causal = causal ? 1 : 0;
+    sa.group = hq / hkv;
+    sa.hist_len = w.hist_len;
+    sa.max_items = w.max_items;
+    sa.hdr = hdr;
+    sa.hist = (int*)(ws + w.hist);
+    sa.prefix = (int*)(ws + w.prefix);
+    sa.items = (WorkItem*)(ws + w.items);
+    if (launch_schedule(sa, s) != cudaSuccess) return USP_ERR_CUDA;
+
+    CUtensorMap mq, mk, mv;
+    if (!make_head_major_map(&mq, q, total_tokens, hq, head_dim) ||
+        !make_head_major_map(&mk, k, total_tokens, hkv, head_dim) ||
+        !make_head_major_map(&mv, v, total_tokens, hkv, head_dim))
+        return USP_ERR_CUDA;
+    FwdArgs fa{};
+    fa.cu = cu_seqlens;
+    fa.items = sa.items;
+    fa.hdr = hdr;
+    fa.o = (__nv_bfloat16*)o;
+    fa.lse = lse;
+    fa.T = total_tokens;
+    fa.group = hq / hkv;
+    fa.causal = sa.causal;
+    fa.scale_log2 = resolve_scale(softmax_scale, head_dim) * 1.4426950408889634f;
+    if (launch_attn_fwd(head_dim, mq, mk, mv, fa, w.max_items, s) != cudaSuccess) return USP_ERR_CUDA;
+    return USP_OK;
+}
+
+extern "C" usp_status usp_attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
+                                          const float* lse, const void* d_o, void* dq, void* dk, void* dv,
+                                          usp_dtype grad_dt, const int32_t* cu_seqlens, int num_seqs,
+                                          int64_t total_tokens, int hq, int hkv, int head_dim, float softmax_scale,
+                                          int causal, void* workspace, size_t ws_bytes, void* stream) {
+    usp_status st = check_common(total_tokens, num_seqs, hq, hkv, head_dim, cu_seqlens);
+    if (st != USP_OK) return st;
+    if (grad_dt == USP_FP16) return USP_ERR_UNSUPPORTED;
+    if (grad_dt != USP_BF16 && grad_dt != USP_FP32) return USP_ERR_INVALID_ARG;
+    if (total_tokens == 0) return reset_status_if_any(workspace, ws_bytes, (cudaStream_t)stream);
+    if (!q || !k || !v || !o || !lse || !d_o || !dq || !dk || !dv || !workspace) return USP_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(d_o) ||
+        !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace))
+        return USP_ERR_INVALID_ARG;
+    const WsLayout w = ws_layout(total_tokens, num_seqs, hq, hkv, head_dim, 1);
+    if (ws_bytes < w.total) return USP_ERR_WORKSPACE;
+    cudaStream_t s = (cudaStream_t)stream;
+    uint8_t* ws = (uint8_t*)workspace;
+    WsHeader* hdr = (WsHeader*)ws;
+    if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return USP_ERR_CUDA;
+    const bool fp32_grads = grad_dt == USP_FP32;
+    float* delta = (float*)(ws + w.delta);
+    // fp32 gradients accumulate straight into the caller's dq; bf16 ones go through the workspace.
+    float* dq_acc = fp32_grads ? (float*)dq : (float*)(ws + w.dq_acc);
+
+    if (launch_bwd_prep((const __nv_bfloat16*)o, (const __nv_bfloat16*)d_o, delta, dq_acc, (int64_t)hq * total_tokens,
+                        head_dim, s) != cudaSuccess)
+        return USP_ERR_CUDA;
+
+    SchedArgs sa{};
+    sa.cu = cu_seqlens;
+    sa.num_seqs = num_seqs;
+    sa.T = total_tokens;
+    sa.heads = hkv;
+    sa.bwd = 1;
+    sa.causal = causal ? 1 : 0;
+    sa.group = hq / hkv;
+    sa.hist_len = w.hist_len;
+    sa.max_items = w.max_items;
+    sa.hdr = hdr;
+    sa.hist = (int*)(ws + w.hist);
+    sa.prefix = (int*)(ws + w.prefix);
+    sa.items = (WorkItem*)(ws + w.items);
+    if (launch_schedule(sa, s) != cudaSuccess) return USP_ERR_CUDA;
+
+    CUtensorMap mq, mk, mv, mdo;
+    if (!make_head_major_map(&mq, q, total_tokens, hq, head_dim) ||
+        !make_head_major_map(&mk, k, total_tokens, hkv, head_dim) ||
+        !make_head_major_map(&mv, v, total_tokens, hkv, head_dim) ||
+        !make_head_major_map(&mdo, d_o, total_tokens, hq, head_dim))
+        return USP_ERR_CUDA;
+    BwdArgs ba{};
+    ba.cu = cu_seqlens;
+    ba.items = sa.items;
+    ba.hdr = hdr;
+    ba.lse = lse;
+    ba.delta = delta;
+    ba.dq_acc = dq_acc;
+    ba.dk = dk;
+    ba.dv = dv;
+    ba.grad_fp32 = fp32_grads ? 1 : 0;
+    ba.T = total_tokens;
+    ba.group = hq / hkv;
+    ba.causal = sa.causal;
+    ba.scale = resolve_scale(softmax_scale, head_dim);
+    ba.scale_log2 = ba.scale * 1.4426950408889634f;
+    if (launch_attn_bwd(head_dim, mq, mk, mv, mdo, ba, w.max_items, s) != cudaSuccess) return USP_ERR_CUDA;
+    if (!fp32_grads &&
+        launch_dq_convert(dq_acc, (__nv_bfloat16*)dq, (int64_t)hq * total_tokens * head_dim, s) != cudaSuccess)
+        return USP_ERR_CUDA;
+    return USP_OK;
+}
+
+extern "C" usp_status usp_get_device_status(const void* workspace, void* stream) {
+    if (!workspace) return USP_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return USP_ERR_CUDA;
+    int status = 0;
+    if (cudaMemcpy(&status, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return USP_ERR_CUDA;
+    return (usp_status)status;
+}
+
+extern "C" const char* usp_status_string(usp_status status) {
+    switch (status) {
+        case USP_OK: return "USP_OK";
+        case USP_ERR_INVALID_ARG: return "USP_ERR_INVALID_ARG";
+        case USP_ERR_UNSUPPORTED: return "USP_ERR_UNSUPPORTED";
+        case USP_ERR_CUDA: return "USP_ERR_CUDA";
+        case USP_ERR_WORKSPACE: return "USP_ERR_WORKSPACE";
+        case USP_ERR_TIMEOUT: return "USP_ERR_TIMEOUT";
+        case USP_ERR_DEVICE_CHECK: return "USP_ERR_DEVICE_CHECK";
+    }
+    return "USP_ERR_UNKNOWN";
+}
+
+extern "C" usp_status usp_debug_wait_timeout(void* workspace, size_t ws_bytes, uint64_t limit_ns, void* stream) {
+    if (!workspace || ws_bytes < sizeof(WsHeader) || !aligned16(workspace)) return USP_ERR_INVALID_ARG;
+    if (limit_ns < 1000) limit_ns = 1000;
+    if (limit_ns > 5000000000ull) limit_ns = 5000000000ull;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (cudaMemsetAsync(workspace, 0, sizeof(WsHeader), s) != cudaSuccess) return USP_ERR_CUDA;
+    if (launch_debug_timeout((WsHeader*)workspace, limit_ns, s) != cudaSuccess) return USP_ERR_CUDA;
+    return USP_OK;
+}
