@@ -152,6 +152,41 @@ usp_status usp_attn_bwd_varlen(const void* q, const void* k, const void* v, cons
  */
 usp_status usp_get_device_status(const void* workspace, void* stream);
 
+/*
+ * usp_attn_fwd_varlen_noalloc -- usp_attn_fwd_varlen for callers that cannot
+ * allocate device memory. This entry point is an addition of this library; the
+ * pages have no counterpart to it.
+ *   Who needs it: code inside a framework whose caching allocator owns all
+ *   device memory and does not tolerate raw cudaMalloc/cudaFree next to it,
+ *   real-time or embedded hosts that reserve a fixed memory budget up front and
+ *   must not allocate per call, and plug-in code called through a hook that has
+ *   no allocator handle and nowhere to keep a workspace between calls. None of
+ *   them can provide the workspace the other attention calls take. Here the
+ *   scratch data (status word, scheduler histogram, varlen work list) lives in
+ *   a static 1 MiB array in the library's own device memory, which every GPU
+ *   that loads the library holds until the process exits. The call allocates
+ *   and frees nothing.
+ *   Arguments, layouts and results are those of usp_attn_fwd_varlen, without
+ *   the workspace. `status` (device int32, may be NULL) receives the
+ *   device-side outcome once the call's kernels finish: USP_OK,
+ *   USP_ERR_DEVICE_CHECK (malformed cu_seqlens; no output written) or
+ *   USP_ERR_TIMEOUT.
+ *   Set-up: the first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current), which may load the
+ *   library's device code; make that first call before any stream capture.
+ *   Sharing: every call uses the same array, which keeps the previous call's
+ *   contents (each call clears the parts that must start at zero). Calls whose
+ *   kernels could overlap on the GPU (two streams, or two host threads without
+ *   ordering) race on it; the caller must serialise them.
+ * Errors: as usp_attn_fwd_varlen, and USP_ERR_WORKSPACE when the work list for
+ *   these sizes does not fit the 1 MiB array (roughly hq * (T/256 + num_seqs)
+ *   above 60000 items), or total_tokens > 2^30; no kernel is launched then.
+ */
+usp_status usp_attn_fwd_varlen_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
+                                       const int32_t* cu_seqlens, int num_seqs, int64_t total_tokens, int hq,
+                                       int hkv, int head_dim, float softmax_scale, int causal, int32_t* status,
+                                       void* stream);
+
 /* Human-readable name of a status code (static string). */
 const char* usp_status_string(usp_status status);
 

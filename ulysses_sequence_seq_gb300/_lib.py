@@ -34,6 +34,7 @@ EXPORTED = (
     "usp_get_device_status",
     "usp_status_string",
     "usp_debug_wait_timeout",
+    "usp_attn_fwd_varlen_noalloc",
 )
 
 
@@ -72,8 +73,9 @@ def load(build_if_missing: bool = True):
     L.usp_status_string.argtypes = [I]
     L.usp_status_string.restype = ctypes.c_char_p
     L.usp_debug_wait_timeout.argtypes = [P, Z, ctypes.c_uint64, P]
+    L.usp_attn_fwd_varlen_noalloc.argtypes = [P, P, P, P, P, P, I, I64, I, I, I, F, I, P, P]
     for name in ("usp_seq_to_head", "usp_head_to_seq", "usp_attn_fwd_varlen", "usp_attn_bwd_varlen",
-                 "usp_get_device_status", "usp_debug_wait_timeout"):
+                 "usp_get_device_status", "usp_debug_wait_timeout", "usp_attn_fwd_varlen_noalloc"):
         getattr(L, name).restype = I
     _lib = L
     return _lib
@@ -154,6 +156,16 @@ def attn_bwd_varlen(q, k, v, o, lse, d_o, dq, dk, dv, grad_dt: int, cu_seqlens, 
         _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(d_o), _ptr(dq), _ptr(dk), _ptr(dv), int(grad_dt),
         _ptr(cu_seqlens), int(num_seqs), int(total_tokens), int(hq), int(hkv), int(head_dim),
         float(softmax_scale), int(bool(causal)), _ptr(workspace), int(ws_bytes), _stream(stream)))
+
+
+def attn_fwd_varlen_noalloc(q, k, v, o, lse, cu_seqlens, num_seqs: int, total_tokens: int, hq: int, hkv: int,
+                            head_dim: int, softmax_scale: float, causal: bool, status=None, stream=None):
+    """The forward without a workspace: scratch lives in the library's static device
+    array (for callers that cannot allocate; calls must not overlap on the GPU)."""
+    _check("usp_attn_fwd_varlen_noalloc", load().usp_attn_fwd_varlen_noalloc(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(cu_seqlens), int(num_seqs), int(total_tokens),
+        int(hq), int(hkv), int(head_dim), float(softmax_scale), int(bool(causal)), _ptr(status),
+        _stream(stream)))
 
 
 def get_device_status(workspace, stream=None) -> int:

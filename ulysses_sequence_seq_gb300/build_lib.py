@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libusp.so")
-SOURCES = ["relayout.cu", "sched.cu", "attn_fwd.cu", "attn_bwd.cu", "usp_api.cu"]
+SOURCES = ["relayout.cu", "sched.cu", "attn_fwd.cu", "attn_bwd.cu", "usp_api.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -65,8 +65,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
             if err:
                 print(err)
     tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [cc, "-shared", "-o", tmp] + [o for o, _ in results] + ARCH + ["-cudart=static", "-lcuda"] \
-        if False else [cc, "-shared", "-o", tmp] + [o for o, _ in results] + ARCH + ["-cudart=static"]
+    cmd = [cc, "-shared", "-o", tmp] + [o for o, _ in results] + ARCH + ["-cudart=static"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")

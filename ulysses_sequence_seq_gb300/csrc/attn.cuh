@@ -51,6 +51,9 @@ cudaError_t launch_bwd_prep(const __nv_bfloat16* o, const __nv_bfloat16* dout, f
 // dq = dq_acc converted to bf16.
 cudaError_t launch_dq_convert(const float* dq_acc, __nv_bfloat16* dq, int64_t n, cudaStream_t s);
 
+// TMA tensor map over a head-major bf16 activation [heads][T][D] (64 x 128 boxes, 128-byte swizzle).
+bool make_head_major_map(CUtensorMap* map, const void* base, int64_t T, int heads, int D);
+
 // Records `code` in the status word after a kernel that waits on an mbarrier nothing arrives on.
 cudaError_t launch_debug_timeout(WsHeader* hdr, uint64_t limit_ns, cudaStream_t s);
 

@@ -34,20 +34,6 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// Tensor map over a head-major bf16 activation [heads][T][D]: boxes of 64 columns x 128
-// rows of one head, 128-byte swizzled (the layout the tensor-core descriptors expect).
-bool make_head_major_map(CUtensorMap* map, const void* base, int64_t T, int heads, int D) {
-    EncodeTiledFn enc = encode_fn();
-    if (!enc) return false;
-    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)T, (cuuint64_t)heads};
-    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)T * D * 2};
-    cuuint32_t box[3] = {64, (cuuint32_t)kTileM, 1};
-    cuuint32_t es[3] = {1, 1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }
 
 usp_status check_common(int64_t T, int num_seqs, int hq, int hkv, int D, const int32_t* cu) {
@@ -72,6 +58,21 @@ float resolve_scale(float softmax_scale, int D) {
 }
 
 }  // namespace
+
+// Tensor map over a head-major bf16 activation [heads][T][D]: boxes of 64 columns x 128
+// rows of one head, 128-byte swizzled (the layout the tensor-core descriptors expect).
+bool make_head_major_map(CUtensorMap* map, const void* base, int64_t T, int heads, int D) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)T, (cuuint64_t)heads};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)T * D * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)kTileM, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace usp
 
 using namespace usp;
