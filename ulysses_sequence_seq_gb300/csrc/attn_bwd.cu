@@ -12,13 +12,17 @@
 // atomics. Everything is computed transposed (key rows on TMEM lanes) so that P^T
 // and dS^T feed the dV and dK MMAs straight from TMEM.
 //
-// Warp roles (320 threads):
-//   warps 0-3  compute group: thread = key row; P^T, dS^T; writes dK, dV at the end
-//   warps 4-7  dQ group: thread = query row; drains the dQ tile with atomics
-//   warp  8    TMA producer: K, V once, then Q / dO blocks into a 2-stage ring
-//   warp  9    MMA issuer and TMEM owner
+// Warp roles (448 threads):
+//   warps 0-3  compute group A: thread = key row, query columns 0-63 of the block
+//   warps 4-7  compute group B: thread = key row, query columns 64-127
+//              (P^T, dS^T; at the end group A writes dV and group B writes dK)
+//   warps 8-11 dQ group: thread = query row; drains the dQ tile, transposed through
+//              shared memory so that each vector atomic covers whole 128-byte lines
+//   warp  12   TMA producer: K, V once, then Q / dO blocks into a 2-stage ring
+//   warp  13   MMA issuer and TMEM owner
 // Tensor memory: S^T/P^T [0,128), dP^T/dS^T then dQ [128,256), dV [256,256+D),
-// dK [384,384+D).
+// dK [384,384+D). Group A keeps its bf16 P^T / dS^T in columns [0,32) of its
+// region and group B in [64,96), so neither overwrites scores the other still reads.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -33,7 +37,9 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kBwdThreads = 320;
+constexpr int kBwdThreads = 448;
+constexpr int kProducerWarp = 12;
+constexpr int kMmaWarp = 13;
 
 template <int D>
 struct BwdSmem {
@@ -44,8 +50,8 @@ struct BwdSmem {
     static constexpr int kQ = 2 * kTileBytes;        // + stage * kTileBytes
     static constexpr int kDO = 4 * kTileBytes;       // + stage * kTileBytes
     static constexpr int kDS = 6 * kTileBytes;       // [128 key rows][128 query cols] bf16, two 64-col panels
-    static constexpr int kLse = kDS + kTileM * kBlockN * 2;  // fp32[128] (log2 units)
-    static constexpr int kDelta = kLse + 512;                // fp32[128]
+    static constexpr int kLse = kDS + kTileM * kBlockN * 2;  // fp32[2][64]: -lse (log2 units), one half per group
+    static constexpr int kDelta = kLse + 512;                // fp32[2][64]: -Delta
     static constexpr int kBars = kDelta + 512;
     static constexpr int bKvFull = 0, bQFull = 1, bDoFull = 3, bQEmpty = 5, bSFull = 7, bDpFull = 8, bPFull = 9,
                          bDsFull = 10, bDqFull = 11, bDqEmpty = 12, bAccFull = 13, bDrain = 14, kNumBars = 15;
@@ -86,7 +92,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
 
-    if (warp == 9) {
+    if (warp == kMmaWarp) {
         tmem_alloc(tmem_slot, 512);
         tmem_relinquish();
     }
@@ -99,8 +105,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         mbar_init(&bars[L::bSFull], 1);
         mbar_init(&bars[L::bDpFull], 1);
-        mbar_init(&bars[L::bPFull], 4);
-        mbar_init(&bars[L::bDsFull], 4);
+        mbar_init(&bars[L::bPFull], 8);
+        mbar_init(&bars[L::bDsFull], 8);
         mbar_init(&bars[L::bDqFull], 1);
         mbar_init(&bars[L::bDqEmpty], 4);
         mbar_init(&bars[L::bAccFull], 1);
@@ -113,7 +119,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tc_fence_after();
     const uint32_t tbase = *tmem_slot;
 
-    if (warp == 8) {
+    if (warp == kProducerWarp) {
         // ------------------------------------------------------------------ TMA producer
         if (lane == 0) {
             prefetch_tmap(&tmQ);
@@ -148,7 +154,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 mbar_wait_drain(&bars[L::bDoFull + (k & 1)], (k >> 1) & 1, kDrainLimitNs);
             }
         }
-    } else if (warp == 9) {
+    } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idT = idesc_bf16_f32(kBlockN, kTileM, false, false);  // S^T, dP^T
@@ -182,16 +188,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 const uint32_t q_s = sQ + st * L::kTileBytes, do_s = sDO + st * L::kTileBytes;
                 if (!mbar_wait(&bars[L::bPFull], k & 1, abort_flag, kWaitLimitNs)) break;
                 tc_fence_after();
+                // bf16 P^T / dS^T of query columns 0-63 sit at column offset 0, of 64-127 at 64
 #pragma unroll
                 for (int kk = 0; kk < kTileM / 16; ++kk)  // dV += P^T . dO
-                    mma_ts(tDV, tS + kk * 8, sdesc_sw128(do_s + kk * 2048, kTileM * 128, 1024), idAcc,
-                           (k > 0 || kk > 0) ? 1u : 0u);
+                    mma_ts(tDV, tS + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_sw128(do_s + kk * 2048, kTileM * 128, 1024),
+                           idAcc, (k > 0 || kk > 0) ? 1u : 0u);
                 if (!mbar_wait(&bars[L::bDsFull], k & 1, abort_flag, kWaitLimitNs)) break;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < kTileM / 16; ++kk)  // dK += dS^T . Q
-                    mma_ts(tDK, tDP + kk * 8, sdesc_sw128(q_s + kk * 2048, kTileM * 128, 1024), idAcc,
-                           (k > 0 || kk > 0) ? 1u : 0u);
+                    mma_ts(tDK, tDP + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_sw128(q_s + kk * 2048, kTileM * 128, 1024),
+                           idAcc, (k > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
                 for (int kk = 0; kk < kBlockN / 16; ++kk)  // dQ = dS . K  (into the dP^T columns)
                     mma_ss(tDP, sdesc_sw128(sDS + kk * 2048, kBlockN * 128, 1024),
@@ -216,50 +223,66 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mma_commit(&bars[L::bDrain]);
             mbar_wait_drain(&bars[L::bDrain], 0, kDrainLimitNs);
         }
-    } else if (warp < 4) {
-        // ------------------------------------------------------------------ compute group (key rows)
-        const int r = warp * 32 + lane;
+    } else if (warp < 8) {
+        // ------------------------------------------------------------------ compute groups (key rows)
+        const int grp = warp >> 2;          // 0: query columns 0-63, 1: 64-127
+        const int r = (warp & 3) * 32 + lane;
         const int kv = kv0 + r;
         const bool kv_ok = kv < e;
-        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-        const uint32_t tS = tbase + lane_off, tDP = tbase + lane_off + 128;
+        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t tS = tbase + lane_off + grp * 64, tDP = tbase + lane_off + 128 + grp * 64;
+        float* lse_g = lse_s + grp * 64;
+        float* delta_g = delta_s + grp * 64;
         const float sl2 = a.scale_log2;
+        const float sc = a.scale;
         bool ok = true;
-        for (int k = 0; k < nsteps; ++k) {
+        // This group's 64 query rows of a step, negated: -lse (log2 units) and -Delta; rows
+        // outside the sample get -lse = -inf, which makes their P exactly zero. Loaded one
+        // step ahead so that their global-memory latency stays off the critical path.
+        float nl_next = -INFINITY, nd_next = 0.f;
+        auto fetch_row_stats = [&](int k) {
             const int h = g * G + k / nq;
+            const int q = s + (i0 + k % nq) * kTileM + grp * 64 + r;
+            const bool q_ok = r < 64 && q < e;
+            nl_next = q_ok ? -__ldg(a.lse + (int64_t)h * a.T + q) * 1.4426950408889634f : -INFINITY;
+            nd_next = q_ok ? -__ldg(a.delta + (int64_t)h * a.T + q) : 0.f;
+        };
+        if (nsteps > 0) fetch_row_stats(0);
+        for (int k = 0; k < nsteps; ++k) {
             const int q0 = s + (i0 + k % nq) * kTileM;
-            // this query block's logsumexp (log2 units) and Delta; rows outside the sample get
-            // lse = +inf, which makes their P exactly zero
-            named_bar_sync(1, 128);
-            {
-                const int q = q0 + r;
-                const bool q_ok = q < e;
-                lse_s[r] = q_ok ? __ldg(a.lse + (int64_t)h * a.T + q) * 1.4426950408889634f : INFINITY;
-                delta_s[r] = q_ok ? __ldg(a.delta + (int64_t)h * a.T + q) : 0.f;
+            named_bar_sync(1 + grp, 128);
+            if (r < 64) {
+                lse_g[r] = nl_next;
+                delta_g[r] = nd_next;
             }
-            named_bar_sync(1, 128);
-            const bool diag = a.causal && (q0 == kv0);
+            named_bar_sync(1 + grp, 128);
+            if (k + 1 < nsteps) fetch_row_stats(k + 1);
+            // element masks are only needed on the diagonal block and on the sample's ragged
+            // last key tile; there query column c (of 128) is visible to key row r iff c >= r
+            const bool mask_blk = (a.causal && q0 == kv0) || (kv0 + kBlockN > e);
+            const int vis_from = (a.causal && q0 == kv0) ? r - grp * 64 : -1;
             if (!mbar_wait(&bars[L::bSFull], k & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
             tc_fence_after();
-            float p[128];
+            float2 psc[32];   // scale * P for this row's 64 query columns, kept for dS
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < 2; ++c) {
                 uint32_t sr[32];
                 tmem_ld32(tS + 32 * c, sr);
                 tmem_ld_wait(sr);
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int col = 32 * c + j;
-                    float x = ex2_approx(fmaf(__uint_as_float(sr[j]), sl2, -lse_s[col]));
-                    if (!kv_ok || (diag && col < r)) x = 0.f;
-                    p[col] = x;
-                }
-            }
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
                 uint32_t pk[16];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(p[32 * c + 2 * j], p[32 * c + 2 * j + 1]);
+                for (int j = 0; j < 16; ++j) {
+                    const int c0 = 32 * c + 2 * j;
+                    const float2 x = fma2(make_float2(__uint_as_float(sr[2 * j]), __uint_as_float(sr[2 * j + 1])),
+                                          make_float2(sl2, sl2), *(const float2*)(lse_g + c0));
+                    float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                    if (mask_blk) {
+                        if (!kv_ok || c0 < vis_from) pp.x = 0.f;
+                        if (!kv_ok || c0 + 1 < vis_from) pp.y = 0.f;
+                    }
+                    pk[j] = pack_bf16x2(pp.x, pp.y);
+                    psc[16 * c + j] = mul2(pp, make_float2(sc, sc));
+                }
                 tmem_st16(tS + 16 * c, pk);
             }
             tmem_st_wait();
@@ -269,9 +292,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
             if (!mbar_wait(&bars[L::bDpFull], k & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
             tc_fence_after();
-            const float sc = a.scale;
+            uint8_t* panel = sm + L::kDS + grp * (kBlockN * 128);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < 2; ++c) {
                 uint32_t dr[32];
                 tmem_ld32(tDP + 32 * c, dr);
                 tmem_ld_wait(dr);
@@ -279,16 +302,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const int c0 = 32 * c + 2 * j;
-                    const float d0 = sc * p[c0] * (__uint_as_float(dr[2 * j]) - delta_s[c0]);
-                    const float d1 = sc * p[c0 + 1] * (__uint_as_float(dr[2 * j + 1]) - delta_s[c0 + 1]);
-                    pk[j] = pack_bf16x2(d0, d1);
+                    const float2 d = add2(make_float2(__uint_as_float(dr[2 * j]), __uint_as_float(dr[2 * j + 1])),
+                                          *(const float2*)(delta_g + c0));
+                    const float2 ds = mul2(psc[16 * c + j], d);
+                    pk[j] = pack_bf16x2(ds.x, ds.y);
                 }
                 tmem_st16(tDP + 16 * c, pk);
                 // the same values, as row r of the [key][query] operand of the dQ MMA
-                uint8_t* panel = sm + L::kDS + (c >> 1) * (kBlockN * 128);
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const uint32_t bytecol = (uint32_t)((c & 1) * 64 + j * 16);
+                    const uint32_t bytecol = (uint32_t)(c * 64 + j * 16);
                     *(uint4*)(panel + sw128_offset(r, bytecol)) =
                         make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
                 }
@@ -301,87 +324,82 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         if (ok && mbar_wait(&bars[L::bAccFull], 0, abort_flag, kWaitLimitNs)) {
             tc_fence_after();
+            // group A writes dV, group B writes dK
             const int64_t row = (int64_t)g * a.T + kv;
+            const uint32_t src = tbase + lane_off + (grp ? 384 : 256);
+            void* dst_base = grp ? a.dk : a.dv;
 #pragma unroll 1
-            for (int which = 0; which < 2; ++which) {
-                const uint32_t src = tbase + lane_off + (which ? 384 : 256);
-                void* dst_base = which ? a.dk : a.dv;
-#pragma unroll 1
-                for (int c = 0; c < D; c += 32) {
-                    uint32_t o[32];
-                    tmem_ld32(src + c, o);
-                    tmem_ld_wait(o);
-                    if (!kv_ok) continue;
-                    if (a.grad_fp32) {
-                        float4* dst = (float4*)((float*)dst_base + row * D + c);
+            for (int c = 0; c < D; c += 32) {
+                uint32_t o[32];
+                tmem_ld32(src + c, o);
+                tmem_ld_wait(o);
+                if (!kv_ok) continue;
+                if (a.grad_fp32) {
+                    float4* dst = (float4*)((float*)dst_base + row * D + c);
 #pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            dst[j] = make_float4(__uint_as_float(o[4 * j]), __uint_as_float(o[4 * j + 1]),
-                                                 __uint_as_float(o[4 * j + 2]), __uint_as_float(o[4 * j + 3]));
-                    } else {
-                        uint4* dst = (uint4*)((__nv_bfloat16*)dst_base + row * D + c);
+                    for (int j = 0; j < 8; ++j)
+                        dst[j] = make_float4(__uint_as_float(o[4 * j]), __uint_as_float(o[4 * j + 1]),
+                                             __uint_as_float(o[4 * j + 2]), __uint_as_float(o[4 * j + 3]));
+                } else {
+                    uint4* dst = (uint4*)((__nv_bfloat16*)dst_base + row * D + c);
 #pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            dst[j] = make_uint4(pack_bf16x2(__uint_as_float(o[8 * j]), __uint_as_float(o[8 * j + 1])),
-                                                pack_bf16x2(__uint_as_float(o[8 * j + 2]), __uint_as_float(o[8 * j + 3])),
-                                                pack_bf16x2(__uint_as_float(o[8 * j + 4]), __uint_as_float(o[8 * j + 5])),
-                                                pack_bf16x2(__uint_as_float(o[8 * j + 6]), __uint_as_float(o[8 * j + 7])));
-                    }
+                    for (int j = 0; j < 4; ++j)
+                        dst[j] = make_uint4(pack_bf16x2(__uint_as_float(o[8 * j]), __uint_as_float(o[8 * j + 1])),
+                                            pack_bf16x2(__uint_as_float(o[8 * j + 2]), __uint_as_float(o[8 * j + 3])),
+                                            pack_bf16x2(__uint_as_float(o[8 * j + 4]), __uint_as_float(o[8 * j + 5])),
+                                            pack_bf16x2(__uint_as_float(o[8 * j + 6]), __uint_as_float(o[8 * j + 7])));
                 }
             }
         }
-    } else {
+    } else if (warp < 12) {
         // ------------------------------------------------------------------ dQ group (query rows)
-        const int w4 = warp - 4;
-        const int r = w4 * 32 + lane;
+        // After the dQ MMA of a step has completed, the dS operand buffer is idle until the
+        // next dP^T MMA (which waits for this group), so each warp borrows 8 KB of it to
+        // transpose its 32 rows x 32 columns chunks: a warp-wide vector atomic then covers
+        // 4 rows x 128 contiguous bytes instead of 32 rows x 16 bytes.
+        const int w4 = warp - 8;
         const uint32_t tDQ = tbase + ((uint32_t)(w4 * 32) << 16) + 128;
+        uint8_t* stage = sm + L::kDS + w4 * 8192;
+        const int sub_row = lane >> 3;   // 0..3: row within a group of four
+        const int chunk = lane & 7;      // 16-byte chunk within a 128-byte row segment
         for (int k = 0; k < nsteps; ++k) {
             const int h = g * G + k / nq;
-            const int q = s + (i0 + k % nq) * kTileM + r;
+            const int qrow0 = s + (i0 + k % nq) * kTileM + w4 * 32;   // first query row of this warp
             if (!mbar_wait(&bars[L::bDqFull], k & 1, abort_flag, kWaitLimitNs)) break;
             tc_fence_after();
-            uint32_t d0[32], d1[32], d2[32], d3[32];
-            tmem_ld32(tDQ + 0, d0);
-            if (D > 32) tmem_ld32(tDQ + 32, d1);
-            if (D > 64) {
-                tmem_ld32(tDQ + 64, d2);
-                tmem_ld32(tDQ + 96, d3);
+            float* dst_base = a.dq_acc + ((int64_t)h * a.T + qrow0) * D;
+#pragma unroll 1
+            for (int c = 0; c < D; c += 32) {
+                uint32_t v[32];
+                tmem_ld32(tDQ + c, v);
+                tmem_ld_wait(v);
+                uint8_t* buf = stage + ((c >> 5) & 1) * 4096;   // alternate 4 KB halves
+#pragma unroll
+                for (int j = 0; j < 8; ++j)   // row `lane`, 16-byte chunk j, XOR-swizzled by row
+                    *(uint4*)(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+                        make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int row = 4 * i + sub_row;
+                    const uint4 x = *(const uint4*)(buf + row * 128 + ((chunk ^ (row & 7)) << 4));
+                    if (qrow0 + row < e)
+                        atomicAdd((float4*)(dst_base + (int64_t)row * D + c) + chunk,
+                                  make_float4(__uint_as_float(x.x), __uint_as_float(x.y), __uint_as_float(x.z),
+                                              __uint_as_float(x.w)));
+                }
+                __syncwarp();
             }
-            tmem_ld_wait();
-            reg_fence(d0);
-            reg_fence(d1);
-            reg_fence(d2);
-            reg_fence(d3);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[L::bDqEmpty]);
-            if (q < e) {
-                float4* dst = (float4*)(a.dq_acc + ((int64_t)h * a.T + q) * D);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    atomicAdd(dst + j, make_float4(__uint_as_float(d0[4 * j]), __uint_as_float(d0[4 * j + 1]),
-                                                   __uint_as_float(d0[4 * j + 2]), __uint_as_float(d0[4 * j + 3])));
-                    if (D > 32)
-                        atomicAdd(dst + 8 + j,
-                                  make_float4(__uint_as_float(d1[4 * j]), __uint_as_float(d1[4 * j + 1]),
-                                              __uint_as_float(d1[4 * j + 2]), __uint_as_float(d1[4 * j + 3])));
-                    if (D > 64) {
-                        atomicAdd(dst + 16 + j,
-                                  make_float4(__uint_as_float(d2[4 * j]), __uint_as_float(d2[4 * j + 1]),
-                                              __uint_as_float(d2[4 * j + 2]), __uint_as_float(d2[4 * j + 3])));
-                        atomicAdd(dst + 24 + j,
-                                  make_float4(__uint_as_float(d3[4 * j]), __uint_as_float(d3[4 * j + 1]),
-                                              __uint_as_float(d3[4 * j + 2]), __uint_as_float(d3[4 * j + 3])));
-                    }
-                }
-            }
         }
     }
 
     __syncwarp();
     tc_fence_before();
     __syncthreads();
-    if (warp == 9) tmem_dealloc(tbase, 512);
+    if (warp == kMmaWarp) tmem_dealloc(tbase, 512);
     if (threadIdx.x == 0 && *abort_flag) atomicCAS(&a.hdr->status, (int)USP_OK, (int)USP_ERR_TIMEOUT);
 }
 

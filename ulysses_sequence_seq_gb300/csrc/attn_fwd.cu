@@ -244,9 +244,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 for (int c = 0; c < 128; ++c)
                     if (c > lim) sv[c] = -INFINITY;
             }
-            float mx = sv[0];
+            // row max over 8 independent chains of three-input max (a single two-input chain
+            // would serialise 127 dependent ops)
+            float mx8[8];
 #pragma unroll
-            for (int c = 1; c < 128; ++c) mx = fmaxf(mx, sv[c]);
+            for (int j = 0; j < 8; ++j) mx8[j] = sv[j];
+#pragma unroll
+            for (int c = 8; c < 120; c += 16)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) mx8[j] = fmax3(mx8[j], sv[c + j], sv[c + 8 + j]);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) mx8[j] = fmaxf(mx8[j], sv[120 + j]);
+            const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
             const float m_blk = mx * sl2;
             if (n == 0) {
                 m = m_blk;
@@ -270,18 +279,22 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 m = m_blk;
             }
             const float mu = (m == -INFINITY) ? 0.f : m;
+            const float2 sl2x2 = make_float2(sl2, sl2), nmu2 = make_float2(-mu, -mu);
+            float2 l4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
-                    const float p0 = ex2_approx(fmaf(sv[32 * c + 2 * j], sl2, -mu));
-                    const float p1 = ex2_approx(fmaf(sv[32 * c + 2 * j + 1], sl2, -mu));
-                    l += p0 + p1;
-                    pk[j] = pack_bf16x2(p0, p1);
+                    const float2 x = fma2(make_float2(sv[32 * c + 2 * j], sv[32 * c + 2 * j + 1]), sl2x2, nmu2);
+                    const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                    l4[j & 3] = add2(l4[j & 3], pp);   // independent partial row sums
+                    pk[j] = pack_bf16x2(pp.x, pp.y);
                 }
                 tmem_st16(tS + 16 * c, pk);
             }
+            const float2 lsum = add2(add2(l4[0], l4[1]), add2(l4[2], l4[3]));
+            l += lsum.x + lsum.y;
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();

@@ -4,8 +4,8 @@
 // made of short items.
 //
 // One CTA: sample tiles are counted and prefix-summed, every (sample, tile) gets a
-// cost in key/value blocks, a counting sort over the cost puts the items in
-// descending cost order, and each (sample, tile) is expanded to all heads, kept
+// cost in key/value blocks, a counting sort over the cost (histogram in shared
+// memory, block-wide scans) puts the items in descending cost order, and each (sample, tile) is expanded to all heads, kept
 // adjacent so that query heads sharing a key/value head run close together.
 #include <cuda_runtime.h>
 
@@ -14,6 +14,9 @@
 #include "tiles.cuh"
 
 namespace usp {
+
+// Cost histograms up to this many buckets (48 KB) live in shared memory.
+constexpr int kSchedSmemHist = 12288;
 
 __device__ __forceinline__ int find_sample(const int* prefix, int nseq, int p) {
     // largest b with prefix[b] <= p (prefix is non-decreasing, prefix[0] = 0)
@@ -26,44 +29,78 @@ __device__ __forceinline__ int find_sample(const int* prefix, int nseq, int p) {
     return lo;
 }
 
+// In-place exclusive prefix sum of data[0..n) by the whole CTA (data in shared or global
+// memory); with `rev` the sum runs from the last element down. Returns the total.
+__device__ int block_exclusive_scan(int* data, int n, bool rev, int* warp_sums) {
+    const int tid = threadIdx.x, nthr = blockDim.x;
+    const int per = (n + nthr - 1) / nthr;
+    const int b0 = tid * per;
+    const int b1 = (b0 + per < n) ? b0 + per : n;
+    int local = 0;
+    for (int i = b0; i < b1; ++i) local += data[rev ? n - 1 - i : i];
+    const int lane = tid & 31, wid = tid >> 5, nwarps = nthr >> 5;
+    int x = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, off);
+        if (lane >= off) x += y;
+    }
+    if (lane == 31) warp_sums[wid] = x;
+    __syncthreads();
+    if (wid == 0) {
+        int w = lane < nwarps ? warp_sums[lane] : 0;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, w, off);
+            if (lane >= off) w += y;
+        }
+        warp_sums[lane] = w;
+    }
+    __syncthreads();
+    int acc = x - local + (wid > 0 ? warp_sums[wid - 1] : 0);
+    const int total = warp_sums[nwarps - 1];
+    for (int i = b0; i < b1; ++i) {
+        const int idx = rev ? n - 1 - i : i;
+        const int v = data[idx];
+        data[idx] = acc;
+        acc += v;
+    }
+    __syncthreads();
+    return total;
+}
+
+__device__ __forceinline__ void fail_schedule(const SchedArgs& a) {
+    a.hdr->status = USP_ERR_DEVICE_CHECK;
+    if (a.bwd) a.hdr->bwd_count = 0;
+    else a.hdr->fwd_count = 0;
+}
+
 __global__ void __launch_bounds__(1024) schedule_kernel(SchedArgs a) {
+    extern __shared__ int hist_smem[];
     __shared__ int bad;
-    __shared__ int total_tiles;
+    __shared__ int warp_sums[32];
     const int tid = threadIdx.x;
     const int nthr = blockDim.x;
+    int* hist = a.hist_len <= kSchedSmemHist ? hist_smem : a.hist;
     if (tid == 0) bad = 0;
-    for (int c = tid; c < a.hist_len; c += nthr) a.hist[c] = 0;
+    for (int c = tid; c < a.hist_len; c += nthr) hist[c] = 0;
     __syncthreads();
     if (tid == 0 && (a.cu[0] != 0 || (int64_t)a.cu[a.num_seqs] != a.T)) bad = 1;
     for (int b = tid; b < a.num_seqs; b += nthr)
         if (a.cu[b + 1] < a.cu[b]) bad = 1;
     __syncthreads();
     if (bad) {
-        if (tid == 0) {
-            a.hdr->status = USP_ERR_DEVICE_CHECK;
-            if (a.bwd) a.hdr->bwd_count = 0;
-            else a.hdr->fwd_count = 0;
-        }
+        if (tid == 0) fail_schedule(a);
         return;
     }
     const int rows = a.bwd ? kBwdRowsPerItem : kFwdRowsPerItem;
-    if (tid == 0) {
-        int acc = 0;
-        for (int b = 0; b < a.num_seqs; ++b) {
-            a.prefix[b] = acc;
-            acc += (a.cu[b + 1] - a.cu[b] + rows - 1) / rows;
-        }
-        a.prefix[a.num_seqs] = acc;
-        total_tiles = acc;
-    }
+    // tiles per sample, then their exclusive prefix sum (prefix[num_seqs] = total)
+    for (int b = tid; b <= a.num_seqs; b += nthr)
+        a.prefix[b] = b < a.num_seqs ? (a.cu[b + 1] - a.cu[b] + rows - 1) / rows : 0;
     __syncthreads();
-    const int ntiles = total_tiles;
+    const int ntiles = block_exclusive_scan(a.prefix, a.num_seqs + 1, false, warp_sums);
     if ((int64_t)ntiles * a.heads > a.max_items) {  // cannot happen for valid cu_seqlens
-        if (tid == 0) {
-            a.hdr->status = USP_ERR_DEVICE_CHECK;
-            if (a.bwd) a.hdr->bwd_count = 0;
-            else a.hdr->fwd_count = 0;
-        }
+        if (tid == 0) fail_schedule(a);
         return;
     }
     for (int p = tid; p < ntiles; p += nthr) {
@@ -72,25 +109,18 @@ __global__ void __launch_bounds__(1024) schedule_kernel(SchedArgs a) {
         const int s = a.cu[b], e = a.cu[b + 1];
         int cost = a.bwd ? bwd_item_cost(tile, s, e, a.causal, a.group) : fwd_item_cost(tile, s, e, a.causal);
         cost = cost < 0 ? 0 : (cost >= a.hist_len ? a.hist_len - 1 : cost);
-        atomicAdd(&a.hist[cost], 1);
+        atomicAdd(&hist[cost], 1);
     }
     __syncthreads();
-    if (tid == 0) {  // exclusive scan from the highest cost down: bucket start offsets
-        int acc = 0;
-        for (int c = a.hist_len - 1; c >= 0; --c) {
-            const int n = a.hist[c];
-            a.hist[c] = acc;
-            acc += n;
-        }
-    }
-    __syncthreads();
+    // bucket start offsets, highest cost first
+    block_exclusive_scan(hist, a.hist_len, true, warp_sums);
     for (int p = tid; p < ntiles; p += nthr) {
         const int b = find_sample(a.prefix, a.num_seqs, p);
         const int tile = p - a.prefix[b];
         const int s = a.cu[b], e = a.cu[b + 1];
         int cost = a.bwd ? bwd_item_cost(tile, s, e, a.causal, a.group) : fwd_item_cost(tile, s, e, a.causal);
         cost = cost < 0 ? 0 : (cost >= a.hist_len ? a.hist_len - 1 : cost);
-        const int pos = atomicAdd(&a.hist[cost], 1);
+        const int pos = atomicAdd(&hist[cost], 1);
         for (int h = 0; h < a.heads; ++h) {
             WorkItem w;
             w.head = h;
@@ -108,7 +138,8 @@ __global__ void __launch_bounds__(1024) schedule_kernel(SchedArgs a) {
 }
 
 cudaError_t launch_schedule(const SchedArgs& a, cudaStream_t s) {
-    schedule_kernel<<<1, 1024, 0, s>>>(a);
+    const size_t smem = a.hist_len <= kSchedSmemHist ? sizeof(int) * (size_t)a.hist_len : 0;
+    schedule_kernel<<<1, 1024, smem, s>>>(a);
     return cudaGetLastError();
 }
 
