@@ -160,49 +160,58 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             constexpr uint32_t idT = idesc_bf16_f32(kBlockN, kTileM, false, false);  // S^T, dP^T
             constexpr uint32_t idAcc = idesc_bf16_f32(kBlockN, D, false, true);     // dV, dK (B MN-major)
             constexpr uint32_t idDq = idesc_bf16_f32(kTileM, D, true, true);        // dQ (A, B MN-major)
+            // 64-bit shared-memory descriptors are built once; a K step only adds a constant to
+            // the start-address field (addresses stay below 2^18, so the field never carries).
+            constexpr uint32_t kPanel = kTileM * 128;  // bytes of one 64-column panel of a tile
             const uint32_t sK = smem_u32(sm + L::kK), sV = smem_u32(sm + L::kV);
             const uint32_t sQ = smem_u32(sm + L::kQ), sDO = smem_u32(sm + L::kDO), sDS = smem_u32(sm + L::kDS);
+            const uint64_t dK_kmaj = sdesc_sw128(sK, 0, 1024), dK_mn = sdesc_sw128(sK, kPanel, 1024);
+            const uint64_t dV_kmaj = sdesc_sw128(sV, 0, 1024);
+            const uint64_t dQ_kmaj = sdesc_sw128(sQ, 0, 1024), dQ_mn = sdesc_sw128(sQ, kPanel, 1024);
+            const uint64_t dDO_kmaj = sdesc_sw128(sDO, 0, 1024), dDO_mn = sdesc_sw128(sDO, kPanel, 1024);
+            const uint64_t dDS_mn = sdesc_sw128(sDS, kBlockN * 128, 1024);
+            constexpr uint64_t kStage = (uint64_t)(L::kTileBytes >> 4);
             const uint32_t tS = tbase, tDP = tbase + 128, tDV = tbase + 256, tDK = tbase + 384;
-            auto issue_t = [&](uint32_t d, uint32_t a_s, uint32_t b_s) {  // d = A . B^T, both K-major
+            auto issue_t = [&](uint32_t d, uint64_t a_desc, uint64_t b_desc) {  // d = A . B^T, both K-major
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk / 4) * (kTileM * 128) + (kk % 4) * 32;
-                    mma_ss(d, sdesc_sw128(a_s + off, 0, 1024), sdesc_sw128(b_s + off, 0, 1024), idT, kk > 0);
+                    const uint64_t off = (uint64_t)((((kk / 4) * kPanel) + (kk % 4) * 32) >> 4);
+                    mma_ss(d, a_desc + off, b_desc + off, idT, kk > 0);
                 }
             };
             bool ok = mbar_wait(&bars[L::bKvFull], 0, abort_flag, kWaitLimitNs);
             if (ok) ok = mbar_wait(&bars[L::bQFull], 0, abort_flag, kWaitLimitNs);
             if (ok) {
                 tc_fence_after();
-                issue_t(tS, sK, sQ);
+                issue_t(tS, dK_kmaj, dQ_kmaj);
                 mma_commit(&bars[L::bSFull]);
                 ok = mbar_wait(&bars[L::bDoFull], 0, abort_flag, kWaitLimitNs);
                 if (ok) {
                     tc_fence_after();
-                    issue_t(tDP, sV, sDO);
+                    issue_t(tDP, dV_kmaj, dDO_kmaj);
                     mma_commit(&bars[L::bDpFull]);
                 }
             }
             for (int k = 0; ok && k < nsteps; ++k) {
                 const int st = k & 1;
-                const uint32_t q_s = sQ + st * L::kTileBytes, do_s = sDO + st * L::kTileBytes;
+                const uint64_t q_mn = dQ_mn + st * kStage, do_mn = dDO_mn + st * kStage;
                 if (!mbar_wait(&bars[L::bPFull], k & 1, abort_flag, kWaitLimitNs)) break;
                 tc_fence_after();
                 // bf16 P^T / dS^T of query columns 0-63 sit at column offset 0, of 64-127 at 64
 #pragma unroll
                 for (int kk = 0; kk < kTileM / 16; ++kk)  // dV += P^T . dO
-                    mma_ts(tDV, tS + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_sw128(do_s + kk * 2048, kTileM * 128, 1024),
-                           idAcc, (k > 0 || kk > 0) ? 1u : 0u);
+                    mma_ts(tDV, tS + (kk >> 2) * 64 + (kk & 3) * 8, do_mn + (uint64_t)((kk * 2048) >> 4), idAcc,
+                           (k > 0 || kk > 0) ? 1u : 0u);
                 if (!mbar_wait(&bars[L::bDsFull], k & 1, abort_flag, kWaitLimitNs)) break;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < kTileM / 16; ++kk)  // dK += dS^T . Q
-                    mma_ts(tDK, tDP + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_sw128(q_s + kk * 2048, kTileM * 128, 1024),
-                           idAcc, (k > 0 || kk > 0) ? 1u : 0u);
+                    mma_ts(tDK, tDP + (kk >> 2) * 64 + (kk & 3) * 8, q_mn + (uint64_t)((kk * 2048) >> 4), idAcc,
+                           (k > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
                 for (int kk = 0; kk < kBlockN / 16; ++kk)  // dQ = dS . K  (into the dP^T columns)
-                    mma_ss(tDP, sdesc_sw128(sDS + kk * 2048, kBlockN * 128, 1024),
-                           sdesc_sw128(sK + kk * 2048, kTileM * 128, 1024), idDq, kk > 0 ? 1u : 0u);
+                    mma_ss(tDP, dDS_mn + (uint64_t)((kk * 2048) >> 4), dK_mn + (uint64_t)((kk * 2048) >> 4), idDq,
+                           kk > 0 ? 1u : 0u);
                 mma_commit(&bars[L::bDqFull]);
                 mma_commit(&bars[L::bQEmpty + st]);
                 if (k + 1 < nsteps) {
@@ -210,12 +219,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     const int ph1 = ((k + 1) >> 1) & 1;
                     if (!mbar_wait(&bars[L::bQFull + st1], ph1, abort_flag, kWaitLimitNs)) break;
                     tc_fence_after();
-                    issue_t(tS, sK, sQ + st1 * L::kTileBytes);
+                    issue_t(tS, dK_kmaj, dQ_kmaj + st1 * kStage);
                     mma_commit(&bars[L::bSFull]);
                     if (!mbar_wait(&bars[L::bDqEmpty], k & 1, abort_flag, kWaitLimitNs)) break;
                     if (!mbar_wait(&bars[L::bDoFull + st1], ph1, abort_flag, kWaitLimitNs)) break;
                     tc_fence_after();
-                    issue_t(tDP, sV, sDO + st1 * L::kTileBytes);
+                    issue_t(tDP, dV_kmaj, dDO_kmaj + st1 * kStage);
                     mma_commit(&bars[L::bDpFull]);
                 }
             }
@@ -263,26 +272,34 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const int vis_from = (a.causal && q0 == kv0) ? r - grp * 64 : -1;
             if (!mbar_wait(&bars[L::bSFull], k & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
             tc_fence_after();
-            float2 psc[32];   // scale * P for this row's 64 query columns, kept for dS
+            // P for this row's 64 query columns as packed bf16 pairs: the values the dV MMA
+            // consumes, kept (32 registers instead of 64) for dS
+            uint32_t pkall[32];
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 uint32_t sr[32];
                 tmem_ld32(tS + 32 * c, sr);
+                float4 nl4[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) nl4[j] = *(const float4*)(lse_g + 32 * c + 4 * j);
                 tmem_ld_wait(sr);
-                uint32_t pk[16];
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const int c0 = 32 * c + 2 * j;
+                    const float4 q4 = nl4[j >> 1];
+                    const float2 nl = (j & 1) ? make_float2(q4.z, q4.w) : make_float2(q4.x, q4.y);
                     const float2 x = fma2(make_float2(__uint_as_float(sr[2 * j]), __uint_as_float(sr[2 * j + 1])),
-                                          make_float2(sl2, sl2), *(const float2*)(lse_g + c0));
+                                          make_float2(sl2, sl2), nl);
                     float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
                     if (mask_blk) {
                         if (!kv_ok || c0 < vis_from) pp.x = 0.f;
                         if (!kv_ok || c0 + 1 < vis_from) pp.y = 0.f;
                     }
-                    pk[j] = pack_bf16x2(pp.x, pp.y);
-                    psc[16 * c + j] = mul2(pp, make_float2(sc, sc));
+                    pkall[16 * c + j] = pack_bf16x2(pp.x, pp.y);
                 }
+                uint32_t pk[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) pk[j] = pkall[16 * c + j];
                 tmem_st16(tS + 16 * c, pk);
             }
             tmem_st_wait();
@@ -297,14 +314,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             for (int c = 0; c < 2; ++c) {
                 uint32_t dr[32];
                 tmem_ld32(tDP + 32 * c, dr);
+                float4 nd4[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) nd4[j] = *(const float4*)(delta_g + 32 * c + 4 * j);
                 tmem_ld_wait(dr);
                 uint32_t pk[16];
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
-                    const int c0 = 32 * c + 2 * j;
-                    const float2 d = add2(make_float2(__uint_as_float(dr[2 * j]), __uint_as_float(dr[2 * j + 1])),
-                                          *(const float2*)(delta_g + c0));
-                    const float2 ds = mul2(psc[16 * c + j], d);
+                    const float4 d4 = nd4[j >> 1];
+                    const float2 nd = (j & 1) ? make_float2(d4.z, d4.w) : make_float2(d4.x, d4.y);
+                    const float2 d = add2(make_float2(__uint_as_float(dr[2 * j]), __uint_as_float(dr[2 * j + 1])), nd);
+                    const uint32_t pb = pkall[16 * c + j];
+                    const float2 psc = mul2(make_float2(__uint_as_float(pb << 16), __uint_as_float(pb & 0xffff0000u)),
+                                            make_float2(sc, sc));
+                    const float2 ds = mul2(psc, d);
                     pk[j] = pack_bf16x2(ds.x, ds.y);
                 }
                 tmem_st16(tDP + 16 * c, pk);
@@ -379,14 +402,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     *(uint4*)(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) =
                         make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
                 __syncwarp();
+                // all eight shared-memory reads first: the compiler may not move a read past an
+                // atomic, so interleaving them would serialise eight load latencies
+                uint4 x[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const int row = 4 * i + sub_row;
-                    const uint4 x = *(const uint4*)(buf + row * 128 + ((chunk ^ (row & 7)) << 4));
+                    x[i] = *(const uint4*)(buf + row * 128 + ((chunk ^ (row & 7)) << 4));
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int row = 4 * i + sub_row;
                     if (qrow0 + row < e)
                         atomicAdd((float4*)(dst_base + (int64_t)row * D + c) + chunk,
-                                  make_float4(__uint_as_float(x.x), __uint_as_float(x.y), __uint_as_float(x.z),
-                                              __uint_as_float(x.w)));
+                                  make_float4(__uint_as_float(x[i].x), __uint_as_float(x[i].y),
+                                              __uint_as_float(x[i].z), __uint_as_float(x[i].w)));
                 }
                 __syncwarp();
             }

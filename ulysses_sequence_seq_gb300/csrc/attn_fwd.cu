@@ -142,25 +142,33 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (lane == 0) {
             constexpr uint32_t idS = idesc_bf16_f32(kTileM, kBlockN, false, false);  // Q.K^T: both K-major
             constexpr uint32_t idO = idesc_bf16_f32(kTileM, D, false, true);         // P.V: V is MN-major
-            const uint32_t sQ[2] = {smem_u32(sm + L::kQ0), smem_u32(sm + L::kQ1)};
-            const uint32_t sK = smem_u32(sm + L::kK), sV = smem_u32(sm + L::kV);
+            // The 64-bit shared-memory descriptors are built once; a K step only adds a constant
+            // to the start-address field (addresses stay below 2^18, so the field never carries).
+            // Rebuilding them per MMA made the issuing thread, not the tensor core, the limit.
+            const uint64_t dQ0 = sdesc_sw128(smem_u32(sm + L::kQ0), 0, 1024);
+            const uint64_t dQ1 = sdesc_sw128(smem_u32(sm + L::kQ1), 0, 1024);
+            const uint64_t dK0 = sdesc_sw128(smem_u32(sm + L::kK), 0, 1024);
+            const uint64_t dK1 = dK0 + (uint64_t)(L::kTileBytes >> 4);
+            const uint64_t dV0 = sdesc_sw128(smem_u32(sm + L::kV), kTileM * 128, 1024);
+            const uint64_t dV1 = dV0 + (uint64_t)(L::kTileBytes >> 4);
             bool ok = mbar_wait(&bars[L::bQFull], 0, abort_flag, kWaitLimitNs);
             auto issue_s = [&](int t, int st) {
+                const uint64_t ad = t ? dQ1 : dQ0, bd = st ? dK1 : dK0;
+                const uint32_t d = tbase + t * 128;
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t off = (k / 4) * (kTileM * 128) + (k % 4) * 32;
-                    const uint64_t ad = sdesc_sw128(sQ[t] + off, 0, 1024);
-                    const uint64_t bd = sdesc_sw128(sK + st * L::kTileBytes + off, 0, 1024);
-                    mma_ss(tbase + t * 128, ad, bd, idS, k > 0);
+                    constexpr uint32_t kPanel = kTileM * 128;
+                    const uint64_t off = (uint64_t)((((k / 4) * kPanel) + (k % 4) * 32) >> 4);
+                    mma_ss(d, ad + off, bd + off, idS, k > 0);
                 }
                 mma_commit(&bars[L::bSFull + t]);
             };
             auto issue_pv = [&](int t, int st, bool acc) {
+                const uint64_t bd = st ? dV1 : dV0;
+                const uint32_t d = tbase + 256 + t * 128, a_t = tbase + t * 128;
 #pragma unroll
-                for (int k = 0; k < kBlockN / 16; ++k) {
-                    const uint64_t bd = sdesc_sw128(sV + st * L::kTileBytes + k * 2048, kTileM * 128, 1024);
-                    mma_ts(tbase + 256 + t * 128, tbase + t * 128 + k * 8, bd, idO, (acc || k > 0) ? 1u : 0u);
-                }
+                for (int k = 0; k < kBlockN / 16; ++k)
+                    mma_ts(d, a_t + k * 8, bd + (uint64_t)((k * 2048) >> 4), idO, (acc || k > 0) ? 1u : 0u);
             };
             if (ok && nmax > 0) {
                 ok = mbar_wait(&bars[L::bKFull], 0, abort_flag, kWaitLimitNs);
