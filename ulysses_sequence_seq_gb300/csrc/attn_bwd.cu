@@ -17,12 +17,14 @@
 //   warps 4-7  compute group B: thread = key row, query columns 64-127
 //              (P^T, dS^T; at the end group A writes dV and group B writes dK)
 //   warps 8-11 dQ group: thread = query row; drains the dQ tile, transposed through
-//              shared memory so that each vector atomic covers whole 128-byte lines
+//              the idle dS buffer so that each vector atomic covers whole 128-byte lines
 //   warp  12   TMA producer: K, V once, then Q / dO blocks into a 2-stage ring
 //   warp  13   MMA issuer and TMEM owner
-// Tensor memory: S^T/P^T [0,128), dP^T/dS^T then dQ [128,256), dV [256,256+D),
-// dK [384,384+D). Group A keeps its bf16 P^T / dS^T in columns [0,32) of its
-// region and group B in [64,96), so neither overwrites scores the other still reads.
+// Tensor memory: [0,128) holds S^T, then bf16 P^T, then dP^T of one step; the dQ
+// tile has its own columns [128,256), so draining it overlaps the next step; dV
+// [256,256+D), dK [384,384+D). Group A keeps its bf16 P^T in columns [0,32) and
+// group B in [64,96), so neither overwrites scores the other still reads. dS lives
+// only in shared memory, where dK reads it K-major and dQ MN-major.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -54,7 +56,8 @@ struct BwdSmem {
     static constexpr int kDelta = kLse + 512;                // fp32[2][64]: -Delta
     static constexpr int kBars = kDelta + 512;
     static constexpr int bKvFull = 0, bQFull = 1, bDoFull = 3, bQEmpty = 5, bSFull = 7, bDpFull = 8, bPFull = 9,
-                         bDsFull = 10, bDqFull = 11, bDqEmpty = 12, bAccFull = 13, bDrain = 14, kNumBars = 15;
+                         bDsFull = 10, bDqFull = 11, bDqEmpty = 12, bAccFull = 13, bDrain = 14, bStageFree = 15,
+                         bDsFree = 16, kNumBars = 17;
     static constexpr int kTmemSlot = kBars + 8 * kNumBars;
     static constexpr int kAbort = kTmemSlot + 8;
     static constexpr int kBytes = kAbort + 8;
@@ -109,6 +112,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(&bars[L::bDsFull], 8);
         mbar_init(&bars[L::bDqFull], 1);
         mbar_init(&bars[L::bDqEmpty], 4);
+        mbar_init(&bars[L::bStageFree], 4);
+        mbar_init(&bars[L::bDsFree], 1);
         mbar_init(&bars[L::bAccFull], 1);
         mbar_init(&bars[L::bDrain], 1);
         *abort_flag = 0;
@@ -158,7 +163,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // ------------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idT = idesc_bf16_f32(kBlockN, kTileM, false, false);  // S^T, dP^T
-            constexpr uint32_t idAcc = idesc_bf16_f32(kBlockN, D, false, true);     // dV, dK (B MN-major)
+            constexpr uint32_t idDv = idesc_bf16_f32(kBlockN, D, false, true);      // dV (A in TMEM)
+            constexpr uint32_t idDk = idesc_bf16_f32(kBlockN, D, false, true);      // dK (A = dS, K-major)
             constexpr uint32_t idDq = idesc_bf16_f32(kTileM, D, true, true);        // dQ (A, B MN-major)
             // 64-bit shared-memory descriptors are built once; a K step only adds a constant to
             // the start-address field (addresses stay below 2^18, so the field never carries).
@@ -169,9 +175,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const uint64_t dV_kmaj = sdesc_sw128(sV, 0, 1024);
             const uint64_t dQ_kmaj = sdesc_sw128(sQ, 0, 1024), dQ_mn = sdesc_sw128(sQ, kPanel, 1024);
             const uint64_t dDO_kmaj = sdesc_sw128(sDO, 0, 1024), dDO_mn = sdesc_sw128(sDO, kPanel, 1024);
-            const uint64_t dDS_mn = sdesc_sw128(sDS, kBlockN * 128, 1024);
+            const uint64_t dDS_kmaj = sdesc_sw128(sDS, 0, 1024), dDS_mn = sdesc_sw128(sDS, kBlockN * 128, 1024);
             constexpr uint64_t kStage = (uint64_t)(L::kTileBytes >> 4);
-            const uint32_t tS = tbase, tDP = tbase + 128, tDV = tbase + 256, tDK = tbase + 384;
+            const uint32_t tS = tbase, tDQ = tbase + 128, tDV = tbase + 256, tDK = tbase + 384;
             auto issue_t = [&](uint32_t d, uint64_t a_desc, uint64_t b_desc) {  // d = A . B^T, both K-major
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
@@ -185,48 +191,47 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 tc_fence_after();
                 issue_t(tS, dK_kmaj, dQ_kmaj);
                 mma_commit(&bars[L::bSFull]);
-                ok = mbar_wait(&bars[L::bDoFull], 0, abort_flag, kWaitLimitNs);
-                if (ok) {
-                    tc_fence_after();
-                    issue_t(tDP, dV_kmaj, dDO_kmaj);
-                    mma_commit(&bars[L::bDpFull]);
-                }
             }
+            // Per step k, with columns [0,128) holding S^T, then P^T, then dP^T:
+            //   dV += P^T.dO, dP^T = V.dO^T, dQ = dS.K -> [128,256), S^T(k+1) = K.Q(k+1)^T, dK += dS^T.Q
+            // dQ goes first so its drain (the longest tail) starts early; S^T of the next block
+            // goes before dK so the compute groups' exponentials overlap dK; the dQ tile has
+            // its own columns, so draining it overlaps the next step.
             for (int k = 0; ok && k < nsteps; ++k) {
                 const int st = k & 1;
-                const uint64_t q_mn = dQ_mn + st * kStage, do_mn = dDO_mn + st * kStage;
+                const uint64_t q_mn = dQ_mn + st * kStage;
                 if (!mbar_wait(&bars[L::bPFull], k & 1, abort_flag, kWaitLimitNs)) break;
+                if (!mbar_wait(&bars[L::bDoFull + st], (k >> 1) & 1, abort_flag, kWaitLimitNs)) break;
                 tc_fence_after();
-                // bf16 P^T / dS^T of query columns 0-63 sit at column offset 0, of 64-127 at 64
+                // bf16 P^T of query columns 0-63 sits at column offset 0, of 64-127 at 64
 #pragma unroll
                 for (int kk = 0; kk < kTileM / 16; ++kk)  // dV += P^T . dO
-                    mma_ts(tDV, tS + (kk >> 2) * 64 + (kk & 3) * 8, do_mn + (uint64_t)((kk * 2048) >> 4), idAcc,
-                           (k > 0 || kk > 0) ? 1u : 0u);
+                    mma_ts(tDV, tS + (kk >> 2) * 64 + (kk & 3) * 8,
+                           dDO_mn + st * kStage + (uint64_t)((kk * 2048) >> 4), idDv, (k > 0 || kk > 0) ? 1u : 0u);
+                issue_t(tS, dV_kmaj, dDO_kmaj + st * kStage);  // dP^T, after dV has read P^T
+                mma_commit(&bars[L::bDpFull]);
                 if (!mbar_wait(&bars[L::bDsFull], k & 1, abort_flag, kWaitLimitNs)) break;
+                if (k > 0 && !mbar_wait(&bars[L::bDqEmpty], (k - 1) & 1, abort_flag, kWaitLimitNs)) break;
                 tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < kTileM / 16; ++kk)  // dK += dS^T . Q
-                    mma_ts(tDK, tDP + (kk >> 2) * 64 + (kk & 3) * 8, q_mn + (uint64_t)((kk * 2048) >> 4), idAcc,
-                           (k > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-                for (int kk = 0; kk < kBlockN / 16; ++kk)  // dQ = dS . K  (into the dP^T columns)
-                    mma_ss(tDP, dDS_mn + (uint64_t)((kk * 2048) >> 4), dK_mn + (uint64_t)((kk * 2048) >> 4), idDq,
+                for (int kk = 0; kk < kBlockN / 16; ++kk)  // dQ = dS . K   (first: its drain is the longest tail)
+                    mma_ss(tDQ, dDS_mn + (uint64_t)((kk * 2048) >> 4), dK_mn + (uint64_t)((kk * 2048) >> 4), idDq,
                            kk > 0 ? 1u : 0u);
                 mma_commit(&bars[L::bDqFull]);
-                mma_commit(&bars[L::bQEmpty + st]);
                 if (k + 1 < nsteps) {
                     const int st1 = (k + 1) & 1;
-                    const int ph1 = ((k + 1) >> 1) & 1;
-                    if (!mbar_wait(&bars[L::bQFull + st1], ph1, abort_flag, kWaitLimitNs)) break;
+                    if (!mbar_wait(&bars[L::bQFull + st1], ((k + 1) >> 1) & 1, abort_flag, kWaitLimitNs)) break;
                     tc_fence_after();
                     issue_t(tS, dK_kmaj, dQ_kmaj + st1 * kStage);
                     mma_commit(&bars[L::bSFull]);
-                    if (!mbar_wait(&bars[L::bDqEmpty], k & 1, abort_flag, kWaitLimitNs)) break;
-                    if (!mbar_wait(&bars[L::bDoFull + st1], ph1, abort_flag, kWaitLimitNs)) break;
-                    tc_fence_after();
-                    issue_t(tDP, dV_kmaj, dDO_kmaj + st1 * kStage);
-                    mma_commit(&bars[L::bDpFull]);
                 }
+#pragma unroll
+                for (int kk = 0; kk < kTileM / 16; ++kk) {  // dK += dS^T . Q  (dS read K-major from shared memory)
+                    const uint64_t off = (uint64_t)((((kk / 4) * (kBlockN * 128)) + (kk % 4) * 32) >> 4);
+                    mma_ss(tDK, dDS_kmaj + off, q_mn + (uint64_t)((kk * 2048) >> 4), idDk, (k > 0 || kk > 0) ? 1u : 0u);
+                }
+                mma_commit(&bars[L::bQEmpty + st]);
+                mma_commit(&bars[L::bDsFree]);  // dK and dQ have both read dS: the buffer may be reused
             }
             mma_commit(&bars[L::bAccFull]);
             mma_commit(&bars[L::bDrain]);
@@ -239,7 +244,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int kv = kv0 + r;
         const bool kv_ok = kv < e;
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-        const uint32_t tS = tbase + lane_off + grp * 64, tDP = tbase + lane_off + 128 + grp * 64;
+        // this group's 64 columns of the S^T / P^T / dP^T region
+        const uint32_t tS = tbase + lane_off + grp * 64;
         float* lse_g = lse_s + grp * 64;
         float* delta_g = delta_s + grp * 64;
         const float sl2 = a.scale_log2;
@@ -308,12 +314,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (lane == 0) mbar_arrive(&bars[L::bPFull]);
 
             if (!mbar_wait(&bars[L::bDpFull], k & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
+            // the dS buffer doubles as the dQ group's staging area for the previous step's tile
+            if (k > 0 && !mbar_wait(&bars[L::bStageFree], (k - 1) & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
             tc_fence_after();
             uint8_t* panel = sm + L::kDS + grp * (kBlockN * 128);
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 uint32_t dr[32];
-                tmem_ld32(tDP + 32 * c, dr);
+                tmem_ld32(tS + 32 * c, dr);
                 float4 nd4[8];
 #pragma unroll
                 for (int j = 0; j < 8; ++j) nd4[j] = *(const float4*)(delta_g + 32 * c + 4 * j);
@@ -330,8 +338,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     const float2 ds = mul2(psc, d);
                     pk[j] = pack_bf16x2(ds.x, ds.y);
                 }
-                tmem_st16(tDP + 16 * c, pk);
-                // the same values, as row r of the [key][query] operand of the dQ MMA
+                // row r of the [key][query] dS operand (read K-major by dK, MN-major by dQ)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const uint32_t bytecol = (uint32_t)(c * 64 + j * 16);
@@ -339,7 +346,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
                 }
             }
-            tmem_st_wait();
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
@@ -376,10 +382,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
     } else if (warp < 12) {
         // ------------------------------------------------------------------ dQ group (query rows)
-        // After the dQ MMA of a step has completed, the dS operand buffer is idle until the
-        // next dP^T MMA (which waits for this group), so each warp borrows 8 KB of it to
-        // transpose its 32 rows x 32 columns chunks: a warp-wide vector atomic then covers
-        // 4 rows x 128 contiguous bytes instead of 32 rows x 16 bytes.
+        // Once the dQ and dK MMAs of a step have read dS, the dS buffer is idle until the
+        // compute groups write the next one (they wait for this group), so each warp
+        // borrows 8 KB of it to transpose its 32 rows x 32 columns chunks: a warp-wide
+        // vector atomic then covers 4 rows x 128 contiguous bytes instead of 32 x 16 bytes.
         const int w4 = warp - 8;
         const uint32_t tDQ = tbase + ((uint32_t)(w4 * 32) << 16) + 128;
         uint8_t* stage = sm + L::kDS + w4 * 8192;
@@ -391,16 +397,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (!mbar_wait(&bars[L::bDqFull], k & 1, abort_flag, kWaitLimitNs)) break;
             tc_fence_after();
             float* dst_base = a.dq_acc + ((int64_t)h * a.T + qrow0) * D;
-#pragma unroll 1
-            for (int c = 0; c < D; c += 32) {
-                uint32_t v[32];
-                tmem_ld32(tDQ + c, v);
-                tmem_ld_wait(v);
-                uint8_t* buf = stage + ((c >> 5) & 1) * 4096;   // alternate 4 KB halves
+            // chunk c+1 is read from TMEM while chunk c goes through shared memory and the atomics
+            uint32_t v[2][32];
+            tmem_ld32(tDQ, v[0]);
+            tmem_ld_wait(v[0]);
+            // dQ is issued before dK, so the dS buffer becomes a staging area only once dK is done
+            if (!mbar_wait(&bars[L::bDsFree], k & 1, abort_flag, kWaitLimitNs)) break;
+#pragma unroll
+            for (int ci = 0; ci < D / 32; ++ci) {
+                const int c = ci * 32;
+                uint32_t (&cur)[32] = v[ci & 1];
+                if (ci + 1 < D / 32) {
+                    tmem_ld32(tDQ + c + 32, v[(ci + 1) & 1]);
+                } else {  // the whole tile has left TMEM: its columns are free for the next dQ
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars[L::bDqEmpty]);
+                }
+                uint8_t* buf = stage + (ci & 1) * 4096;   // alternate 4 KB halves
 #pragma unroll
                 for (int j = 0; j < 8; ++j)   // row `lane`, 16-byte chunk j, XOR-swizzled by row
                     *(uint4*)(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) =
-                        make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                        make_uint4(cur[4 * j], cur[4 * j + 1], cur[4 * j + 2], cur[4 * j + 3]);
                 __syncwarp();
                 // all eight shared-memory reads first: the compiler may not move a read past an
                 // atomic, so interleaving them would serialise eight load latencies
@@ -409,6 +427,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 for (int i = 0; i < 8; ++i) {
                     const int row = 4 * i + sub_row;
                     x[i] = *(const uint4*)(buf + row * 128 + ((chunk ^ (row & 7)) << 4));
+                }
+                if (ci + 1 == D / 32) {  // last reads of the staging area done: the dS buffer is free again
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars[L::bStageFree]);
                 }
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
@@ -419,10 +441,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                               __uint_as_float(x[i].z), __uint_as_float(x[i].w)));
                 }
                 __syncwarp();
+                if (ci + 1 < D / 32) tmem_ld_wait(v[(ci + 1) & 1]);
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[L::bDqEmpty]);
         }
     }
 
