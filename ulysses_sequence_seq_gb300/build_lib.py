@@ -8,6 +8,7 @@ from __future__ import annotations
 
 import concurrent.futures as cf
 import os
+import re
 import shutil
 import subprocess
 
@@ -18,6 +19,12 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libusp.so")
 SOURCES = ["relayout.cu", "sched.cu", "attn_fwd.cu", "attn_bwd.cu", "usp_api.cu", "noalloc.cu"]
+
+# Kernels that rebalance registers between warpgroups with setmaxnreg: the increase waits
+# until the decreases have returned enough of the registers the CTA was launched with, so
+# the launch allocation (registers per thread reported by ptxas) must be at least this
+# many, or the kernel would never get past that point. Checked on every build.
+MIN_LAUNCH_REGS = {"attn_fwd_kernel": 168}
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -41,14 +48,36 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(f) <= t for f in _inputs())
 
 
+def check_launch_registers(ptxas_log: str) -> None:
+    """Fail the build when a setmaxnreg kernel was allocated fewer launch registers than its split needs."""
+    current = None
+    seen = {}
+    for line in ptxas_log.splitlines():
+        m = re.search(r"Compiling entry function '([^']+)'", line)
+        if m:
+            current = m.group(1)
+            continue
+        m = re.search(r"Used (\d+) registers", line)
+        if m and current:
+            for name in MIN_LAUNCH_REGS:
+                if name in current:
+                    seen.setdefault(name, []).append(int(m.group(1)))
+    for name, need in MIN_LAUNCH_REGS.items():
+        got = seen.get(name)
+        if not got:
+            raise RuntimeError(f"ptxas report for {name} not found; cannot check its register split")
+        if min(got) < need:
+            raise RuntimeError(f"{name} launched with {min(got)} registers per thread; its setmaxnreg "
+                               f"split needs {need}")
+
+
 def build(force: bool = False, verbose: bool = False) -> str:
     if not force and up_to_date():
         return LIB
     os.makedirs(OUT_DIR, exist_ok=True)
     cc = nvcc()
-    common = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
-    if verbose:
-        common += ["-Xptxas", "-v"]
+    common = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC,
+                     "-Xptxas", "-v"]
 
     def compile_one(src):
         obj = os.path.join(OUT_DIR, src.replace(".cu", ".o"))
@@ -64,6 +93,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
         for _, err in results:
             if err:
                 print(err)
+    check_launch_registers("\n".join(err for _, err in results))
     tmp = LIB + f".tmp{os.getpid()}"
     cmd = [cc, "-shared", "-o", tmp] + [o for o, _ in results] + ARCH + ["-cudart=static"]
     r = subprocess.run(cmd, capture_output=True, text=True)

@@ -5,7 +5,7 @@
 // Entrenamiento de Secuencias Largas", and HF guide "Configurar" on packed samples).
 //
 // One CTA takes one work item: a query head and two 128-row query tiles of one
-// sample. Warp roles (320 threads):
+// sample. Warp roles (384 threads, warps 10-11 idle):
 //   warps 0-3  softmax group for query tile 0 (thread = one query row = one TMEM lane)
 //   warps 4-7  softmax group for query tile 1
 //   warp  8    TMA producer: Q tiles once, then K/V blocks into a 2-stage ring
@@ -30,7 +30,14 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kFwdThreads = 320;
+constexpr int kFwdThreads = 384;  // 3 warpgroups: two softmax groups, one for load / MMA (2 warps idle)
+// Register shares (per thread) after setmaxnreg: the load/MMA warpgroup needs few, the
+// softmax groups hold a 128-column score row each. Launched with kLaunchRegs per thread,
+// 128 * (2 * kSoftmaxRegs + kAuxRegs) must not exceed kFwdThreads * kLaunchRegs.
+constexpr int kLaunchRegs = 168;
+constexpr int kSoftmaxRegs = 208;
+constexpr int kAuxRegs = 72;
+static_assert(128 * (2 * kSoftmaxRegs + kAuxRegs) <= kFwdThreads * kLaunchRegs, "register split exceeds the launch pool");
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 template <int D>
@@ -52,7 +59,7 @@ struct FwdSmem {
 };
 
 template <int D>
-__global__ void __launch_bounds__(kFwdThreads, 1)
+__global__ void __maxnreg__(kLaunchRegs)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdArgs a) {
     using L = FwdSmem<D>;
@@ -101,7 +108,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     tc_fence_after();
     const uint32_t tbase = *tmem_slot;
 
-    if (warp == 8) {
+    if (warp >= 10) {
+        regs_decrease<kAuxRegs>();  // idle warps of the load/MMA warpgroup
+    } else if (warp == 8) {
+        regs_decrease<kAuxRegs>();
         // ------------------------------------------------------------------ TMA producer
         if (lane == 0) {
             prefetch_tmap(&tmQ);
@@ -138,6 +148,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             }
         }
     } else if (warp == 9) {
+        regs_decrease<kAuxRegs>();
         // ------------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idS = idesc_bf16_f32(kTileM, kBlockN, false, false);  // Q.K^T: both K-major
@@ -210,6 +221,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             mbar_wait_drain(&bars[L::bDrain], 0, kDrainLimitNs);
         }
     } else {
+        regs_increase<kSoftmaxRegs>();
         // ------------------------------------------------------------------ softmax groups
         const int t = warp >> 2;
         const int q0 = t ? q01 : q00;
