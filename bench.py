@@ -1,10 +1,12 @@
 """Benchmark of the Ulysses sequence-parallel hot path on GB300.
 
 One step = the whole per-layer attention path for all sp simulated ranks of one
-GPU: seq->head re-layout of Q, K, V; causal packed attention forward; head->seq of
-O; seq->head of dO; attention backward; head->seq of dQ, dK, dV. The metric is
-algorithmic attention TFLOP/s (4*D FLOPs per allowed (query, key) pair per query
-head forward, 10*D backward), plus re-layout GB/s against HBM.
+GPU: seq->head swap of Q, K, V; causal packed attention forward; head->seq of O;
+seq->head of dO; attention backward; head->seq of dQ, dK, dV. By default the swaps
+are fused into the attention kernels (usp_ulysses_attn_fwd / _bwd read and write the
+seq-sharded layout); --unfused runs them as separate re-layout kernels. The metric
+is algorithmic attention TFLOP/s (4*D FLOPs per allowed (query, key) pair per query
+head forward, 10*D backward), plus the stand-alone re-layout kernels' GB/s against HBM.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl usp|reference]
        [--workload llama|tiny|packed|gqa|long]
@@ -104,6 +106,16 @@ class ClockSampler:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
+def max_over_ranks(value: float, dist=None, device="cpu") -> float:
+    """The largest `value` over all ranks (timing is reported for the slowest rank)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return value
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def oracle_sample_step(w, tokens: int):
     """The oracle's fwd+bwd on one head over the first `tokens` tokens of the workload's
     first sample; returns (seconds, algorithmic FLOPs credited, threads)."""
@@ -181,16 +193,31 @@ def run_usp(args, w):
     hq_, hk_, hv_, hdo_ = (to_host_pinned(seq_sharded_bits(w, t)) for t in ("q", "k", "v", "do"))
     xq, xk, xv, xdo = (t.to(dev) for t in (hq_, hk_, hv_, hdo_))
     cu = torch.from_numpy(w.cu_seqlens()).to(dev)
-    layer = usp.UlyssesAttention(T, w.num_seqs, H, HKV, D, sp, causal=True, device=dev)
+    fused = not args.unfused
+    layer = usp.UlyssesAttention(T, w.num_seqs, H, HKV, D, sp, causal=True, device=dev, fused=fused)
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)   # > L2 (129 MB)
     stream = torch.cuda.current_stream(dev)
 
+    # events: 0 start | 1 after the seq->head swaps (unfused) | 2 after the forward |
+    #         3 after the O / dO swaps (unfused) | 4 after the backward | 5 end
     def step(ev=None):
         if ev is None:
             layer.forward(xq, xk, xv, cu)
             layer.backward(xdo, cu)
             return
         ev[0].record(stream)
+        if fused:
+            ev[1].record(stream)
+            usp.ulysses_attn_fwd(xq, xk, xv, layer.o_seq, layer.lse, cu, layer.B, T, sp, H, HKV, D, layer.scale,
+                                 True, layer.ws, layer.ws_bytes)
+            ev[2].record(stream)
+            ev[3].record(stream)
+            usp.ulysses_attn_bwd(xq, xk, xv, layer.o_seq, layer.lse, xdo, layer.dq_seq, layer.dk_seq, layer.dv_seq,
+                                 usp.USP_BF16, cu, layer.B, T, sp, H, HKV, D, layer.scale, True, layer.ws,
+                                 layer.ws_bytes)
+            ev[4].record(stream)
+            ev[5].record(stream)
+            return
         usp.seq_to_head(xq, layer.q_h, sp)
         usp.seq_to_head(xk, layer.k_h, sp)
         usp.seq_to_head(xv, layer.v_h, sp)
@@ -237,15 +264,34 @@ def run_usp(args, w):
     step_ms = [e[0].elapsed_time(e[5]) for e in evs]
     fwd_ms = [e[1].elapsed_time(e[2]) for e in evs]
     bwd_ms = [e[3].elapsed_time(e[4]) for e in evs]
-    rel_ms = [e[0].elapsed_time(e[1]) + e[2].elapsed_time(e[3]) + e[4].elapsed_time(e[5]) for e in evs]
-    total_ms = sum(step_ms)
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), dist, dev)
     ms_per_step = total_ms / args.steps
     fwd_fl, bwd_fl = attention_flops(w)
     value = (fwd_fl + bwd_fl) * world / (ms_per_step * 1e-3) / 1e12
+
+    # ---- the stand-alone layout swaps (usp_seq_to_head / usp_head_to_seq) on this workload's
+    # eight tensors, L2 flushed before each: the metric's re-layout GB/s against HBM
+    rel_bufs = [(xq, H), (xk, HKV), (xv, HKV), (xdo, H)]
+    rel_tmp = {hh: torch.empty(T * hh * D, dtype=torch.bfloat16, device=dev) for hh in {H, HKV}}
+    rel_back = {hh: torch.empty(T * hh * D, dtype=torch.bfloat16, device=dev) for hh in {H, HKV}}
+    rel_ms = []
+    r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for it in range(args.steps + 1):
+        tot = 0.0
+        for to_head in (True, False):          # a layer swaps Q, K, V (and dO) together
+            flush.zero_()
+            r0.record(stream)
+            for x, hh in rel_bufs:
+                if to_head:
+                    usp.seq_to_head(x, rel_tmp[hh].view(sp, hh // sp, T, D), sp)
+                else:
+                    usp.head_to_seq(rel_tmp[hh].view(sp, hh // sp, T, D), rel_back[hh].view(sp, T // sp, hh, D), sp)
+            r1.record(stream)
+            r1.synchronize()
+            tot += r0.elapsed_time(r1)
+        if it > 0:                             # the first pass is a warm-up
+            rel_ms.append(tot)
+    relayout_bytes = sum(2 * 2 * T * hh * D for _, hh in rel_bufs) * 2   # read + write, both directions
 
     # ---- end to end through the public API: pinned host inputs in, results back to host
     out_host = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
@@ -284,8 +330,6 @@ def run_usp(args, w):
     fwd_mean = statistics.mean(fwd_ms)
     bwd_tflops = bwd_fl / (bwd_mean * 1e-3) / 1e12
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    # eight tensor swaps per step (Q, K, V, O, dO, dQ, dK, dV), each read once and written once
-    relayout_bytes = 2 * 2 * T * D * (H + HKV + HKV + H + H + H + HKV + HKV)
     rel_gbs = relayout_bytes / (statistics.mean(rel_ms) * 1e-3) / 1e9
     hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     cpu = None
@@ -296,21 +340,30 @@ def run_usp(args, w):
         cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                "sample": f"one query head, causal fwd+bwd over the first {L} tokens of sample 0 "
                          f"({dt:.1f} s of float64 C oracle work)"}
-    launches_per_step = 3 + 1 + 1 + 1 + 1 + 1 + 1 + 1 + 1 + 3
+    # fused: schedule + attn_fwd | bwd_prep + schedule + attn_bwd + dq_convert;
+    # unfused adds the eight re-layout launches
+    launches_per_step = 6 if fused else 14
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": workload_desc(w), "seq_len": T, "heads": H, "kv_heads": HKV, "head_dim": D,
                    "sp": sp, "parallelism": f"replicas x{world} (sp={sp} simulated per GPU)",
+                   "path": "fused layout swaps (usp_ulysses_attn_fwd/bwd)" if fused else
+                           "separate re-layout kernels around usp_attn_fwd/bwd_varlen",
                    "l2": "flushed between timed steps (512 MB write outside the events)",
-                   "fwd_ms": fwd_mean, "bwd_ms": bwd_mean, "relayout_ms": statistics.mean(rel_ms),
+                   "fwd_ms": fwd_mean, "bwd_ms": bwd_mean,
                    "fwd_tflops": fwd_fl / (fwd_mean * 1e-3) / 1e12, "bwd_tflops": bwd_tflops},
-        "roofline": {"bound": "tensor", "kernel": "usp_attn_bwd_varlen (attn_bwd_kernel + prep + convert)",
+        "roofline": {"bound": "tensor",
+                     "kernel": ("usp_ulysses_attn_bwd" if fused else "usp_attn_bwd_varlen") +
+                               " call: attn_bwd_kernel + bwd_prep + schedule + dq_convert",
                      "achieved": bwd_tflops, "peak": peak, "unit": "TFLOP/s", "frac": bwd_tflops / peak,
                      "peak_source": f"{peak_src} bf16 burst", "traffic": None},
         "relayout": {"achieved_gbs": rel_gbs, "peak_gbs": hbm, "frac": rel_gbs / hbm,
-                     "peak_source": f"{peak_src} hbm copy", "bytes_per_step": relayout_bytes},
+                     "peak_source": f"{peak_src} hbm copy", "bytes": relayout_bytes,
+                     "what": "usp_seq_to_head on Q, K, V, dO back to back, then usp_head_to_seq on the four; "
+                             "L2 flushed before each batch",
+                     "ms": statistics.mean(rel_ms)},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
@@ -331,6 +384,7 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=2048)
     ap.add_argument("--cpu-tokens", type=int, default=4096)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--unfused", action="store_true", help="time separate re-layout kernels around the attention")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     from ulysses_sequence_seq_gb300.synth import WORKLOADS

@@ -7,7 +7,9 @@ device buffer:
 * :func:`seq_to_head` / :func:`head_to_seq` -- the two all-to-alls as
   device-local permutations [sp][T/sp][H][D] <-> [sp][H/sp][T][D];
 * :func:`attn_fwd_varlen` / :func:`attn_bwd_varlen` -- causal, packed-sample
-  (cu_seqlens) softmax attention forward and backward on tcgen05 tensor cores.
+  (cu_seqlens) softmax attention forward and backward on tcgen05 tensor cores;
+* :func:`ulysses_attn_fwd` / :func:`ulysses_attn_bwd` -- the same with both layout
+  swaps fused into the attention kernels (seq-sharded tensors in and out).
 
 :class:`UlyssesAttention` chains them into the layer-level step: the seq-sharded
 Q, K, V of all ranks in, the seq-sharded attention output out, and the same in
@@ -19,11 +21,11 @@ import math
 
 from ._lib import (USP_BF16, USP_FP16, USP_FP32, USP_OK, UspError, attn_bwd_varlen, attn_fwd_varlen,  # noqa: F401
                    attn_workspace_size, debug_wait_timeout, get_device_status, head_to_seq, load, seq_to_head,
-                   status_string)
+                   status_string, ulysses_attn_bwd, ulysses_attn_fwd)
 
 __all__ = [
-    "seq_to_head", "head_to_seq", "attn_fwd_varlen", "attn_bwd_varlen", "attn_workspace_size",
-    "get_device_status", "status_string", "UspError", "UlyssesAttention", "load",
+    "seq_to_head", "head_to_seq", "attn_fwd_varlen", "attn_bwd_varlen", "ulysses_attn_fwd", "ulysses_attn_bwd",
+    "attn_workspace_size", "get_device_status", "status_string", "UspError", "UlyssesAttention", "load",
 ]
 
 
@@ -33,38 +35,50 @@ class UlyssesAttention:
     Buffers are allocated once for a fixed (T, num_seqs, hq, hkv, D, sp) and reused.
     ``forward`` takes seq-sharded bf16 tensors ([sp][T/sp][H][D] or [T][H][D]) and
     returns the seq-sharded output; ``backward`` takes the seq-sharded output
-    gradient and returns seq-sharded dQ, dK, dV.
+    gradient and returns seq-sharded dQ, dK, dV. With ``fused=True`` (the default)
+    the layout swaps happen inside the attention kernels; with ``fused=False`` they
+    run as separate re-layout kernels around head-sharded attention.
     """
 
     def __init__(self, total_tokens: int, num_seqs: int, hq: int, hkv: int, head_dim: int, sp: int,
-                 causal: bool = True, softmax_scale: float = 0.0, device="cuda", grad_dtype=None):
+                 causal: bool = True, softmax_scale: float = 0.0, device="cuda", grad_dtype=None,
+                 fused: bool = True):
         import torch
         self.T, self.B, self.hq, self.hkv, self.D, self.sp = total_tokens, num_seqs, hq, hkv, head_dim, sp
         self.causal = causal
+        self.fused = fused
         self.scale = softmax_scale if softmax_scale > 0 else 1.0 / math.sqrt(head_dim)
         self.grad_dtype = grad_dtype or torch.bfloat16
         bf = torch.bfloat16
         T, D = total_tokens, head_dim
-        self.q_h = torch.empty(hq, T, D, dtype=bf, device=device)
-        self.k_h = torch.empty(hkv, T, D, dtype=bf, device=device)
-        self.v_h = torch.empty(hkv, T, D, dtype=bf, device=device)
-        self.o_h = torch.empty(hq, T, D, dtype=bf, device=device)
-        self.do_h = torch.empty(hq, T, D, dtype=bf, device=device)
+        if not fused:
+            self.q_h = torch.empty(hq, T, D, dtype=bf, device=device)
+            self.k_h = torch.empty(hkv, T, D, dtype=bf, device=device)
+            self.v_h = torch.empty(hkv, T, D, dtype=bf, device=device)
+            self.o_h = torch.empty(hq, T, D, dtype=bf, device=device)
+            self.do_h = torch.empty(hq, T, D, dtype=bf, device=device)
+            gd = self.grad_dtype
+            self.dq_h = torch.empty(hq, T, D, dtype=gd, device=device)
+            self.dk_h = torch.empty(hkv, T, D, dtype=gd, device=device)
+            self.dv_h = torch.empty(hkv, T, D, dtype=gd, device=device)
         self.lse = torch.empty(hq, T, dtype=torch.float32, device=device)
         self.o_seq = torch.empty(T, hq, D, dtype=bf, device=device)
         gd = self.grad_dtype
-        self.dq_h = torch.empty(hq, T, D, dtype=gd, device=device)
-        self.dk_h = torch.empty(hkv, T, D, dtype=gd, device=device)
-        self.dv_h = torch.empty(hkv, T, D, dtype=gd, device=device)
         self.dq_seq = torch.empty(T, hq, D, dtype=gd, device=device)
         self.dk_seq = torch.empty(T, hkv, D, dtype=gd, device=device)
         self.dv_seq = torch.empty(T, hkv, D, dtype=gd, device=device)
         self.ws_bytes = max(attn_workspace_size(T, num_seqs, hq, hkv, D, False),
                             attn_workspace_size(T, num_seqs, hq, hkv, D, True))
         self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=device)
+        self._saved = None
 
     def forward(self, xq, xk, xv, cu_seqlens, stream=None):
         sp = self.sp
+        if self.fused:
+            ulysses_attn_fwd(xq, xk, xv, self.o_seq, self.lse, cu_seqlens, self.B, self.T, sp, self.hq, self.hkv,
+                             self.D, self.scale, self.causal, self.ws, self.ws_bytes, stream)
+            self._saved = (xq, xk, xv)
+            return self.o_seq
         seq_to_head(xq, self.q_h, sp, stream)
         seq_to_head(xk, self.k_h, sp, stream)
         seq_to_head(xv, self.v_h, sp, stream)
@@ -76,8 +90,16 @@ class UlyssesAttention:
     def backward(self, d_out, cu_seqlens, stream=None):
         import torch
         sp = self.sp
-        seq_to_head(d_out, self.do_h, sp, stream)
         gdt = USP_FP32 if self.grad_dtype == torch.float32 else USP_BF16
+        if self.fused:
+            if self._saved is None:
+                raise RuntimeError("backward() needs a forward() first")
+            xq, xk, xv = self._saved
+            ulysses_attn_bwd(xq, xk, xv, self.o_seq, self.lse, d_out, self.dq_seq, self.dk_seq, self.dv_seq, gdt,
+                             cu_seqlens, self.B, self.T, sp, self.hq, self.hkv, self.D, self.scale, self.causal,
+                             self.ws, self.ws_bytes, stream)
+            return self.dq_seq, self.dk_seq, self.dv_seq
+        seq_to_head(d_out, self.do_h, sp, stream)
         attn_bwd_varlen(self.q_h, self.k_h, self.v_h, self.o_h, self.lse, self.do_h, self.dq_h, self.dk_h,
                         self.dv_h, gdt, cu_seqlens, self.B, self.T, self.hq, self.hkv, self.D, self.scale,
                         self.causal, self.ws, self.ws_bytes, stream)

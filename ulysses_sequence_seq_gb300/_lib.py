@@ -35,6 +35,8 @@ EXPORTED = (
     "usp_status_string",
     "usp_debug_wait_timeout",
     "usp_attn_fwd_varlen_noalloc",
+    "usp_ulysses_attn_fwd",
+    "usp_ulysses_attn_bwd",
 )
 
 
@@ -74,8 +76,11 @@ def load(build_if_missing: bool = True):
     L.usp_status_string.restype = ctypes.c_char_p
     L.usp_debug_wait_timeout.argtypes = [P, Z, ctypes.c_uint64, P]
     L.usp_attn_fwd_varlen_noalloc.argtypes = [P, P, P, P, P, P, I, I64, I, I, I, F, I, P, P]
+    L.usp_ulysses_attn_fwd.argtypes = [P, P, P, P, P, P, I, I64, I, I, I, I, F, I, P, Z, P]
+    L.usp_ulysses_attn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I, P, I, I64, I, I, I, I, F, I, P, Z, P]
     for name in ("usp_seq_to_head", "usp_head_to_seq", "usp_attn_fwd_varlen", "usp_attn_bwd_varlen",
-                 "usp_get_device_status", "usp_debug_wait_timeout", "usp_attn_fwd_varlen_noalloc"):
+                 "usp_get_device_status", "usp_debug_wait_timeout", "usp_attn_fwd_varlen_noalloc",
+                 "usp_ulysses_attn_fwd", "usp_ulysses_attn_bwd"):
         getattr(L, name).restype = I
     _lib = L
     return _lib
@@ -155,6 +160,25 @@ def attn_bwd_varlen(q, k, v, o, lse, d_o, dq, dk, dv, grad_dt: int, cu_seqlens, 
     _check("usp_attn_bwd_varlen", load().usp_attn_bwd_varlen(
         _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(d_o), _ptr(dq), _ptr(dk), _ptr(dv), int(grad_dt),
         _ptr(cu_seqlens), int(num_seqs), int(total_tokens), int(hq), int(hkv), int(head_dim),
+        float(softmax_scale), int(bool(causal)), _ptr(workspace), int(ws_bytes), _stream(stream)))
+
+
+def ulysses_attn_fwd(q, k, v, o, lse, cu_seqlens, num_seqs: int, total_tokens: int, sp: int, hq: int, hkv: int,
+                     head_dim: int, softmax_scale: float, causal: bool, workspace, ws_bytes: int, stream=None):
+    """Fused forward on the seq-sharded layout: q, k, v, o are [sp][T/sp][H][D]."""
+    _check("usp_ulysses_attn_fwd", load().usp_ulysses_attn_fwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(cu_seqlens), int(num_seqs), int(total_tokens), int(sp),
+        int(hq), int(hkv), int(head_dim), float(softmax_scale), int(bool(causal)), _ptr(workspace), int(ws_bytes),
+        _stream(stream)))
+
+
+def ulysses_attn_bwd(q, k, v, o, lse, d_o, dq, dk, dv, grad_dt: int, cu_seqlens, num_seqs: int, total_tokens: int,
+                     sp: int, hq: int, hkv: int, head_dim: int, softmax_scale: float, causal: bool, workspace,
+                     ws_bytes: int, stream=None):
+    """Fused backward on the seq-sharded layout: every activation and gradient is [sp][T/sp][H][D]."""
+    _check("usp_ulysses_attn_bwd", load().usp_ulysses_attn_bwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(d_o), _ptr(dq), _ptr(dk), _ptr(dv), int(grad_dt),
+        _ptr(cu_seqlens), int(num_seqs), int(total_tokens), int(sp), int(hq), int(hkv), int(head_dim),
         float(softmax_scale), int(bool(causal)), _ptr(workspace), int(ws_bytes), _stream(stream)))
 
 

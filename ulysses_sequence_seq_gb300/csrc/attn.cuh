@@ -13,11 +13,13 @@ struct FwdArgs {
     const int32_t* cu;
     const WorkItem* items;
     WsHeader* hdr;
-    __nv_bfloat16* o;   // [hq][T][D]
+    __nv_bfloat16* o;   // [hq][T][D] (head-major) or [T][hq][D] (token_major)
     float* lse;         // [hq][T], natural log
     int64_t T;
+    int hq;
     int group;          // hq / hkv
     int causal;
+    int token_major;    // q, k, v, o in the seq-sharded [T][H][D] layout
     float scale_log2;   // softmax scale * log2(e)
 };
 
@@ -31,10 +33,14 @@ struct BwdArgs {
     const float* lse;    // [hq][T]
     const float* delta;  // [hq][T]
     float* dq_acc;       // [hq][T][D] fp32 accumulator (atomic adds)
-    void* dk;            // [hkv][T][D]
-    void* dv;            // [hkv][T][D]
+    void* dk;            // [hkv][T][D] (head-major) or [T][hkv][D] (token_major)
+    void* dv;            // same layout as dk
     int grad_fp32;       // 1: dk/dv written as fp32, 0: bf16
     int64_t T;
+    int hq;
+    int hkv;
+    int token_major;     // q, k, v, o, dO, dk, dv in the seq-sharded [T][H][D] layout
+    int dq_token_major;  // dq_acc is the caller's fp32 dq in the [T][hq][D] layout
     int group;
     int causal;
     float scale;         // softmax scale
@@ -44,15 +50,19 @@ struct BwdArgs {
 cudaError_t launch_attn_bwd(int head_dim, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                             const CUtensorMap& dout, const BwdArgs& a, int grid, cudaStream_t s);
 
-// Delta_i = dO_i . O_i (fp32) for every query row, and zeroes the dQ accumulator.
+// Delta_i = dO_i . O_i (fp32, [hq][T]) for every query row, and zeroes the dQ accumulator.
+// o / dout are head-major or token-major (token_major); the accumulator is head-major
+// unless dq_token_major.
 cudaError_t launch_bwd_prep(const __nv_bfloat16* o, const __nv_bfloat16* dout, float* delta, float* dq_acc,
-                            int64_t rows, int head_dim, cudaStream_t s);
+                            int64_t T, int hq, int head_dim, int token_major, int dq_token_major, cudaStream_t s);
 
-// dq = dq_acc converted to bf16.
-cudaError_t launch_dq_convert(const float* dq_acc, __nv_bfloat16* dq, int64_t n, cudaStream_t s);
+// dq (bf16, head-major or token-major) = the head-major fp32 accumulator rounded to bf16.
+cudaError_t launch_dq_convert(const float* dq_acc, __nv_bfloat16* dq, int64_t T, int hq, int head_dim,
+                              int token_major, cudaStream_t s);
 
-// TMA tensor map over a head-major bf16 activation [heads][T][D] (64 x 128 boxes, 128-byte swizzle).
-bool make_head_major_map(CUtensorMap* map, const void* base, int64_t T, int heads, int D);
+// TMA tensor map over a bf16 activation, head-major [heads][T][D] or token-major
+// [T][heads][D]: boxes of 64 columns x 128 rows of one head, 128-byte swizzle.
+bool make_activation_map(CUtensorMap* map, const void* base, int64_t T, int heads, int D, int token_major);
 
 // Records `code` in the status word after a kernel that waits on an mbarrier nothing arrives on.
 cudaError_t launch_debug_timeout(WsHeader* hdr, uint64_t limit_ns, cudaStream_t s);

@@ -39,9 +39,17 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kBwdThreads = 448;
-constexpr int kProducerWarp = 12;
-constexpr int kMmaWarp = 13;
+// The query columns of a block are split over kGroups compute warpgroups (thread = key
+// row, kGroupCols columns each); more, narrower groups give the latency-bound exp / dS
+// arithmetic more warps to hide behind.
+constexpr int kGroups = 2;
+constexpr int kGroupCols = kBlockN / kGroups;
+constexpr int kComputeWarps = 4 * kGroups;
+constexpr int kDqWarp0 = kComputeWarps;          // 4 warps
+constexpr int kProducerWarp = kComputeWarps + 4;
+constexpr int kMmaWarp = kComputeWarps + 5;
+constexpr int kBwdThreads = 32 * (kComputeWarps + 6);
+static_assert(kGroupCols % 32 == 0, "a compute group covers whole 32-column TMEM loads");
 
 template <int D>
 struct BwdSmem {
@@ -108,8 +116,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         mbar_init(&bars[L::bSFull], 1);
         mbar_init(&bars[L::bDpFull], 1);
-        mbar_init(&bars[L::bPFull], 8);
-        mbar_init(&bars[L::bDsFull], 8);
+        mbar_init(&bars[L::bPFull], kComputeWarps);
+        mbar_init(&bars[L::bDsFull], kComputeWarps);
         mbar_init(&bars[L::bDqFull], 1);
         mbar_init(&bars[L::bDqEmpty], 4);
         mbar_init(&bars[L::bStageFree], 4);
@@ -133,8 +141,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             prefetch_tmap(&tmDO);
             mbar_arrive_expect_tx(&bars[L::bKvFull], 2 * L::kTileBytes);
             for (int p = 0; p < L::kPanels; ++p) {
-                tma_load_3d(sm + L::kK + p * (kTileM * 128), &tmK, &bars[L::bKvFull], p * 64, kv0, g);
-                tma_load_3d(sm + L::kV + p * (kTileM * 128), &tmV, &bars[L::bKvFull], p * 64, kv0, g);
+                tma_load_rows(sm + L::kK + p * (kTileM * 128), &tmK, &bars[L::bKvFull], p * 64, kv0, g, a.token_major);
+                tma_load_rows(sm + L::kV + p * (kTileM * 128), &tmV, &bars[L::bKvFull], p * 64, kv0, g, a.token_major);
             }
             int issued = 0;
             for (int k = 0; k < nsteps; ++k) {
@@ -145,12 +153,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 const int q0 = s + (i0 + k % nq) * kTileM;
                 mbar_arrive_expect_tx(&bars[L::bQFull + st], L::kTileBytes);
                 for (int p = 0; p < L::kPanels; ++p)
-                    tma_load_3d(sm + L::kQ + st * L::kTileBytes + p * (kTileM * 128), &tmQ, &bars[L::bQFull + st],
-                                p * 64, q0, h);
+                    tma_load_rows(sm + L::kQ + st * L::kTileBytes + p * (kTileM * 128), &tmQ, &bars[L::bQFull + st],
+                                  p * 64, q0, h, a.token_major);
                 mbar_arrive_expect_tx(&bars[L::bDoFull + st], L::kTileBytes);
                 for (int p = 0; p < L::kPanels; ++p)
-                    tma_load_3d(sm + L::kDO + st * L::kTileBytes + p * (kTileM * 128), &tmDO,
-                                &bars[L::bDoFull + st], p * 64, q0, h);
+                    tma_load_rows(sm + L::kDO + st * L::kTileBytes + p * (kTileM * 128), &tmDO,
+                                  &bars[L::bDoFull + st], p * 64, q0, h, a.token_major);
                 issued = k + 1;
             }
             mbar_wait_drain(&bars[L::bKvFull], 0, kDrainLimitNs);
@@ -203,10 +211,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 if (!mbar_wait(&bars[L::bPFull], k & 1, abort_flag, kWaitLimitNs)) break;
                 if (!mbar_wait(&bars[L::bDoFull + st], (k >> 1) & 1, abort_flag, kWaitLimitNs)) break;
                 tc_fence_after();
-                // bf16 P^T of query columns 0-63 sits at column offset 0, of 64-127 at 64
+                // each group's bf16 P^T sits at the start of its own kGroupCols-wide column range
 #pragma unroll
                 for (int kk = 0; kk < kTileM / 16; ++kk)  // dV += P^T . dO
-                    mma_ts(tDV, tS + (kk >> 2) * 64 + (kk & 3) * 8,
+                    mma_ts(tDV, tS + ((16 * kk) / kGroupCols) * kGroupCols + ((16 * kk) % kGroupCols) / 2,
                            dDO_mn + st * kStage + (uint64_t)((kk * 2048) >> 4), idDv, (k > 0 || kk > 0) ? 1u : 0u);
                 issue_t(tS, dV_kmaj, dDO_kmaj + st * kStage);  // dP^T, after dV has read P^T
                 mma_commit(&bars[L::bDpFull]);
@@ -237,28 +245,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mma_commit(&bars[L::bDrain]);
             mbar_wait_drain(&bars[L::bDrain], 0, kDrainLimitNs);
         }
-    } else if (warp < 8) {
+    } else if (warp < kComputeWarps) {
         // ------------------------------------------------------------------ compute groups (key rows)
-        const int grp = warp >> 2;          // 0: query columns 0-63, 1: 64-127
+        const int grp = warp >> 2;          // query columns [grp * kGroupCols, (grp + 1) * kGroupCols)
         const int r = (warp & 3) * 32 + lane;
         const int kv = kv0 + r;
         const bool kv_ok = kv < e;
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-        // this group's 64 columns of the S^T / P^T / dP^T region
-        const uint32_t tS = tbase + lane_off + grp * 64;
-        float* lse_g = lse_s + grp * 64;
-        float* delta_g = delta_s + grp * 64;
+        // this group's columns of the S^T / P^T / dP^T region
+        const uint32_t tS = tbase + lane_off + grp * kGroupCols;
+        float* lse_g = lse_s + grp * kGroupCols;
+        float* delta_g = delta_s + grp * kGroupCols;
         const float sl2 = a.scale_log2;
         const float sc = a.scale;
         bool ok = true;
-        // This group's 64 query rows of a step, negated: -lse (log2 units) and -Delta; rows
+        // This group's query rows of a step, negated: -lse (log2 units) and -Delta; rows
         // outside the sample get -lse = -inf, which makes their P exactly zero. Loaded one
         // step ahead so that their global-memory latency stays off the critical path.
         float nl_next = -INFINITY, nd_next = 0.f;
         auto fetch_row_stats = [&](int k) {
             const int h = g * G + k / nq;
-            const int q = s + (i0 + k % nq) * kTileM + grp * 64 + r;
-            const bool q_ok = r < 64 && q < e;
+            const int q = s + (i0 + k % nq) * kTileM + grp * kGroupCols + r;
+            const bool q_ok = r < kGroupCols && q < e;
             nl_next = q_ok ? -__ldg(a.lse + (int64_t)h * a.T + q) * 1.4426950408889634f : -INFINITY;
             nd_next = q_ok ? -__ldg(a.delta + (int64_t)h * a.T + q) : 0.f;
         };
@@ -266,7 +274,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int k = 0; k < nsteps; ++k) {
             const int q0 = s + (i0 + k % nq) * kTileM;
             named_bar_sync(1 + grp, 128);
-            if (r < 64) {
+            if (r < kGroupCols) {
                 lse_g[r] = nl_next;
                 delta_g[r] = nd_next;
             }
@@ -275,14 +283,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             // element masks are only needed on the diagonal block and on the sample's ragged
             // last key tile; there query column c (of 128) is visible to key row r iff c >= r
             const bool mask_blk = (a.causal && q0 == kv0) || (kv0 + kBlockN > e);
-            const int vis_from = (a.causal && q0 == kv0) ? r - grp * 64 : -1;
+            const int vis_from = (a.causal && q0 == kv0) ? r - grp * kGroupCols : -1;
             if (!mbar_wait(&bars[L::bSFull], k & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
             tc_fence_after();
-            // P for this row's 64 query columns as packed bf16 pairs: the values the dV MMA
-            // consumes, kept (32 registers instead of 64) for dS
-            uint32_t pkall[32];
+            // P for this row's query columns as packed bf16 pairs: the values the dV MMA
+            // consumes, kept (half the registers of fp32) for dS
+            uint32_t pkall[kGroupCols / 2];
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
+            for (int c = 0; c < kGroupCols / 32; ++c) {
                 uint32_t sr[32];
                 tmem_ld32(tS + 32 * c, sr);
                 float4 nl4[8];
@@ -317,9 +325,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             // the dS buffer doubles as the dQ group's staging area for the previous step's tile
             if (k > 0 && !mbar_wait(&bars[L::bStageFree], (k - 1) & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
             tc_fence_after();
-            uint8_t* panel = sm + L::kDS + grp * (kBlockN * 128);
+            uint8_t* panel = sm + L::kDS + ((grp * kGroupCols) / 64) * (kBlockN * 128);
+            const uint32_t col_bytes = (uint32_t)((grp * kGroupCols) % 64) * 2;   // within the 64-column panel
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
+            for (int c = 0; c < kGroupCols / 32; ++c) {
                 uint32_t dr[32];
                 tmem_ld32(tS + 32 * c, dr);
                 float4 nd4[8];
@@ -341,7 +350,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 // row r of the [key][query] dS operand (read K-major by dK, MN-major by dQ)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const uint32_t bytecol = (uint32_t)(c * 64 + j * 16);
+                    const uint32_t bytecol = col_bytes + (uint32_t)(c * 64 + j * 16);
                     *(uint4*)(panel + sw128_offset(r, bytecol)) =
                         make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
                 }
@@ -353,12 +362,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         if (ok && mbar_wait(&bars[L::bAccFull], 0, abort_flag, kWaitLimitNs)) {
             tc_fence_after();
-            // group A writes dV, group B writes dK
-            const int64_t row = (int64_t)g * a.T + kv;
-            const uint32_t src = tbase + lane_off + (grp ? 384 : 256);
-            void* dst_base = grp ? a.dk : a.dv;
+            // the groups split dV (first half of the groups) and dK (second half) by columns
+            constexpr int kPerHalf = kGroups / 2;
+            const int which = grp / kPerHalf;                 // 0: dV, 1: dK
+            const int c_begin = (grp % kPerHalf) * (D / kPerHalf), c_end = c_begin + D / kPerHalf;
+            const int64_t row = act_row(g, kv, a.T, a.hkv, a.token_major);
+            const uint32_t src = tbase + lane_off + (which ? 384 : 256);
+            void* dst_base = which ? a.dk : a.dv;
 #pragma unroll 1
-            for (int c = 0; c < D; c += 32) {
+            for (int c = c_begin; c < c_end; c += 32) {
                 uint32_t o[32];
                 tmem_ld32(src + c, o);
                 tmem_ld_wait(o);
@@ -380,13 +392,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 }
             }
         }
-    } else if (warp < 12) {
+    } else if (warp < kDqWarp0 + 4) {
         // ------------------------------------------------------------------ dQ group (query rows)
         // Once the dQ and dK MMAs of a step have read dS, the dS buffer is idle until the
         // compute groups write the next one (they wait for this group), so each warp
         // borrows 8 KB of it to transpose its 32 rows x 32 columns chunks: a warp-wide
         // vector atomic then covers 4 rows x 128 contiguous bytes instead of 32 x 16 bytes.
-        const int w4 = warp - 8;
+        const int w4 = warp - kDqWarp0;
         const uint32_t tDQ = tbase + ((uint32_t)(w4 * 32) << 16) + 128;
         uint8_t* stage = sm + L::kDS + w4 * 8192;
         const int sub_row = lane >> 3;   // 0..3: row within a group of four
@@ -396,7 +408,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const int qrow0 = s + (i0 + k % nq) * kTileM + w4 * 32;   // first query row of this warp
             if (!mbar_wait(&bars[L::bDqFull], k & 1, abort_flag, kWaitLimitNs)) break;
             tc_fence_after();
-            float* dst_base = a.dq_acc + ((int64_t)h * a.T + qrow0) * D;
+            // row `row` of this warp's 32 query rows: dst_base + row * dq_rs
+            const int64_t dq_rs = (int64_t)(a.dq_token_major ? a.hq : 1) * D;
+            float* dst_base = a.dq_acc + act_row(h, qrow0, a.T, a.hq, a.dq_token_major) * D;
             // chunk c+1 is read from TMEM while chunk c goes through shared memory and the atomics
             uint32_t v[2][32];
             tmem_ld32(tDQ, v[0]);
@@ -436,7 +450,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 for (int i = 0; i < 8; ++i) {
                     const int row = 4 * i + sub_row;
                     if (qrow0 + row < e)
-                        atomicAdd((float4*)(dst_base + (int64_t)row * D + c) + chunk,
+                        atomicAdd((float4*)(dst_base + (int64_t)row * dq_rs + c) + chunk,
                                   make_float4(__uint_as_float(x[i].x), __uint_as_float(x[i].y),
                                               __uint_as_float(x[i].z), __uint_as_float(x[i].w)));
                 }
@@ -458,18 +472,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 template <int D>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __restrict__ o,
                                                        const __nv_bfloat16* __restrict__ dout, float* __restrict__ delta,
-                                                       float* __restrict__ dq_acc, int64_t rows) {
-    constexpr int TPR = D / 8;
+                                                       float* __restrict__ dq_acc, int64_t T, int H, int token_major,
+                                                       int dq_token_major) {
+    constexpr int TPR = D / 8;   // threads per row, 8 elements (16 bytes of bf16) each
+    const int h = blockIdx.y;
     const int sub = threadIdx.x % TPR;
-    const int64_t rows_per_cta = 256 / TPR;
+    constexpr int64_t kRowsPerCta = 256 / TPR;
     // the loop bound is uniform across the CTA so that every lane reaches the shuffles
-    for (int64_t base = (int64_t)blockIdx.x * rows_per_cta; base < rows; base += (int64_t)gridDim.x * rows_per_cta) {
-        const int64_t row = base + threadIdx.x / TPR;
-        const bool valid = row < rows;
+    for (int64_t base = (int64_t)blockIdx.x * kRowsPerCta; base < T; base += (int64_t)gridDim.x * kRowsPerCta) {
+        const int64_t t = base + threadIdx.x / TPR;
+        const bool valid = t < T;
         float acc = 0.f;
         if (valid) {
-            const uint4 ov = __ldg((const uint4*)(o + row * D) + sub);
-            const uint4 dv = __ldg((const uint4*)(dout + row * D) + sub);
+            const int64_t arow = act_row(h, t, T, H, token_major);
+            const uint4 ov = __ldg((const uint4*)(o + arow * D) + sub);
+            const uint4 dv = __ldg((const uint4*)(dout + arow * D) + sub);
             const __nv_bfloat162* o2 = (const __nv_bfloat162*)&ov;
             const __nv_bfloat162* d2 = (const __nv_bfloat162*)&dv;
 #pragma unroll
@@ -483,19 +500,27 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
 #pragma unroll
         for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
         if (valid) {
-            if (sub == 0) delta[row] = acc;
-            float4* z = (float4*)(dq_acc + row * D) + 2 * sub;
+            if (sub == 0) delta[(int64_t)h * T + t] = acc;
+            float4* z = (float4*)(dq_acc + act_row(h, t, T, H, dq_token_major) * D) + 2 * sub;
             z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
             z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
     }
 }
 
+// fp32 head-major accumulator -> bf16 dq (head-major or token-major); D4 (= D / 4, a power
+// of two) threads per row, 4 elements each
+template <int D4>
 __global__ void __launch_bounds__(256) dq_convert_kernel(const float4* __restrict__ src, uint2* __restrict__ dst,
-                                                         int64_t n4) {
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (int64_t)gridDim.x * blockDim.x) {
-        const float4 v = src[i];
-        dst[i] = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+                                                         int64_t T, int H, int token_major) {
+    const int h = blockIdx.y;
+    const float4* s_head = src + (int64_t)h * T * D4;
+    const int64_t n = T * D4;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t t = i / D4;
+        const int c = (int)(i % D4);
+        const float4 v = s_head[i];
+        dst[act_row(h, t, T, H, token_major) * D4 + c] = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
     }
 }
 
@@ -528,9 +553,12 @@ cudaError_t launch_bwd_impl(const CUtensorMap& q, const CUtensorMap& k, const CU
     return cudaGetLastError();
 }
 
-int grid_for(int64_t work_items, int per_cta) {
+// CTAs for `work_items` units at `per_cta` units each, capped so that all `ys` rows of the
+// grid together keep about 16 CTAs per SM.
+int grid_for(int64_t work_items, int per_cta, int ys = 1) {
     int64_t g = (work_items + per_cta - 1) / per_cta;
-    if (g > 152 * 16) g = 152 * 16;
+    const int64_t cap = (152 * 16 + ys - 1) / ys;
+    if (g > cap) g = cap;
     if (g < 1) g = 1;
     return (int)g;
 }
@@ -544,18 +572,24 @@ cudaError_t launch_attn_bwd(int head_dim, const CUtensorMap& q, const CUtensorMa
 }
 
 cudaError_t launch_bwd_prep(const __nv_bfloat16* o, const __nv_bfloat16* dout, float* delta, float* dq_acc,
-                            int64_t rows, int head_dim, cudaStream_t s) {
-    if (head_dim == 128) {
-        bwd_prep_kernel<128><<<grid_for(rows, 256 / 16), 256, 0, s>>>(o, dout, delta, dq_acc, rows);
-    } else {
-        bwd_prep_kernel<64><<<grid_for(rows, 256 / 8), 256, 0, s>>>(o, dout, delta, dq_acc, rows);
-    }
+                            int64_t T, int hq, int head_dim, int token_major, int dq_token_major, cudaStream_t s) {
+    const int tpr = head_dim / 8;
+    const dim3 grid(grid_for(T, 256 / tpr, hq), hq);
+    if (head_dim == 128)
+        bwd_prep_kernel<128><<<grid, 256, 0, s>>>(o, dout, delta, dq_acc, T, hq, token_major, dq_token_major);
+    else
+        bwd_prep_kernel<64><<<grid, 256, 0, s>>>(o, dout, delta, dq_acc, T, hq, token_major, dq_token_major);
     return cudaGetLastError();
 }
 
-cudaError_t launch_dq_convert(const float* dq_acc, __nv_bfloat16* dq, int64_t n, cudaStream_t s) {
-    const int64_t n4 = n / 4;
-    dq_convert_kernel<<<grid_for(n4, 256), 256, 0, s>>>((const float4*)dq_acc, (uint2*)dq, n4);
+cudaError_t launch_dq_convert(const float* dq_acc, __nv_bfloat16* dq, int64_t T, int hq, int head_dim,
+                              int token_major, cudaStream_t s) {
+    const int D4 = head_dim / 4;
+    const dim3 grid(grid_for(T * D4, 256, hq), hq);
+    if (D4 == 32)
+        dq_convert_kernel<32><<<grid, 256, 0, s>>>((const float4*)dq_acc, (uint2*)dq, T, hq, token_major);
+    else
+        dq_convert_kernel<16><<<grid, 256, 0, s>>>((const float4*)dq_acc, (uint2*)dq, T, hq, token_major);
     return cudaGetLastError();
 }
 

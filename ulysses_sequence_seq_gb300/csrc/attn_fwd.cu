@@ -121,8 +121,8 @@ __global__ void __maxnreg__(kLaunchRegs)
             mbar_arrive_expect_tx(&bars[L::bQFull], ntiles * L::kTileBytes);
             for (int t = 0; t < ntiles; ++t)
                 for (int p = 0; p < L::kPanels; ++p)
-                    tma_load_3d(sm + (t ? L::kQ1 : L::kQ0) + p * (kTileM * 128), &tmQ, &bars[L::bQFull], p * 64,
-                                t ? q01 : q00, h);
+                    tma_load_rows(sm + (t ? L::kQ1 : L::kQ0) + p * (kTileM * 128), &tmQ, &bars[L::bQFull], p * 64,
+                                  t ? q01 : q00, h, a.token_major);
             int issued = 0;
             for (int n = 0; n < nmax; ++n) {
                 const int st = n & 1;
@@ -131,12 +131,12 @@ __global__ void __maxnreg__(kLaunchRegs)
                 const int row = s + n * kBlockN;
                 mbar_arrive_expect_tx(&bars[L::bKFull + st], L::kTileBytes);
                 for (int p = 0; p < L::kPanels; ++p)
-                    tma_load_3d(sm + L::kK + st * L::kTileBytes + p * (kTileM * 128), &tmK, &bars[L::bKFull + st],
-                                p * 64, row, kvh);
+                    tma_load_rows(sm + L::kK + st * L::kTileBytes + p * (kTileM * 128), &tmK, &bars[L::bKFull + st],
+                                  p * 64, row, kvh, a.token_major);
                 mbar_arrive_expect_tx(&bars[L::bVFull + st], L::kTileBytes);
                 for (int p = 0; p < L::kPanels; ++p)
-                    tma_load_3d(sm + L::kV + st * L::kTileBytes + p * (kTileM * 128), &tmV, &bars[L::bVFull + st],
-                                p * 64, row, kvh);
+                    tma_load_rows(sm + L::kV + st * L::kTileBytes + p * (kTileM * 128), &tmV, &bars[L::bVFull + st],
+                                  p * 64, row, kvh, a.token_major);
                 issued = n + 1;
             }
             // Before the CTA may exit, every copy it issued must have landed. The last
@@ -324,7 +324,7 @@ __global__ void __maxnreg__(kLaunchRegs)
             tc_fence_after();
             const bool valid = i < e;
             const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
-            __nv_bfloat16* orow = a.o + ((int64_t)h * a.T + i) * D;
+            __nv_bfloat16* orow = a.o + act_row(h, i, a.T, a.hq, a.token_major) * D;
 #pragma unroll 1
             for (int c = 0; c < D; c += 32) {
                 uint32_t o[32];

@@ -49,6 +49,12 @@ struct WsLayout {
     int max_items;
 };
 
+// Row (of head_dim elements) holding token t of head h: head-major [H][T][D] (the
+// head-sharded layout) or token-major [T][H][D] (the seq-sharded layout of all ranks).
+__host__ __device__ __forceinline__ int64_t act_row(int h, int64_t t, int64_t T, int H, int token_major) {
+    return token_major ? t * H + h : (int64_t)h * T + t;
+}
+
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 inline int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }

@@ -106,9 +106,9 @@ extern "C" usp_status usp_attn_fwd_varlen_noalloc(const void* q, const void* k, 
     if (launch_schedule(sa, s) != cudaSuccess) return USP_ERR_CUDA;
 
     CUtensorMap mq, mk, mv;
-    if (!make_head_major_map(&mq, q, total_tokens, hq, head_dim) ||
-        !make_head_major_map(&mk, k, total_tokens, hkv, head_dim) ||
-        !make_head_major_map(&mv, v, total_tokens, hkv, head_dim))
+    if (!make_activation_map(&mq, q, total_tokens, hq, head_dim, 0) ||
+        !make_activation_map(&mk, k, total_tokens, hkv, head_dim, 0) ||
+        !make_activation_map(&mv, v, total_tokens, hkv, head_dim, 0))
         return USP_ERR_CUDA;
     FwdArgs fa{};
     fa.cu = cu_seqlens;
@@ -117,6 +117,7 @@ extern "C" usp_status usp_attn_fwd_varlen_noalloc(const void* q, const void* k, 
     fa.o = (__nv_bfloat16*)o;
     fa.lse = lse;
     fa.T = total_tokens;
+    fa.hq = hq;
     fa.group = hq / hkv;
     fa.causal = sa.causal;
     fa.scale_log2 = (softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)head_dim)) * 1.4426950408889634f;

@@ -108,6 +108,16 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* m
         : "memory");
 }
 
+// Rows [t0, t0+box) x columns [x, x+64) of head h from an activation map: head-major maps
+// are (D, T, H), token-major (seq-sharded) maps (D, H, T); both land as [rows][64] in smem.
+__device__ __forceinline__ void tma_load_rows(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int x, int t0,
+                                              int h, int token_major) {
+    if (token_major)
+        tma_load_3d(smem_dst, map, bar, x, h, t0);
+    else
+        tma_load_3d(smem_dst, map, bar, x, t0, h);
+}
+
 // Make generic-proxy writes to shared memory visible to the async proxy (tensor cores, TMA).
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -59,14 +59,24 @@ float resolve_scale(float softmax_scale, int D) {
 
 }  // namespace
 
-// Tensor map over a head-major bf16 activation [heads][T][D]: boxes of 64 columns x 128
-// rows of one head, 128-byte swizzled (the layout the tensor-core descriptors expect).
-bool make_head_major_map(CUtensorMap* map, const void* base, int64_t T, int heads, int D) {
+// Tensor map over a bf16 activation, 64-column x 128-row boxes of one head, 128-byte
+// swizzled (the layout the tensor-core descriptors expect). Head-major [heads][T][D] maps
+// are (D, T, heads); token-major [T][heads][D] maps are (D, heads, T), so the strides grow.
+bool make_activation_map(CUtensorMap* map, const void* base, int64_t T, int heads, int D, int token_major) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
-    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)T, (cuuint64_t)heads};
-    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)T * D * 2};
-    cuuint32_t box[3] = {64, (cuuint32_t)kTileM, 1};
+    const cuuint64_t row = (cuuint64_t)D * 2;
+    cuuint64_t dims[3], strides[2];
+    cuuint32_t box[3];
+    if (token_major) {
+        dims[0] = (cuuint64_t)D; dims[1] = (cuuint64_t)heads; dims[2] = (cuuint64_t)T;
+        strides[0] = row; strides[1] = row * (cuuint64_t)heads;
+        box[0] = 64; box[1] = 1; box[2] = (cuuint32_t)kTileM;
+    } else {
+        dims[0] = (cuuint64_t)D; dims[1] = (cuuint64_t)T; dims[2] = (cuuint64_t)heads;
+        strides[0] = row; strides[1] = row * (cuuint64_t)T;
+        box[0] = 64; box[1] = (cuuint32_t)kTileM; box[2] = 1;
+    }
     cuuint32_t es[3] = {1, 1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -83,19 +93,20 @@ extern "C" size_t usp_attn_workspace_size(int64_t total_tokens, int num_seqs, in
     return ws_layout(total_tokens, num_seqs, hq, hkv, head_dim, bwd ? 1 : 0).total;
 }
 
-extern "C" usp_status usp_attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
-                                          const int32_t* cu_seqlens, int num_seqs, int64_t total_tokens, int hq,
-                                          int hkv, int head_dim, float softmax_scale, int causal, void* workspace,
-                                          size_t ws_bytes, void* stream) {
+namespace usp {
+namespace {
+
+usp_status attn_fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* cu_seqlens,
+                         int num_seqs, int64_t total_tokens, int hq, int hkv, int head_dim, float softmax_scale,
+                         int causal, void* workspace, size_t ws_bytes, cudaStream_t s, int token_major) {
     usp_status st = check_common(total_tokens, num_seqs, hq, hkv, head_dim, cu_seqlens);
     if (st != USP_OK) return st;
-    if (total_tokens == 0) return reset_status_if_any(workspace, ws_bytes, (cudaStream_t)stream);
+    if (total_tokens == 0) return reset_status_if_any(workspace, ws_bytes, s);
     if (!q || !k || !v || !o || !lse || !workspace) return USP_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(workspace))
         return USP_ERR_INVALID_ARG;
     const WsLayout w = ws_layout(total_tokens, num_seqs, hq, hkv, head_dim, 0);
     if (ws_bytes < w.total) return USP_ERR_WORKSPACE;
-    cudaStream_t s = (cudaStream_t)stream;
     uint8_t* ws = (uint8_t*)workspace;
     WsHeader* hdr = (WsHeader*)ws;
     if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return USP_ERR_CUDA;
@@ -117,9 +128,9 @@ extern "C" usp_status usp_attn_fwd_varlen(const void* q, const void* k, const vo
     if (launch_schedule(sa, s) != cudaSuccess) return USP_ERR_CUDA;
 
     CUtensorMap mq, mk, mv;
-    if (!make_head_major_map(&mq, q, total_tokens, hq, head_dim) ||
-        !make_head_major_map(&mk, k, total_tokens, hkv, head_dim) ||
-        !make_head_major_map(&mv, v, total_tokens, hkv, head_dim))
+    if (!make_activation_map(&mq, q, total_tokens, hq, head_dim, token_major) ||
+        !make_activation_map(&mk, k, total_tokens, hkv, head_dim, token_major) ||
+        !make_activation_map(&mv, v, total_tokens, hkv, head_dim, token_major))
         return USP_ERR_CUDA;
     FwdArgs fa{};
     fa.cu = cu_seqlens;
@@ -128,40 +139,42 @@ extern "C" usp_status usp_attn_fwd_varlen(const void* q, const void* k, const vo
     fa.o = (__nv_bfloat16*)o;
     fa.lse = lse;
     fa.T = total_tokens;
+    fa.hq = hq;
     fa.group = hq / hkv;
     fa.causal = sa.causal;
+    fa.token_major = token_major;
     fa.scale_log2 = resolve_scale(softmax_scale, head_dim) * 1.4426950408889634f;
     if (launch_attn_fwd(head_dim, mq, mk, mv, fa, w.max_items, s) != cudaSuccess) return USP_ERR_CUDA;
     return USP_OK;
 }
 
-extern "C" usp_status usp_attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
-                                          const float* lse, const void* d_o, void* dq, void* dk, void* dv,
-                                          usp_dtype grad_dt, const int32_t* cu_seqlens, int num_seqs,
-                                          int64_t total_tokens, int hq, int hkv, int head_dim, float softmax_scale,
-                                          int causal, void* workspace, size_t ws_bytes, void* stream) {
+usp_status attn_bwd_impl(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                         const void* d_o, void* dq, void* dk, void* dv, usp_dtype grad_dt, const int32_t* cu_seqlens,
+                         int num_seqs, int64_t total_tokens, int hq, int hkv, int head_dim, float softmax_scale,
+                         int causal, void* workspace, size_t ws_bytes, cudaStream_t s, int token_major) {
     usp_status st = check_common(total_tokens, num_seqs, hq, hkv, head_dim, cu_seqlens);
     if (st != USP_OK) return st;
     if (grad_dt == USP_FP16) return USP_ERR_UNSUPPORTED;
     if (grad_dt != USP_BF16 && grad_dt != USP_FP32) return USP_ERR_INVALID_ARG;
-    if (total_tokens == 0) return reset_status_if_any(workspace, ws_bytes, (cudaStream_t)stream);
+    if (total_tokens == 0) return reset_status_if_any(workspace, ws_bytes, s);
     if (!q || !k || !v || !o || !lse || !d_o || !dq || !dk || !dv || !workspace) return USP_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(d_o) ||
         !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace))
         return USP_ERR_INVALID_ARG;
     const WsLayout w = ws_layout(total_tokens, num_seqs, hq, hkv, head_dim, 1);
     if (ws_bytes < w.total) return USP_ERR_WORKSPACE;
-    cudaStream_t s = (cudaStream_t)stream;
     uint8_t* ws = (uint8_t*)workspace;
     WsHeader* hdr = (WsHeader*)ws;
     if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return USP_ERR_CUDA;
     const bool fp32_grads = grad_dt == USP_FP32;
     float* delta = (float*)(ws + w.delta);
-    // fp32 gradients accumulate straight into the caller's dq; bf16 ones go through the workspace.
+    // fp32 gradients accumulate straight into the caller's dq (in its layout); bf16 ones go
+    // through the head-major workspace accumulator and a final conversion.
     float* dq_acc = fp32_grads ? (float*)dq : (float*)(ws + w.dq_acc);
+    const int dq_token_major = fp32_grads ? token_major : 0;
 
-    if (launch_bwd_prep((const __nv_bfloat16*)o, (const __nv_bfloat16*)d_o, delta, dq_acc, (int64_t)hq * total_tokens,
-                        head_dim, s) != cudaSuccess)
+    if (launch_bwd_prep((const __nv_bfloat16*)o, (const __nv_bfloat16*)d_o, delta, dq_acc, total_tokens, hq, head_dim,
+                        token_major, dq_token_major, s) != cudaSuccess)
         return USP_ERR_CUDA;
 
     SchedArgs sa{};
@@ -181,10 +194,10 @@ extern "C" usp_status usp_attn_bwd_varlen(const void* q, const void* k, const vo
     if (launch_schedule(sa, s) != cudaSuccess) return USP_ERR_CUDA;
 
     CUtensorMap mq, mk, mv, mdo;
-    if (!make_head_major_map(&mq, q, total_tokens, hq, head_dim) ||
-        !make_head_major_map(&mk, k, total_tokens, hkv, head_dim) ||
-        !make_head_major_map(&mv, v, total_tokens, hkv, head_dim) ||
-        !make_head_major_map(&mdo, d_o, total_tokens, hq, head_dim))
+    if (!make_activation_map(&mq, q, total_tokens, hq, head_dim, token_major) ||
+        !make_activation_map(&mk, k, total_tokens, hkv, head_dim, token_major) ||
+        !make_activation_map(&mv, v, total_tokens, hkv, head_dim, token_major) ||
+        !make_activation_map(&mdo, d_o, total_tokens, hq, head_dim, token_major))
         return USP_ERR_CUDA;
     BwdArgs ba{};
     ba.cu = cu_seqlens;
@@ -197,15 +210,69 @@ extern "C" usp_status usp_attn_bwd_varlen(const void* q, const void* k, const vo
     ba.dv = dv;
     ba.grad_fp32 = fp32_grads ? 1 : 0;
     ba.T = total_tokens;
+    ba.hq = hq;
+    ba.hkv = hkv;
+    ba.token_major = token_major;
+    ba.dq_token_major = dq_token_major;
     ba.group = hq / hkv;
     ba.causal = sa.causal;
     ba.scale = resolve_scale(softmax_scale, head_dim);
     ba.scale_log2 = ba.scale * 1.4426950408889634f;
     if (launch_attn_bwd(head_dim, mq, mk, mv, mdo, ba, w.max_items, s) != cudaSuccess) return USP_ERR_CUDA;
     if (!fp32_grads &&
-        launch_dq_convert(dq_acc, (__nv_bfloat16*)dq, (int64_t)hq * total_tokens * head_dim, s) != cudaSuccess)
+        launch_dq_convert(dq_acc, (__nv_bfloat16*)dq, total_tokens, hq, head_dim, token_major, s) != cudaSuccess)
         return USP_ERR_CUDA;
     return USP_OK;
+}
+
+// sp simulated ranks: the head counts must divide over them and the sequence must be
+// padded to a multiple of sp_size (HF guide, "Configurar").
+usp_status check_sp(int sp, int64_t total_tokens, int hq, int hkv) {
+    if (sp < 1 || hq < 1 || hkv < 1 || total_tokens < 0) return USP_ERR_INVALID_ARG;
+    if (hq % sp != 0 || hkv % sp != 0 || total_tokens % sp != 0) return USP_ERR_INVALID_ARG;
+    return USP_OK;
+}
+
+}  // namespace
+}  // namespace usp
+
+extern "C" usp_status usp_attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                                          const int32_t* cu_seqlens, int num_seqs, int64_t total_tokens, int hq,
+                                          int hkv, int head_dim, float softmax_scale, int causal, void* workspace,
+                                          size_t ws_bytes, void* stream) {
+    return attn_fwd_impl(q, k, v, o, lse, cu_seqlens, num_seqs, total_tokens, hq, hkv, head_dim, softmax_scale,
+                         causal, workspace, ws_bytes, (cudaStream_t)stream, 0);
+}
+
+extern "C" usp_status usp_attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
+                                          const float* lse, const void* d_o, void* dq, void* dk, void* dv,
+                                          usp_dtype grad_dt, const int32_t* cu_seqlens, int num_seqs,
+                                          int64_t total_tokens, int hq, int hkv, int head_dim, float softmax_scale,
+                                          int causal, void* workspace, size_t ws_bytes, void* stream) {
+    return attn_bwd_impl(q, k, v, o, lse, d_o, dq, dk, dv, grad_dt, cu_seqlens, num_seqs, total_tokens, hq, hkv,
+                         head_dim, softmax_scale, causal, workspace, ws_bytes, (cudaStream_t)stream, 0);
+}
+
+extern "C" usp_status usp_ulysses_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                                           const int32_t* cu_seqlens, int num_seqs, int64_t total_tokens, int sp,
+                                           int hq, int hkv, int head_dim, float softmax_scale, int causal,
+                                           void* workspace, size_t ws_bytes, void* stream) {
+    const usp_status st = check_sp(sp, total_tokens, hq, hkv);
+    if (st != USP_OK) return st;
+    return attn_fwd_impl(q, k, v, o, lse, cu_seqlens, num_seqs, total_tokens, hq, hkv, head_dim, softmax_scale,
+                         causal, workspace, ws_bytes, (cudaStream_t)stream, 1);
+}
+
+extern "C" usp_status usp_ulysses_attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                                           const float* lse, const void* d_o, void* dq, void* dk, void* dv,
+                                           usp_dtype grad_dt, const int32_t* cu_seqlens, int num_seqs,
+                                           int64_t total_tokens, int sp, int hq, int hkv, int head_dim,
+                                           float softmax_scale, int causal, void* workspace, size_t ws_bytes,
+                                           void* stream) {
+    const usp_status st = check_sp(sp, total_tokens, hq, hkv);
+    if (st != USP_OK) return st;
+    return attn_bwd_impl(q, k, v, o, lse, d_o, dq, dk, dv, grad_dt, cu_seqlens, num_seqs, total_tokens, hq, hkv,
+                         head_dim, softmax_scale, causal, workspace, ws_bytes, (cudaStream_t)stream, 1);
 }
 
 extern "C" usp_status usp_get_device_status(const void* workspace, void* stream) {
