@@ -43,6 +43,24 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+# DRAM bytes (read + write) of one attn_bwd_kernel launch from an ncu capture of this
+# bench's own command, keyed by workload, path and the kernel source they were taken on;
+# any change to the kernel source makes the figure stale and it is reported as null.
+MEASURED_BWD_TRAFFIC = {
+    ("llama", True): ("3575786b6c699152", 1.895166e9 + 0.986106e9),
+}
+
+
+def bwd_traffic(w, fused):
+    import hashlib
+    entry = MEASURED_BWD_TRAFFIC.get((w.name, fused))
+    if entry is None:
+        return None
+    with open(os.path.join(ROOT, "ulysses_sequence_seq_gb300", "csrc", "attn_bwd.cu"), "rb") as f:
+        digest = hashlib.sha256(f.read()).hexdigest()[:16]
+    return entry[1] if digest == entry[0] else None
+
+
 def workload_desc(w):
     kind = "packed" if w.num_seqs > 1 else "single sequence"
     return (f"{w.name}: {w.total_tokens} tokens ({kind}, {w.num_seqs} samples), sp={w.sp}, hq={w.hq}, "
@@ -358,7 +376,8 @@ def run_usp(args, w):
                      "kernel": ("usp_ulysses_attn_bwd" if fused else "usp_attn_bwd_varlen") +
                                " call: attn_bwd_kernel + bwd_prep + schedule + dq_convert",
                      "achieved": bwd_tflops, "peak": peak, "unit": "TFLOP/s", "frac": bwd_tflops / peak,
-                     "peak_source": f"{peak_src} bf16 burst", "traffic": None},
+                     "peak_source": f"{peak_src} bf16 burst", "traffic": bwd_traffic(w, fused),
+                     "traffic_of": "attn_bwd_kernel, DRAM read+write bytes per launch (ncu)"},
         "relayout": {"achieved_gbs": rel_gbs, "peak_gbs": hbm, "frac": rel_gbs / hbm,
                      "peak_source": f"{peak_src} hbm copy", "bytes": relayout_bytes,
                      "what": "usp_seq_to_head on Q, K, V, dO back to back, then usp_head_to_seq on the four; "
