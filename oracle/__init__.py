@@ -10,8 +10,10 @@ benchmark's CPU-baseline / reference leg import this package; the library
   explicit mask predicate (C, ``attn_ref.c``), for all or for listed rows.
 * :mod:`oracle.brute` -- pure-Python attention and finite differences for tiny
   inputs.
+* :mod:`oracle.sp_loss` -- position_ids <-> cu_seqlens, the label shift, good-token
+  counts per SP rank and the good-token weighted loss over the ranks.
 
-Every function is pinned by ``tests/test_oracle_pins.py``.
+Every function is pinned by ``tests/test_oracle_pins.py`` and ``tests/test_oracle_sp_loss.py``.
 """
 from __future__ import annotations
 
@@ -21,7 +23,7 @@ import math
 import numpy as np
 
 from .build import build_oracle
-from . import relayout  # noqa: F401
+from . import relayout, sp_loss  # noqa: F401
 
 _lib = None
 

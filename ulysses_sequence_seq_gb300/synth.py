@@ -112,6 +112,28 @@ def custom_workload(name: str, lengths, sp: int, hq: int, hkv: int, head_dim: in
     return Workload(name, index, int(sum(lengths)), sp, hq, hkv, head_dim, causal, lengths)
 
 
+# ----------------------------------------------------------------------------- labels
+def packed_labels(cu_seqlens, vocab: int = 32000, seed: int = 0, max_prompt_frac: float = 0.5) -> np.ndarray:
+    """int64 labels of packed fine-tuning samples: each sample opens with a prompt span of
+    -100 (at least its first token, up to ``max_prompt_frac`` of it), the rest are token ids
+    drawn uniformly from [0, vocab)."""
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    T = int(cu[-1])
+    rng = np.random.default_rng(seed)
+    lab = rng.integers(0, vocab, size=T, dtype=np.int64)
+    for b in range(len(cu) - 1):
+        L = int(cu[b + 1] - cu[b])
+        if L:
+            prompt = 1 + int(rng.integers(0, max(1, int(L * max_prompt_frac))))
+            lab[cu[b]:cu[b] + prompt] = -100
+    return lab
+
+
+def token_losses(T: int, seed: int = 0) -> np.ndarray:
+    """float32 per-token losses (exponential, mean 2) standing in for a model's cross entropy."""
+    return np.random.default_rng(seed).exponential(2.0, size=T).astype(np.float32)
+
+
 # ----------------------------------------------------------------------------- bf16 packing
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     """Round float32 to bf16 (nearest, ties to even) and return the uint16 bit patterns."""
