@@ -189,7 +189,7 @@ def run_usp(args, w):
     import torch
 
     import ulysses_sequence_seq_gb300 as usp
-    from ulysses_sequence_seq_gb300.synth import seq_sharded_bits
+    from ulysses_sequence_seq_gb300.synth import packed_labels, seq_sharded_bits
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -311,6 +311,36 @@ def run_usp(args, w):
             rel_ms.append(tot)
     relayout_bytes = sum(2 * 2 * T * hh * D for _, hh in rel_bufs) * 2   # read + write, both directions
 
+    # ---- sample and loss bookkeeping on the device: cu_seqlens -> position_ids ->
+    # cu_seqlens (padded to 2x the samples), label shift with per-rank good-token counts,
+    # weighted loss over the sp ranks; L2 flushed before each pass
+    max_seqs = 2 * w.num_seqs
+    pos_d = torch.empty(T, dtype=torch.int64, device=dev)
+    cu_pad = torch.empty(max_seqs + 1, dtype=torch.int32, device=dev)
+    nseq_d = torch.empty(1, dtype=torch.int32, device=dev)
+    pws_bytes = usp.position_ids_workspace_size(T)
+    pws = torch.zeros(pws_bytes, dtype=torch.uint8, device=dev)
+    labels_d = torch.from_numpy(packed_labels(w.cu_seqlens(), vocab=32000, seed=1000 * w.index + 50)).to(dev)
+    shifted_d = torch.empty(T, dtype=torch.int64, device=dev)
+    good_d = torch.empty(sp, dtype=torch.int64, device=dev)
+    rank_loss_d = torch.rand(sp, dtype=torch.float32, device=dev) * 4
+    loss_d = torch.empty((), dtype=torch.float32, device=dev)
+    book_ms = []
+    for it in range(args.steps + 1):
+        flush.zero_()
+        r0.record(stream)
+        usp.cu_seqlens_to_position_ids(cu, w.num_seqs, T, pos_d)
+        usp.position_ids_to_cu_seqlens(pos_d, T, cu_pad, max_seqs, nseq_d, pws, pws_bytes)
+        usp.shift_labels(labels_d, cu_pad, max_seqs, T, sp, shifted_d, good_d)
+        usp.sp_weighted_loss(rank_loss_d, good_d, sp, loss_d)
+        r1.record(stream)
+        r1.synchronize()
+        if it > 0:
+            book_ms.append(r0.elapsed_time(r1))
+    if usp.get_device_status(pws) != usp.USP_OK or int(nseq_d.item()) != w.num_seqs:
+        raise RuntimeError("position_ids -> cu_seqlens failed on the bench workload")
+    book_bytes = 8 * T + 8 * T + 16 * T     # write ids; read ids; read labels + write shifted
+
     # ---- end to end through the public API: pinned host inputs in, results back to host
     out_host = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
                 for t in (layer.o_seq, layer.dq_seq, layer.dk_seq, layer.dv_seq)]
@@ -383,6 +413,11 @@ def run_usp(args, w):
                      "what": "usp_seq_to_head on Q, K, V, dO back to back, then usp_head_to_seq on the four; "
                              "L2 flushed before each batch",
                      "ms": statistics.mean(rel_ms)},
+        "sp_bookkeeping": {"ms": statistics.mean(book_ms), "bytes": book_bytes,
+                           "achieved_gbs": book_bytes / (statistics.mean(book_ms) * 1e-3) / 1e9,
+                           "what": "usp_cu_seqlens_to_position_ids, usp_position_ids_to_cu_seqlens (padded), "
+                                   "usp_shift_labels (+ good tokens per rank), usp_sp_weighted_loss; "
+                                   "7 launches, L2 flushed before each pass; latency-bound at this T"},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,

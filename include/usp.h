@@ -224,6 +224,93 @@ usp_status usp_attn_fwd_varlen_noalloc(const void* q, const void* k, const void*
                                        int hkv, int head_dim, float softmax_scale, int causal, int32_t* status,
                                        void* stream);
 
+/* ------------------------------------------------------------------------------
+ * Sample boundaries, label shift and loss over the SP ranks.
+ *
+ * Bookkeeping that the HF Transformers "Ulysses sequence parallelism" guide
+ * (section on the Accelerate configuration file) lists around the attention:
+ * position_ids generation, the label shift and the loss aggregation across SP
+ * ranks. The jianying88 article on DeepSpeed Ulysses in Transformers (section
+ * "3. 跨 rank 的加权 loss 聚合") defines the aggregation. Readings where the
+ * pages leave a step open: position ids count up from 0 inside each packed
+ * sample; a token's shifted label is the next token's label inside its sample
+ * and -100 on the sample's last token; the weighted mean over zero good tokens
+ * is 0. On one device the seq-sharded [sp][T/sp] buffers of all ranks are one
+ * contiguous [T] buffer, so every call below takes all T tokens at once.
+ * ------------------------------------------------------------------------------ */
+
+/* Bytes of workspace usp_position_ids_to_cu_seqlens needs for total_tokens
+ * (256 + 4 per 2048 tokens); 0 when total_tokens < 0. */
+size_t usp_position_ids_workspace_size(int64_t total_tokens);
+
+/*
+ * usp_position_ids_to_cu_seqlens -- sample boundaries of a packed row from its
+ * position ids, on the device, so that the attention can follow without a host
+ * synchronisation.
+ *   position_ids : int64[T] device (T = total_tokens < 2^31). A sample starts
+ *                  wherever the id is 0; elsewhere the id must be the previous
+ *                  token's id + 1.
+ *   cu_seqlens   : int32[max_seqs + 1] device, written: the n sample starts,
+ *                  then T in cu_seqlens[n..max_seqs]. Padding entries describe
+ *                  empty samples, so the attention calls accept the array with
+ *                  num_seqs = max_seqs.
+ *   num_seqs     : int32 device (may be NULL): receives n.
+ *   workspace    : device, 16-byte aligned, usp_position_ids_workspace_size
+ *                  bytes; its first int32 is the status word read by
+ *                  usp_get_device_status.
+ *   All work is enqueued on `stream`; nothing is allocated.
+ * Errors: USP_ERR_INVALID_ARG (NULL or misaligned pointer, T < 0 or >= 2^31,
+ *   max_seqs < 1); USP_ERR_WORKSPACE. On the device: malformed ids set the status
+ *   word to USP_ERR_DEVICE_CHECK and leave cu_seqlens and num_seqs unwritten; more
+ *   than max_seqs samples set USP_ERR_DEVICE_CHECK, leave cu_seqlens unwritten and
+ *   still write n to num_seqs. T = 0 writes cu_seqlens = 0 and n = 0.
+ */
+usp_status usp_position_ids_to_cu_seqlens(const int64_t* position_ids, int64_t total_tokens, int32_t* cu_seqlens,
+                                          int max_seqs, int32_t* num_seqs, void* workspace, size_t workspace_bytes,
+                                          void* stream);
+
+/*
+ * usp_cu_seqlens_to_position_ids -- position id of every token (its offset in its
+ * own sample): position_ids[t] = t - cu_seqlens[b] for the sample b holding t.
+ *   cu_seqlens   : int32[num_seqs + 1] device, non-decreasing, 0 first, T last
+ *                  (empty samples allowed). A malformed array gives unspecified
+ *                  ids, but every access stays in bounds.
+ *   position_ids : int64[T] device, written.
+ * Errors: USP_ERR_INVALID_ARG (NULL/misaligned pointer, num_seqs < 1 when T > 0,
+ *   T < 0 or >= 2^31). T = 0 does nothing.
+ */
+usp_status usp_cu_seqlens_to_position_ids(const int32_t* cu_seqlens, int num_seqs, int64_t total_tokens,
+                                          int64_t* position_ids, void* stream);
+
+/*
+ * usp_shift_labels -- labels shifted inside packed samples, and each SP rank's
+ * count of good tokens.
+ *   labels       : int64[T] device (-100 = ignored).
+ *   cu_seqlens   : int32[num_seqs + 1] device, as for the attention calls.
+ *   shift_labels : int64[T] device, written: shift[t] = labels[t+1] when t+1 is in
+ *                  t's sample, else -100. Must not overlap `labels`.
+ *   good_tokens  : int64[sp] device, written: good_tokens[r] = number of t in rank
+ *                  r's shard [r*T/sp, (r+1)*T/sp) with shift[t] != -100.
+ * Errors: USP_ERR_INVALID_ARG (NULL/misaligned pointer, overlap, sp < 1, T % sp,
+ *   num_seqs < 1 when T > 0, T >= 2^31). A malformed cu_seqlens gives unspecified
+ *   results with every access in bounds.
+ */
+usp_status usp_shift_labels(const int64_t* labels, const int32_t* cu_seqlens, int num_seqs, int64_t total_tokens,
+                            int sp, int64_t* shift_labels, int64_t* good_tokens, void* stream);
+
+/*
+ * usp_sp_weighted_loss -- the loss of the whole SP group from each rank's loss and
+ * good-token count: sum over ranks with good_tokens[r] > 0 of
+ * rank_loss[r] * good_tokens[r], divided by the sum of good_tokens; 0 when no rank
+ * has a good token. Ranks without good tokens are left out, so their loss (NaN for
+ * a mean over nothing) does not reach the result. Accumulated in float64.
+ *   rank_loss   : float32[sp] device;  good_tokens : int64[sp] device;
+ *   loss        : float32 device, written.
+ * Errors: USP_ERR_INVALID_ARG (NULL/misaligned pointer, sp < 1).
+ */
+usp_status usp_sp_weighted_loss(const float* rank_loss, const int64_t* good_tokens, int sp, float* loss,
+                                void* stream);
+
 /* Human-readable name of a status code (static string). */
 const char* usp_status_string(usp_status status);
 

@@ -9,7 +9,11 @@ device buffer:
 * :func:`attn_fwd_varlen` / :func:`attn_bwd_varlen` -- causal, packed-sample
   (cu_seqlens) softmax attention forward and backward on tcgen05 tensor cores;
 * :func:`ulysses_attn_fwd` / :func:`ulysses_attn_bwd` -- the same with both layout
-  swaps fused into the attention kernels (seq-sharded tensors in and out).
+  swaps fused into the attention kernels (seq-sharded tensors in and out);
+* :func:`position_ids_to_cu_seqlens`, :func:`cu_seqlens_to_position_ids`,
+  :func:`shift_labels`, :func:`sp_weighted_loss` -- the sample and loss bookkeeping
+  around the attention, on the device; :mod:`.sp_group` gathers each rank's loss
+  and good-token count over a real SP process group.
 
 :class:`UlyssesAttention` chains them into the layer-level step: the seq-sharded
 Q, K, V of all ranks in, the seq-sharded attention output out, and the same in
@@ -20,12 +24,16 @@ from __future__ import annotations
 import math
 
 from ._lib import (USP_BF16, USP_FP16, USP_FP32, USP_OK, UspError, attn_bwd_varlen, attn_fwd_varlen,  # noqa: F401
-                   attn_workspace_size, debug_wait_timeout, get_device_status, head_to_seq, load, seq_to_head,
-                   status_string, ulysses_attn_bwd, ulysses_attn_fwd)
+                   attn_workspace_size, cu_seqlens_to_position_ids, debug_wait_timeout, get_device_status,
+                   head_to_seq, load, position_ids_to_cu_seqlens, position_ids_workspace_size, seq_to_head,
+                   shift_labels, sp_weighted_loss, status_string, ulysses_attn_bwd, ulysses_attn_fwd)
+from .sp_group import gather_loss_and_good, sp_group_loss  # noqa: F401
 
 __all__ = [
     "seq_to_head", "head_to_seq", "attn_fwd_varlen", "attn_bwd_varlen", "ulysses_attn_fwd", "ulysses_attn_bwd",
     "attn_workspace_size", "get_device_status", "status_string", "UspError", "UlyssesAttention", "load",
+    "position_ids_to_cu_seqlens", "position_ids_workspace_size", "cu_seqlens_to_position_ids", "shift_labels",
+    "sp_weighted_loss", "gather_loss_and_good", "sp_group_loss",
 ]
 
 

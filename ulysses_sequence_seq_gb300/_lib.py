@@ -37,6 +37,11 @@ EXPORTED = (
     "usp_attn_fwd_varlen_noalloc",
     "usp_ulysses_attn_fwd",
     "usp_ulysses_attn_bwd",
+    "usp_position_ids_workspace_size",
+    "usp_position_ids_to_cu_seqlens",
+    "usp_cu_seqlens_to_position_ids",
+    "usp_shift_labels",
+    "usp_sp_weighted_loss",
 )
 
 
@@ -78,9 +83,16 @@ def load(build_if_missing: bool = True):
     L.usp_attn_fwd_varlen_noalloc.argtypes = [P, P, P, P, P, P, I, I64, I, I, I, F, I, P, P]
     L.usp_ulysses_attn_fwd.argtypes = [P, P, P, P, P, P, I, I64, I, I, I, I, F, I, P, Z, P]
     L.usp_ulysses_attn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I, P, I, I64, I, I, I, I, F, I, P, Z, P]
+    L.usp_position_ids_workspace_size.argtypes = [I64]
+    L.usp_position_ids_workspace_size.restype = Z
+    L.usp_position_ids_to_cu_seqlens.argtypes = [P, I64, P, I, P, P, Z, P]
+    L.usp_cu_seqlens_to_position_ids.argtypes = [P, I, I64, P, P]
+    L.usp_shift_labels.argtypes = [P, P, I, I64, I, P, P, P]
+    L.usp_sp_weighted_loss.argtypes = [P, P, I, P, P]
     for name in ("usp_seq_to_head", "usp_head_to_seq", "usp_attn_fwd_varlen", "usp_attn_bwd_varlen",
                  "usp_get_device_status", "usp_debug_wait_timeout", "usp_attn_fwd_varlen_noalloc",
-                 "usp_ulysses_attn_fwd", "usp_ulysses_attn_bwd"):
+                 "usp_ulysses_attn_fwd", "usp_ulysses_attn_bwd", "usp_position_ids_to_cu_seqlens",
+                 "usp_cu_seqlens_to_position_ids", "usp_shift_labels", "usp_sp_weighted_loss"):
         getattr(L, name).restype = I
     _lib = L
     return _lib
@@ -190,6 +202,33 @@ def attn_fwd_varlen_noalloc(q, k, v, o, lse, cu_seqlens, num_seqs: int, total_to
         _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(cu_seqlens), int(num_seqs), int(total_tokens),
         int(hq), int(hkv), int(head_dim), float(softmax_scale), int(bool(causal)), _ptr(status),
         _stream(stream)))
+
+
+def position_ids_workspace_size(total_tokens: int) -> int:
+    return int(load().usp_position_ids_workspace_size(int(total_tokens)))
+
+
+def position_ids_to_cu_seqlens(position_ids, total_tokens: int, cu_seqlens, max_seqs: int, num_seqs, workspace,
+                               ws_bytes: int, stream=None):
+    _check("usp_position_ids_to_cu_seqlens", load().usp_position_ids_to_cu_seqlens(
+        _ptr(position_ids), int(total_tokens), _ptr(cu_seqlens), int(max_seqs), _ptr(num_seqs), _ptr(workspace),
+        int(ws_bytes), _stream(stream)))
+
+
+def cu_seqlens_to_position_ids(cu_seqlens, num_seqs: int, total_tokens: int, position_ids, stream=None):
+    _check("usp_cu_seqlens_to_position_ids", load().usp_cu_seqlens_to_position_ids(
+        _ptr(cu_seqlens), int(num_seqs), int(total_tokens), _ptr(position_ids), _stream(stream)))
+
+
+def shift_labels(labels, cu_seqlens, num_seqs: int, total_tokens: int, sp: int, shifted, good_tokens, stream=None):
+    _check("usp_shift_labels", load().usp_shift_labels(
+        _ptr(labels), _ptr(cu_seqlens), int(num_seqs), int(total_tokens), int(sp), _ptr(shifted),
+        _ptr(good_tokens), _stream(stream)))
+
+
+def sp_weighted_loss(rank_loss, good_tokens, sp: int, loss, stream=None):
+    _check("usp_sp_weighted_loss", load().usp_sp_weighted_loss(
+        _ptr(rank_loss), _ptr(good_tokens), int(sp), _ptr(loss), _stream(stream)))
 
 
 def get_device_status(workspace, stream=None) -> int:
