@@ -48,7 +48,7 @@ struct BwdArgs {
 };
 
 cudaError_t launch_attn_bwd(int head_dim, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                            const CUtensorMap& dout, const BwdArgs& a, int grid, cudaStream_t s);
+                            const CUtensorMap& dout, const CUtensorMap& dq, const BwdArgs& a, int grid, cudaStream_t s);
 
 // Delta_i = dO_i . O_i (fp32, [hq][T]) for every query row, and zeroes the dQ accumulator.
 // o / dout are head-major or token-major (token_major); the accumulator is head-major
@@ -63,6 +63,9 @@ cudaError_t launch_dq_convert(const float* dq_acc, __nv_bfloat16* dq, int64_t T,
 // TMA tensor map over a bf16 activation, head-major [heads][T][D] or token-major
 // [T][heads][D]: boxes of 64 columns x 128 rows of one head, 128-byte swizzle.
 bool make_activation_map(CUtensorMap* map, const void* base, int64_t T, int heads, int D, int token_major);
+// fp32 dQ accumulator ([heads][T][D] or [T][heads][D]) in 32-column x 32-row boxes with the
+// 128-byte swizzle, the target of the backward's bulk tensor reductions.
+bool make_dq_accum_map(CUtensorMap* map, float* base, int64_t T, int heads, int D, int token_major);
 
 // Records `code` in the status word after a kernel that waits on an mbarrier nothing arrives on.
 cudaError_t launch_debug_timeout(WsHeader* hdr, uint64_t limit_ns, cudaStream_t s);

@@ -8,23 +8,28 @@
 // One CTA owns a 128-row key/value tile of one sample and one key/value head and
 // walks every query block that sees it (from the diagonal on when causal), for all
 // query heads of its GQA group, so dK and dV accumulate in tensor memory and are
-// written once. dQ partial tiles are added into an fp32 accumulator with vector
-// atomics. Everything is computed transposed (key rows on TMEM lanes) so that P^T
-// and dS^T feed the dV and dK MMAs straight from TMEM.
+// written once. dQ partial tiles are added into an fp32 accumulator by TMA bulk
+// reductions. Everything is computed transposed (key rows on TMEM lanes) so that P^T
+// feeds the dV MMA straight from TMEM.
+//
+// Each query block is processed as two independent halves of 64 query columns: S, dP,
+// dV and dK are issued per half, so the tensor cores run one half's MMAs while the
+// warps of the other half compute P or dS. Only dQ waits for both halves.
 //
 // Warp roles (448 threads):
-//   warps 0-3  compute group A: thread = key row, query columns 0-63 of the block
-//   warps 4-7  compute group B: thread = key row, query columns 64-127
-//              (P^T, dS^T; at the end group A writes dV and group B writes dK)
-//   warps 8-11 dQ group: thread = query row; drains the dQ tile, transposed through
-//              the idle dS buffer so that each vector atomic covers whole 128-byte lines
-//   warp  12   TMA producer: K, V once, then Q / dO blocks into a 2-stage ring
+//   warps 0-3  compute half A: thread = key row, query columns 0-63 of the block
+//   warps 4-7  compute half B: thread = key row, query columns 64-127
+//              (at the end half A writes dV and half B writes dK)
+//   warps 8-11 dQ group: thread = query row; moves each dQ tile from TMEM into its own
+//              128-byte-swizzled staging buffers and adds it to the accumulator with
+//              bulk tensor reductions (whole 128-byte lines, no per-thread atomics)
+//   warp  12   TMA producer: K, V once, then Q blocks into a 2-stage ring, dO blocks
+//              into one buffer (dO is consumed early in a step)
 //   warp  13   MMA issuer and TMEM owner
-// Tensor memory: [0,128) holds S^T, then bf16 P^T, then dP^T of one step; the dQ
-// tile has its own columns [128,256), so draining it overlaps the next step; dV
-// [256,256+D), dK [384,384+D). Group A keeps its bf16 P^T in columns [0,32) and
-// group B in [64,96), so neither overwrites scores the other still reads. dS lives
-// only in shared memory, where dK reads it K-major and dQ MN-major.
+// Tensor memory: [0,128) holds S^T, then bf16 P^T, then dP^T: half A in [0,64) and half
+// B in [64,128), each with its bf16 P^T at the start of its range; dQ [128,256); dV
+// [256,256+D); dK [384,384+D). dS lives only in shared memory, where dK reads it K-major
+// and dQ MN-major.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -39,17 +44,13 @@ namespace {
 
 using namespace ptx;
 
-// The query columns of a block are split over kGroups compute warpgroups (thread = key
-// row, kGroupCols columns each); more, narrower groups give the latency-bound exp / dS
-// arithmetic more warps to hide behind.
-constexpr int kGroups = 2;
-constexpr int kGroupCols = kBlockN / kGroups;
-constexpr int kComputeWarps = 4 * kGroups;
+constexpr int kHalfCols = kBlockN / 2;           // query columns per half
+constexpr int kComputeWarps = 8;                 // two warpgroups, one per half
 constexpr int kDqWarp0 = kComputeWarps;          // 4 warps
 constexpr int kProducerWarp = kComputeWarps + 4;
 constexpr int kMmaWarp = kComputeWarps + 5;
 constexpr int kBwdThreads = 32 * (kComputeWarps + 6);
-static_assert(kGroupCols % 32 == 0, "a compute group covers whole 32-column TMEM loads");
+constexpr int kDqChunkBytes = 32 * 32 * 4;       // one warp's 32 query rows x 32 fp32 columns
 
 template <int D>
 struct BwdSmem {
@@ -58,26 +59,28 @@ struct BwdSmem {
     static constexpr int kK = 0;
     static constexpr int kV = kTileBytes;
     static constexpr int kQ = 2 * kTileBytes;        // + stage * kTileBytes
-    static constexpr int kDO = 4 * kTileBytes;       // + stage * kTileBytes
-    static constexpr int kDS = 6 * kTileBytes;       // [128 key rows][128 query cols] bf16, two 64-col panels
-    static constexpr int kLse = kDS + kTileM * kBlockN * 2;  // fp32[2][64]: -lse (log2 units), one half per group
-    static constexpr int kDelta = kLse + 512;                // fp32[2][64]: -Delta
+    static constexpr int kDO = 4 * kTileBytes;
+    static constexpr int kDS = 5 * kTileBytes;       // [128 key rows][128 query cols] bf16, two 64-col panels
+    static constexpr int kStage = kDS + kTileM * kBlockN * 2;   // dQ staging: 4 warps x 2 chunks
+    static constexpr int kLse = kStage + 4 * 2 * kDqChunkBytes;  // fp32[2][64]: -lse (log2 units), one half each
+    static constexpr int kDelta = kLse + 512;                   // fp32[2][64]: -Delta
     static constexpr int kBars = kDelta + 512;
-    static constexpr int bKvFull = 0, bQFull = 1, bDoFull = 3, bQEmpty = 5, bSFull = 7, bDpFull = 8, bPFull = 9,
-                         bDsFull = 10, bDqFull = 11, bDqEmpty = 12, bAccFull = 13, bDrain = 14, bStageFree = 15,
-                         bDsFree = 16, kNumBars = 17;
+    static constexpr int bKvFull = 0, bQFull = 1, bQEmpty = 3, bDoFull = 5, bDoEmpty = 6, bSFull = 7, bPFull = 9,
+                         bDpFull = 11, bDsFull = 13, bDqFull = 15, bDqEmpty = 16, bAccFull = 17, bDrain = 18,
+                         kNumBars = 19;
     static constexpr int kTmemSlot = kBars + 8 * kNumBars;
     static constexpr int kAbort = kTmemSlot + 8;
     static constexpr int kBytes = kAbort + 8;
     static constexpr int kAlloc = kBytes + 1024;
 };
 static_assert(BwdSmem<128>::kAlloc <= 232448, "backward shared memory exceeds the per-CTA limit");
+static_assert(BwdSmem<128>::kStage % 1024 == 0, "dQ staging must keep the 128-byte swizzle atoms aligned");
 
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                    const BwdArgs a) {
+                    const __grid_constant__ CUtensorMap tmDQ, const BwdArgs a) {
     using L = BwdSmem<D>;
     const int count = a.hdr->bwd_count;
     if ((int)blockIdx.x >= count) return;
@@ -111,17 +114,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(&bars[L::bKvFull], 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars[L::bQFull + i], 1);
-            mbar_init(&bars[L::bDoFull + i], 1);
             mbar_init(&bars[L::bQEmpty + i], 1);
+            mbar_init(&bars[L::bSFull + i], 1);
+            mbar_init(&bars[L::bPFull + i], 4);
+            mbar_init(&bars[L::bDpFull + i], 1);
+            mbar_init(&bars[L::bDsFull + i], 4);
         }
-        mbar_init(&bars[L::bSFull], 1);
-        mbar_init(&bars[L::bDpFull], 1);
-        mbar_init(&bars[L::bPFull], kComputeWarps);
-        mbar_init(&bars[L::bDsFull], kComputeWarps);
+        mbar_init(&bars[L::bDoFull], 1);
+        mbar_init(&bars[L::bDoEmpty], 1);
         mbar_init(&bars[L::bDqFull], 1);
         mbar_init(&bars[L::bDqEmpty], 4);
-        mbar_init(&bars[L::bStageFree], 4);
-        mbar_init(&bars[L::bDsFree], 1);
         mbar_init(&bars[L::bAccFull], 1);
         mbar_init(&bars[L::bDrain], 1);
         *abort_flag = 0;
@@ -147,35 +149,43 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             int issued = 0;
             for (int k = 0; k < nsteps; ++k) {
                 const int st = k & 1;
-                if (k >= 2 && !mbar_wait(&bars[L::bQEmpty + st], ((k >> 1) - 1) & 1, abort_flag, kWaitLimitNs))
-                    break;
                 const int h = g * G + k / nq;
                 const int q0 = s + (i0 + k % nq) * kTileM;
+                if (k >= 2 && !mbar_wait(&bars[L::bQEmpty + st], ((k >> 1) - 1) & 1, abort_flag, kWaitLimitNs))
+                    break;
                 mbar_arrive_expect_tx(&bars[L::bQFull + st], L::kTileBytes);
                 for (int p = 0; p < L::kPanels; ++p)
                     tma_load_rows(sm + L::kQ + st * L::kTileBytes + p * (kTileM * 128), &tmQ, &bars[L::bQFull + st],
                                   p * 64, q0, h, a.token_major);
-                mbar_arrive_expect_tx(&bars[L::bDoFull + st], L::kTileBytes);
+                // the single dO buffer is free once both halves' dV and dP of the previous block are done
+                if (k >= 1 && !mbar_wait(&bars[L::bDoEmpty], (k - 1) & 1, abort_flag, kWaitLimitNs)) {
+                    issued = -(k + 1);   // Q(k) is in flight, dO(k) is not
+                    break;
+                }
+                mbar_arrive_expect_tx(&bars[L::bDoFull], L::kTileBytes);
                 for (int p = 0; p < L::kPanels; ++p)
-                    tma_load_rows(sm + L::kDO + st * L::kTileBytes + p * (kTileM * 128), &tmDO,
-                                  &bars[L::bDoFull + st], p * 64, q0, h, a.token_major);
+                    tma_load_rows(sm + L::kDO + p * (kTileM * 128), &tmDO, &bars[L::bDoFull], p * 64, q0, h,
+                                  a.token_major);
                 issued = k + 1;
             }
+            // let every copy in flight land before the CTA can exit
             mbar_wait_drain(&bars[L::bKvFull], 0, kDrainLimitNs);
-            for (int k = issued - 2 < 0 ? 0 : issued - 2; k < issued; ++k) {
+            const int q_issued = issued < 0 ? -issued : issued;
+            const int do_issued = issued < 0 ? -issued - 1 : issued;
+            for (int k = q_issued - 2 < 0 ? 0 : q_issued - 2; k < q_issued; ++k)
                 mbar_wait_drain(&bars[L::bQFull + (k & 1)], (k >> 1) & 1, kDrainLimitNs);
-                mbar_wait_drain(&bars[L::bDoFull + (k & 1)], (k >> 1) & 1, kDrainLimitNs);
-            }
+            if (do_issued > 0) mbar_wait_drain(&bars[L::bDoFull], (do_issued - 1) & 1, kDrainLimitNs);
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idT = idesc_bf16_f32(kBlockN, kTileM, false, false);  // S^T, dP^T
-            constexpr uint32_t idDv = idesc_bf16_f32(kBlockN, D, false, true);      // dV (A in TMEM)
-            constexpr uint32_t idDk = idesc_bf16_f32(kBlockN, D, false, true);      // dK (A = dS, K-major)
-            constexpr uint32_t idDq = idesc_bf16_f32(kTileM, D, true, true);        // dQ (A, B MN-major)
-            // 64-bit shared-memory descriptors are built once; a K step only adds a constant to
-            // the start-address field (addresses stay below 2^18, so the field never carries).
+            constexpr uint32_t idH = idesc_bf16_f32(kBlockN, kHalfCols, false, false);  // S^T, dP^T of one half
+            constexpr uint32_t idDv = idesc_bf16_f32(kBlockN, D, false, true);         // dV (A in TMEM)
+            constexpr uint32_t idDk = idesc_bf16_f32(kBlockN, D, false, true);         // dK (A = dS, K-major)
+            constexpr uint32_t idDq = idesc_bf16_f32(kTileM, D, true, true);           // dQ (A, B MN-major)
+            // 64-bit shared-memory descriptors are built once; a K step or a row offset only
+            // adds a constant to the start-address field (addresses stay below 2^18, so the
+            // field never carries).
             constexpr uint32_t kPanel = kTileM * 128;  // bytes of one 64-column panel of a tile
             const uint32_t sK = smem_u32(sm + L::kK), sV = smem_u32(sm + L::kV);
             const uint32_t sQ = smem_u32(sm + L::kQ), sDO = smem_u32(sm + L::kDO), sDS = smem_u32(sm + L::kDS);
@@ -184,89 +194,102 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const uint64_t dQ_kmaj = sdesc_sw128(sQ, 0, 1024), dQ_mn = sdesc_sw128(sQ, kPanel, 1024);
             const uint64_t dDO_kmaj = sdesc_sw128(sDO, 0, 1024), dDO_mn = sdesc_sw128(sDO, kPanel, 1024);
             const uint64_t dDS_kmaj = sdesc_sw128(sDS, 0, 1024), dDS_mn = sdesc_sw128(sDS, kBlockN * 128, 1024);
-            constexpr uint64_t kStage = (uint64_t)(L::kTileBytes >> 4);
+            constexpr uint64_t kStageQ = (uint64_t)(L::kTileBytes >> 4);
+            constexpr uint64_t kHalfRows = (uint64_t)((kHalfCols * 128) >> 4);   // 64 rows of a K-major tile
             const uint32_t tS = tbase, tDQ = tbase + 128, tDV = tbase + 256, tDK = tbase + 384;
-            auto issue_t = [&](uint32_t d, uint64_t a_desc, uint64_t b_desc) {  // d = A . B^T, both K-major
+            // d[128 x 64] = A . B^T over K = D, both operands K-major (S^T and dP^T of one half)
+            auto issue_half = [&](uint32_t d, uint64_t a_desc, uint64_t b_desc) {
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t off = (uint64_t)((((kk / 4) * kPanel) + (kk % 4) * 32) >> 4);
-                    mma_ss(d, a_desc + off, b_desc + off, idT, kk > 0);
+                    mma_ss(d, a_desc + off, b_desc + off, idH, kk > 0);
                 }
             };
             bool ok = mbar_wait(&bars[L::bKvFull], 0, abort_flag, kWaitLimitNs);
             if (ok) ok = mbar_wait(&bars[L::bQFull], 0, abort_flag, kWaitLimitNs);
             if (ok) {
                 tc_fence_after();
-                issue_t(tS, dK_kmaj, dQ_kmaj);
-                mma_commit(&bars[L::bSFull]);
+                for (int hf = 0; hf < 2; ++hf) {
+                    issue_half(tS + hf * kHalfCols, dK_kmaj, dQ_kmaj + hf * kHalfRows);
+                    mma_commit(&bars[L::bSFull + hf]);
+                }
             }
-            // Per step k, with columns [0,128) holding S^T, then P^T, then dP^T:
-            //   dV += P^T.dO, dP^T = V.dO^T, dQ = dS.K -> [128,256), S^T(k+1) = K.Q(k+1)^T, dK += dS^T.Q
-            // dQ goes first so its drain (the longest tail) starts early; S^T of the next block
-            // goes before dK so the compute groups' exponentials overlap dK; the dQ tile has
-            // its own columns, so draining it overlaps the next step.
+            // Per step k and half hf: dV += P^T.dO, dP^T = V.dO^T (after P), then S^T of the
+            // next block and dK += dS^T.Q (after dS); dQ = dS.K once both halves wrote dS. The
+            // tensor cores run in issue order, so the commit that releases a half's dP^T also
+            // covers the previous block's dQ and dK reads of the dS buffer that half rewrites.
             for (int k = 0; ok && k < nsteps; ++k) {
                 const int st = k & 1;
-                const uint64_t q_mn = dQ_mn + st * kStage;
-                if (!mbar_wait(&bars[L::bPFull], k & 1, abort_flag, kWaitLimitNs)) break;
-                if (!mbar_wait(&bars[L::bDoFull + st], (k >> 1) & 1, abort_flag, kWaitLimitNs)) break;
-                tc_fence_after();
-                // each group's bf16 P^T sits at the start of its own kGroupCols-wide column range
+                if (!mbar_wait(&bars[L::bDoFull], k & 1, abort_flag, kWaitLimitNs)) break;
+                for (int hf = 0; ok && hf < 2; ++hf) {
+                    if (!mbar_wait(&bars[L::bPFull + hf], k & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
+                    tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < kTileM / 16; ++kk)  // dV += P^T . dO
-                    mma_ts(tDV, tS + ((16 * kk) / kGroupCols) * kGroupCols + ((16 * kk) % kGroupCols) / 2,
-                           dDO_mn + st * kStage + (uint64_t)((kk * 2048) >> 4), idDv, (k > 0 || kk > 0) ? 1u : 0u);
-                issue_t(tS, dV_kmaj, dDO_kmaj + st * kStage);  // dP^T, after dV has read P^T
-                mma_commit(&bars[L::bDpFull]);
-                if (!mbar_wait(&bars[L::bDsFull], k & 1, abort_flag, kWaitLimitNs)) break;
+                    for (int kk = 0; kk < kHalfCols / 16; ++kk)  // dV += P^T . dO over this half's queries
+                        mma_ts(tDV, tS + hf * kHalfCols + 8 * kk,
+                               dDO_mn + (uint64_t)((((hf * kHalfCols) / 16 + kk) * 2048) >> 4), idDv,
+                               (k > 0 || hf > 0 || kk > 0) ? 1u : 0u);
+                    issue_half(tS + hf * kHalfCols, dV_kmaj, dDO_kmaj + hf * kHalfRows);  // dP^T, after dV read P^T
+                    mma_commit(&bars[L::bDpFull + hf]);
+                }
+                if (!ok) break;
+                mma_commit(&bars[L::bDoEmpty]);
+                for (int hf = 0; ok && hf < 2; ++hf) {
+                    if (!mbar_wait(&bars[L::bDsFull + hf], k & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
+                    tc_fence_after();
+                    if (k + 1 < nsteps) {  // S^T of the next block first: it heads this half's next step
+                        const int st1 = st ^ 1;
+                        if (hf == 0 &&
+                            !mbar_wait(&bars[L::bQFull + st1], ((k + 1) >> 1) & 1, abort_flag, kWaitLimitNs)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        issue_half(tS + hf * kHalfCols, dK_kmaj, dQ_kmaj + st1 * kStageQ + hf * kHalfRows);
+                        mma_commit(&bars[L::bSFull + hf]);
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < kHalfCols / 16; ++kk)  // dK += dS^T . Q over this half's queries
+                        mma_ss(tDK, dDS_kmaj + (uint64_t)((hf * kBlockN * 128 + kk * 32) >> 4),
+                               dQ_mn + st * kStageQ + (uint64_t)((((hf * kHalfCols) / 16 + kk) * 2048) >> 4), idDk,
+                               (k > 0 || hf > 0 || kk > 0) ? 1u : 0u);
+                }
+                if (!ok) break;
+                mma_commit(&bars[L::bQEmpty + st]);
                 if (k > 0 && !mbar_wait(&bars[L::bDqEmpty], (k - 1) & 1, abort_flag, kWaitLimitNs)) break;
                 tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < kBlockN / 16; ++kk)  // dQ = dS . K   (first: its drain is the longest tail)
+                for (int kk = 0; kk < kBlockN / 16; ++kk)  // dQ = dS . K
                     mma_ss(tDQ, dDS_mn + (uint64_t)((kk * 2048) >> 4), dK_mn + (uint64_t)((kk * 2048) >> 4), idDq,
                            kk > 0 ? 1u : 0u);
                 mma_commit(&bars[L::bDqFull]);
-                if (k + 1 < nsteps) {
-                    const int st1 = (k + 1) & 1;
-                    if (!mbar_wait(&bars[L::bQFull + st1], ((k + 1) >> 1) & 1, abort_flag, kWaitLimitNs)) break;
-                    tc_fence_after();
-                    issue_t(tS, dK_kmaj, dQ_kmaj + st1 * kStage);
-                    mma_commit(&bars[L::bSFull]);
-                }
-#pragma unroll
-                for (int kk = 0; kk < kTileM / 16; ++kk) {  // dK += dS^T . Q  (dS read K-major from shared memory)
-                    const uint64_t off = (uint64_t)((((kk / 4) * (kBlockN * 128)) + (kk % 4) * 32) >> 4);
-                    mma_ss(tDK, dDS_kmaj + off, q_mn + (uint64_t)((kk * 2048) >> 4), idDk, (k > 0 || kk > 0) ? 1u : 0u);
-                }
-                mma_commit(&bars[L::bQEmpty + st]);
-                mma_commit(&bars[L::bDsFree]);  // dK and dQ have both read dS: the buffer may be reused
             }
             mma_commit(&bars[L::bAccFull]);
             mma_commit(&bars[L::bDrain]);
             mbar_wait_drain(&bars[L::bDrain], 0, kDrainLimitNs);
         }
     } else if (warp < kComputeWarps) {
-        // ------------------------------------------------------------------ compute groups (key rows)
-        const int grp = warp >> 2;          // query columns [grp * kGroupCols, (grp + 1) * kGroupCols)
+        // ------------------------------------------------------------------ compute halves (key rows)
+        const int grp = warp >> 2;          // query columns [grp * kHalfCols, (grp + 1) * kHalfCols)
         const int r = (warp & 3) * 32 + lane;
         const int kv = kv0 + r;
         const bool kv_ok = kv < e;
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-        // this group's columns of the S^T / P^T / dP^T region
-        const uint32_t tS = tbase + lane_off + grp * kGroupCols;
-        float* lse_g = lse_s + grp * kGroupCols;
-        float* delta_g = delta_s + grp * kGroupCols;
+        // this half's columns of the S^T / P^T / dP^T region
+        const uint32_t tS = tbase + lane_off + grp * kHalfCols;
+        float* lse_g = lse_s + grp * kHalfCols;
+        float* delta_g = delta_s + grp * kHalfCols;
         const float sl2 = a.scale_log2;
         const float sc = a.scale;
         bool ok = true;
-        // This group's query rows of a step, negated: -lse (log2 units) and -Delta; rows
+        // This half's query rows of a step, negated: -lse (log2 units) and -Delta; rows
         // outside the sample get -lse = -inf, which makes their P exactly zero. Loaded one
         // step ahead so that their global-memory latency stays off the critical path.
         float nl_next = -INFINITY, nd_next = 0.f;
         auto fetch_row_stats = [&](int k) {
             const int h = g * G + k / nq;
-            const int q = s + (i0 + k % nq) * kTileM + grp * kGroupCols + r;
-            const bool q_ok = r < kGroupCols && q < e;
+            const int q = s + (i0 + k % nq) * kTileM + grp * kHalfCols + r;
+            const bool q_ok = r < kHalfCols && q < e;
             nl_next = q_ok ? -__ldg(a.lse + (int64_t)h * a.T + q) * 1.4426950408889634f : -INFINITY;
             nd_next = q_ok ? -__ldg(a.delta + (int64_t)h * a.T + q) : 0.f;
         };
@@ -274,7 +297,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int k = 0; k < nsteps; ++k) {
             const int q0 = s + (i0 + k % nq) * kTileM;
             named_bar_sync(1 + grp, 128);
-            if (r < kGroupCols) {
+            if (r < kHalfCols) {
                 lse_g[r] = nl_next;
                 delta_g[r] = nd_next;
             }
@@ -283,14 +306,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             // element masks are only needed on the diagonal block and on the sample's ragged
             // last key tile; there query column c (of 128) is visible to key row r iff c >= r
             const bool mask_blk = (a.causal && q0 == kv0) || (kv0 + kBlockN > e);
-            const int vis_from = (a.causal && q0 == kv0) ? r - grp * kGroupCols : -1;
-            if (!mbar_wait(&bars[L::bSFull], k & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
+            const int vis_from = (a.causal && q0 == kv0) ? r - grp * kHalfCols : -1;
+            if (!mbar_wait(&bars[L::bSFull + grp], k & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
             tc_fence_after();
             // P for this row's query columns as packed bf16 pairs: the values the dV MMA
             // consumes, kept (half the registers of fp32) for dS
-            uint32_t pkall[kGroupCols / 2];
+            uint32_t pkall[kHalfCols / 2];
 #pragma unroll
-            for (int c = 0; c < kGroupCols / 32; ++c) {
+            for (int c = 0; c < kHalfCols / 32; ++c) {
                 uint32_t sr[32];
                 tmem_ld32(tS + 32 * c, sr);
                 float4 nl4[8];
@@ -319,16 +342,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[L::bPFull]);
+            if (lane == 0) mbar_arrive(&bars[L::bPFull + grp]);
 
-            if (!mbar_wait(&bars[L::bDpFull], k & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
-            // the dS buffer doubles as the dQ group's staging area for the previous step's tile
-            if (k > 0 && !mbar_wait(&bars[L::bStageFree], (k - 1) & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
+            // dP^T of this half; its commit also covers the previous block's reads of the dS buffer
+            if (!mbar_wait(&bars[L::bDpFull + grp], k & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
             tc_fence_after();
-            uint8_t* panel = sm + L::kDS + ((grp * kGroupCols) / 64) * (kBlockN * 128);
-            const uint32_t col_bytes = (uint32_t)((grp * kGroupCols) % 64) * 2;   // within the 64-column panel
+            uint8_t* panel = sm + L::kDS + grp * (kBlockN * 128);
 #pragma unroll
-            for (int c = 0; c < kGroupCols / 32; ++c) {
+            for (int c = 0; c < kHalfCols / 32; ++c) {
                 uint32_t dr[32];
                 tmem_ld32(tS + 32 * c, dr);
                 float4 nd4[8];
@@ -350,7 +371,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 // row r of the [key][query] dS operand (read K-major by dK, MN-major by dQ)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const uint32_t bytecol = col_bytes + (uint32_t)(c * 64 + j * 16);
+                    const uint32_t bytecol = (uint32_t)(c * 64 + j * 16);
                     *(uint4*)(panel + sw128_offset(r, bytecol)) =
                         make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
                 }
@@ -358,19 +379,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[L::bDsFull]);
+            if (lane == 0) mbar_arrive(&bars[L::bDsFull + grp]);
         }
         if (ok && mbar_wait(&bars[L::bAccFull], 0, abort_flag, kWaitLimitNs)) {
             tc_fence_after();
-            // the groups split dV (first half of the groups) and dK (second half) by columns
-            constexpr int kPerHalf = kGroups / 2;
-            const int which = grp / kPerHalf;                 // 0: dV, 1: dK
-            const int c_begin = (grp % kPerHalf) * (D / kPerHalf), c_end = c_begin + D / kPerHalf;
+            // half A writes dV, half B writes dK
             const int64_t row = act_row(g, kv, a.T, a.hkv, a.token_major);
-            const uint32_t src = tbase + lane_off + (which ? 384 : 256);
-            void* dst_base = which ? a.dk : a.dv;
+            const uint32_t src = tbase + lane_off + (grp ? 384 : 256);
+            void* dst_base = grp ? a.dk : a.dv;
 #pragma unroll 1
-            for (int c = c_begin; c < c_end; c += 32) {
+            for (int c = 0; c < D; c += 32) {
                 uint32_t o[32];
                 tmem_ld32(src + c, o);
                 tmem_ld_wait(o);
@@ -394,29 +412,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
     } else if (warp < kDqWarp0 + 4) {
         // ------------------------------------------------------------------ dQ group (query rows)
-        // Once the dQ and dK MMAs of a step have read dS, the dS buffer is idle until the
-        // compute groups write the next one (they wait for this group), so each warp
-        // borrows 8 KB of it to transpose its 32 rows x 32 columns chunks: a warp-wide
-        // vector atomic then covers 4 rows x 128 contiguous bytes instead of 32 x 16 bytes.
+        // Each warp owns 32 query rows of the tile: per 32-column chunk it loads 32 x 32 fp32
+        // from TMEM, writes them to one of its two staging buffers in the 128-byte swizzle the
+        // dQ tensor map expects, and one lane hands the box to the TMA unit, which adds it to
+        // the accumulator at L2. Query rows past the sample end carry exact zeros (their P is
+        // zero), so whole boxes can be added; rows past the tensor end are skipped by the TMA.
         const int w4 = warp - kDqWarp0;
         const uint32_t tDQ = tbase + ((uint32_t)(w4 * 32) << 16) + 128;
-        uint8_t* stage = sm + L::kDS + w4 * 8192;
-        const int sub_row = lane >> 3;   // 0..3: row within a group of four
-        const int chunk = lane & 7;      // 16-byte chunk within a 128-byte row segment
+        uint8_t* stage = sm + L::kStage + w4 * (2 * kDqChunkBytes);
+        if (lane == 0) prefetch_tmap(&tmDQ);
         for (int k = 0; k < nsteps; ++k) {
             const int h = g * G + k / nq;
             const int qrow0 = s + (i0 + k % nq) * kTileM + w4 * 32;   // first query row of this warp
             if (!mbar_wait(&bars[L::bDqFull], k & 1, abort_flag, kWaitLimitNs)) break;
             tc_fence_after();
-            // row `row` of this warp's 32 query rows: dst_base + row * dq_rs
-            const int64_t dq_rs = (int64_t)(a.dq_token_major ? a.hq : 1) * D;
-            float* dst_base = a.dq_acc + act_row(h, qrow0, a.T, a.hq, a.dq_token_major) * D;
-            // chunk c+1 is read from TMEM while chunk c goes through shared memory and the atomics
+            // chunk c+1 is read from TMEM while chunk c is staged
             uint32_t v[2][32];
             tmem_ld32(tDQ, v[0]);
             tmem_ld_wait(v[0]);
-            // dQ is issued before dK, so the dS buffer becomes a staging area only once dK is done
-            if (!mbar_wait(&bars[L::bDsFree], k & 1, abort_flag, kWaitLimitNs)) break;
 #pragma unroll
             for (int ci = 0; ci < D / 32; ++ci) {
                 const int c = ci * 32;
@@ -428,36 +441,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&bars[L::bDqEmpty]);
                 }
-                uint8_t* buf = stage + (ci & 1) * 4096;   // alternate 4 KB halves
+                uint8_t* buf = stage + (ci & 1) * kDqChunkBytes;
+                // the reduction that last used this buffer (two chunks ago) must have read it
+                if (lane == 0) bulk_wait_group_read<1>();
+                __syncwarp();
 #pragma unroll
                 for (int j = 0; j < 8; ++j)   // row `lane`, 16-byte chunk j, XOR-swizzled by row
                     *(uint4*)(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) =
                         make_uint4(cur[4 * j], cur[4 * j + 1], cur[4 * j + 2], cur[4 * j + 3]);
+                fence_proxy_async_smem();
                 __syncwarp();
-                // all eight shared-memory reads first: the compiler may not move a read past an
-                // atomic, so interleaving them would serialise eight load latencies
-                uint4 x[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int row = 4 * i + sub_row;
-                    x[i] = *(const uint4*)(buf + row * 128 + ((chunk ^ (row & 7)) << 4));
+                if (lane == 0) {
+                    tma_reduce_add_rows(&tmDQ, buf, c, qrow0, h, a.dq_token_major);
+                    bulk_commit_group();
                 }
-                if (ci + 1 == D / 32) {  // last reads of the staging area done: the dS buffer is free again
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&bars[L::bStageFree]);
-                }
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int row = 4 * i + sub_row;
-                    if (qrow0 + row < e)
-                        atomicAdd((float4*)(dst_base + (int64_t)row * dq_rs + c) + chunk,
-                                  make_float4(__uint_as_float(x[i].x), __uint_as_float(x[i].y),
-                                              __uint_as_float(x[i].z), __uint_as_float(x[i].w)));
-                }
-                __syncwarp();
                 if (ci + 1 < D / 32) tmem_ld_wait(v[(ci + 1) & 1]);
             }
         }
+        if (lane == 0) bulk_wait_group<0>();
     }
 
     __syncwarp();
@@ -541,7 +542,7 @@ __global__ void debug_timeout_kernel(WsHeader* hdr, uint64_t limit_ns) {
 
 template <int D>
 cudaError_t launch_bwd_impl(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& dout,
-                            const BwdArgs& a, int grid, cudaStream_t s) {
+                            const CUtensorMap& dq, const BwdArgs& a, int grid, cudaStream_t s) {
     using L = BwdSmem<D>;
     static bool attr_set = false;
     if (!attr_set) {
@@ -549,7 +550,7 @@ cudaError_t launch_bwd_impl(const CUtensorMap& q, const CUtensorMap& k, const CU
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    attn_bwd_kernel<D><<<grid, kBwdThreads, L::kAlloc, s>>>(q, k, v, dout, a);
+    attn_bwd_kernel<D><<<grid, kBwdThreads, L::kAlloc, s>>>(q, k, v, dout, dq, a);
     return cudaGetLastError();
 }
 
@@ -566,9 +567,9 @@ int grid_for(int64_t work_items, int per_cta, int ys = 1) {
 }  // namespace
 
 cudaError_t launch_attn_bwd(int head_dim, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                            const CUtensorMap& dout, const BwdArgs& a, int grid, cudaStream_t s) {
-    if (head_dim == 128) return launch_bwd_impl<128>(q, k, v, dout, a, grid, s);
-    return launch_bwd_impl<64>(q, k, v, dout, a, grid, s);
+                            const CUtensorMap& dout, const CUtensorMap& dq, const BwdArgs& a, int grid, cudaStream_t s) {
+    if (head_dim == 128) return launch_bwd_impl<128>(q, k, v, dout, dq, a, grid, s);
+    return launch_bwd_impl<64>(q, k, v, dout, dq, a, grid, s);
 }
 
 cudaError_t launch_bwd_prep(const __nv_bfloat16* o, const __nv_bfloat16* dout, float* delta, float* dq_acc,

@@ -118,6 +118,34 @@ __device__ __forceinline__ void tma_load_rows(void* smem_dst, const CUtensorMap*
         tma_load_3d(smem_dst, map, bar, x, t0, h);
 }
 
+// 3-D tiled element-wise add of a shared-memory box into global memory, done by the TMA
+// unit at L2 (elements outside the tensor are skipped); tracked by bulk async-groups.
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, const void* smem_src, int x, int y, int z) {
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(smem_u32(smem_src)), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+__device__ __forceinline__ void tma_reduce_add_rows(const CUtensorMap* map, const void* smem_src, int x, int t0, int h,
+                                                    int token_major) {
+    if (token_major)
+        tma_reduce_add_3d(map, smem_src, x, h, t0);
+    else
+        tma_reduce_add_3d(map, smem_src, x, t0, h);
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until at most N of this thread's bulk groups still read their shared-memory source.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// Wait until at most N of this thread's bulk groups are still in flight.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group() {
+    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // Make generic-proxy writes to shared memory visible to the async proxy (tensor cores, TMA).
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -83,6 +83,27 @@ bool make_activation_map(CUtensorMap* map, const void* base, int64_t T, int head
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_dq_accum_map(CUtensorMap* map, float* base, int64_t T, int heads, int D, int token_major) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t row = (cuuint64_t)D * 4;
+    cuuint64_t dims[3], strides[2];
+    cuuint32_t box[3];
+    if (token_major) {
+        dims[0] = (cuuint64_t)D; dims[1] = (cuuint64_t)heads; dims[2] = (cuuint64_t)T;
+        strides[0] = row; strides[1] = row * (cuuint64_t)heads;
+        box[0] = 32; box[1] = 1; box[2] = 32;
+    } else {
+        dims[0] = (cuuint64_t)D; dims[1] = (cuuint64_t)T; dims[2] = (cuuint64_t)heads;
+        strides[0] = row; strides[1] = row * (cuuint64_t)T;
+        box[0] = 32; box[1] = 32; box[2] = 1;
+    }
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace usp
 
 using namespace usp;
@@ -193,11 +214,12 @@ usp_status attn_bwd_impl(const void* q, const void* k, const void* v, const void
     sa.items = (WorkItem*)(ws + w.items);
     if (launch_schedule(sa, s) != cudaSuccess) return USP_ERR_CUDA;
 
-    CUtensorMap mq, mk, mv, mdo;
+    CUtensorMap mq, mk, mv, mdo, mdq;
     if (!make_activation_map(&mq, q, total_tokens, hq, head_dim, token_major) ||
         !make_activation_map(&mk, k, total_tokens, hkv, head_dim, token_major) ||
         !make_activation_map(&mv, v, total_tokens, hkv, head_dim, token_major) ||
-        !make_activation_map(&mdo, d_o, total_tokens, hq, head_dim, token_major))
+        !make_activation_map(&mdo, d_o, total_tokens, hq, head_dim, token_major) ||
+        !make_dq_accum_map(&mdq, dq_acc, total_tokens, hq, head_dim, dq_token_major))
         return USP_ERR_CUDA;
     BwdArgs ba{};
     ba.cu = cu_seqlens;
@@ -218,7 +240,7 @@ usp_status attn_bwd_impl(const void* q, const void* k, const void* v, const void
     ba.causal = sa.causal;
     ba.scale = resolve_scale(softmax_scale, head_dim);
     ba.scale_log2 = ba.scale * 1.4426950408889634f;
-    if (launch_attn_bwd(head_dim, mq, mk, mv, mdo, ba, w.max_items, s) != cudaSuccess) return USP_ERR_CUDA;
+    if (launch_attn_bwd(head_dim, mq, mk, mv, mdo, mdq, ba, w.max_items, s) != cudaSuccess) return USP_ERR_CUDA;
     if (!fp32_grads &&
         launch_dq_convert(dq_acc, (__nv_bfloat16*)dq, total_tokens, hq, head_dim, token_major, s) != cudaSuccess)
         return USP_ERR_CUDA;
