@@ -96,7 +96,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int nsteps = nq * G;
 
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    // 1024-byte aligned base for the 128-byte swizzle atoms, derived from smem_raw by an
+    // offset so the compiler keeps it in the shared window (LDS/STS, not generic accesses)
+    uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t* bars = (uint64_t*)(sm + L::kBars);
     uint32_t* tmem_slot = (uint32_t*)(sm + L::kTmemSlot);
     volatile int* abort_flag = (volatile int*)(sm + L::kAbort);
