@@ -134,25 +134,27 @@ def max_over_ranks(value: float, dist=None, device="cpu") -> float:
     return float(t.item())
 
 
-def oracle_sample_step(w, tokens: int):
-    """The oracle's fwd+bwd on one head over the first `tokens` tokens of the workload's
-    first sample; returns (seconds, algorithmic FLOPs credited, threads)."""
+def oracle_sample_step(w, tokens: int, heads: int = 1):
+    """The oracle's fwd+bwd on the first `heads` query heads (MHA: each with its own
+    key/value head) over the first `tokens` tokens of the workload's first sample;
+    returns (seconds, algorithmic FLOPs credited, threads, tokens)."""
     import numpy as np
 
     import oracle
     from ulysses_sequence_seq_gb300.synth import head_bits
     L = min(tokens, w.lengths[0])
-    q = head_bits(w, "q", 0)[None, :L]
-    k = head_bits(w, "k", 0)[None, :L]
-    v = head_bits(w, "v", 0)[None, :L]
-    do = head_bits(w, "do", 0)[None, :L]
+    hs = range(heads)
+    q = np.stack([head_bits(w, "q", h)[:L] for h in hs])
+    k = np.stack([head_bits(w, "k", h % w.hkv)[:L] for h in hs])
+    v = np.stack([head_bits(w, "v", h % w.hkv)[:L] for h in hs])
+    do = np.stack([head_bits(w, "do", h)[:L] for h in hs])
     cu = np.array([0, L], dtype=np.int32)
     t0 = time.perf_counter()
     oracle.attn_fwd(q, k, v, cu)
     oracle.attn_bwd(q, k, v, do, cu)
     dt = time.perf_counter() - t0
     pairs = L * (L + 1) // 2
-    return dt, 14.0 * w.head_dim * pairs, oracle.num_threads(), L
+    return dt, 14.0 * w.head_dim * pairs * heads, oracle.num_threads(), L
 
 
 def run_reference(args, w):
@@ -384,9 +386,11 @@ def run_usp(args, w):
     if world == 1 and not args.no_cpu_baseline:
         from oracle.build import build_oracle
         build_oracle()
-        dt, fl, threads, L = oracle_sample_step(w, args.cpu_tokens)
+        dt1, _, _, _ = oracle_sample_step(w, args.cpu_tokens)          # calibration: one head
+        nh = max(1, min(w.hq, math.ceil(12.0 / max(dt1, 1e-3))))         # about 12 s of oracle work
+        dt, fl, threads, L = oracle_sample_step(w, args.cpu_tokens, nh)
         cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-               "sample": f"one query head, causal fwd+bwd over the first {L} tokens of sample 0 "
+               "sample": f"{nh} query heads, causal fwd+bwd over the first {L} tokens of sample 0 "
                          f"({dt:.1f} s of float64 C oracle work)"}
     # fused: schedule + attn_fwd | bwd_prep + schedule + attn_bwd + dq_convert;
     # unfused adds the eight re-layout launches
