@@ -67,14 +67,43 @@ struct BwdSmem {
     static constexpr int kBars = kDelta + 512;
     static constexpr int bKvFull = 0, bQFull = 1, bQEmpty = 3, bDoFull = 5, bDoEmpty = 6, bSFull = 7, bPFull = 9,
                          bDpFull = 11, bDsFull = 13, bDqFull = 15, bDqEmpty = 16, bAccFull = 17, bDrain = 18,
-                         kNumBars = 19;
-    static constexpr int kTmemSlot = kBars + 8 * kNumBars;
+                         bKvEmpty = 19, bAccEmpty = 20, bItem = 21, kNumBars = 25;   // bItem: 4-slot ring
+    static constexpr int kItemRing = kBars + 8 * kNumBars;        // int[4]: work item of each slot
+    static constexpr int kTmemSlot = kItemRing + 16;
     static constexpr int kAbort = kTmemSlot + 8;
     static constexpr int kBytes = kAbort + 8;
     static constexpr int kAlloc = kBytes + 1024;
 };
 static_assert(BwdSmem<128>::kAlloc <= 232448, "backward shared memory exceeds the per-CTA limit");
 static_assert(BwdSmem<128>::kStage % 1024 == 0, "dQ staging must keep the 128-byte swizzle atoms aligned");
+
+// One backward work item: a key/value tile of one sample and one key/value head, and the
+// query blocks (of every query head of its GQA group) that see it.
+struct BwdItem {
+    int g, s, e, kv0, i0, nq, nsteps;
+};
+__device__ __forceinline__ BwdItem bwd_item(const BwdArgs& a, int idx) {
+    const WorkItem it = a.items[idx];
+    BwdItem b;
+    b.g = it.head;
+    b.s = a.cu[it.seq];
+    b.e = a.cu[it.seq + 1];
+    b.kv0 = b.s + it.tile * kBlockN;
+    b.i0 = first_query_block_for_kv_block(it.tile, a.causal);
+    b.nq = query_blocks_in_sample(b.s, b.e) - b.i0;
+    b.nsteps = b.nq * a.group;
+    return b;
+}
+
+// The CTA's j-th work item, published by the producer in a 4-slot ring; false when the
+// wait gave up (abort). No role runs more than two items behind the producer, so a
+// slot is never rewritten while a reader still needs it.
+__device__ __forceinline__ bool read_item(uint64_t* item_bars, volatile int* ring, int j, volatile int* abort_flag,
+                                          int& idx) {
+    if (!mbar_wait(&item_bars[j & 3], (j >> 2) & 1, abort_flag, kWaitLimitNs)) return false;
+    idx = ring[j & 3];
+    return true;
+}
 
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
@@ -86,14 +115,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if ((int)blockIdx.x >= count) return;
     // once any CTA of this launch has timed out, the rest skip their work
     if (*(volatile int*)&a.hdr->status != (int)USP_OK) return;
-    const WorkItem it = a.items[blockIdx.x];
-    const int g = it.head;  // key/value head
-    const int s = a.cu[it.seq], e = a.cu[it.seq + 1];
-    const int kv0 = s + it.tile * kBlockN;
-    const int i0 = first_query_block_for_kv_block(it.tile, a.causal);
-    const int nq = query_blocks_in_sample(s, e) - i0;  // query blocks per query head
     const int G = a.group;
-    const int nsteps = nq * G;
 
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned base for the 128-byte swizzle atoms, derived from smem_raw by an
@@ -104,6 +126,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     volatile int* abort_flag = (volatile int*)(sm + L::kAbort);
     float* lse_s = (float*)(sm + L::kLse);
     float* delta_s = (float*)(sm + L::kDelta);
+    volatile int* item_ring = (volatile int*)(sm + L::kItemRing);
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
@@ -128,6 +151,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(&bars[L::bDqEmpty], 4);
         mbar_init(&bars[L::bAccFull], 1);
         mbar_init(&bars[L::bDrain], 1);
+        mbar_init(&bars[L::bKvEmpty], 1);
+        mbar_init(&bars[L::bAccEmpty], kComputeWarps);
+        for (int i = 0; i < 4; ++i) mbar_init(&bars[L::bItem + i], 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -136,6 +162,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tc_fence_after();
     const uint32_t tbase = *tmem_slot;
 
+    // Persistent CTAs: each one takes work items in the scheduler's order (heaviest first),
+    // its first one by its index and the rest from a counter, until the list is done. Every
+    // per-step barrier phase follows the CTA's running step count `gk` across items; the
+    // per-item ones (K/V, dK/dV accumulators) follow the item count `j`.
+    uint64_t* item_bars = &bars[L::bItem];
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------------ TMA producer
         if (lane == 0) {
@@ -143,40 +174,58 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             prefetch_tmap(&tmK);
             prefetch_tmap(&tmV);
             prefetch_tmap(&tmDO);
-            mbar_arrive_expect_tx(&bars[L::bKvFull], 2 * L::kTileBytes);
-            for (int p = 0; p < L::kPanels; ++p) {
-                tma_load_rows(sm + L::kK + p * (kTileM * 128), &tmK, &bars[L::bKvFull], p * 64, kv0, g, a.token_major);
-                tma_load_rows(sm + L::kV + p * (kTileM * 128), &tmV, &bars[L::bKvFull], p * 64, kv0, g, a.token_major);
-            }
-            int issued = 0;
-            for (int k = 0; k < nsteps; ++k) {
-                const int st = k & 1;
-                const int h = g * G + k / nq;
-                const int q0 = s + (i0 + k % nq) * kTileM;
-                if (k >= 2 && !mbar_wait(&bars[L::bQEmpty + st], ((k >> 1) - 1) & 1, abort_flag, kWaitLimitNs))
-                    break;
-                mbar_arrive_expect_tx(&bars[L::bQFull + st], L::kTileBytes);
-                for (int p = 0; p < L::kPanels; ++p)
-                    tma_load_rows(sm + L::kQ + st * L::kTileBytes + p * (kTileM * 128), &tmQ, &bars[L::bQFull + st],
-                                  p * 64, q0, h, a.token_major);
-                // the single dO buffer is free once both halves' dV and dP of the previous block are done
-                if (k >= 1 && !mbar_wait(&bars[L::bDoEmpty], (k - 1) & 1, abort_flag, kWaitLimitNs)) {
-                    issued = -(k + 1);   // Q(k) is in flight, dO(k) is not
-                    break;
+            bool ok = true;
+            int gk = 0, q_total = 0, do_total = 0, kv_total = 0;
+            for (int j = 0; ok; ++j) {
+                const int idx = j == 0 ? (int)blockIdx.x : (int)gridDim.x + atomicAdd(&a.hdr->bwd_next, 1);
+                item_ring[j & 3] = idx;
+                mbar_arrive(&item_bars[j & 3]);   // release: the slot write is visible to its readers
+                if (idx >= count) break;
+                const BwdItem w = bwd_item(a, idx);
+                for (int k = 0; k < w.nsteps; ++k, ++gk) {
+                    const int st = gk & 1;
+                    const int h = w.g * G + k / w.nq;
+                    const int q0 = w.s + (w.i0 + k % w.nq) * kTileM;
+                    if (gk >= 2 && !mbar_wait(&bars[L::bQEmpty + st], ((gk >> 1) - 1) & 1, abort_flag, kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&bars[L::bQFull + st], L::kTileBytes);
+                    for (int p = 0; p < L::kPanels; ++p)
+                        tma_load_rows(sm + L::kQ + st * L::kTileBytes + p * (kTileM * 128), &tmQ,
+                                      &bars[L::bQFull + st], p * 64, q0, h, a.token_major);
+                    ++q_total;
+                    // the single dO buffer is free once both halves' dV and dP of the previous block are done
+                    if (gk >= 1 && !mbar_wait(&bars[L::bDoEmpty], (gk - 1) & 1, abort_flag, kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&bars[L::bDoFull], L::kTileBytes);
+                    for (int p = 0; p < L::kPanels; ++p)
+                        tma_load_rows(sm + L::kDO + p * (kTileM * 128), &tmDO, &bars[L::bDoFull], p * 64, q0, h,
+                                      a.token_major);
+                    ++do_total;
+                    if (k == 0) {  // K, V once the previous item's last MMA has read them
+                        if (j > 0 && !mbar_wait(&bars[L::bKvEmpty], (j - 1) & 1, abort_flag, kWaitLimitNs)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&bars[L::bKvFull], 2 * L::kTileBytes);
+                        for (int p = 0; p < L::kPanels; ++p) {
+                            tma_load_rows(sm + L::kK + p * (kTileM * 128), &tmK, &bars[L::bKvFull], p * 64, w.kv0,
+                                          w.g, a.token_major);
+                            tma_load_rows(sm + L::kV + p * (kTileM * 128), &tmV, &bars[L::bKvFull], p * 64, w.kv0,
+                                          w.g, a.token_major);
+                        }
+                        ++kv_total;
+                    }
                 }
-                mbar_arrive_expect_tx(&bars[L::bDoFull], L::kTileBytes);
-                for (int p = 0; p < L::kPanels; ++p)
-                    tma_load_rows(sm + L::kDO + p * (kTileM * 128), &tmDO, &bars[L::bDoFull], p * 64, q0, h,
-                                  a.token_major);
-                issued = k + 1;
             }
             // let every copy in flight land before the CTA can exit
-            mbar_wait_drain(&bars[L::bKvFull], 0, kDrainLimitNs);
-            const int q_issued = issued < 0 ? -issued : issued;
-            const int do_issued = issued < 0 ? -issued - 1 : issued;
-            for (int k = q_issued - 2 < 0 ? 0 : q_issued - 2; k < q_issued; ++k)
-                mbar_wait_drain(&bars[L::bQFull + (k & 1)], (k >> 1) & 1, kDrainLimitNs);
-            if (do_issued > 0) mbar_wait_drain(&bars[L::bDoFull], (do_issued - 1) & 1, kDrainLimitNs);
+            if (kv_total > 0) mbar_wait_drain(&bars[L::bKvFull], (kv_total - 1) & 1, kDrainLimitNs);
+            for (int q = q_total - 2 < 0 ? 0 : q_total - 2; q < q_total; ++q)
+                mbar_wait_drain(&bars[L::bQFull + (q & 1)], (q >> 1) & 1, kDrainLimitNs);
+            if (do_total > 0) mbar_wait_drain(&bars[L::bDoFull], (do_total - 1) & 1, kDrainLimitNs);
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------------ MMA issuer
@@ -207,66 +256,79 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     mma_ss(d, a_desc + off, b_desc + off, idH, kk > 0);
                 }
             };
-            bool ok = mbar_wait(&bars[L::bKvFull], 0, abort_flag, kWaitLimitNs);
-            if (ok) ok = mbar_wait(&bars[L::bQFull], 0, abort_flag, kWaitLimitNs);
-            if (ok) {
+            bool ok = true;
+            int gk = 0;
+            for (int j = 0; ok; ++j) {
+                int idx;
+                if (!read_item(item_bars, item_ring, j, abort_flag, idx)) break;
+                if (idx >= count) break;
+                const int nsteps = bwd_item(a, idx).nsteps;
+                if (!mbar_wait(&bars[L::bKvFull], j & 1, abort_flag, kWaitLimitNs)) break;
+                if (!mbar_wait(&bars[L::bQFull + (gk & 1)], (gk >> 1) & 1, abort_flag, kWaitLimitNs)) break;
                 tc_fence_after();
                 for (int hf = 0; hf < 2; ++hf) {
-                    issue_half(tS + hf * kHalfCols, dK_kmaj, dQ_kmaj + hf * kHalfRows);
+                    issue_half(tS + hf * kHalfCols, dK_kmaj, dQ_kmaj + (gk & 1) * kStageQ + hf * kHalfRows);
                     mma_commit(&bars[L::bSFull + hf]);
                 }
-            }
-            // Per step k and half hf: dV += P^T.dO, dP^T = V.dO^T (after P), then S^T of the
-            // next block and dK += dS^T.Q (after dS); dQ = dS.K once both halves wrote dS. The
-            // tensor cores run in issue order, so the commit that releases a half's dP^T also
-            // covers the previous block's dQ and dK reads of the dS buffer that half rewrites.
-            for (int k = 0; ok && k < nsteps; ++k) {
-                const int st = k & 1;
-                if (!mbar_wait(&bars[L::bDoFull], k & 1, abort_flag, kWaitLimitNs)) break;
-                for (int hf = 0; ok && hf < 2; ++hf) {
-                    if (!mbar_wait(&bars[L::bPFull + hf], k & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
-                    tc_fence_after();
-#pragma unroll
-                    for (int kk = 0; kk < kHalfCols / 16; ++kk)  // dV += P^T . dO over this half's queries
-                        mma_ts(tDV, tS + hf * kHalfCols + 8 * kk,
-                               dDO_mn + (uint64_t)((((hf * kHalfCols) / 16 + kk) * 2048) >> 4), idDv,
-                               (k > 0 || hf > 0 || kk > 0) ? 1u : 0u);
-                    issue_half(tS + hf * kHalfCols, dV_kmaj, dDO_kmaj + hf * kHalfRows);  // dP^T, after dV read P^T
-                    mma_commit(&bars[L::bDpFull + hf]);
-                }
-                if (!ok) break;
-                mma_commit(&bars[L::bDoEmpty]);
-                for (int hf = 0; ok && hf < 2; ++hf) {
-                    if (!mbar_wait(&bars[L::bDsFull + hf], k & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
-                    tc_fence_after();
-                    if (k + 1 < nsteps) {  // S^T of the next block first: it heads this half's next step
-                        const int st1 = st ^ 1;
-                        if (hf == 0 &&
-                            !mbar_wait(&bars[L::bQFull + st1], ((k + 1) >> 1) & 1, abort_flag, kWaitLimitNs)) {
-                            ok = false;
-                            break;
-                        }
+                // the epilogue of the previous item must have read dK and dV out of TMEM
+                if (j > 0 && !mbar_wait(&bars[L::bAccEmpty], (j - 1) & 1, abort_flag, kWaitLimitNs)) break;
+                // Per step k and half hf: dV += P^T.dO, dP^T = V.dO^T (after P), then S^T of the
+                // next block and dK += dS^T.Q (after dS); dQ = dS.K once both halves wrote dS. The
+                // tensor cores run in issue order, so the commit that releases a half's dP^T also
+                // covers the previous block's dQ and dK reads of the dS buffer that half rewrites.
+                for (int k = 0; ok && k < nsteps; ++k, ++gk) {
+                    const int st = gk & 1;
+                    if (!mbar_wait(&bars[L::bDoFull], gk & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
+                    for (int hf = 0; ok && hf < 2; ++hf) {
+                        if (!mbar_wait(&bars[L::bPFull + hf], gk & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
                         tc_fence_after();
-                        issue_half(tS + hf * kHalfCols, dK_kmaj, dQ_kmaj + st1 * kStageQ + hf * kHalfRows);
-                        mma_commit(&bars[L::bSFull + hf]);
-                    }
 #pragma unroll
-                    for (int kk = 0; kk < kHalfCols / 16; ++kk)  // dK += dS^T . Q over this half's queries
-                        mma_ss(tDK, dDS_kmaj + (uint64_t)((hf * kBlockN * 128 + kk * 32) >> 4),
-                               dQ_mn + st * kStageQ + (uint64_t)((((hf * kHalfCols) / 16 + kk) * 2048) >> 4), idDk,
-                               (k > 0 || hf > 0 || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < kHalfCols / 16; ++kk)  // dV += P^T . dO over this half's queries
+                            mma_ts(tDV, tS + hf * kHalfCols + 8 * kk,
+                                   dDO_mn + (uint64_t)((((hf * kHalfCols) / 16 + kk) * 2048) >> 4), idDv,
+                                   (k > 0 || hf > 0 || kk > 0) ? 1u : 0u);
+                        issue_half(tS + hf * kHalfCols, dV_kmaj, dDO_kmaj + hf * kHalfRows);  // dP^T, after dV read P^T
+                        mma_commit(&bars[L::bDpFull + hf]);
+                    }
+                    if (!ok) break;
+                    mma_commit(&bars[L::bDoEmpty]);
+                    for (int hf = 0; ok && hf < 2; ++hf) {
+                        if (!mbar_wait(&bars[L::bDsFull + hf], gk & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
+                        tc_fence_after();
+                        if (k + 1 < nsteps) {  // S^T of the next block first: it heads this half's next step
+                            const int st1 = st ^ 1;
+                            if (hf == 0 && !mbar_wait(&bars[L::bQFull + st1], ((gk + 1) >> 1) & 1, abort_flag,
+                                                      kWaitLimitNs)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            issue_half(tS + hf * kHalfCols, dK_kmaj, dQ_kmaj + st1 * kStageQ + hf * kHalfRows);
+                            mma_commit(&bars[L::bSFull + hf]);
+                        }
+#pragma unroll
+                        for (int kk = 0; kk < kHalfCols / 16; ++kk)  // dK += dS^T . Q over this half's queries
+                            mma_ss(tDK, dDS_kmaj + (uint64_t)((hf * kBlockN * 128 + kk * 32) >> 4),
+                                   dQ_mn + st * kStageQ + (uint64_t)((((hf * kHalfCols) / 16 + kk) * 2048) >> 4),
+                                   idDk, (k > 0 || hf > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    if (!ok) break;
+                    mma_commit(&bars[L::bQEmpty + st]);
+                    if (gk > 0 && !mbar_wait(&bars[L::bDqEmpty], (gk - 1) & 1, abort_flag, kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < kBlockN / 16; ++kk)  // dQ = dS . K
+                        mma_ss(tDQ, dDS_mn + (uint64_t)((kk * 2048) >> 4), dK_mn + (uint64_t)((kk * 2048) >> 4), idDq,
+                               kk > 0 ? 1u : 0u);
+                    mma_commit(&bars[L::bDqFull]);
                 }
                 if (!ok) break;
-                mma_commit(&bars[L::bQEmpty + st]);
-                if (k > 0 && !mbar_wait(&bars[L::bDqEmpty], (k - 1) & 1, abort_flag, kWaitLimitNs)) break;
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < kBlockN / 16; ++kk)  // dQ = dS . K
-                    mma_ss(tDQ, dDS_mn + (uint64_t)((kk * 2048) >> 4), dK_mn + (uint64_t)((kk * 2048) >> 4), idDq,
-                           kk > 0 ? 1u : 0u);
-                mma_commit(&bars[L::bDqFull]);
+                mma_commit(&bars[L::bKvEmpty]);   // K and V have been read for the last time
+                mma_commit(&bars[L::bAccFull]);   // dK and dV of this item are final
             }
-            mma_commit(&bars[L::bAccFull]);
             mma_commit(&bars[L::bDrain]);
             mbar_wait_drain(&bars[L::bDrain], 0, kDrainLimitNs);
         }
@@ -274,8 +336,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // ------------------------------------------------------------------ compute halves (key rows)
         const int grp = warp >> 2;          // query columns [grp * kHalfCols, (grp + 1) * kHalfCols)
         const int r = (warp & 3) * 32 + lane;
-        const int kv = kv0 + r;
-        const bool kv_ok = kv < e;
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         // this half's columns of the S^T / P^T / dP^T region
         const uint32_t tS = tbase + lane_off + grp * kHalfCols;
@@ -284,109 +344,120 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const float sl2 = a.scale_log2;
         const float sc = a.scale;
         bool ok = true;
-        // This half's query rows of a step, negated: -lse (log2 units) and -Delta; rows
-        // outside the sample get -lse = -inf, which makes their P exactly zero. Loaded one
-        // step ahead so that their global-memory latency stays off the critical path.
-        float nl_next = -INFINITY, nd_next = 0.f;
-        auto fetch_row_stats = [&](int k) {
-            const int h = g * G + k / nq;
-            const int q = s + (i0 + k % nq) * kTileM + grp * kHalfCols + r;
-            const bool q_ok = r < kHalfCols && q < e;
-            nl_next = q_ok ? -__ldg(a.lse + (int64_t)h * a.T + q) * 1.4426950408889634f : -INFINITY;
-            nd_next = q_ok ? -__ldg(a.delta + (int64_t)h * a.T + q) : 0.f;
-        };
-        if (nsteps > 0) fetch_row_stats(0);
-        for (int k = 0; k < nsteps; ++k) {
-            const int q0 = s + (i0 + k % nq) * kTileM;
-            named_bar_sync(1 + grp, 128);
-            if (r < kHalfCols) {
-                lse_g[r] = nl_next;
-                delta_g[r] = nd_next;
-            }
-            named_bar_sync(1 + grp, 128);
-            if (k + 1 < nsteps) fetch_row_stats(k + 1);
-            // element masks are only needed on the diagonal block and on the sample's ragged
-            // last key tile; there query column c (of 128) is visible to key row r iff c >= r
-            const bool mask_blk = (a.causal && q0 == kv0) || (kv0 + kBlockN > e);
-            const int vis_from = (a.causal && q0 == kv0) ? r - grp * kHalfCols : -1;
-            if (!mbar_wait(&bars[L::bSFull + grp], k & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
-            tc_fence_after();
-            // P for this row's query columns as packed bf16 pairs: the values the dV MMA
-            // consumes, kept (half the registers of fp32) for dS
-            uint32_t pkall[kHalfCols / 2];
+        int gk = 0;
+        for (int j = 0; ok; ++j) {
+            int idx;
+            if (!read_item(item_bars, item_ring, j, abort_flag, idx)) break;
+            if (idx >= count) break;
+            const BwdItem w = bwd_item(a, idx);
+            const int kv = w.kv0 + r;
+            const bool kv_ok = kv < w.e;
+            // This half's query rows of a step, negated: -lse (log2 units) and -Delta; rows
+            // outside the sample get -lse = -inf, which makes their P exactly zero. Loaded one
+            // step ahead so that their global-memory latency stays off the critical path.
+            float nl_next = -INFINITY, nd_next = 0.f;
+            auto fetch_row_stats = [&](int k) {
+                const int h = w.g * G + k / w.nq;
+                const int q = w.s + (w.i0 + k % w.nq) * kTileM + grp * kHalfCols + r;
+                const bool q_ok = r < kHalfCols && q < w.e;
+                nl_next = q_ok ? -__ldg(a.lse + (int64_t)h * a.T + q) * 1.4426950408889634f : -INFINITY;
+                nd_next = q_ok ? -__ldg(a.delta + (int64_t)h * a.T + q) : 0.f;
+            };
+            fetch_row_stats(0);
+            for (int k = 0; k < w.nsteps; ++k, ++gk) {
+                const int q0 = w.s + (w.i0 + k % w.nq) * kTileM;
+                named_bar_sync(1 + grp, 128);
+                if (r < kHalfCols) {
+                    lse_g[r] = nl_next;
+                    delta_g[r] = nd_next;
+                }
+                named_bar_sync(1 + grp, 128);
+                if (k + 1 < w.nsteps) fetch_row_stats(k + 1);
+                // element masks are only needed on the diagonal block and on the sample's ragged
+                // last key tile; there query column c (of 128) is visible to key row r iff c >= r
+                const bool mask_blk = (a.causal && q0 == w.kv0) || (w.kv0 + kBlockN > w.e);
+                const int vis_from = (a.causal && q0 == w.kv0) ? r - grp * kHalfCols : -1;
+                if (!mbar_wait(&bars[L::bSFull + grp], gk & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
+                tc_fence_after();
+                // P for this row's query columns as packed bf16 pairs: the values the dV MMA
+                // consumes, kept (half the registers of fp32) for dS
+                uint32_t pkall[kHalfCols / 2];
 #pragma unroll
-            for (int c = 0; c < kHalfCols / 32; ++c) {
-                uint32_t sr[32];
-                tmem_ld32(tS + 32 * c, sr);
-                float4 nl4[8];
+                for (int c = 0; c < kHalfCols / 32; ++c) {
+                    uint32_t sr[32];
+                    tmem_ld32(tS + 32 * c, sr);
+                    float4 nl4[8];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) nl4[j] = *(const float4*)(lse_g + 32 * c + 4 * j);
-                tmem_ld_wait(sr);
+                    for (int jj = 0; jj < 8; ++jj) nl4[jj] = *(const float4*)(lse_g + 32 * c + 4 * jj);
+                    tmem_ld_wait(sr);
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int c0 = 32 * c + 2 * j;
-                    const float4 q4 = nl4[j >> 1];
-                    const float2 nl = (j & 1) ? make_float2(q4.z, q4.w) : make_float2(q4.x, q4.y);
-                    const float2 x = fma2(make_float2(__uint_as_float(sr[2 * j]), __uint_as_float(sr[2 * j + 1])),
-                                          make_float2(sl2, sl2), nl);
-                    float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-                    if (mask_blk) {
-                        if (!kv_ok || c0 < vis_from) pp.x = 0.f;
-                        if (!kv_ok || c0 + 1 < vis_from) pp.y = 0.f;
+                    for (int jj = 0; jj < 16; ++jj) {
+                        const int c0 = 32 * c + 2 * jj;
+                        const float4 q4 = nl4[jj >> 1];
+                        const float2 nl = (jj & 1) ? make_float2(q4.z, q4.w) : make_float2(q4.x, q4.y);
+                        const float2 x = fma2(make_float2(__uint_as_float(sr[2 * jj]), __uint_as_float(sr[2 * jj + 1])),
+                                              make_float2(sl2, sl2), nl);
+                        float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                        if (mask_blk) {
+                            if (!kv_ok || c0 < vis_from) pp.x = 0.f;
+                            if (!kv_ok || c0 + 1 < vis_from) pp.y = 0.f;
+                        }
+                        pkall[16 * c + jj] = pack_bf16x2(pp.x, pp.y);
                     }
-                    pkall[16 * c + j] = pack_bf16x2(pp.x, pp.y);
-                }
-                uint32_t pk[16];
+                    uint32_t pk[16];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) pk[j] = pkall[16 * c + j];
-                tmem_st16(tS + 16 * c, pk);
-            }
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[L::bPFull + grp]);
+                    for (int jj = 0; jj < 16; ++jj) pk[jj] = pkall[16 * c + jj];
+                    tmem_st16(tS + 16 * c, pk);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[L::bPFull + grp]);
 
-            // dP^T of this half; its commit also covers the previous block's reads of the dS buffer
-            if (!mbar_wait(&bars[L::bDpFull + grp], k & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
-            tc_fence_after();
-            uint8_t* panel = sm + L::kDS + grp * (kBlockN * 128);
+                // dP^T of this half; its commit also covers the previous block's reads of the dS buffer
+                if (!mbar_wait(&bars[L::bDpFull + grp], gk & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
+                tc_fence_after();
+                uint8_t* panel = sm + L::kDS + grp * (kBlockN * 128);
 #pragma unroll
-            for (int c = 0; c < kHalfCols / 32; ++c) {
-                uint32_t dr[32];
-                tmem_ld32(tS + 32 * c, dr);
-                float4 nd4[8];
+                for (int c = 0; c < kHalfCols / 32; ++c) {
+                    uint32_t dr[32];
+                    tmem_ld32(tS + 32 * c, dr);
+                    float4 nd4[8];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) nd4[j] = *(const float4*)(delta_g + 32 * c + 4 * j);
-                tmem_ld_wait(dr);
-                uint32_t pk[16];
+                    for (int jj = 0; jj < 8; ++jj) nd4[jj] = *(const float4*)(delta_g + 32 * c + 4 * jj);
+                    tmem_ld_wait(dr);
+                    uint32_t pk[16];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const float4 d4 = nd4[j >> 1];
-                    const float2 nd = (j & 1) ? make_float2(d4.z, d4.w) : make_float2(d4.x, d4.y);
-                    const float2 d = add2(make_float2(__uint_as_float(dr[2 * j]), __uint_as_float(dr[2 * j + 1])), nd);
-                    const uint32_t pb = pkall[16 * c + j];
-                    const float2 psc = mul2(make_float2(__uint_as_float(pb << 16), __uint_as_float(pb & 0xffff0000u)),
-                                            make_float2(sc, sc));
-                    const float2 ds = mul2(psc, d);
-                    pk[j] = pack_bf16x2(ds.x, ds.y);
+                    for (int jj = 0; jj < 16; ++jj) {
+                        const float4 d4 = nd4[jj >> 1];
+                        const float2 nd = (jj & 1) ? make_float2(d4.z, d4.w) : make_float2(d4.x, d4.y);
+                        const float2 d =
+                            add2(make_float2(__uint_as_float(dr[2 * jj]), __uint_as_float(dr[2 * jj + 1])), nd);
+                        const uint32_t pb = pkall[16 * c + jj];
+                        const float2 psc = mul2(
+                            make_float2(__uint_as_float(pb << 16), __uint_as_float(pb & 0xffff0000u)),
+                            make_float2(sc, sc));
+                        const float2 ds = mul2(psc, d);
+                        pk[jj] = pack_bf16x2(ds.x, ds.y);
+                    }
+                    // row r of the [key][query] dS operand (read K-major by dK, MN-major by dQ)
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) {
+                        const uint32_t bytecol = (uint32_t)(c * 64 + jj * 16);
+                        *(uint4*)(panel + sw128_offset(r, bytecol)) =
+                            make_uint4(pk[4 * jj], pk[4 * jj + 1], pk[4 * jj + 2], pk[4 * jj + 3]);
+                    }
                 }
-                // row r of the [key][query] dS operand (read K-major by dK, MN-major by dQ)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const uint32_t bytecol = (uint32_t)(c * 64 + j * 16);
-                    *(uint4*)(panel + sw128_offset(r, bytecol)) =
-                        make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[L::bDsFull + grp]);
             }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[L::bDsFull + grp]);
-        }
-        if (ok && mbar_wait(&bars[L::bAccFull], 0, abort_flag, kWaitLimitNs)) {
+            if (!ok || !mbar_wait(&bars[L::bAccFull], j & 1, abort_flag, kWaitLimitNs)) break;
             tc_fence_after();
-            // half A writes dV, half B writes dK
-            const int64_t row = act_row(g, kv, a.T, a.hkv, a.token_major);
+            // half A writes dV, half B writes dK; TMEM is handed back to the next item's MMAs as
+            // soon as the last chunk has been read, before the global stores finish
+            const int64_t row = act_row(w.g, kv, a.T, a.hkv, a.token_major);
             const uint32_t src = tbase + lane_off + (grp ? 384 : 256);
             void* dst_base = grp ? a.dk : a.dv;
 #pragma unroll 1
@@ -394,21 +465,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 uint32_t o[32];
                 tmem_ld32(src + c, o);
                 tmem_ld_wait(o);
+                if (c + 32 == D) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars[L::bAccEmpty]);
+                }
                 if (!kv_ok) continue;
                 if (a.grad_fp32) {
                     float4* dst = (float4*)((float*)dst_base + row * D + c);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        dst[j] = make_float4(__uint_as_float(o[4 * j]), __uint_as_float(o[4 * j + 1]),
-                                             __uint_as_float(o[4 * j + 2]), __uint_as_float(o[4 * j + 3]));
+                    for (int jj = 0; jj < 8; ++jj)
+                        dst[jj] = make_float4(__uint_as_float(o[4 * jj]), __uint_as_float(o[4 * jj + 1]),
+                                              __uint_as_float(o[4 * jj + 2]), __uint_as_float(o[4 * jj + 3]));
                 } else {
                     uint4* dst = (uint4*)((__nv_bfloat16*)dst_base + row * D + c);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        dst[j] = make_uint4(pack_bf16x2(__uint_as_float(o[8 * j]), __uint_as_float(o[8 * j + 1])),
-                                            pack_bf16x2(__uint_as_float(o[8 * j + 2]), __uint_as_float(o[8 * j + 3])),
-                                            pack_bf16x2(__uint_as_float(o[8 * j + 4]), __uint_as_float(o[8 * j + 5])),
-                                            pack_bf16x2(__uint_as_float(o[8 * j + 6]), __uint_as_float(o[8 * j + 7])));
+                    for (int jj = 0; jj < 4; ++jj)
+                        dst[jj] = make_uint4(pack_bf16x2(__uint_as_float(o[8 * jj]), __uint_as_float(o[8 * jj + 1])),
+                                             pack_bf16x2(__uint_as_float(o[8 * jj + 2]), __uint_as_float(o[8 * jj + 3])),
+                                             pack_bf16x2(__uint_as_float(o[8 * jj + 4]), __uint_as_float(o[8 * jj + 5])),
+                                             pack_bf16x2(__uint_as_float(o[8 * jj + 6]), __uint_as_float(o[8 * jj + 7])));
                 }
             }
         }
@@ -423,41 +499,49 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t tDQ = tbase + ((uint32_t)(w4 * 32) << 16) + 128;
         uint8_t* stage = sm + L::kStage + w4 * (2 * kDqChunkBytes);
         if (lane == 0) prefetch_tmap(&tmDQ);
-        for (int k = 0; k < nsteps; ++k) {
-            const int h = g * G + k / nq;
-            const int qrow0 = s + (i0 + k % nq) * kTileM + w4 * 32;   // first query row of this warp
-            if (!mbar_wait(&bars[L::bDqFull], k & 1, abort_flag, kWaitLimitNs)) break;
-            tc_fence_after();
-            // chunk c+1 is read from TMEM while chunk c is staged
-            uint32_t v[2][32];
-            tmem_ld32(tDQ, v[0]);
-            tmem_ld_wait(v[0]);
+        bool ok = true;
+        int gk = 0;
+        for (int j = 0; ok; ++j) {
+            int idx;
+            if (!read_item(item_bars, item_ring, j, abort_flag, idx)) break;
+            if (idx >= count) break;
+            const BwdItem w = bwd_item(a, idx);
+            for (int k = 0; k < w.nsteps; ++k, ++gk) {
+                const int h = w.g * G + k / w.nq;
+                const int qrow0 = w.s + (w.i0 + k % w.nq) * kTileM + w4 * 32;   // first query row of this warp
+                if (!mbar_wait(&bars[L::bDqFull], gk & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
+                tc_fence_after();
+                // chunk c+1 is read from TMEM while chunk c is staged
+                uint32_t v[2][32];
+                tmem_ld32(tDQ, v[0]);
+                tmem_ld_wait(v[0]);
 #pragma unroll
-            for (int ci = 0; ci < D / 32; ++ci) {
-                const int c = ci * 32;
-                uint32_t (&cur)[32] = v[ci & 1];
-                if (ci + 1 < D / 32) {
-                    tmem_ld32(tDQ + c + 32, v[(ci + 1) & 1]);
-                } else {  // the whole tile has left TMEM: its columns are free for the next dQ
-                    tc_fence_before();
+                for (int ci = 0; ci < D / 32; ++ci) {
+                    const int c = ci * 32;
+                    uint32_t (&cur)[32] = v[ci & 1];
+                    if (ci + 1 < D / 32) {
+                        tmem_ld32(tDQ + c + 32, v[(ci + 1) & 1]);
+                    } else {  // the whole tile has left TMEM: its columns are free for the next dQ
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&bars[L::bDqEmpty]);
+                    }
+                    uint8_t* buf = stage + (ci & 1) * kDqChunkBytes;
+                    // the reduction that last used this buffer (two chunks ago) must have read it
+                    if (lane == 0) bulk_wait_group_read<1>();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&bars[L::bDqEmpty]);
-                }
-                uint8_t* buf = stage + (ci & 1) * kDqChunkBytes;
-                // the reduction that last used this buffer (two chunks ago) must have read it
-                if (lane == 0) bulk_wait_group_read<1>();
-                __syncwarp();
 #pragma unroll
-                for (int j = 0; j < 8; ++j)   // row `lane`, 16-byte chunk j, XOR-swizzled by row
-                    *(uint4*)(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) =
-                        make_uint4(cur[4 * j], cur[4 * j + 1], cur[4 * j + 2], cur[4 * j + 3]);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    tma_reduce_add_rows(&tmDQ, buf, c, qrow0, h, a.dq_token_major);
-                    bulk_commit_group();
+                    for (int jj = 0; jj < 8; ++jj)   // row `lane`, 16-byte chunk jj, XOR-swizzled by row
+                        *(uint4*)(buf + lane * 128 + ((jj ^ (lane & 7)) << 4)) =
+                            make_uint4(cur[4 * jj], cur[4 * jj + 1], cur[4 * jj + 2], cur[4 * jj + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_reduce_add_rows(&tmDQ, buf, c, qrow0, h, a.dq_token_major);
+                        bulk_commit_group();
+                    }
+                    if (ci + 1 < D / 32) tmem_ld_wait(v[(ci + 1) & 1]);
                 }
-                if (ci + 1 < D / 32) tmem_ld_wait(v[(ci + 1) & 1]);
             }
         }
         if (lane == 0) bulk_wait_group<0>();
@@ -552,6 +636,15 @@ cudaError_t launch_bwd_impl(const CUtensorMap& q, const CUtensorMap& k, const CU
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
+    // persistent CTAs, one per SM (the shared-memory footprint allows no more)
+    static int sms = 0;
+    if (sms == 0) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+    }
+    if (grid > sms) grid = sms;
     attn_bwd_kernel<D><<<grid, kBwdThreads, L::kAlloc, s>>>(q, k, v, dout, dq, a);
     return cudaGetLastError();
 }

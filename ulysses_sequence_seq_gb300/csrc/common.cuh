@@ -41,6 +41,7 @@ struct WsHeader {
     int fwd_count;
     int bwd_count;
     int max_cost;
+    int bwd_next;  // backward work items handed out past the first one of each CTA
 };
 
 struct WsLayout {
