@@ -81,6 +81,10 @@ static_assert(BwdSmem<128>::kStage % 1024 == 0, "dQ staging must keep the 128-by
 // query blocks (of every query head of its GQA group) that see it.
 struct BwdItem {
     int g, s, e, kv0, i0, nq, nsteps;
+    // first row of the query block of step k: query head g * group + k / nq, blocks walked
+    // from the sample's last one down to the diagonal, so CTAs that start together share
+    // their query blocks
+    __device__ __forceinline__ int q0(int k) const { return s + (i0 + nq - 1 - k % nq) * kTileM; }
 };
 __device__ __forceinline__ BwdItem bwd_item(const BwdArgs& a, int idx) {
     const WorkItem it = a.items[idx];
@@ -185,7 +189,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 for (int k = 0; k < w.nsteps; ++k, ++gk) {
                     const int st = gk & 1;
                     const int h = w.g * G + k / w.nq;
-                    const int q0 = w.s + (w.i0 + k % w.nq) * kTileM;
+                    const int q0 = w.q0(k);
                     if (gk >= 2 && !mbar_wait(&bars[L::bQEmpty + st], ((gk >> 1) - 1) & 1, abort_flag, kWaitLimitNs)) {
                         ok = false;
                         break;
@@ -358,14 +362,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             float nl_next = -INFINITY, nd_next = 0.f;
             auto fetch_row_stats = [&](int k) {
                 const int h = w.g * G + k / w.nq;
-                const int q = w.s + (w.i0 + k % w.nq) * kTileM + grp * kHalfCols + r;
+                const int q = w.q0(k) + grp * kHalfCols + r;
                 const bool q_ok = r < kHalfCols && q < w.e;
                 nl_next = q_ok ? -__ldg(a.lse + (int64_t)h * a.T + q) * 1.4426950408889634f : -INFINITY;
                 nd_next = q_ok ? -__ldg(a.delta + (int64_t)h * a.T + q) : 0.f;
             };
             fetch_row_stats(0);
             for (int k = 0; k < w.nsteps; ++k, ++gk) {
-                const int q0 = w.s + (w.i0 + k % w.nq) * kTileM;
+                const int q0 = w.q0(k);
                 named_bar_sync(1 + grp, 128);
                 if (r < kHalfCols) {
                     lse_g[r] = nl_next;
@@ -508,7 +512,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const BwdItem w = bwd_item(a, idx);
             for (int k = 0; k < w.nsteps; ++k, ++gk) {
                 const int h = w.g * G + k / w.nq;
-                const int qrow0 = w.s + (w.i0 + k % w.nq) * kTileM + w4 * 32;   // first query row of this warp
+                const int qrow0 = w.q0(k) + w4 * 32;   // first query row of this warp
                 if (!mbar_wait(&bars[L::bDqFull], gk & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
                 tc_fence_after();
                 // chunk c+1 is read from TMEM while chunk c is staged

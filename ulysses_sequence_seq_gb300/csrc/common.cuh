@@ -33,6 +33,7 @@ struct WorkItem {
 //   [0, 256)         header: status word, forward item count, backward item count
 //   hist             int32[hist_len]   scheduler cost histogram / bucket cursors
 //   tiles_prefix     int32[num_seqs+1] tiles per sample, prefix-summed
+//   sample_base      int32[num_seqs+1] backward: first tile of each sample in the work order
 //   items            WorkItem[max_items]
 //   delta            fp32[hq][T]       backward only: Delta_i = dO_i . O_i
 //   dq_acc           fp32[hq][T][D]    backward only: dQ accumulator
@@ -45,7 +46,7 @@ struct WsHeader {
 };
 
 struct WsLayout {
-    size_t hist, prefix, items, delta, dq_acc, total;
+    size_t hist, prefix, sbase, items, delta, dq_acc, total;
     int hist_len;
     int max_items;
 };
@@ -73,6 +74,8 @@ inline WsLayout ws_layout(int64_t T, int num_seqs, int hq, int hkv, int D, int b
     w.hist = off;
     off = align256(off + sizeof(int) * (size_t)w.hist_len);
     w.prefix = off;
+    off = align256(off + sizeof(int) * (size_t)(num_seqs + 1));
+    w.sbase = off;
     off = align256(off + sizeof(int) * (size_t)(num_seqs + 1));
     w.items = off;
     off = align256(off + sizeof(WorkItem) * (size_t)w.max_items);

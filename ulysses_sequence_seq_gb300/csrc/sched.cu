@@ -1,12 +1,18 @@
 // Varlen work scheduler: validates cu_seqlens on the device and builds the list of
-// attention work items, heaviest first (longest-processing-time order), so that the
-// long causal tiles at the end of long samples start early and the grid's tail is
-// made of short items.
+// attention work items.
 //
-// One CTA: sample tiles are counted and prefix-summed, every (sample, tile) gets a
-// cost in key/value blocks, a counting sort over the cost (histogram in shared
-// memory, block-wide scans) puts the items in descending cost order, and each (sample, tile) is expanded to all heads, kept
-// adjacent so that query heads sharing a key/value head run close together.
+// Forward: heaviest first (longest-processing-time order), so that the long causal
+// tiles at the end of long samples start early and the grid's tail is made of short
+// items. Every (sample, tile) gets a cost in key/value blocks, a counting sort over the
+// cost (histogram in shared memory, block-wide scans) orders them, and each is expanded
+// to all heads, kept adjacent.
+//
+// Backward: samples longest first (counting sort over their tile counts), and within a
+// sample head by head, tiles in ascending order (heaviest first). The persistent
+// backward CTAs take items in this order, so the CTAs running at any time work on the
+// key/value tiles of one or a few (sample, head) pairs and walk the same query blocks:
+// the Q, dO and dQ blocks they share stay in L2 instead of being fetched once per tile.
+// The tail is still made of the cheapest tiles of the shortest samples.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -103,11 +109,48 @@ __global__ void __launch_bounds__(1024) schedule_kernel(SchedArgs a) {
         if (tid == 0) fail_schedule(a);
         return;
     }
+    if (a.bwd) {
+        // samples by tile count, longest first: bucket c holds samples of c tiles, and its
+        // share of the work order is (samples in it) x c tiles
+        for (int b = tid; b < a.num_seqs; b += nthr) {
+            const int nt = a.prefix[b + 1] - a.prefix[b];
+            atomicAdd(&hist[nt < a.hist_len ? nt : a.hist_len - 1], 1);
+        }
+        __syncthreads();
+        for (int c = tid; c < a.hist_len; c += nthr) hist[c] *= c;
+        __syncthreads();
+        block_exclusive_scan(hist, a.hist_len, true, warp_sums);
+        for (int b = tid; b < a.num_seqs; b += nthr) {
+            const int nt = a.prefix[b + 1] - a.prefix[b];
+            a.sbase[b] = atomicAdd(&hist[nt < a.hist_len ? nt : a.hist_len - 1], nt);
+        }
+        __syncthreads();
+        for (int p = tid; p < ntiles; p += nthr) {
+            const int b = find_sample(a.prefix, a.num_seqs, p);
+            const int tile = p - a.prefix[b];
+            const int nt = a.prefix[b + 1] - a.prefix[b];
+            const int s = a.cu[b], e = a.cu[b + 1];
+            const int cost = bwd_item_cost(tile, s, e, a.causal, a.group);
+            for (int h = 0; h < a.heads; ++h) {
+                WorkItem w;
+                w.head = h;
+                w.seq = b;
+                w.tile = tile;
+                w.cost = cost;
+                a.items[(int64_t)a.sbase[b] * a.heads + (int64_t)h * nt + tile] = w;
+            }
+        }
+        if (tid == 0) {
+            a.hdr->status = USP_OK;
+            a.hdr->bwd_count = ntiles * a.heads;
+        }
+        return;
+    }
     for (int p = tid; p < ntiles; p += nthr) {
         const int b = find_sample(a.prefix, a.num_seqs, p);
         const int tile = p - a.prefix[b];
         const int s = a.cu[b], e = a.cu[b + 1];
-        int cost = a.bwd ? bwd_item_cost(tile, s, e, a.causal, a.group) : fwd_item_cost(tile, s, e, a.causal);
+        int cost = fwd_item_cost(tile, s, e, a.causal);
         cost = cost < 0 ? 0 : (cost >= a.hist_len ? a.hist_len - 1 : cost);
         atomicAdd(&hist[cost], 1);
     }
@@ -118,7 +161,7 @@ __global__ void __launch_bounds__(1024) schedule_kernel(SchedArgs a) {
         const int b = find_sample(a.prefix, a.num_seqs, p);
         const int tile = p - a.prefix[b];
         const int s = a.cu[b], e = a.cu[b + 1];
-        int cost = a.bwd ? bwd_item_cost(tile, s, e, a.causal, a.group) : fwd_item_cost(tile, s, e, a.causal);
+        int cost = fwd_item_cost(tile, s, e, a.causal);
         cost = cost < 0 ? 0 : (cost >= a.hist_len ? a.hist_len - 1 : cost);
         const int pos = atomicAdd(&hist[cost], 1);
         for (int h = 0; h < a.heads; ++h) {
@@ -132,8 +175,7 @@ __global__ void __launch_bounds__(1024) schedule_kernel(SchedArgs a) {
     }
     if (tid == 0) {
         a.hdr->status = USP_OK;
-        if (a.bwd) a.hdr->bwd_count = ntiles * a.heads;
-        else a.hdr->fwd_count = ntiles * a.heads;
+        a.hdr->fwd_count = ntiles * a.heads;
     }
 }
 

@@ -20,6 +20,7 @@ struct SchedArgs {
     WsHeader* hdr;
     int* hist;
     int* prefix;
+    int* sbase;          // backward: per-sample start in the work order, in tiles
     WorkItem* items;
 };
 

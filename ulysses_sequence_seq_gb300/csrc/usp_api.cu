@@ -145,6 +145,7 @@ usp_status attn_fwd_impl(const void* q, const void* k, const void* v, void* o, f
     sa.hdr = hdr;
     sa.hist = (int*)(ws + w.hist);
     sa.prefix = (int*)(ws + w.prefix);
+    sa.sbase = (int*)(ws + w.sbase);
     sa.items = (WorkItem*)(ws + w.items);
     if (launch_schedule(sa, s) != cudaSuccess) return USP_ERR_CUDA;
 
@@ -211,6 +212,7 @@ usp_status attn_bwd_impl(const void* q, const void* k, const void* v, const void
     sa.hdr = hdr;
     sa.hist = (int*)(ws + w.hist);
     sa.prefix = (int*)(ws + w.prefix);
+    sa.sbase = (int*)(ws + w.sbase);
     sa.items = (WorkItem*)(ws + w.items);
     if (launch_schedule(sa, s) != cudaSuccess) return USP_ERR_CUDA;
 
