@@ -180,8 +180,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             prefetch_tmap(&tmDO);
             bool ok = true;
             int gk = 0, q_total = 0, do_total = 0, kv_total = 0;
-            for (int j = 0; ok; ++j) {
-                const int idx = j == 0 ? (int)blockIdx.x : (int)gridDim.x + atomicAdd(&a.hdr->bwd_next, 1);
+            int next_idx = (int)blockIdx.x;
+            for (int j = 0; ok && next_idx >= 0; ++j) {
+                const int idx = next_idx;
+                next_idx = -1;
                 item_ring[j & 3] = idx;
                 mbar_arrive(&item_bars[j & 3]);   // release: the slot write is visible to its readers
                 if (idx >= count) break;
@@ -222,6 +224,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                           w.g, a.token_major);
                         }
                         ++kv_total;
+                    }
+                    // two blocks before the end, reserve the next item and pull its K and V
+                    // into L2, so that its start does not wait on DRAM
+                    if (k == (w.nsteps >= 2 ? w.nsteps - 2 : 0)) {
+                        next_idx = (int)gridDim.x + atomicAdd(&a.hdr->bwd_next, 1);
+                        if (next_idx < count) {
+                            const BwdItem nw = bwd_item(a, next_idx);
+                            for (int p = 0; p < L::kPanels; ++p) {
+                                tma_prefetch_rows(&tmK, p * 64, nw.kv0, nw.g, a.token_major);
+                                tma_prefetch_rows(&tmV, p * 64, nw.kv0, nw.g, a.token_major);
+                            }
+                        }
                     }
                 }
             }

@@ -103,6 +103,7 @@ extern "C" usp_status usp_attn_fwd_varlen_noalloc(const void* q, const void* k, 
     sa.hist = (int*)(ws + w.hist);
     sa.prefix = (int*)(ws + w.prefix);
     sa.sbase = (int*)(ws + w.sbase);
+    sa.head_major_from = head_major_from_tokens(hkv, head_dim, sa.bwd);
     sa.items = (WorkItem*)(ws + w.items);
     if (launch_schedule(sa, s) != cudaSuccess) return USP_ERR_CUDA;
 

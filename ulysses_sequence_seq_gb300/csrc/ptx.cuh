@@ -118,6 +118,15 @@ __device__ __forceinline__ void tma_load_rows(void* smem_dst, const CUtensorMap*
         tma_load_3d(smem_dst, map, bar, x, t0, h);
 }
 
+// Pull a tile into L2 ahead of its load (no shared memory, no completion tracking).
+__device__ __forceinline__ void tma_prefetch_rows(const CUtensorMap* map, int x, int t0, int h, int token_major) {
+    const int y = token_major ? h : t0, z = token_major ? t0 : h;
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+
 // 3-D tiled element-wise add of a shared-memory box into global memory, done by the TMA
 // unit at L2 (elements outside the tensor are skipped); tracked by bulk async-groups.
 __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, const void* smem_src, int x, int y, int z) {

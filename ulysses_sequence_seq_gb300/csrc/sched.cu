@@ -1,18 +1,13 @@
 // Varlen work scheduler: validates cu_seqlens on the device and builds the list of
 // attention work items.
 //
-// Forward: heaviest first (longest-processing-time order), so that the long causal
-// tiles at the end of long samples start early and the grid's tail is made of short
-// items. Every (sample, tile) gets a cost in key/value blocks, a counting sort over the
-// cost (histogram in shared memory, block-wide scans) orders them, and each is expanded
-// to all heads, kept adjacent.
-//
-// Backward: samples longest first (counting sort over their tile counts), and within a
-// sample head by head, tiles in ascending order (heaviest first). The persistent
-// backward CTAs take items in this order, so the CTAs running at any time work on the
-// key/value tiles of one or a few (sample, head) pairs and walk the same query blocks:
-// the Q, dO and dQ blocks they share stay in L2 instead of being fetched once per tile.
-// The tail is still made of the cheapest tiles of the shortest samples.
+// Order: samples longest first (a counting sort over their tile counts, histogram in
+// shared memory, block-wide scans), and within a sample head by head, each head's
+// tiles heaviest first. CTAs started close together then work on the tiles of one or a
+// few (sample, head) pairs and walk the same key/value blocks (forward) or query blocks
+// (backward), so the blocks they share stay in L2 instead of being fetched once per
+// tile; the grid's tail is made of the cheapest tiles of the shortest samples. Heads
+// sharing a key/value head are adjacent.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -109,73 +104,48 @@ __global__ void __launch_bounds__(1024) schedule_kernel(SchedArgs a) {
         if (tid == 0) fail_schedule(a);
         return;
     }
-    if (a.bwd) {
-        // samples by tile count, longest first: bucket c holds samples of c tiles, and its
-        // share of the work order is (samples in it) x c tiles
-        for (int b = tid; b < a.num_seqs; b += nthr) {
-            const int nt = a.prefix[b + 1] - a.prefix[b];
-            atomicAdd(&hist[nt < a.hist_len ? nt : a.hist_len - 1], 1);
-        }
-        __syncthreads();
-        for (int c = tid; c < a.hist_len; c += nthr) hist[c] *= c;
-        __syncthreads();
-        block_exclusive_scan(hist, a.hist_len, true, warp_sums);
-        for (int b = tid; b < a.num_seqs; b += nthr) {
-            const int nt = a.prefix[b + 1] - a.prefix[b];
-            a.sbase[b] = atomicAdd(&hist[nt < a.hist_len ? nt : a.hist_len - 1], nt);
-        }
-        __syncthreads();
-        for (int p = tid; p < ntiles; p += nthr) {
-            const int b = find_sample(a.prefix, a.num_seqs, p);
-            const int tile = p - a.prefix[b];
-            const int nt = a.prefix[b + 1] - a.prefix[b];
-            const int s = a.cu[b], e = a.cu[b + 1];
-            const int cost = bwd_item_cost(tile, s, e, a.causal, a.group);
-            for (int h = 0; h < a.heads; ++h) {
-                WorkItem w;
-                w.head = h;
-                w.seq = b;
-                w.tile = tile;
-                w.cost = cost;
-                a.items[(int64_t)a.sbase[b] * a.heads + (int64_t)h * nt + tile] = w;
-            }
-        }
-        if (tid == 0) {
-            a.hdr->status = USP_OK;
-            a.hdr->bwd_count = ntiles * a.heads;
-        }
-        return;
-    }
-    for (int p = tid; p < ntiles; p += nthr) {
-        const int b = find_sample(a.prefix, a.num_seqs, p);
-        const int tile = p - a.prefix[b];
-        const int s = a.cu[b], e = a.cu[b + 1];
-        int cost = fwd_item_cost(tile, s, e, a.causal);
-        cost = cost < 0 ? 0 : (cost >= a.hist_len ? a.hist_len - 1 : cost);
-        atomicAdd(&hist[cost], 1);
+    // samples by tile count, longest first: bucket c holds samples of c tiles, and its
+    // share of the work order is (samples in it) x c tiles
+    for (int b = tid; b < a.num_seqs; b += nthr) {
+        const int nt = a.prefix[b + 1] - a.prefix[b];
+        atomicAdd(&hist[nt < a.hist_len ? nt : a.hist_len - 1], 1);
     }
     __syncthreads();
-    // bucket start offsets, highest cost first
+    for (int c = tid; c < a.hist_len; c += nthr) hist[c] *= c;
+    __syncthreads();
     block_exclusive_scan(hist, a.hist_len, true, warp_sums);
+    for (int b = tid; b < a.num_seqs; b += nthr) {
+        const int nt = a.prefix[b + 1] - a.prefix[b];
+        a.sbase[b] = atomicAdd(&hist[nt < a.hist_len ? nt : a.hist_len - 1], nt);
+    }
+    __syncthreads();
+    // within a sample, tiles heaviest first (the forward's last query tiles see the most
+    // key/value blocks, the backward's first key/value tiles see the most query blocks):
+    // head by head for long samples, whose shared blocks would not stay in L2 otherwise;
+    // rank by rank across all heads for short ones, whose blocks all fit in L2 and whose
+    // heaviest tiles should start first
     for (int p = tid; p < ntiles; p += nthr) {
         const int b = find_sample(a.prefix, a.num_seqs, p);
         const int tile = p - a.prefix[b];
+        const int nt = a.prefix[b + 1] - a.prefix[b];
         const int s = a.cu[b], e = a.cu[b + 1];
-        int cost = fwd_item_cost(tile, s, e, a.causal);
-        cost = cost < 0 ? 0 : (cost >= a.hist_len ? a.hist_len - 1 : cost);
-        const int pos = atomicAdd(&hist[cost], 1);
+        const int cost = a.bwd ? bwd_item_cost(tile, s, e, a.causal, a.group) : fwd_item_cost(tile, s, e, a.causal);
+        const int rank = a.bwd ? tile : nt - 1 - tile;
+        const bool head_major = e - s >= a.head_major_from;
         for (int h = 0; h < a.heads; ++h) {
             WorkItem w;
             w.head = h;
             w.seq = b;
             w.tile = tile;
             w.cost = cost;
-            a.items[(int64_t)pos * a.heads + h] = w;
+            const int64_t pos = head_major ? (int64_t)h * nt + rank : (int64_t)rank * a.heads + h;
+            a.items[(int64_t)a.sbase[b] * a.heads + pos] = w;
         }
     }
     if (tid == 0) {
         a.hdr->status = USP_OK;
-        a.hdr->fwd_count = ntiles * a.heads;
+        if (a.bwd) a.hdr->bwd_count = ntiles * a.heads;
+        else a.hdr->fwd_count = ntiles * a.heads;
     }
 }
 

@@ -20,10 +20,21 @@ struct SchedArgs {
     WsHeader* hdr;
     int* hist;
     int* prefix;
-    int* sbase;          // backward: per-sample start in the work order, in tiles
+    int* sbase;          // per-sample start in the work order, in tiles
+    int head_major_from; // samples of at least this many tokens are ordered head by head
     WorkItem* items;
 };
 
 cudaError_t launch_schedule(const SchedArgs& a, cudaStream_t s);
+
+// Sample length from which work items are ordered head by head: the backward always (its
+// persistent CTAs follow the list order closely), the forward once a sample's keys and
+// values for all heads exceed half of the 129 MB L2.
+inline int head_major_from_tokens(int hkv, int head_dim, int bwd) {
+    if (bwd) return 0;
+    const int64_t kv_bytes_per_token = 2ll * hkv * head_dim * 2;
+    const int64_t t = (int64_t)(64ll << 20) / (kv_bytes_per_token > 0 ? kv_bytes_per_token : 1);
+    return (int)(t + 1);
+}
 
 }  // namespace usp

@@ -146,6 +146,7 @@ usp_status attn_fwd_impl(const void* q, const void* k, const void* v, void* o, f
     sa.hist = (int*)(ws + w.hist);
     sa.prefix = (int*)(ws + w.prefix);
     sa.sbase = (int*)(ws + w.sbase);
+    sa.head_major_from = head_major_from_tokens(hkv, head_dim, sa.bwd);
     sa.items = (WorkItem*)(ws + w.items);
     if (launch_schedule(sa, s) != cudaSuccess) return USP_ERR_CUDA;
 
@@ -213,6 +214,7 @@ usp_status attn_bwd_impl(const void* q, const void* k, const void* v, const void
     sa.hist = (int*)(ws + w.hist);
     sa.prefix = (int*)(ws + w.prefix);
     sa.sbase = (int*)(ws + w.sbase);
+    sa.head_major_from = head_major_from_tokens(hkv, head_dim, sa.bwd);
     sa.items = (WorkItem*)(ws + w.items);
     if (launch_schedule(sa, s) != cudaSuccess) return USP_ERR_CUDA;
 
