@@ -90,6 +90,29 @@ usp_status usp_head_to_seq(const void* in, void* out, int sp, int64_t total_toke
                            int head_dim, usp_dtype dt, void* stream);
 
 /*
+ * usp_seq_to_head_kv / usp_head_to_seq_kv_grad -- the swaps for key/value heads,
+ * including models with fewer key/value heads than ranks.
+ *   Passage: HF Transformers guide, "Configurar" (heads must divide over sp_size);
+ *   with GQA, query head h reads key/value head h / (hq / hkv). When hkv < sp
+ *   (and sp % hkv == 0) each rank needs the one key/value head its query heads read,
+ *   kv head r * hkv / sp, so every head is replicated sp / hkv times: this build's
+ *   reading of the replication a GQA model needs for sp above its KV head count.
+ *   hkv % sp == 0: identical to usp_seq_to_head / usp_head_to_seq.
+ *   hkv < sp:  seq_to_head_kv writes out [sp][1][T][head_dim] with
+ *              out[r][0][t] = in[t][r * hkv / sp];
+ *              head_to_seq_kv_grad reads in [sp][1][T][head_dim] (per-rank gradients
+ *              of the replicas) and writes out[t][g] = sum over the sp / hkv replicas
+ *              of head g, accumulated in fp32 in rank order and rounded once
+ *              (grad dt USP_BF16 or USP_FP32).
+ * Errors: as usp_seq_to_head, and USP_ERR_INVALID_ARG when neither hkv % sp nor
+ *   sp % hkv is 0; USP_ERR_UNSUPPORTED for an fp16 gradient sum.
+ */
+usp_status usp_seq_to_head_kv(const void* in, void* out, int sp, int64_t total_tokens, int hkv, int head_dim,
+                              usp_dtype dt, void* stream);
+usp_status usp_head_to_seq_kv_grad(const void* in, void* out, int sp, int64_t total_tokens, int hkv, int head_dim,
+                                   usp_dtype dt, void* stream);
+
+/*
  * usp_attn_workspace_size -- bytes of workspace the attention calls need for
  * these sizes (bwd != 0: for usp_attn_bwd_varlen, which also needs per-row
  * Delta and, for bf16 gradients, an fp32 dQ accumulator). The workspace holds
@@ -157,8 +180,10 @@ usp_status usp_attn_bwd_varlen(const void* q, const void* k, const void* v, cons
  *   q   : bf16 [sp][T/sp][hq][D]      k, v : bf16 [sp][T/sp][hkv][D]
  *   o   : bf16 [sp][T/sp][hq][D]      lse  : fp32 [hq][T] (as usp_attn_fwd_varlen)
  *   The workspace is that of usp_attn_fwd_varlen for the same sizes.
- * Errors: as usp_attn_fwd_varlen, and USP_ERR_INVALID_ARG when sp < 1, hq % sp,
- *   hkv % sp or total_tokens % sp is non-zero (guide, "Configurar").
+ * Errors: as usp_attn_fwd_varlen, and USP_ERR_INVALID_ARG when sp < 1, hq % sp or
+ *   total_tokens % sp is non-zero (guide, "Configurar"), or when neither hkv % sp nor
+ *   sp % hkv is zero. hkv < sp with sp % hkv == 0 is the replicated key/value case of
+ *   usp_seq_to_head_kv: the kernels read each shared head in place.
  */
 usp_status usp_ulysses_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                                 const int32_t* cu_seqlens, int num_seqs, int64_t total_tokens, int sp, int hq,

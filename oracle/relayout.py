@@ -65,3 +65,39 @@ def seq_to_head_elem(x: np.ndarray, sp: int, r: int, hl: int, t: int, d: int):
     T = x.size // (H * D)
     S, Hl = T // sp, H // sp
     return x.reshape(sp, S, H, D)[t // S, t % S, r * Hl + hl, d]
+
+
+def kv_replication(sp: int, hkv: int) -> int:
+    """Ranks sharing one key/value head: 1 when the heads split over the ranks, sp / hkv
+    when there are fewer heads than ranks (each rank then needs the head its query heads
+    read: query head h of rank r reads kv head h // (hq / hkv), which for every h of rank
+    r is r * hkv // sp)."""
+    if hkv % sp == 0:
+        return 1
+    if sp % hkv == 0:
+        return sp // hkv
+    raise ValueError("key/value heads must divide over sp_size or divide it")
+
+
+def seq_to_head_kv(x: np.ndarray, sp: int) -> np.ndarray:
+    """[T][hkv][D] bits -> [max(sp, hkv)][T][D]: rank r's heads; with fewer heads than
+    ranks, out[r] = x[:, r * hkv // sp]."""
+    T, hkv, D = x.shape
+    rep = kv_replication(sp, hkv)
+    if rep == 1:
+        return np.ascontiguousarray(x.transpose(1, 0, 2))
+    out = np.empty((sp, T, D), dtype=x.dtype)
+    for r in range(sp):
+        out[r] = x[:, r * hkv // sp, :]
+    return out
+
+
+def head_to_seq_kv_grad(y: np.ndarray, sp: int, hkv: int) -> np.ndarray:
+    """[max(sp, hkv)][T][D] float gradients -> [T][hkv][D]: the gradient of a replicated
+    head is the sum of its replicas' gradients (float64 here)."""
+    rep = kv_replication(sp, hkv)
+    _, T, D = y.shape
+    out = np.zeros((T, hkv, D), dtype=np.float64)
+    for r in range(y.shape[0]):
+        out[:, r // rep, :] += y[r].astype(np.float64)
+    return out

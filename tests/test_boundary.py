@@ -103,3 +103,15 @@ def test_workspace_sizes_grow_with_problem():
     # the backward holds Delta and an fp32 dQ accumulator: at least 4*hq*T*(D+1) bytes
     assert b >= 4 * 32 * 8192 * 129
     assert ws(-1, 1, 4, 4, 128, False) == 0
+
+
+def test_kv_swap_validation():
+    L = _lib.load()
+    f, g = L.usp_seq_to_head_kv, L.usp_head_to_seq_kv_grad
+    assert f(A, B, 8, 0, 2, 128, _lib.USP_BF16, None) == _lib.USP_OK            # empty, replicated
+    assert f(A, B, 4, 64, 3, 128, _lib.USP_BF16, None) == _lib.USP_ERR_INVALID_ARG  # 3 heads over 4 ranks
+    assert f(A, B, 8, 63, 2, 128, _lib.USP_BF16, None) == _lib.USP_ERR_INVALID_ARG  # tokens % sp
+    assert f(A, A + 4096, 8, 64, 2, 128, _lib.USP_BF16, None) == _lib.USP_ERR_INVALID_ARG  # overlap
+    assert g(A, B, 4, 64, 3, 128, _lib.USP_FP32, None) == _lib.USP_ERR_INVALID_ARG
+    assert g(A, B, 8, 64, 2, 128, _lib.USP_FP16, None) == _lib.USP_ERR_UNSUPPORTED   # fp16 sums
+    assert g(0, B, 8, 64, 2, 128, _lib.USP_FP32, None) == _lib.USP_ERR_INVALID_ARG

@@ -119,6 +119,6 @@ def test_fused_rejects_sp_violations():
     lse = torch.zeros(4, 64, device="cuda")
     cu = torch.tensor([0, 64], dtype=torch.int32, device="cuda")
     ws = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
-    for sp, hq, hkv, T in ((3, 4, 4, 64), (2, 4, 1, 64), (8, 4, 4, 64)):
+    for sp, hq, hkv, T in ((3, 4, 4, 64), (2, 6, 3, 64), (8, 4, 4, 64)):
         with pytest.raises(usp.UspError):
             usp.ulysses_attn_fwd(z, z, z, z, lse, cu, 1, T, sp, hq, hkv, 64, 0.0, True, ws, ws.numel())

@@ -335,3 +335,55 @@ def test_bwd_subsets_equal_full():
     assert np.array_equal(sq, dq[[2, 0]][:, rows])
     assert np.allclose(sk, dk[[1]][:, keys], rtol=0, atol=1e-13)
     assert np.allclose(sv, dv[[1]][:, keys], rtol=0, atol=1e-13)
+
+
+# ======================================================== key/value heads over the ranks
+@pytest.mark.parametrize("hq,hkv,sp", [(32, 8, 8), (32, 8, 16), (32, 2, 8), (8, 1, 4), (32, 32, 4), (8, 8, 8)])
+def test_kv_replica_is_the_head_each_rank_reads(hq, hkv, sp):
+    """Rank r's query heads [r*Hl, (r+1)*Hl) read kv heads h // G; the head the rank
+    receives must be exactly that head (so there is only one)."""
+    G, Hl = hq // hkv, hq // sp
+    T, D = 8 * sp, 1
+    x = index_pattern_bits(T, hkv, D)          # value = t * hkv + h
+    y = relayout.seq_to_head_kv(x.reshape(T, hkv, D), sp)
+    rep = relayout.kv_replication(sp, hkv)
+    per_rank = y.shape[0] // sp                # key/value heads held by each rank
+    for r in range(sp):
+        needed = sorted({h // G for h in range(r * Hl, (r + 1) * Hl)})
+        held = sorted({int(v) % hkv for v in y[r * per_rank:(r + 1) * per_rank].ravel()})
+        assert held == needed
+        assert all(int(v) // hkv == t for i in range(per_rank) for t, v in enumerate(y[r * per_rank + i, :, 0]))
+    assert (rep == 1) == (hkv % sp == 0)
+
+
+def test_kv_swap_without_replication_is_the_plain_swap():
+    rng = np.random.default_rng(41)
+    T, H, D, sp = 16, 8, 4, 4
+    x = rand_bits(rng, (T, H, D))
+    plain = relayout.seq_to_head(x.reshape(sp, T // sp, H, D), sp).reshape(H, T, D)
+    assert np.array_equal(relayout.seq_to_head_kv(x, sp), plain)
+
+
+@pytest.mark.parametrize("hkv,sp", [(2, 8), (1, 4), (4, 4), (8, 2)])
+def test_kv_grad_is_the_adjoint_of_the_replication(hkv, sp):
+    """<R x, y> = <x, R^T y>: the gradient of a replication is the sum over replicas."""
+    rng = np.random.default_rng(hkv * 10 + sp)
+    T, D = 12, 3
+    x = rng.standard_normal((T, hkv, D))
+    y = rng.standard_normal((max(sp, hkv), T, D))
+    xb = f32_to_bf16_bits(x.astype(np.float32))
+    rx = f64(relayout.seq_to_head_kv(xb, sp))
+    lhs = float((rx * y).sum())
+    rhs = float((f64(xb) * relayout.head_to_seq_kv_grad(y, sp, hkv)).sum())
+    assert abs(lhs - rhs) <= 1e-9 * max(1.0, abs(lhs))
+
+
+def test_kv_grad_of_identical_replicas_scales():
+    y1 = np.arange(24, dtype=np.float64).reshape(1, 6, 4)
+    y = np.concatenate([y1] * 4)               # four ranks sharing one head
+    assert np.array_equal(relayout.head_to_seq_kv_grad(y, 4, 1), 4 * y1.transpose(1, 0, 2))
+
+
+def test_kv_replication_rejects_indivisible():
+    with pytest.raises(ValueError):
+        relayout.kv_replication(4, 3)

@@ -25,7 +25,7 @@ import math
 
 from ._lib import (USP_BF16, USP_FP16, USP_FP32, USP_OK, UspError, attn_bwd_varlen, attn_fwd_varlen,  # noqa: F401
                    attn_workspace_size, cu_seqlens_to_position_ids, debug_wait_timeout, get_device_status,
-                   head_to_seq, load, position_ids_to_cu_seqlens, position_ids_workspace_size, seq_to_head,
+                   head_to_seq, head_to_seq_kv_grad, load, position_ids_to_cu_seqlens, seq_to_head_kv, position_ids_workspace_size, seq_to_head,
                    shift_labels, sp_weighted_loss, status_string, ulysses_attn_bwd, ulysses_attn_fwd)
 from .sp_group import gather_loss_and_good, sp_group_loss  # noqa: F401
 
@@ -33,7 +33,7 @@ __all__ = [
     "seq_to_head", "head_to_seq", "attn_fwd_varlen", "attn_bwd_varlen", "ulysses_attn_fwd", "ulysses_attn_bwd",
     "attn_workspace_size", "get_device_status", "status_string", "UspError", "UlyssesAttention", "load",
     "position_ids_to_cu_seqlens", "position_ids_workspace_size", "cu_seqlens_to_position_ids", "shift_labels",
-    "sp_weighted_loss", "gather_loss_and_good", "sp_group_loss",
+    "sp_weighted_loss", "gather_loss_and_good", "sp_group_loss", "seq_to_head_kv", "head_to_seq_kv_grad",
 ]
 
 
@@ -59,24 +59,28 @@ class UlyssesAttention:
         self.grad_dtype = grad_dtype or torch.bfloat16
         bf = torch.bfloat16
         T, D = total_tokens, head_dim
+        # key/value heads of the head-sharded layout: split over the ranks, or with fewer
+        # heads than ranks one replicated head per rank
+        self.hkv_h = max(hkv, sp)
         if not fused:
+            hk = self.hkv_h
             self.q_h = torch.empty(hq, T, D, dtype=bf, device=device)
-            self.k_h = torch.empty(hkv, T, D, dtype=bf, device=device)
-            self.v_h = torch.empty(hkv, T, D, dtype=bf, device=device)
+            self.k_h = torch.empty(hk, T, D, dtype=bf, device=device)
+            self.v_h = torch.empty(hk, T, D, dtype=bf, device=device)
             self.o_h = torch.empty(hq, T, D, dtype=bf, device=device)
             self.do_h = torch.empty(hq, T, D, dtype=bf, device=device)
             gd = self.grad_dtype
             self.dq_h = torch.empty(hq, T, D, dtype=gd, device=device)
-            self.dk_h = torch.empty(hkv, T, D, dtype=gd, device=device)
-            self.dv_h = torch.empty(hkv, T, D, dtype=gd, device=device)
+            self.dk_h = torch.empty(hk, T, D, dtype=gd, device=device)
+            self.dv_h = torch.empty(hk, T, D, dtype=gd, device=device)
         self.lse = torch.empty(hq, T, dtype=torch.float32, device=device)
         self.o_seq = torch.empty(T, hq, D, dtype=bf, device=device)
         gd = self.grad_dtype
         self.dq_seq = torch.empty(T, hq, D, dtype=gd, device=device)
         self.dk_seq = torch.empty(T, hkv, D, dtype=gd, device=device)
         self.dv_seq = torch.empty(T, hkv, D, dtype=gd, device=device)
-        self.ws_bytes = max(attn_workspace_size(T, num_seqs, hq, hkv, D, False),
-                            attn_workspace_size(T, num_seqs, hq, hkv, D, True))
+        self.ws_bytes = max(attn_workspace_size(T, num_seqs, hq, h, D, b) for h in (hkv, self.hkv_h)
+                            for b in (False, True))
         self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=device)
         self._saved = None
 
@@ -88,10 +92,10 @@ class UlyssesAttention:
             self._saved = (xq, xk, xv)
             return self.o_seq
         seq_to_head(xq, self.q_h, sp, stream)
-        seq_to_head(xk, self.k_h, sp, stream)
-        seq_to_head(xv, self.v_h, sp, stream)
+        seq_to_head_kv(xk, self.k_h, sp, stream)
+        seq_to_head_kv(xv, self.v_h, sp, stream)
         attn_fwd_varlen(self.q_h, self.k_h, self.v_h, self.o_h, self.lse, cu_seqlens, self.B, self.T, self.hq,
-                        self.hkv, self.D, self.scale, self.causal, self.ws, self.ws_bytes, stream)
+                        self.hkv_h, self.D, self.scale, self.causal, self.ws, self.ws_bytes, stream)
         head_to_seq(self.o_h, self.o_seq, sp, stream)
         return self.o_seq
 
@@ -109,11 +113,11 @@ class UlyssesAttention:
             return self.dq_seq, self.dk_seq, self.dv_seq
         seq_to_head(d_out, self.do_h, sp, stream)
         attn_bwd_varlen(self.q_h, self.k_h, self.v_h, self.o_h, self.lse, self.do_h, self.dq_h, self.dk_h,
-                        self.dv_h, gdt, cu_seqlens, self.B, self.T, self.hq, self.hkv, self.D, self.scale,
+                        self.dv_h, gdt, cu_seqlens, self.B, self.T, self.hq, self.hkv_h, self.D, self.scale,
                         self.causal, self.ws, self.ws_bytes, stream)
         head_to_seq(self.dq_h, self.dq_seq, sp, stream)
-        head_to_seq(self.dk_h, self.dk_seq, sp, stream)
-        head_to_seq(self.dv_h, self.dv_seq, sp, stream)
+        head_to_seq_kv_grad(self.dk_h, self.dk_seq, sp, self.hkv, stream)
+        head_to_seq_kv_grad(self.dv_h, self.dv_seq, sp, self.hkv, stream)
         return self.dq_seq, self.dk_seq, self.dv_seq
 
     def device_status(self, stream=None) -> int:

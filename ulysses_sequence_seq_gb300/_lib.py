@@ -37,6 +37,8 @@ EXPORTED = (
     "usp_attn_fwd_varlen_noalloc",
     "usp_ulysses_attn_fwd",
     "usp_ulysses_attn_bwd",
+    "usp_seq_to_head_kv",
+    "usp_head_to_seq_kv_grad",
     "usp_position_ids_workspace_size",
     "usp_position_ids_to_cu_seqlens",
     "usp_cu_seqlens_to_position_ids",
@@ -83,6 +85,8 @@ def load(build_if_missing: bool = True):
     L.usp_attn_fwd_varlen_noalloc.argtypes = [P, P, P, P, P, P, I, I64, I, I, I, F, I, P, P]
     L.usp_ulysses_attn_fwd.argtypes = [P, P, P, P, P, P, I, I64, I, I, I, I, F, I, P, Z, P]
     L.usp_ulysses_attn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I, P, I, I64, I, I, I, I, F, I, P, Z, P]
+    L.usp_seq_to_head_kv.argtypes = [P, P, I, I64, I, I, I, P]
+    L.usp_head_to_seq_kv_grad.argtypes = [P, P, I, I64, I, I, I, P]
     L.usp_position_ids_workspace_size.argtypes = [I64]
     L.usp_position_ids_workspace_size.restype = Z
     L.usp_position_ids_to_cu_seqlens.argtypes = [P, I64, P, I, P, P, Z, P]
@@ -92,7 +96,8 @@ def load(build_if_missing: bool = True):
     for name in ("usp_seq_to_head", "usp_head_to_seq", "usp_attn_fwd_varlen", "usp_attn_bwd_varlen",
                  "usp_get_device_status", "usp_debug_wait_timeout", "usp_attn_fwd_varlen_noalloc",
                  "usp_ulysses_attn_fwd", "usp_ulysses_attn_bwd", "usp_position_ids_to_cu_seqlens",
-                 "usp_cu_seqlens_to_position_ids", "usp_shift_labels", "usp_sp_weighted_loss"):
+                 "usp_cu_seqlens_to_position_ids", "usp_shift_labels", "usp_sp_weighted_loss",
+                 "usp_seq_to_head_kv", "usp_head_to_seq_kv_grad"):
         getattr(L, name).restype = I
     _lib = L
     return _lib
@@ -150,6 +155,26 @@ def head_to_seq(y, out, sp: int, stream=None):
     H = y.numel() // (T * D)
     _check("usp_head_to_seq", load().usp_head_to_seq(_ptr(y), _ptr(out), int(sp), int(T), int(H), int(D),
                                                      _dtype_code(y), _stream(stream)))
+    return out
+
+
+def seq_to_head_kv(x, out, sp: int, stream=None):
+    """x: [sp][T/sp][hkv][D] -> out: [max(sp, hkv)][T][D] grouped per rank; with fewer
+    heads than ranks each head is replicated to sp / hkv consecutive ranks."""
+    H, D = x.shape[-2], x.shape[-1]
+    T = x.numel() // (H * D)
+    _check("usp_seq_to_head_kv", load().usp_seq_to_head_kv(_ptr(x), _ptr(out), int(sp), int(T), int(H), int(D),
+                                                            _dtype_code(x), _stream(stream)))
+    return out
+
+
+def head_to_seq_kv_grad(y, out, sp: int, hkv: int, stream=None):
+    """y: [max(sp, hkv)][T][D] per-rank key/value gradients -> out: [sp][T/sp][hkv][D];
+    the gradients of a replicated head are summed."""
+    D = y.shape[-1]
+    T = y.numel() // (D * max(sp, hkv))
+    _check("usp_head_to_seq_kv_grad", load().usp_head_to_seq_kv_grad(_ptr(y), _ptr(out), int(sp), int(T), int(hkv),
+                                                                      int(D), _dtype_code(y), _stream(stream)))
     return out
 
 

@@ -255,7 +255,10 @@ usp_status attn_bwd_impl(const void* q, const void* k, const void* v, const void
 // padded to a multiple of sp_size (HF guide, "Configurar").
 usp_status check_sp(int sp, int64_t total_tokens, int hq, int hkv) {
     if (sp < 1 || hq < 1 || hkv < 1 || total_tokens < 0) return USP_ERR_INVALID_ARG;
-    if (hq % sp != 0 || hkv % sp != 0 || total_tokens % sp != 0) return USP_ERR_INVALID_ARG;
+    if (hq % sp != 0 || total_tokens % sp != 0) return USP_ERR_INVALID_ARG;
+    // key/value heads either split over the ranks or, with fewer heads than ranks, each
+    // replicated over sp / hkv ranks (the fused kernels read the shared head in place)
+    if (hkv % sp != 0 && sp % hkv != 0) return USP_ERR_INVALID_ARG;
     return USP_OK;
 }
 
