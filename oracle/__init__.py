@@ -36,13 +36,15 @@ def _load():
         lib.oracle_attn_fwd.restype = ctypes.c_int
         lib.oracle_attn_fwd.argtypes = [p, p, p, p, ctypes.c_int, ctypes.c_int64, ctypes.c_int,
                                         ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int,
-                                        p, ctypes.c_int, p, ctypes.c_int64, p, p]
+                                        p, ctypes.c_int, p, ctypes.c_int64, p, p, ctypes.c_int]
         lib.oracle_attn_bwd.restype = ctypes.c_int
         lib.oracle_attn_bwd.argtypes = [p, p, p, p, p, ctypes.c_int, ctypes.c_int64, ctypes.c_int,
                                         ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int,
                                         p, ctypes.c_int, p, ctypes.c_int64,
                                         p, ctypes.c_int, p, ctypes.c_int64,
-                                        p, p, p, p, p]
+                                        p, p, p, p, p, ctypes.c_int]
+        lib.oracle_decode16.restype = None
+        lib.oracle_decode16.argtypes = [p, ctypes.c_int64, ctypes.c_int, p]
         lib.oracle_num_threads.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -58,8 +60,22 @@ def _ptr(a):
 
 def _bits(a):
     a = np.ascontiguousarray(a)
-    assert a.dtype == np.uint16, "oracle inputs are bf16 bit patterns (uint16)"
+    assert a.dtype == np.uint16, "oracle inputs are 16-bit patterns (uint16)"
     return a
+
+
+def _f16_flag(dtype: str) -> int:
+    if dtype not in ("bf16", "f16"):
+        raise ValueError("dtype is 'bf16' or 'f16'")
+    return 1 if dtype == "f16" else 0
+
+
+def decode16(bits, dtype: str = "bf16") -> np.ndarray:
+    """The oracle's exact 16-bit -> float64 decoding (bf16 or IEEE fp16)."""
+    b = _bits(bits)
+    out = np.empty(b.shape, dtype=np.float64)
+    _load().oracle_decode16(_ptr(b), int(b.size), _f16_flag(dtype), _ptr(out))
+    return out
 
 
 def _opt_list(x, dtype):
@@ -69,10 +85,11 @@ def _opt_list(x, dtype):
     return arr, int(arr.size)
 
 
-def attn_fwd(q, k, v, cu_seqlens, causal=True, scale=None, heads=None, rows=None):
+def attn_fwd(q, k, v, cu_seqlens, causal=True, scale=None, heads=None, rows=None, dtype="bf16"):
     """float64 O [nheads][nrows][D] and LSE [nheads][nrows].
 
-    q: uint16 [hq][T][D]; k, v: uint16 [hkv][T][D]; cu_seqlens: int32 [B+1].
+    q: uint16 [hq][T][D]; k, v: uint16 [hkv][T][D] (bf16 or fp16 bits per `dtype`);
+    cu_seqlens: int32 [B+1].
     """
     q, k, v = _bits(q), _bits(k), _bits(v)
     hq, T, D = q.shape
@@ -88,14 +105,14 @@ def attn_fwd(q, k, v, cu_seqlens, causal=True, scale=None, heads=None, rows=None
     lse = np.zeros((nh_out, nr_out), dtype=np.float64)
     rc = _load().oracle_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(cu), len(cu) - 1, T, hq, hkv, D,
                                  float(scale), int(bool(causal)), _ptr(h_arr), nh, _ptr(r_arr), nr,
-                                 _ptr(o), _ptr(lse))
+                                 _ptr(o), _ptr(lse), _f16_flag(dtype))
     if rc != 0:
         raise ValueError("oracle_attn_fwd: invalid arguments or cu_seqlens")
     return o, lse
 
 
 def attn_bwd(q, k, v, do, cu_seqlens, causal=True, scale=None, q_heads=None, q_rows=None,
-             kv_heads=None, k_rows=None, want_stats=False):
+             kv_heads=None, k_rows=None, want_stats=False, dtype="bf16"):
     """float64 dQ [nqh][nqr][D], dK/dV [nkvh][nkr][D] (and lse, Delta of the dQ rows)."""
     q, k, v, do = _bits(q), _bits(k), _bits(v), _bits(do)
     hq, T, D = q.shape
@@ -119,7 +136,7 @@ def attn_bwd(q, k, v, do, cu_seqlens, causal=True, scale=None, q_heads=None, q_r
     rc = _load().oracle_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(cu), len(cu) - 1, T, hq,
                                  hkv, D, float(scale), int(bool(causal)),
                                  _ptr(qh), nqh, _ptr(qr), nqr, _ptr(kh), nkh, _ptr(kr), nkr,
-                                 _ptr(dq), _ptr(dk), _ptr(dv), _ptr(lse), _ptr(dl))
+                                 _ptr(dq), _ptr(dk), _ptr(dv), _ptr(lse), _ptr(dl), _f16_flag(dtype))
     if rc != 0:
         raise ValueError("oracle_attn_bwd: invalid arguments or cu_seqlens")
     if want_stats:

@@ -33,7 +33,8 @@
  * are the textbook derivative of softmax attention.
  *
  * Query head h reads key/value head h / (hq/hkv) (contiguous GQA groups).
- * Inputs are bf16 bit patterns (uint16), converted exactly to double.
+ * Inputs are 16-bit patterns (uint16) of bf16, or of IEEE binary16 (fp16) when the
+ * call's in_f16 flag is set, converted exactly to double.
  * Layout of every activation: [heads][T][D], row-major.
  */
 #include <math.h>
@@ -49,6 +50,26 @@ static double bf16_to_double(uint16_t b) {
     float f;
     memcpy(&f, &u, sizeof f);
     return (double)f;
+}
+
+/* IEEE 754 binary16: sign, 5 exponent bits (bias 15), 10 fraction bits. */
+static double f16_to_double(uint16_t h) {
+    const int sign = (h >> 15) & 1, ex = (h >> 10) & 0x1f, man = h & 0x3ff;
+    double v;
+    if (ex == 0) v = ldexp((double)man, -24);                 /* zero and subnormals: man * 2^-24 */
+    else if (ex == 31) v = man ? NAN : INFINITY;
+    else v = ldexp((double)(man | 0x400), ex - 25);           /* 1.man * 2^(ex - 15) */
+    return sign ? -v : v;
+}
+
+/* Element type of the current call's inputs (set before any parallel region). */
+static int g_in_f16 = 0;
+
+static double elem_to_double(uint16_t b) { return g_in_f16 ? f16_to_double(b) : bf16_to_double(b); }
+
+/* The decoder on its own, so that it can be checked against other implementations. */
+void oracle_decode16(const uint16_t* in, int64_t n, int f16, double* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = f16 ? f16_to_double(in[i]) : bf16_to_double(in[i]);
 }
 
 /* seg[t] = b such that cu[b] <= t < cu[b+1]; returns 0 on success. */
@@ -69,7 +90,7 @@ static int allowed(const int32_t* seg, int64_t i, int64_t j, int causal) {
 
 static double dot_bf16(const uint16_t* a, const uint16_t* b, int D) {
     double s = 0.0;
-    for (int d = 0; d < D; ++d) s += bf16_to_double(a[d]) * bf16_to_double(b[d]);
+    for (int d = 0; d < D; ++d) s += elem_to_double(a[d]) * elem_to_double(b[d]);
     return s;
 }
 
@@ -93,7 +114,7 @@ static double row_scores_lse(const uint16_t* qi, const uint16_t* kh, const int32
 
 /*
  * Forward.  Computes O and LSE for the listed query heads and rows.
- *   q [hq][T][D], k/v [hkv][T][D]           bf16 bits
+ *   q [hq][T][D], k/v [hkv][T][D]           16-bit patterns (bf16, or fp16 with in_f16)
  *   heads[nheads] (NULL: all hq heads), rows[nrows] (NULL: all T rows)
  *   o   [nheads][nrows][D] double, lse [nheads][nrows] double (either may be NULL)
  * Returns 0, or -1 when cu_seqlens is malformed or an argument is invalid.
@@ -102,8 +123,9 @@ int oracle_attn_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                     const int32_t* cu, int nseq, int64_t T, int hq, int hkv, int D,
                     double scale, int causal,
                     const int32_t* heads, int nheads, const int64_t* rows, int64_t nrows,
-                    double* o, double* lse) {
+                    double* o, double* lse, int in_f16) {
     if (hq <= 0 || hkv <= 0 || hq % hkv != 0 || D <= 0 || T < 0 || nseq < 0) return -1;
+    g_in_f16 = in_f16 ? 1 : 0;
     int32_t* seg = (int32_t*)malloc(sizeof(int32_t) * (size_t)(T > 0 ? T : 1));
     if (!seg) return -1;
     if (build_segments(cu, nseq, T, seg) != 0) { free(seg); return -1; }
@@ -129,7 +151,7 @@ int oracle_attn_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                 for (int64_t j = 0; j < T; ++j) {
                     if (!allowed(seg, i, j, causal)) continue;
                     const double p = exp(s[j] - l);
-                    for (int d = 0; d < D; ++d) acc[d] += p * bf16_to_double(vh[j * D + d]);
+                    for (int d = 0; d < D; ++d) acc[d] += p * elem_to_double(vh[j * D + d]);
                 }
                 if (o) for (int d = 0; d < D; ++d) o[((int64_t)hi * nrows + ri) * D + d] = acc[d];
                 if (lse) lse[(int64_t)hi * nrows + ri] = l;
@@ -155,8 +177,9 @@ int oracle_attn_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, con
                     double scale, int causal,
                     const int32_t* q_heads, int nqh, const int64_t* q_rows, int64_t nqr,
                     const int32_t* kv_heads, int nkvh, const int64_t* k_rows, int64_t nkr,
-                    double* dq, double* dk, double* dv, double* lse_out, double* delta_out) {
+                    double* dq, double* dk, double* dv, double* lse_out, double* delta_out, int in_f16) {
     if (hq <= 0 || hkv <= 0 || hq % hkv != 0 || D <= 0 || T < 0 || nseq < 0) return -1;
+    g_in_f16 = in_f16 ? 1 : 0;
     int32_t* seg = (int32_t*)malloc(sizeof(int32_t) * (size_t)(T > 0 ? T : 1));
     if (!seg) return -1;
     if (build_segments(cu, nseq, T, seg) != 0) { free(seg); return -1; }
@@ -234,7 +257,7 @@ int oracle_attn_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, con
                             const double p = exp(sij - lse_all[i]);
                             const double dp = dot_bf16(doh + i * D, vh + j * D, D);
                             const double ds = p * (dp - del_all[i]);
-                            for (int d = 0; d < D; ++d) acc[d] += ds * bf16_to_double(kh[j * D + d]);
+                            for (int d = 0; d < D; ++d) acc[d] += ds * elem_to_double(kh[j * D + d]);
                         }
                         if (dq) for (int d = 0; d < D; ++d) dq[((int64_t)hi * nqr + ri) * D + d] = scale * acc[d];
                         if (lse_out) lse_out[(int64_t)hi * nqr + ri] = lse_all[i];
@@ -259,8 +282,8 @@ int oracle_attn_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, con
                             const double dp = dot_bf16(doh + i * D, vh + j * D, D);
                             const double ds = p * (dp - del_all[i]);
                             for (int d = 0; d < D; ++d) {
-                                ak[d] += ds * bf16_to_double(qh[i * D + d]);
-                                av[d] += p * bf16_to_double(doh[i * D + d]);
+                                ak[d] += ds * elem_to_double(qh[i * D + d]);
+                                av[d] += p * elem_to_double(doh[i * D + d]);
                             }
                         }
                         /* the first query head of a group initialises, the others add */

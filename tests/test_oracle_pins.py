@@ -387,3 +387,40 @@ def test_kv_grad_of_identical_replicas_scales():
 def test_kv_replication_rejects_indivisible():
     with pytest.raises(ValueError):
         relayout.kv_replication(4, 3)
+
+
+# ================================================================ fp16 inputs
+def test_decoders_exhaustive():
+    """Every 16-bit pattern decodes as numpy's own float16 / the bf16 bit layout says."""
+    allbits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    got16 = oracle.decode16(allbits, "f16")
+    want16 = allbits.view(np.float16).astype(np.float64)
+    assert np.array_equal(np.isnan(got16), np.isnan(want16))
+    ok = ~np.isnan(want16)
+    assert np.array_equal(got16[ok], want16[ok])
+    gotb = oracle.decode16(allbits, "bf16")
+    wantb = (allbits.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+    ok = ~np.isnan(wantb)
+    assert np.array_equal(gotb[ok], wantb[ok]) and np.array_equal(np.isnan(gotb), np.isnan(wantb))
+
+
+def test_f16_attention_equals_bf16_attention_on_shared_values():
+    """Inputs exactly representable in both types give the same float64 attention."""
+    rng = np.random.default_rng(52)
+    H, T, D = 2, 40, 16
+    cu = np.array([0, 17, 40], dtype=np.int32)
+    xs = []
+    for _ in range(4):
+        b = rand_bits(rng, (H, T, D))
+        x = f64(b)
+        x[np.abs(x) < 2.0 ** -14] = 0.0            # outside fp16's normal range: drop
+        xs.append(x.astype(np.float32))
+    bf = [f32_to_bf16_bits(x) for x in xs]
+    hf = [x.astype(np.float16).view(np.uint16) for x in xs]
+    assert all(np.array_equal(f64(b), oracle.decode16(h, "f16")) for b, h in zip(bf, hf))
+    o1, l1 = oracle.attn_fwd(bf[0], bf[1], bf[2], cu)
+    o2, l2 = oracle.attn_fwd(hf[0], hf[1], hf[2], cu, dtype="f16")
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+    g1 = oracle.attn_bwd(bf[0], bf[1], bf[2], bf[3], cu)
+    g2 = oracle.attn_bwd(hf[0], hf[1], hf[2], hf[3], cu, dtype="f16")
+    assert all(np.array_equal(a, b) for a, b in zip(g1, g2))

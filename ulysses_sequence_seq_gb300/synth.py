@@ -146,39 +146,49 @@ def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
     return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
 
 
+def f32_to_f16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 to IEEE fp16 (numpy's conversion: nearest, ties to even) as uint16 bits."""
+    return np.ascontiguousarray(x, dtype=np.float32).astype(np.float16).view(np.uint16)
+
+
+def to_bits(x: np.ndarray, dtype: str) -> np.ndarray:
+    return f32_to_f16_bits(x) if dtype == "f16" else f32_to_bf16_bits(x)
+
+
 # ----------------------------------------------------------------------------- activations
-def head_bits(w: Workload, tensor: str, head: int, std: float = 1.0) -> np.ndarray:
-    """One head of one activation tensor: uint16 bf16 bits, shape [T][D]."""
+def head_bits(w: Workload, tensor: str, head: int, std: float = 1.0, dtype: str = "bf16") -> np.ndarray:
+    """One head of one activation tensor: uint16 bits (bf16, or fp16 for dtype "f16") of
+    the same N(0, std^2) float32 draws, shape [T][D]."""
     seed = 1000 * w.index + TENSORS[tensor]
     rng = np.random.default_rng([seed, head])
     x = rng.standard_normal((w.total_tokens, w.head_dim), dtype=np.float32)
     if std != 1.0:
         x *= np.float32(std)
-    return f32_to_bf16_bits(x)
+    return to_bits(x, dtype)
 
 
 def num_heads(w: Workload, tensor: str) -> int:
     return w.hkv if tensor in ("k", "v") else w.hq
 
 
-def head_sharded_bits(w: Workload, tensor: str, heads=None) -> np.ndarray:
-    """Head-sharded activation [H][T][D] (uint16 bf16 bits) for the listed heads."""
+def head_sharded_bits(w: Workload, tensor: str, heads=None, dtype: str = "bf16") -> np.ndarray:
+    """Head-sharded activation [H][T][D] (uint16 bits) for the listed heads."""
     if heads is None:
         heads = range(num_heads(w, tensor))
     heads = list(heads)
     out = np.empty((len(heads), w.total_tokens, w.head_dim), dtype=np.uint16)
     for i, h in enumerate(heads):
-        out[i] = head_bits(w, tensor, h)
+        out[i] = head_bits(w, tensor, h, dtype=dtype)
     return out
 
 
-def seq_sharded_bits(w: Workload, tensor: str) -> np.ndarray:
-    """Seq-sharded activation [sp][T/sp][H][D] (uint16 bf16 bits): the same draws as
+def seq_sharded_bits(w: Workload, tensor: str, dtype: str = "bf16") -> np.ndarray:
+    """Seq-sharded activation [sp][T/sp][H][D] (uint16 bits): the same draws as
     :func:`head_sharded_bits`, stored token-major."""
     H = num_heads(w, tensor)
     out = np.empty((w.total_tokens, H, w.head_dim), dtype=np.uint16)
     for h in range(H):
-        out[:, h, :] = head_bits(w, tensor, h)
+        out[:, h, :] = head_bits(w, tensor, h, dtype=dtype)
     return out.reshape(w.sp, w.total_tokens // w.sp, H, w.head_dim)
 
 
