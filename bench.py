@@ -206,15 +206,21 @@ def run_usp(args, w):
     dev = torch.device("cuda", local_rank)
     T, H, HKV, D, sp = w.total_tokens, w.hq, w.hkv, w.head_dim, w.sp
 
+    f16 = args.dtype == "f16"
+    if f16 and args.unfused:
+        raise SystemExit("fp16 activations run on the fused path only")
+    act_dtype = torch.float16 if f16 else torch.bfloat16
+    grad_code = usp.USP_FP16 if f16 else usp.USP_BF16
+
     def to_host_pinned(bits):
-        t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+        t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(act_dtype)
         return t.pin_memory()
 
-    hq_, hk_, hv_, hdo_ = (to_host_pinned(seq_sharded_bits(w, t)) for t in ("q", "k", "v", "do"))
+    hq_, hk_, hv_, hdo_ = (to_host_pinned(seq_sharded_bits(w, t, dtype=args.dtype)) for t in ("q", "k", "v", "do"))
     xq, xk, xv, xdo = (t.to(dev) for t in (hq_, hk_, hv_, hdo_))
     cu = torch.from_numpy(w.cu_seqlens()).to(dev)
     fused = not args.unfused
-    layer = usp.UlyssesAttention(T, w.num_seqs, H, HKV, D, sp, causal=True, device=dev, fused=fused)
+    layer = usp.UlyssesAttention(T, w.num_seqs, H, HKV, D, sp, causal=True, device=dev, fused=fused, dtype=act_dtype)
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)   # > L2 (129 MB)
     stream = torch.cuda.current_stream(dev)
 
@@ -233,7 +239,7 @@ def run_usp(args, w):
             ev[2].record(stream)
             ev[3].record(stream)
             usp.ulysses_attn_bwd(xq, xk, xv, layer.o_seq, layer.lse, xdo, layer.dq_seq, layer.dk_seq, layer.dv_seq,
-                                 usp.USP_BF16, cu, layer.B, T, sp, H, HKV, D, layer.scale, True, layer.ws,
+                                 grad_code, cu, layer.B, T, sp, H, HKV, D, layer.scale, True, layer.ws,
                                  layer.ws_bytes)
             ev[4].record(stream)
             ev[5].record(stream)
@@ -398,7 +404,7 @@ def run_usp(args, w):
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "vs_baseline": None, "dtype": args.dtype, "data": "synthetic",
         "config": {"workload": workload_desc(w), "seq_len": T, "heads": H, "kv_heads": HKV, "head_dim": D,
                    "sp": sp, "parallelism": f"replicas x{world} (sp={sp} simulated per GPU)",
                    "path": "fused layout swaps (usp_ulysses_attn_fwd/bwd)" if fused else
@@ -443,6 +449,8 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=4096)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--unfused", action="store_true", help="time separate re-layout kernels around the attention")
+    ap.add_argument("--dtype", default="bf16", choices=["bf16", "f16"],
+                    help="activation type (fp32 accumulation and softmax either way)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     from ulysses_sequence_seq_gb300.synth import WORKLOADS

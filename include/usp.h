@@ -177,8 +177,11 @@ usp_status usp_attn_bwd_varlen(const void* q, const void* k, const void* v, cons
  *   device the swap only changes which rows the kernel reads: head h of token t lives
  *   at row t*H + h of the seq-sharded buffer and at row h*T + t of the head-sharded
  *   one, whatever sp is.
- *   q   : bf16 [sp][T/sp][hq][D]      k, v : bf16 [sp][T/sp][hkv][D]
- *   o   : bf16 [sp][T/sp][hq][D]      lse  : fp32 [hq][T] (as usp_attn_fwd_varlen)
+ *   q   : dt [sp][T/sp][hq][D]        k, v : dt [sp][T/sp][hkv][D]
+ *   o   : dt [sp][T/sp][hq][D]        lse  : fp32 [hq][T] (as usp_attn_fwd_varlen)
+ *   dt  : USP_BF16 or USP_FP16, the type of q, k, v and o. Scores, softmax and the
+ *         accumulators are fp32 either way; P is rounded to dt before the P.V MMA,
+ *         whose operands must share a type. USP_FP32 returns USP_ERR_UNSUPPORTED.
  *   The workspace is that of usp_attn_fwd_varlen for the same sizes.
  * Errors: as usp_attn_fwd_varlen, and USP_ERR_INVALID_ARG when sp < 1, hq % sp or
  *   total_tokens % sp is non-zero (guide, "Configurar"), or when neither hkv % sp nor
@@ -187,16 +190,17 @@ usp_status usp_attn_bwd_varlen(const void* q, const void* k, const void* v, cons
  */
 usp_status usp_ulysses_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                                 const int32_t* cu_seqlens, int num_seqs, int64_t total_tokens, int sp, int hq,
-                                int hkv, int head_dim, float softmax_scale, int causal, void* workspace,
-                                size_t ws_bytes, void* stream);
+                                int hkv, int head_dim, float softmax_scale, int causal, usp_dtype dt,
+                                void* workspace, size_t ws_bytes, void* stream);
 
 /*
  * usp_ulysses_attn_bwd -- the backward attention step with the layout swaps fused:
  * the seq-sharded dO in, the seq-sharded dq, dk, dv out. Equals usp_seq_to_head on dO,
  * usp_attn_bwd_varlen (on the head-sharded q, k, v, o), then usp_head_to_seq on the
  * three gradients.
- *   q, o, d_o : bf16 [sp][T/sp][hq][D]; k, v : bf16 [sp][T/sp][hkv][D]; lse : fp32 [hq][T].
- *   dq : [sp][T/sp][hq][D], dk, dv : [sp][T/sp][hkv][D] of grad_dt (USP_BF16 or USP_FP32).
+ *   q, o, d_o : dt [sp][T/sp][hq][D]; k, v : dt [sp][T/sp][hkv][D]; lse : fp32 [hq][T];
+ *   dt USP_BF16 or USP_FP16 (P and dS are rounded to dt before their MMAs).
+ *   dq : [sp][T/sp][hq][D], dk, dv : [sp][T/sp][hkv][D] of grad_dt: dt or USP_FP32.
  *   The workspace is that of usp_attn_bwd_varlen for the same sizes.
  * Errors: as usp_attn_bwd_varlen, and the sp rules of usp_ulysses_attn_fwd.
  */
@@ -204,7 +208,7 @@ usp_status usp_ulysses_attn_bwd(const void* q, const void* k, const void* v, con
                                 const float* lse, const void* d_o, void* dq, void* dk, void* dv,
                                 usp_dtype grad_dt, const int32_t* cu_seqlens, int num_seqs, int64_t total_tokens,
                                 int sp, int hq, int hkv, int head_dim, float softmax_scale, int causal,
-                                void* workspace, size_t ws_bytes, void* stream);
+                                usp_dtype dt, void* workspace, size_t ws_bytes, void* stream);
 
 /*
  * usp_get_device_status -- synchronises `stream`, then returns the status word

@@ -78,3 +78,9 @@ class Problem:
                             self.hq, self.hkv, self.D, 0.0, self.causal, self.ws, self.ws_bytes)
         status = usp.get_device_status(self.ws)
         return dq, dk, dv, status
+
+
+def dev_16(bits: np.ndarray, dtype) -> torch.Tensor:
+    """uint16 bit patterns -> CUDA tensor of the 16-bit `dtype` (bf16 or fp16) with those bits."""
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16))
+    return t.view(dtype).cuda()

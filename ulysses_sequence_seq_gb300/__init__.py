@@ -50,14 +50,19 @@ class UlyssesAttention:
 
     def __init__(self, total_tokens: int, num_seqs: int, hq: int, hkv: int, head_dim: int, sp: int,
                  causal: bool = True, softmax_scale: float = 0.0, device="cuda", grad_dtype=None,
-                 fused: bool = True):
+                 fused: bool = True, dtype=None):
         import torch
         self.T, self.B, self.hq, self.hkv, self.D, self.sp = total_tokens, num_seqs, hq, hkv, head_dim, sp
         self.causal = causal
         self.fused = fused
         self.scale = softmax_scale if softmax_scale > 0 else 1.0 / math.sqrt(head_dim)
-        self.grad_dtype = grad_dtype or torch.bfloat16
-        bf = torch.bfloat16
+        self.dtype = dtype or torch.bfloat16
+        if self.dtype not in (torch.bfloat16, torch.float16):
+            raise TypeError("activations must be bf16 or fp16")
+        if self.dtype == torch.float16 and not fused:
+            raise ValueError("fp16 activations run on the fused path")
+        self.grad_dtype = grad_dtype or self.dtype
+        bf = self.dtype
         T, D = total_tokens, head_dim
         # key/value heads of the head-sharded layout: split over the ranks, or with fewer
         # heads than ranks one replicated head per rank
@@ -102,7 +107,7 @@ class UlyssesAttention:
     def backward(self, d_out, cu_seqlens, stream=None):
         import torch
         sp = self.sp
-        gdt = USP_FP32 if self.grad_dtype == torch.float32 else USP_BF16
+        gdt = {torch.float32: USP_FP32, torch.bfloat16: USP_BF16, torch.float16: USP_FP16}[self.grad_dtype]
         if self.fused:
             if self._saved is None:
                 raise RuntimeError("backward() needs a forward() first")

@@ -83,8 +83,8 @@ def load(build_if_missing: bool = True):
     L.usp_status_string.restype = ctypes.c_char_p
     L.usp_debug_wait_timeout.argtypes = [P, Z, ctypes.c_uint64, P]
     L.usp_attn_fwd_varlen_noalloc.argtypes = [P, P, P, P, P, P, I, I64, I, I, I, F, I, P, P]
-    L.usp_ulysses_attn_fwd.argtypes = [P, P, P, P, P, P, I, I64, I, I, I, I, F, I, P, Z, P]
-    L.usp_ulysses_attn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I, P, I, I64, I, I, I, I, F, I, P, Z, P]
+    L.usp_ulysses_attn_fwd.argtypes = [P, P, P, P, P, P, I, I64, I, I, I, I, F, I, I, P, Z, P]
+    L.usp_ulysses_attn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I, P, I, I64, I, I, I, I, F, I, I, P, Z, P]
     L.usp_seq_to_head_kv.argtypes = [P, P, I, I64, I, I, I, P]
     L.usp_head_to_seq_kv_grad.argtypes = [P, P, I, I64, I, I, I, P]
     L.usp_position_ids_workspace_size.argtypes = [I64]
@@ -138,6 +138,10 @@ def _dtype_code(t) -> int:
     if t.dtype == torch.float32:
         return USP_FP32
     raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _input_dtype(x) -> int:
+    return _dtype_code(x) if hasattr(x, "dtype") else USP_BF16
 
 
 def seq_to_head(x, out, sp: int, stream=None):
@@ -202,21 +206,23 @@ def attn_bwd_varlen(q, k, v, o, lse, d_o, dq, dk, dv, grad_dt: int, cu_seqlens, 
 
 def ulysses_attn_fwd(q, k, v, o, lse, cu_seqlens, num_seqs: int, total_tokens: int, sp: int, hq: int, hkv: int,
                      head_dim: int, softmax_scale: float, causal: bool, workspace, ws_bytes: int, stream=None):
-    """Fused forward on the seq-sharded layout: q, k, v, o are [sp][T/sp][H][D]."""
+    """Fused forward on the seq-sharded layout: q, k, v, o are [sp][T/sp][H][D], bf16 or
+    fp16 (taken from q)."""
     _check("usp_ulysses_attn_fwd", load().usp_ulysses_attn_fwd(
         _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(cu_seqlens), int(num_seqs), int(total_tokens), int(sp),
-        int(hq), int(hkv), int(head_dim), float(softmax_scale), int(bool(causal)), _ptr(workspace), int(ws_bytes),
-        _stream(stream)))
+        int(hq), int(hkv), int(head_dim), float(softmax_scale), int(bool(causal)), _input_dtype(q), _ptr(workspace),
+        int(ws_bytes), _stream(stream)))
 
 
 def ulysses_attn_bwd(q, k, v, o, lse, d_o, dq, dk, dv, grad_dt: int, cu_seqlens, num_seqs: int, total_tokens: int,
                      sp: int, hq: int, hkv: int, head_dim: int, softmax_scale: float, causal: bool, workspace,
                      ws_bytes: int, stream=None):
-    """Fused backward on the seq-sharded layout: every activation and gradient is [sp][T/sp][H][D]."""
+    """Fused backward on the seq-sharded layout: every activation and gradient is [sp][T/sp][H][D];
+    activations bf16 or fp16 (taken from q), gradients of grad_dt (that type or fp32)."""
     _check("usp_ulysses_attn_bwd", load().usp_ulysses_attn_bwd(
         _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(d_o), _ptr(dq), _ptr(dk), _ptr(dv), int(grad_dt),
         _ptr(cu_seqlens), int(num_seqs), int(total_tokens), int(sp), int(hq), int(hkv), int(head_dim),
-        float(softmax_scale), int(bool(causal)), _ptr(workspace), int(ws_bytes), _stream(stream)))
+        float(softmax_scale), int(bool(causal)), _input_dtype(q), _ptr(workspace), int(ws_bytes), _stream(stream)))
 
 
 def attn_fwd_varlen_noalloc(q, k, v, o, lse, cu_seqlens, num_seqs: int, total_tokens: int, hq: int, hkv: int,

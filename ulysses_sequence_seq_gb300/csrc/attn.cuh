@@ -13,7 +13,7 @@ struct FwdArgs {
     const int32_t* cu;
     const WorkItem* items;
     WsHeader* hdr;
-    __nv_bfloat16* o;   // [hq][T][D] (head-major) or [T][hq][D] (token_major)
+    uint16_t* o;        // 16-bit [hq][T][D] (head-major) or [T][hq][D] (token_major)
     float* lse;         // [hq][T], natural log
     int64_t T;
     int hq;
@@ -21,6 +21,7 @@ struct FwdArgs {
     int causal;
     int token_major;    // q, k, v, o in the seq-sharded [T][H][D] layout
     float scale_log2;   // softmax scale * log2(e)
+    int f16;            // 16-bit inputs and outputs are fp16 (else bf16)
 };
 
 cudaError_t launch_attn_fwd(int head_dim, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
@@ -35,7 +36,8 @@ struct BwdArgs {
     float* dq_acc;       // [hq][T][D] fp32 accumulator (atomic adds)
     void* dk;            // [hkv][T][D] (head-major) or [T][hkv][D] (token_major)
     void* dv;            // same layout as dk
-    int grad_fp32;       // 1: dk/dv written as fp32, 0: bf16
+    int grad_fp32;       // 1: dk/dv written as fp32, 0: in the input's 16-bit type
+    int f16;             // 16-bit inputs and outputs are fp16 (else bf16)
     int64_t T;
     int hq;
     int hkv;
@@ -53,14 +55,16 @@ cudaError_t launch_attn_bwd(int head_dim, const CUtensorMap& q, const CUtensorMa
 // Delta_i = dO_i . O_i (fp32, [hq][T]) for every query row, and zeroes the dQ accumulator.
 // o / dout are head-major or token-major (token_major); the accumulator is head-major
 // unless dq_token_major.
-cudaError_t launch_bwd_prep(const __nv_bfloat16* o, const __nv_bfloat16* dout, float* delta, float* dq_acc,
-                            int64_t T, int hq, int head_dim, int token_major, int dq_token_major, cudaStream_t s);
+// o / dout are bf16, or fp16 when f16.
+cudaError_t launch_bwd_prep(const void* o, const void* dout, float* delta, float* dq_acc, int64_t T, int hq,
+                            int head_dim, int token_major, int dq_token_major, int f16, cudaStream_t s);
 
-// dq (bf16, head-major or token-major) = the head-major fp32 accumulator rounded to bf16.
-cudaError_t launch_dq_convert(const float* dq_acc, __nv_bfloat16* dq, int64_t T, int hq, int head_dim,
-                              int token_major, cudaStream_t s);
+// dq (16-bit, head-major or token-major) = the head-major fp32 accumulator rounded to bf16,
+// or to fp16 when f16.
+cudaError_t launch_dq_convert(const float* dq_acc, void* dq, int64_t T, int hq, int head_dim, int token_major,
+                              int f16, cudaStream_t s);
 
-// TMA tensor map over a bf16 activation, head-major [heads][T][D] or token-major
+// TMA tensor map over a 16-bit activation (bf16 or fp16: the copy moves bytes), head-major [heads][T][D] or token-major
 // [T][heads][D]: boxes of 64 columns x 128 rows of one head, 128-byte swizzle.
 bool make_activation_map(CUtensorMap* map, const void* base, int64_t T, int heads, int D, int token_major);
 // fp32 dQ accumulator ([heads][T][D] or [T][heads][D]) in 32-column x 32-row boxes with the

@@ -109,7 +109,7 @@ __device__ __forceinline__ bool read_item(uint64_t* item_bars, volatile int* rin
     return true;
 }
 
-template <int D>
+template <int D, bool F16>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -248,10 +248,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idH = idesc_bf16_f32(kBlockN, kHalfCols, false, false);  // S^T, dP^T of one half
-            constexpr uint32_t idDv = idesc_bf16_f32(kBlockN, D, false, true);         // dV (A in TMEM)
-            constexpr uint32_t idDk = idesc_bf16_f32(kBlockN, D, false, true);         // dK (A = dS, K-major)
-            constexpr uint32_t idDq = idesc_bf16_f32(kTileM, D, true, true);           // dQ (A, B MN-major)
+            constexpr uint32_t idH = idesc_16b_f32(kBlockN, kHalfCols, false, false, F16);  // S^T, dP^T of one half
+            constexpr uint32_t idDv = idesc_16b_f32(kBlockN, D, false, true, F16);         // dV (A in TMEM)
+            constexpr uint32_t idDk = idesc_16b_f32(kBlockN, D, false, true, F16);         // dK (A = dS, K-major)
+            constexpr uint32_t idDq = idesc_16b_f32(kTileM, D, true, true, F16);           // dQ (A, B MN-major)
             // 64-bit shared-memory descriptors are built once; a K step or a row offset only
             // adds a constant to the start-address field (addresses stay below 2^18, so the
             // field never carries).
@@ -420,7 +420,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                             if (!kv_ok || c0 < vis_from) pp.x = 0.f;
                             if (!kv_ok || c0 + 1 < vis_from) pp.y = 0.f;
                         }
-                        pkall[16 * c + jj] = pack_bf16x2(pp.x, pp.y);
+                        pkall[16 * c + jj] = pack2<F16>(pp.x, pp.y);
                     }
                     uint32_t pk[16];
 #pragma unroll
@@ -452,11 +452,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         const float2 d =
                             add2(make_float2(__uint_as_float(dr[2 * jj]), __uint_as_float(dr[2 * jj + 1])), nd);
                         const uint32_t pb = pkall[16 * c + jj];
-                        const float2 psc = mul2(
-                            make_float2(__uint_as_float(pb << 16), __uint_as_float(pb & 0xffff0000u)),
-                            make_float2(sc, sc));
+                        const float2 psc = mul2(unpack2<F16>(pb), make_float2(sc, sc));
                         const float2 ds = mul2(psc, d);
-                        pk[jj] = pack_bf16x2(ds.x, ds.y);
+                        pk[jj] = pack2<F16>(ds.x, ds.y);
                     }
                     // row r of the [key][query] dS operand (read K-major by dK, MN-major by dQ)
 #pragma unroll
@@ -496,13 +494,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         dst[jj] = make_float4(__uint_as_float(o[4 * jj]), __uint_as_float(o[4 * jj + 1]),
                                               __uint_as_float(o[4 * jj + 2]), __uint_as_float(o[4 * jj + 3]));
                 } else {
-                    uint4* dst = (uint4*)((__nv_bfloat16*)dst_base + row * D + c);
+                    uint4* dst = (uint4*)((uint16_t*)dst_base + row * D + c);
 #pragma unroll
                     for (int jj = 0; jj < 4; ++jj)
-                        dst[jj] = make_uint4(pack_bf16x2(__uint_as_float(o[8 * jj]), __uint_as_float(o[8 * jj + 1])),
-                                             pack_bf16x2(__uint_as_float(o[8 * jj + 2]), __uint_as_float(o[8 * jj + 3])),
-                                             pack_bf16x2(__uint_as_float(o[8 * jj + 4]), __uint_as_float(o[8 * jj + 5])),
-                                             pack_bf16x2(__uint_as_float(o[8 * jj + 6]), __uint_as_float(o[8 * jj + 7])));
+                        dst[jj] = make_uint4(pack2<F16>(__uint_as_float(o[8 * jj]), __uint_as_float(o[8 * jj + 1])),
+                                             pack2<F16>(__uint_as_float(o[8 * jj + 2]), __uint_as_float(o[8 * jj + 3])),
+                                             pack2<F16>(__uint_as_float(o[8 * jj + 4]), __uint_as_float(o[8 * jj + 5])),
+                                             pack2<F16>(__uint_as_float(o[8 * jj + 6]), __uint_as_float(o[8 * jj + 7])));
                 }
             }
         }
@@ -573,13 +571,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // Delta_i = dO_i . O_i in fp32, and zero row i of the dQ accumulator. TPR threads per row,
-// each owning 8 consecutive elements (one 16-byte vector of bf16).
-template <int D>
-__global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __restrict__ o,
-                                                       const __nv_bfloat16* __restrict__ dout, float* __restrict__ delta,
-                                                       float* __restrict__ dq_acc, int64_t T, int H, int token_major,
-                                                       int dq_token_major) {
-    constexpr int TPR = D / 8;   // threads per row, 8 elements (16 bytes of bf16) each
+// each owning 8 consecutive elements (one 16-byte vector of 16-bit values).
+template <int D, bool F16>
+__global__ void __launch_bounds__(256) bwd_prep_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
+                                                       float* __restrict__ delta, float* __restrict__ dq_acc, int64_t T,
+                                                       int H, int token_major, int dq_token_major) {
+    constexpr int TPR = D / 8;   // threads per row, 8 elements (16 bytes) each
     const int h = blockIdx.y;
     const int sub = threadIdx.x % TPR;
     constexpr int64_t kRowsPerCta = 256 / TPR;
@@ -592,12 +589,12 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
             const int64_t arow = act_row(h, t, T, H, token_major);
             const uint4 ov = __ldg((const uint4*)(o + arow * D) + sub);
             const uint4 dv = __ldg((const uint4*)(dout + arow * D) + sub);
-            const __nv_bfloat162* o2 = (const __nv_bfloat162*)&ov;
-            const __nv_bfloat162* d2 = (const __nv_bfloat162*)&dv;
+            const uint32_t o2[4] = {ov.x, ov.y, ov.z, ov.w};
+            const uint32_t d2[4] = {dv.x, dv.y, dv.z, dv.w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const float2 x = __bfloat1622float2(o2[j]);
-                const float2 y = __bfloat1622float2(d2[j]);
+                const float2 x = unpack2<F16>(o2[j]);
+                const float2 y = unpack2<F16>(d2[j]);
                 acc = fmaf(x.x, y.x, acc);
                 acc = fmaf(x.y, y.y, acc);
             }
@@ -613,9 +610,9 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
     }
 }
 
-// fp32 head-major accumulator -> bf16 dq (head-major or token-major); D4 (= D / 4, a power
-// of two) threads per row, 4 elements each
-template <int D4>
+// fp32 head-major accumulator -> 16-bit dq (head-major or token-major); D4 (= D / 4, a
+// power of two) threads per row, 4 elements each
+template <int D4, bool F16>
 __global__ void __launch_bounds__(256) dq_convert_kernel(const float4* __restrict__ src, uint2* __restrict__ dst,
                                                          int64_t T, int H, int token_major) {
     const int h = blockIdx.y;
@@ -625,7 +622,7 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float4* __restric
         const int64_t t = i / D4;
         const int c = (int)(i % D4);
         const float4 v = s_head[i];
-        dst[act_row(h, t, T, H, token_major) * D4 + c] = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+        dst[act_row(h, t, T, H, token_major) * D4 + c] = make_uint2(pack2<F16>(v.x, v.y), pack2<F16>(v.z, v.w));
     }
 }
 
@@ -644,13 +641,14 @@ __global__ void debug_timeout_kernel(WsHeader* hdr, uint64_t limit_ns) {
     }
 }
 
-template <int D>
+template <int D, bool F16>
 cudaError_t launch_bwd_impl(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& dout,
                             const CUtensorMap& dq, const BwdArgs& a, int grid, cudaStream_t s) {
     using L = BwdSmem<D>;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+        cudaError_t e =
+            cudaFuncSetAttribute(attn_bwd_kernel<D, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
@@ -663,7 +661,7 @@ cudaError_t launch_bwd_impl(const CUtensorMap& q, const CUtensorMap& k, const CU
         if (e != cudaSuccess) return e;
     }
     if (grid > sms) grid = sms;
-    attn_bwd_kernel<D><<<grid, kBwdThreads, L::kAlloc, s>>>(q, k, v, dout, dq, a);
+    attn_bwd_kernel<D, F16><<<grid, kBwdThreads, L::kAlloc, s>>>(q, k, v, dout, dq, a);
     return cudaGetLastError();
 }
 
@@ -681,29 +679,45 @@ int grid_for(int64_t work_items, int per_cta, int ys = 1) {
 
 cudaError_t launch_attn_bwd(int head_dim, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                             const CUtensorMap& dout, const CUtensorMap& dq, const BwdArgs& a, int grid, cudaStream_t s) {
-    if (head_dim == 128) return launch_bwd_impl<128>(q, k, v, dout, dq, a, grid, s);
-    return launch_bwd_impl<64>(q, k, v, dout, dq, a, grid, s);
+    if (a.f16) {
+        if (head_dim == 128) return launch_bwd_impl<128, true>(q, k, v, dout, dq, a, grid, s);
+        return launch_bwd_impl<64, true>(q, k, v, dout, dq, a, grid, s);
+    }
+    if (head_dim == 128) return launch_bwd_impl<128, false>(q, k, v, dout, dq, a, grid, s);
+    return launch_bwd_impl<64, false>(q, k, v, dout, dq, a, grid, s);
 }
 
-cudaError_t launch_bwd_prep(const __nv_bfloat16* o, const __nv_bfloat16* dout, float* delta, float* dq_acc,
-                            int64_t T, int hq, int head_dim, int token_major, int dq_token_major, cudaStream_t s) {
+cudaError_t launch_bwd_prep(const void* o, const void* dout, float* delta, float* dq_acc, int64_t T, int hq,
+                            int head_dim, int token_major, int dq_token_major, int f16, cudaStream_t s) {
     const int tpr = head_dim / 8;
     const dim3 grid(grid_for(T, 256 / tpr, hq), hq);
-    if (head_dim == 128)
-        bwd_prep_kernel<128><<<grid, 256, 0, s>>>(o, dout, delta, dq_acc, T, hq, token_major, dq_token_major);
+    const uint16_t* o16 = (const uint16_t*)o;
+    const uint16_t* d16 = (const uint16_t*)dout;
+    if (head_dim == 128 && f16)
+        bwd_prep_kernel<128, true><<<grid, 256, 0, s>>>(o16, d16, delta, dq_acc, T, hq, token_major, dq_token_major);
+    else if (head_dim == 128)
+        bwd_prep_kernel<128, false><<<grid, 256, 0, s>>>(o16, d16, delta, dq_acc, T, hq, token_major, dq_token_major);
+    else if (f16)
+        bwd_prep_kernel<64, true><<<grid, 256, 0, s>>>(o16, d16, delta, dq_acc, T, hq, token_major, dq_token_major);
     else
-        bwd_prep_kernel<64><<<grid, 256, 0, s>>>(o, dout, delta, dq_acc, T, hq, token_major, dq_token_major);
+        bwd_prep_kernel<64, false><<<grid, 256, 0, s>>>(o16, d16, delta, dq_acc, T, hq, token_major, dq_token_major);
     return cudaGetLastError();
 }
 
-cudaError_t launch_dq_convert(const float* dq_acc, __nv_bfloat16* dq, int64_t T, int hq, int head_dim,
-                              int token_major, cudaStream_t s) {
+cudaError_t launch_dq_convert(const float* dq_acc, void* dq, int64_t T, int hq, int head_dim, int token_major,
+                              int f16, cudaStream_t s) {
     const int D4 = head_dim / 4;
     const dim3 grid(grid_for(T * D4, 256, hq), hq);
-    if (D4 == 32)
-        dq_convert_kernel<32><<<grid, 256, 0, s>>>((const float4*)dq_acc, (uint2*)dq, T, hq, token_major);
+    const float4* src = (const float4*)dq_acc;
+    uint2* dst = (uint2*)dq;
+    if (D4 == 32 && f16)
+        dq_convert_kernel<32, true><<<grid, 256, 0, s>>>(src, dst, T, hq, token_major);
+    else if (D4 == 32)
+        dq_convert_kernel<32, false><<<grid, 256, 0, s>>>(src, dst, T, hq, token_major);
+    else if (f16)
+        dq_convert_kernel<16, true><<<grid, 256, 0, s>>>(src, dst, T, hq, token_major);
     else
-        dq_convert_kernel<16><<<grid, 256, 0, s>>>((const float4*)dq_acc, (uint2*)dq, T, hq, token_major);
+        dq_convert_kernel<16, false><<<grid, 256, 0, s>>>(src, dst, T, hq, token_major);
     return cudaGetLastError();
 }
 

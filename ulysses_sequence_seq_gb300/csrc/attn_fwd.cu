@@ -11,7 +11,7 @@
 //   warp  8    TMA producer: Q tiles once, then K/V blocks into a 2-stage ring
 //   warp  9    MMA issuer (one thread) and TMEM owner
 // Tensor memory (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [384,384+D).
-// P (bf16) overwrites the first 64 columns of its S tile and feeds the P.V MMA
+// P (bf16 or fp16, the input type) overwrites the first 64 columns of its S tile and feeds the P.V MMA
 // straight from TMEM. The two tiles ping-pong: while one softmax group works on
 // its S, the tensor core runs the other tile's P.V and next Q.K^T.
 // The O rescale is lazy: the running max is only moved when a row's max grows by
@@ -43,7 +43,7 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 template <int D>
 struct FwdSmem {
     static constexpr int kPanels = D / 64;
-    static constexpr int kTileBytes = kTileM * D * 2;  // one 128-row bf16 tile
+    static constexpr int kTileBytes = kTileM * D * 2;  // one 128-row tile of 16-bit elements
     static constexpr int kQ0 = 0;
     static constexpr int kQ1 = kTileBytes;
     static constexpr int kK = 2 * kTileBytes;          // + stage * kTileBytes
@@ -58,7 +58,7 @@ struct FwdSmem {
     static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment of the base
 };
 
-template <int D>
+template <int D, bool F16>
 __global__ void __maxnreg__(kLaunchRegs)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdArgs a) {
@@ -151,8 +151,8 @@ __global__ void __maxnreg__(kLaunchRegs)
         regs_decrease<kAuxRegs>();
         // ------------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idS = idesc_bf16_f32(kTileM, kBlockN, false, false);  // Q.K^T: both K-major
-            constexpr uint32_t idO = idesc_bf16_f32(kTileM, D, false, true);         // P.V: V is MN-major
+            constexpr uint32_t idS = idesc_16b_f32(kTileM, kBlockN, false, false, F16);  // Q.K^T: both K-major
+            constexpr uint32_t idO = idesc_16b_f32(kTileM, D, false, true, F16);         // P.V: V is MN-major
             // The 64-bit shared-memory descriptors are built once; a K step only adds a constant
             // to the start-address field (addresses stay below 2^18, so the field never carries).
             // Rebuilding them per MMA made the issuing thread, not the tensor core, the limit.
@@ -309,7 +309,7 @@ __global__ void __maxnreg__(kLaunchRegs)
                     const float2 x = fma2(make_float2(sv[32 * c + 2 * j], sv[32 * c + 2 * j + 1]), sl2x2, nmu2);
                     const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
                     l4[j & 3] = add2(l4[j & 3], pp);   // independent partial row sums
-                    pk[j] = pack_bf16x2(pp.x, pp.y);
+                    pk[j] = pack2<F16>(pp.x, pp.y);
                 }
                 tmem_st16(tS + 16 * c, pk);
             }
@@ -324,7 +324,7 @@ __global__ void __maxnreg__(kLaunchRegs)
             tc_fence_after();
             const bool valid = i < e;
             const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
-            __nv_bfloat16* orow = a.o + act_row(h, i, a.T, a.hq, a.token_major) * D;
+            uint16_t* orow = a.o + act_row(h, i, a.T, a.hq, a.token_major) * D;
 #pragma unroll 1
             for (int c = 0; c < D; c += 32) {
                 uint32_t o[32];
@@ -333,7 +333,7 @@ __global__ void __maxnreg__(kLaunchRegs)
                 uint32_t pk[16];
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
-                    pk[j] = pack_bf16x2(__uint_as_float(o[2 * j]) * inv_l, __uint_as_float(o[2 * j + 1]) * inv_l);
+                    pk[j] = pack2<F16>(__uint_as_float(o[2 * j]) * inv_l, __uint_as_float(o[2 * j + 1]) * inv_l);
                 if (valid) {
                     uint4* dst = (uint4*)(orow + c);
 #pragma unroll
@@ -351,17 +351,18 @@ __global__ void __maxnreg__(kLaunchRegs)
     if (threadIdx.x == 0 && *abort_flag) atomicCAS(&a.hdr->status, (int)USP_OK, (int)USP_ERR_TIMEOUT);
 }
 
-template <int D>
+template <int D, bool F16>
 cudaError_t launch_fwd_impl(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const FwdArgs& a,
                             int grid, cudaStream_t s) {
     using L = FwdSmem<D>;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+        cudaError_t e =
+            cudaFuncSetAttribute(attn_fwd_kernel<D, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    attn_fwd_kernel<D><<<grid, kFwdThreads, L::kAlloc, s>>>(q, k, v, a);
+    attn_fwd_kernel<D, F16><<<grid, kFwdThreads, L::kAlloc, s>>>(q, k, v, a);
     return cudaGetLastError();
 }
 
@@ -369,8 +370,12 @@ cudaError_t launch_fwd_impl(const CUtensorMap& q, const CUtensorMap& k, const CU
 
 cudaError_t launch_attn_fwd(int head_dim, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                             const FwdArgs& a, int grid, cudaStream_t s) {
-    if (head_dim == 128) return launch_fwd_impl<128>(q, k, v, a, grid, s);
-    return launch_fwd_impl<64>(q, k, v, a, grid, s);
+    if (a.f16) {
+        if (head_dim == 128) return launch_fwd_impl<128, true>(q, k, v, a, grid, s);
+        return launch_fwd_impl<64, true>(q, k, v, a, grid, s);
+    }
+    if (head_dim == 128) return launch_fwd_impl<128, false>(q, k, v, a, grid, s);
+    return launch_fwd_impl<64, false>(q, k, v, a, grid, s);
 }
 
 }  // namespace usp

@@ -116,7 +116,7 @@ extern "C" usp_status usp_attn_fwd_varlen_noalloc(const void* q, const void* k, 
     fa.cu = cu_seqlens;
     fa.items = sa.items;
     fa.hdr = hdr;
-    fa.o = (__nv_bfloat16*)o;
+    fa.o = (uint16_t*)o;
     fa.lse = lse;
     fa.T = total_tokens;
     fa.hq = hq;

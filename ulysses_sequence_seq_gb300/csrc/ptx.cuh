@@ -213,6 +213,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_ma
     return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
+// The same for 16-bit inputs of either kind: A/B format 0 = f16, 1 = bf16 (both operands
+// of one MMA always share the type).
+__host__ __device__ constexpr uint32_t idesc_16b_f32(int M, int N, bool a_mn_major, bool b_mn_major, bool f16) {
+    return f16 ? (idesc_bf16_f32(M, N, a_mn_major, b_mn_major) & ~((7u << 7) | (7u << 10)))
+               : idesc_bf16_f32(M, N, a_mn_major, b_mn_major);
+}
 
 // Shared-memory matrix descriptor, 128-byte swizzle.
 //   bits 0-13 start address >> 4, 16-29 leading byte offset >> 4, 32-45 stride byte offset >> 4,
@@ -290,6 +296,29 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Two fp32 values to the kernel's 16-bit element type (round to nearest even), and back.
+template <bool F16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    return F16 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi);
+}
+template <bool F16>
+__device__ __forceinline__ float2 unpack2(uint32_t v) {
+    if (F16) {
+        float2 r;
+        asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\tcvt.f32.f16 %0, lo;\n\tcvt.f32.f16 %1, hi;\n\t}"
+            : "=f"(r.x), "=f"(r.y)
+            : "r"(v));
+        return r;
+    }
+    return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
 }
 
 __device__ __forceinline__ float ex2_approx(float x) {

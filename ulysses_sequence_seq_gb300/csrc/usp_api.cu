@@ -119,9 +119,11 @@ namespace {
 
 usp_status attn_fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* cu_seqlens,
                          int num_seqs, int64_t total_tokens, int hq, int hkv, int head_dim, float softmax_scale,
-                         int causal, void* workspace, size_t ws_bytes, cudaStream_t s, int token_major) {
+                         int causal, void* workspace, size_t ws_bytes, cudaStream_t s, int token_major,
+                         usp_dtype dt = USP_BF16) {
     usp_status st = check_common(total_tokens, num_seqs, hq, hkv, head_dim, cu_seqlens);
     if (st != USP_OK) return st;
+    if (dt != USP_BF16 && dt != USP_FP16) return dt == USP_FP32 ? USP_ERR_UNSUPPORTED : USP_ERR_INVALID_ARG;
     if (total_tokens == 0) return reset_status_if_any(workspace, ws_bytes, s);
     if (!q || !k || !v || !o || !lse || !workspace) return USP_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(workspace))
@@ -159,7 +161,8 @@ usp_status attn_fwd_impl(const void* q, const void* k, const void* v, void* o, f
     fa.cu = cu_seqlens;
     fa.items = sa.items;
     fa.hdr = hdr;
-    fa.o = (__nv_bfloat16*)o;
+    fa.o = (uint16_t*)o;
+    fa.f16 = dt == USP_FP16 ? 1 : 0;
     fa.lse = lse;
     fa.T = total_tokens;
     fa.hq = hq;
@@ -174,11 +177,14 @@ usp_status attn_fwd_impl(const void* q, const void* k, const void* v, void* o, f
 usp_status attn_bwd_impl(const void* q, const void* k, const void* v, const void* o, const float* lse,
                          const void* d_o, void* dq, void* dk, void* dv, usp_dtype grad_dt, const int32_t* cu_seqlens,
                          int num_seqs, int64_t total_tokens, int hq, int hkv, int head_dim, float softmax_scale,
-                         int causal, void* workspace, size_t ws_bytes, cudaStream_t s, int token_major) {
+                         int causal, void* workspace, size_t ws_bytes, cudaStream_t s, int token_major,
+                         usp_dtype dt = USP_BF16) {
     usp_status st = check_common(total_tokens, num_seqs, hq, hkv, head_dim, cu_seqlens);
     if (st != USP_OK) return st;
-    if (grad_dt == USP_FP16) return USP_ERR_UNSUPPORTED;
-    if (grad_dt != USP_BF16 && grad_dt != USP_FP32) return USP_ERR_INVALID_ARG;
+    if (dt != USP_BF16 && dt != USP_FP16) return dt == USP_FP32 ? USP_ERR_UNSUPPORTED : USP_ERR_INVALID_ARG;
+    // gradients in the inputs' 16-bit type or in fp32
+    if (grad_dt != dt && grad_dt != USP_FP32)
+        return (grad_dt == USP_BF16 || grad_dt == USP_FP16) ? USP_ERR_UNSUPPORTED : USP_ERR_INVALID_ARG;
     if (total_tokens == 0) return reset_status_if_any(workspace, ws_bytes, s);
     if (!q || !k || !v || !o || !lse || !d_o || !dq || !dk || !dv || !workspace) return USP_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(d_o) ||
@@ -196,8 +202,9 @@ usp_status attn_bwd_impl(const void* q, const void* k, const void* v, const void
     float* dq_acc = fp32_grads ? (float*)dq : (float*)(ws + w.dq_acc);
     const int dq_token_major = fp32_grads ? token_major : 0;
 
-    if (launch_bwd_prep((const __nv_bfloat16*)o, (const __nv_bfloat16*)d_o, delta, dq_acc, total_tokens, hq, head_dim,
-                        token_major, dq_token_major, s) != cudaSuccess)
+    const int f16 = dt == USP_FP16 ? 1 : 0;
+    if (launch_bwd_prep(o, d_o, delta, dq_acc, total_tokens, hq, head_dim, token_major, dq_token_major, f16, s) !=
+        cudaSuccess)
         return USP_ERR_CUDA;
 
     SchedArgs sa{};
@@ -235,6 +242,7 @@ usp_status attn_bwd_impl(const void* q, const void* k, const void* v, const void
     ba.dk = dk;
     ba.dv = dv;
     ba.grad_fp32 = fp32_grads ? 1 : 0;
+    ba.f16 = f16;
     ba.T = total_tokens;
     ba.hq = hq;
     ba.hkv = hkv;
@@ -246,7 +254,7 @@ usp_status attn_bwd_impl(const void* q, const void* k, const void* v, const void
     ba.scale_log2 = ba.scale * 1.4426950408889634f;
     if (launch_attn_bwd(head_dim, mq, mk, mv, mdo, mdq, ba, w.max_items, s) != cudaSuccess) return USP_ERR_CUDA;
     if (!fp32_grads &&
-        launch_dq_convert(dq_acc, (__nv_bfloat16*)dq, total_tokens, hq, head_dim, token_major, s) != cudaSuccess)
+        launch_dq_convert(dq_acc, dq, total_tokens, hq, head_dim, token_major, f16, s) != cudaSuccess)
         return USP_ERR_CUDA;
     return USP_OK;
 }
@@ -285,23 +293,23 @@ extern "C" usp_status usp_attn_bwd_varlen(const void* q, const void* k, const vo
 extern "C" usp_status usp_ulysses_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                                            const int32_t* cu_seqlens, int num_seqs, int64_t total_tokens, int sp,
                                            int hq, int hkv, int head_dim, float softmax_scale, int causal,
-                                           void* workspace, size_t ws_bytes, void* stream) {
+                                           usp_dtype dt, void* workspace, size_t ws_bytes, void* stream) {
     const usp_status st = check_sp(sp, total_tokens, hq, hkv);
     if (st != USP_OK) return st;
     return attn_fwd_impl(q, k, v, o, lse, cu_seqlens, num_seqs, total_tokens, hq, hkv, head_dim, softmax_scale,
-                         causal, workspace, ws_bytes, (cudaStream_t)stream, 1);
+                         causal, workspace, ws_bytes, (cudaStream_t)stream, 1, dt);
 }
 
 extern "C" usp_status usp_ulysses_attn_bwd(const void* q, const void* k, const void* v, const void* o,
                                            const float* lse, const void* d_o, void* dq, void* dk, void* dv,
                                            usp_dtype grad_dt, const int32_t* cu_seqlens, int num_seqs,
                                            int64_t total_tokens, int sp, int hq, int hkv, int head_dim,
-                                           float softmax_scale, int causal, void* workspace, size_t ws_bytes,
-                                           void* stream) {
+                                           float softmax_scale, int causal, usp_dtype dt, void* workspace,
+                                           size_t ws_bytes, void* stream) {
     const usp_status st = check_sp(sp, total_tokens, hq, hkv);
     if (st != USP_OK) return st;
     return attn_bwd_impl(q, k, v, o, lse, d_o, dq, dk, dv, grad_dt, cu_seqlens, num_seqs, total_tokens, hq, hkv,
-                         head_dim, softmax_scale, causal, workspace, ws_bytes, (cudaStream_t)stream, 1);
+                         head_dim, softmax_scale, causal, workspace, ws_bytes, (cudaStream_t)stream, 1, dt);
 }
 
 extern "C" usp_status usp_get_device_status(const void* workspace, void* stream) {
