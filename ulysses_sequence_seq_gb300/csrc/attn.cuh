@@ -49,8 +49,11 @@ struct BwdArgs {
     float scale_log2;    // softmax scale * log2(e)
 };
 
+// dk, dv: 16-bit gradient maps (make_activation_map) for whole-tile stores; not read for
+// fp32 gradients.
 cudaError_t launch_attn_bwd(int head_dim, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                            const CUtensorMap& dout, const CUtensorMap& dq, const BwdArgs& a, int grid, cudaStream_t s);
+                            const CUtensorMap& dout, const CUtensorMap& dq, const CUtensorMap& dk, const CUtensorMap& dv,
+                            const BwdArgs& a, int grid, cudaStream_t s);
 
 // Delta_i = dO_i . O_i (fp32, [hq][T]) for every query row, and zeroes the dQ accumulator.
 // o / dout are head-major or token-major (token_major); the accumulator is head-major

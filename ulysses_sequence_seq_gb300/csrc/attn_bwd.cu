@@ -109,11 +109,14 @@ __device__ __forceinline__ bool read_item(uint64_t* item_bars, volatile int* rin
     return true;
 }
 
+// 448 threads = 14 warps, one CTA per SM; two of the four SM sub-partitions hold four
+// warps, so 16384 registers per sub-partition cap a thread at 128.
 template <int D, bool F16>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                    const __grid_constant__ CUtensorMap tmDQ, const BwdArgs a) {
+                    const __grid_constant__ CUtensorMap tmDQ, const __grid_constant__ CUtensorMap tmDK,
+                    const __grid_constant__ CUtensorMap tmDV, const BwdArgs a) {
     using L = BwdSmem<D>;
     const int count = a.hdr->bwd_count;
     if ((int)blockIdx.x >= count) return;
@@ -363,25 +366,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const float sc = a.scale;
         bool ok = true;
         int gk = 0;
-        for (int j = 0; ok; ++j) {
-            int idx;
-            if (!read_item(item_bars, item_ring, j, abort_flag, idx)) break;
-            if (idx >= count) break;
+        // This half's query rows of a step, negated: -lse (log2 units) and -Delta; rows outside
+        // the sample get -lse = -inf, which makes their P exactly zero. Loaded one step ahead
+        // (the first step of the next item before this item's epilogue), so that their
+        // global-memory latency stays off the critical path.
+        float nl_next = -INFINITY, nd_next = 0.f;
+        auto fetch_row_stats = [&](const BwdItem& it, int k) {
+            const int h = it.g * G + k / it.nq;
+            const int q = it.q0(k) + grp * kHalfCols + r;
+            const bool q_ok = r < kHalfCols && q < it.e;
+            nl_next = q_ok ? -__ldg(a.lse + (int64_t)h * a.T + q) * 1.4426950408889634f : -INFINITY;
+            nd_next = q_ok ? -__ldg(a.delta + (int64_t)h * a.T + q) : 0.f;
+        };
+        int idx = count;
+        if (!read_item(item_bars, item_ring, 0, abort_flag, idx)) ok = false;
+        if (ok && idx < count) fetch_row_stats(bwd_item(a, idx), 0);
+        for (int j = 0; ok && idx < count; ++j) {
             const BwdItem w = bwd_item(a, idx);
             const int kv = w.kv0 + r;
             const bool kv_ok = kv < w.e;
-            // This half's query rows of a step, negated: -lse (log2 units) and -Delta; rows
-            // outside the sample get -lse = -inf, which makes their P exactly zero. Loaded one
-            // step ahead so that their global-memory latency stays off the critical path.
-            float nl_next = -INFINITY, nd_next = 0.f;
-            auto fetch_row_stats = [&](int k) {
-                const int h = w.g * G + k / w.nq;
-                const int q = w.q0(k) + grp * kHalfCols + r;
-                const bool q_ok = r < kHalfCols && q < w.e;
-                nl_next = q_ok ? -__ldg(a.lse + (int64_t)h * a.T + q) * 1.4426950408889634f : -INFINITY;
-                nd_next = q_ok ? -__ldg(a.delta + (int64_t)h * a.T + q) : 0.f;
-            };
-            fetch_row_stats(0);
             for (int k = 0; k < w.nsteps; ++k, ++gk) {
                 const int q0 = w.q0(k);
                 named_bar_sync(1 + grp, 128);
@@ -390,7 +393,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     delta_g[r] = nd_next;
                 }
                 named_bar_sync(1 + grp, 128);
-                if (k + 1 < w.nsteps) fetch_row_stats(k + 1);
+                if (k + 1 < w.nsteps) fetch_row_stats(w, k + 1);
                 // element masks are only needed on the diagonal block and on the sample's ragged
                 // last key tile; there query column c (of 128) is visible to key row r iff c >= r
                 const bool mask_blk = (a.causal && q0 == w.kv0) || (w.kv0 + kBlockN > w.e);
@@ -469,12 +472,76 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars[L::bDsFull + grp]);
             }
+            if (!ok) break;
+            // the next item, and its first step's row statistics, before this item's epilogue
+            int idx_next = count;
+            if (!read_item(item_bars, item_ring, j + 1, abort_flag, idx_next)) ok = false;
+            if (ok && idx_next < count) fetch_row_stats(bwd_item(a, idx_next), 0);
+            idx = idx_next;
             if (!ok || !mbar_wait(&bars[L::bAccFull], j & 1, abort_flag, kWaitLimitNs)) break;
             tc_fence_after();
             // half A writes dV, half B writes dK; TMEM is handed back to the next item's MMAs as
             // soon as the last chunk has been read, before the global stores finish
-            const int64_t row = act_row(w.g, kv, a.T, a.hkv, a.token_major);
             const uint32_t src = tbase + lane_off + (grp ? 384 : 256);
+            if (!a.grad_fp32 && w.kv0 + kBlockN <= w.e) {
+                // Whole 16-bit tile: each half stages its accumulator through its own 64-column
+                // dS panel, 64 columns per round, and writes each round with one TMA store, so
+                // the rows leave as full lines instead of 16-byte pieces 256 bytes apart. The
+                // second round is read and packed before the first store, so TMEM goes back to
+                // the next item's MMAs at once; the panel is this half's own, so the next item's
+                // dS needs no other half's store to finish.
+                uint8_t* panel = sm + L::kDS + grp * (kBlockN * 128);
+                uint32_t held[32 * (D / 64 - 1) + 1];   // columns 64..D-1, two per word (none for D = 64)
+                static_assert(D == 64 || D == 128, "the epilogue holds at most one extra 64-column panel");
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(src + 32 * c, o);
+                    tmem_ld_wait(o);
+                    if (c + 1 == D / 32) {   // the accumulator has been read: TMEM back to the MMAs
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&bars[L::bAccEmpty]);
+                    }
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint32_t p0 = pack2<F16>(__uint_as_float(o[8 * q]), __uint_as_float(o[8 * q + 1]));
+                        const uint32_t p1 = pack2<F16>(__uint_as_float(o[8 * q + 2]), __uint_as_float(o[8 * q + 3]));
+                        const uint32_t p2 = pack2<F16>(__uint_as_float(o[8 * q + 4]), __uint_as_float(o[8 * q + 5]));
+                        const uint32_t p3 = pack2<F16>(__uint_as_float(o[8 * q + 6]), __uint_as_float(o[8 * q + 7]));
+                        const int col = 32 * c + 8 * q;   // first of the 8 columns in this 16-byte chunk
+                        if (col < 64) {
+                            *(uint4*)(panel + sw128_offset(r, (uint32_t)(col * 2))) = make_uint4(p0, p1, p2, p3);
+                        } else if (D > 64) {
+                            const int i = (col - 64) / 2;
+                            held[i] = p0;
+                            held[i + 1] = p1;
+                            held[i + 2] = p2;
+                            held[i + 3] = p3;
+                        }
+                    }
+                }
+#pragma unroll 1
+                for (int round = 0; round < D / 64; ++round) {
+                    if (round > 0) {   // columns 64..127 into the panel the first store has released
+#pragma unroll
+                        for (int jj = 0; jj < 8; ++jj)
+                            *(uint4*)(panel + sw128_offset(r, (uint32_t)(jj * 16))) =
+                                make_uint4(held[4 * jj], held[4 * jj + 1], held[4 * jj + 2], held[4 * jj + 3]);
+                    }
+                    fence_proxy_async_smem();
+                    named_bar_sync(1 + grp, 128);
+                    if (r == 0) {
+                        tma_store_rows(grp ? &tmDK : &tmDV, panel, round * 64, w.kv0, w.g, a.token_major);
+                        bulk_commit_group();
+                        bulk_wait_group_read<0>();
+                    }
+                    named_bar_sync(1 + grp, 128);
+                }
+                continue;
+            }
+            // fp32 gradients, or a sample's ragged last tile: row by row
+            const int64_t row = act_row(w.g, kv, a.T, a.hkv, a.token_major);
             void* dst_base = grp ? a.dk : a.dv;
 #pragma unroll 1
             for (int c = 0; c < D; c += 32) {
@@ -504,6 +571,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 }
             }
         }
+        if (r == 0) bulk_wait_group<0>();   // the last tile stores have landed
     } else if (warp < kDqWarp0 + 4) {
         // ------------------------------------------------------------------ dQ group (query rows)
         // Each warp owns 32 query rows of the tile: per 32-column chunk it loads 32 x 32 fp32
@@ -643,7 +711,8 @@ __global__ void debug_timeout_kernel(WsHeader* hdr, uint64_t limit_ns) {
 
 template <int D, bool F16>
 cudaError_t launch_bwd_impl(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& dout,
-                            const CUtensorMap& dq, const BwdArgs& a, int grid, cudaStream_t s) {
+                            const CUtensorMap& dq, const CUtensorMap& dk, const CUtensorMap& dv, const BwdArgs& a,
+                            int grid, cudaStream_t s) {
     using L = BwdSmem<D>;
     static bool attr_set = false;
     if (!attr_set) {
@@ -661,7 +730,7 @@ cudaError_t launch_bwd_impl(const CUtensorMap& q, const CUtensorMap& k, const CU
         if (e != cudaSuccess) return e;
     }
     if (grid > sms) grid = sms;
-    attn_bwd_kernel<D, F16><<<grid, kBwdThreads, L::kAlloc, s>>>(q, k, v, dout, dq, a);
+    attn_bwd_kernel<D, F16><<<grid, kBwdThreads, L::kAlloc, s>>>(q, k, v, dout, dq, dk, dv, a);
     return cudaGetLastError();
 }
 
@@ -678,13 +747,14 @@ int grid_for(int64_t work_items, int per_cta, int ys = 1) {
 }  // namespace
 
 cudaError_t launch_attn_bwd(int head_dim, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                            const CUtensorMap& dout, const CUtensorMap& dq, const BwdArgs& a, int grid, cudaStream_t s) {
+                            const CUtensorMap& dout, const CUtensorMap& dq, const CUtensorMap& dk, const CUtensorMap& dv,
+                            const BwdArgs& a, int grid, cudaStream_t s) {
     if (a.f16) {
-        if (head_dim == 128) return launch_bwd_impl<128, true>(q, k, v, dout, dq, a, grid, s);
-        return launch_bwd_impl<64, true>(q, k, v, dout, dq, a, grid, s);
+        if (head_dim == 128) return launch_bwd_impl<128, true>(q, k, v, dout, dq, dk, dv, a, grid, s);
+        return launch_bwd_impl<64, true>(q, k, v, dout, dq, dk, dv, a, grid, s);
     }
-    if (head_dim == 128) return launch_bwd_impl<128, false>(q, k, v, dout, dq, a, grid, s);
-    return launch_bwd_impl<64, false>(q, k, v, dout, dq, a, grid, s);
+    if (head_dim == 128) return launch_bwd_impl<128, false>(q, k, v, dout, dq, dk, dv, a, grid, s);
+    return launch_bwd_impl<64, false>(q, k, v, dout, dq, dk, dv, a, grid, s);
 }
 
 cudaError_t launch_bwd_prep(const void* o, const void* dout, float* delta, float* dq_acc, int64_t T, int hq,

@@ -118,6 +118,17 @@ __device__ __forceinline__ void tma_load_rows(void* smem_dst, const CUtensorMap*
         tma_load_3d(smem_dst, map, bar, x, t0, h);
 }
 
+// 3-D tiled store of a shared-memory box to global memory (rows past the tensor end are
+// skipped), tracked by bulk async-groups.
+__device__ __forceinline__ void tma_store_rows(const CUtensorMap* map, const void* smem_src, int x, int t0, int h,
+                                               int token_major) {
+    const int y = token_major ? h : t0, z = token_major ? t0 : h;
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(smem_u32(smem_src)), "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+
 // Pull a tile into L2 ahead of its load (no shared memory, no completion tracking).
 __device__ __forceinline__ void tma_prefetch_rows(const CUtensorMap* map, int x, int t0, int h, int token_major) {
     const int y = token_major ? h : t0, z = token_major ? t0 : h;
@@ -376,6 +387,10 @@ __device__ __forceinline__ void regs_decrease() {
 // Named barrier among `nthreads` threads (multiple of 32) of the CTA.
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+// Arrive on a named barrier without waiting (the other participants wait with bar.sync).
+__device__ __forceinline__ void named_bar_arrive(int id, int nthreads) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 }  // namespace ptx

@@ -225,13 +225,21 @@ usp_status attn_bwd_impl(const void* q, const void* k, const void* v, const void
     sa.items = (WorkItem*)(ws + w.items);
     if (launch_schedule(sa, s) != cudaSuccess) return USP_ERR_CUDA;
 
-    CUtensorMap mq, mk, mv, mdo, mdq;
+    CUtensorMap mq, mk, mv, mdo, mdq, mdk, mdv;
     if (!make_activation_map(&mq, q, total_tokens, hq, head_dim, token_major) ||
         !make_activation_map(&mk, k, total_tokens, hkv, head_dim, token_major) ||
         !make_activation_map(&mv, v, total_tokens, hkv, head_dim, token_major) ||
         !make_activation_map(&mdo, d_o, total_tokens, hq, head_dim, token_major) ||
         !make_dq_accum_map(&mdq, dq_acc, total_tokens, hq, head_dim, dq_token_major))
         return USP_ERR_CUDA;
+    // 16-bit dK/dV leave as whole tiles through these maps; fp32 gradients are stored by rows
+    if (fp32_grads) {
+        mdk = mk;
+        mdv = mv;
+    } else if (!make_activation_map(&mdk, dk, total_tokens, hkv, head_dim, token_major) ||
+               !make_activation_map(&mdv, dv, total_tokens, hkv, head_dim, token_major)) {
+        return USP_ERR_CUDA;
+    }
     BwdArgs ba{};
     ba.cu = cu_seqlens;
     ba.items = sa.items;
@@ -252,7 +260,8 @@ usp_status attn_bwd_impl(const void* q, const void* k, const void* v, const void
     ba.causal = sa.causal;
     ba.scale = resolve_scale(softmax_scale, head_dim);
     ba.scale_log2 = ba.scale * 1.4426950408889634f;
-    if (launch_attn_bwd(head_dim, mq, mk, mv, mdo, mdq, ba, w.max_items, s) != cudaSuccess) return USP_ERR_CUDA;
+    if (launch_attn_bwd(head_dim, mq, mk, mv, mdo, mdq, mdk, mdv, ba, w.max_items, s) != cudaSuccess)
+        return USP_ERR_CUDA;
     if (!fp32_grads &&
         launch_dq_convert(dq_acc, dq, total_tokens, hq, head_dim, token_major, f16, s) != cudaSuccess)
         return USP_ERR_CUDA;
