@@ -24,8 +24,9 @@ struct FwdArgs {
     int f16;            // 16-bit inputs and outputs are fp16 (else bf16)
 };
 
+// o: the output map (make_activation_map over o) for whole-tile stores.
 cudaError_t launch_attn_fwd(int head_dim, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                            const FwdArgs& a, int grid, cudaStream_t s);
+                            const CUtensorMap& o, const FwdArgs& a, int grid, cudaStream_t s);
 
 struct BwdArgs {
     const int32_t* cu;

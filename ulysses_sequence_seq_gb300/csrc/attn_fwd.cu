@@ -61,7 +61,7 @@ struct FwdSmem {
 template <int D, bool F16>
 __global__ void __maxnreg__(kLaunchRegs)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, const FwdArgs a) {
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO, const FwdArgs a) {
     using L = FwdSmem<D>;
     const int count = a.hdr->fwd_count;
     if ((int)blockIdx.x >= count) return;
@@ -324,20 +324,51 @@ __global__ void __maxnreg__(kLaunchRegs)
             tc_fence_after();
             const bool valid = i < e;
             const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
-            uint16_t* orow = a.o + act_row(h, i, a.T, a.hq, a.token_major) * D;
+            if (q0 + kTileM <= e) {
+                // Whole tile: stage O in this tile's Q buffer (its last reader, the final Q.K^T,
+                // completed before the P.V this group just waited for) and write it with TMA
+                // stores, so the rows leave as full lines instead of 16-byte pieces.
+                uint8_t* qt = sm + (t ? L::kQ1 : L::kQ0);
 #pragma unroll 1
-            for (int c = 0; c < D; c += 32) {
-                uint32_t o[32];
-                tmem_ld32(tO + c, o);
-                tmem_ld_wait(o);
-                uint32_t pk[16];
+                for (int c = 0; c < D; c += 32) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + c, o);
+                    tmem_ld_wait(o);
 #pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    pk[j] = pack2<F16>(__uint_as_float(o[2 * j]) * inv_l, __uint_as_float(o[2 * j + 1]) * inv_l);
-                if (valid) {
-                    uint4* dst = (uint4*)(orow + c);
+                    for (int q = 0; q < 4; ++q) {
+                        const int col = c + 8 * q;   // [128 rows][D] as D/64 panels of [128][64], 128-byte swizzle
+                        *(uint4*)(qt + (col / 64) * (kTileM * 128) + sw128_offset(rq, (uint32_t)((col % 64) * 2))) =
+                            make_uint4(pack2<F16>(__uint_as_float(o[8 * q]) * inv_l, __uint_as_float(o[8 * q + 1]) * inv_l),
+                                       pack2<F16>(__uint_as_float(o[8 * q + 2]) * inv_l, __uint_as_float(o[8 * q + 3]) * inv_l),
+                                       pack2<F16>(__uint_as_float(o[8 * q + 4]) * inv_l, __uint_as_float(o[8 * q + 5]) * inv_l),
+                                       pack2<F16>(__uint_as_float(o[8 * q + 6]) * inv_l, __uint_as_float(o[8 * q + 7]) * inv_l));
+                    }
+                }
+                fence_proxy_async_smem();
+                named_bar_sync(1 + t, 128);
+                if (rq == 0) {
+                    for (int p = 0; p < L::kPanels; ++p)
+                        tma_store_rows(&tmO, qt + p * (kTileM * 128), p * 64, q0, h, a.token_major);
+                    bulk_commit_group();
+                }
+                if (rq == 0) bulk_wait_group_read<0>();   // the buffer is read before the CTA ends
+            } else {   // a sample's ragged last tile: row by row, rows past the end skipped
+                uint16_t* orow = a.o + act_row(h, i, a.T, a.hq, a.token_major) * D;
+#pragma unroll 1
+                for (int c = 0; c < D; c += 32) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + c, o);
+                    tmem_ld_wait(o);
+                    uint32_t pk[16];
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                    for (int j = 0; j < 16; ++j)
+                        pk[j] = pack2<F16>(__uint_as_float(o[2 * j]) * inv_l, __uint_as_float(o[2 * j + 1]) * inv_l);
+                    if (valid) {
+                        uint4* dst = (uint4*)(orow + c);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                    }
                 }
             }
             if (valid) a.lse[(int64_t)h * a.T + i] = (m + __log2f(l)) * 0.69314718055994530942f;
@@ -352,8 +383,8 @@ __global__ void __maxnreg__(kLaunchRegs)
 }
 
 template <int D, bool F16>
-cudaError_t launch_fwd_impl(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const FwdArgs& a,
-                            int grid, cudaStream_t s) {
+cudaError_t launch_fwd_impl(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& o,
+                            const FwdArgs& a, int grid, cudaStream_t s) {
     using L = FwdSmem<D>;
     static bool attr_set = false;
     if (!attr_set) {
@@ -362,20 +393,20 @@ cudaError_t launch_fwd_impl(const CUtensorMap& q, const CUtensorMap& k, const CU
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    attn_fwd_kernel<D, F16><<<grid, kFwdThreads, L::kAlloc, s>>>(q, k, v, a);
+    attn_fwd_kernel<D, F16><<<grid, kFwdThreads, L::kAlloc, s>>>(q, k, v, o, a);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_attn_fwd(int head_dim, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                            const FwdArgs& a, int grid, cudaStream_t s) {
+                            const CUtensorMap& o, const FwdArgs& a, int grid, cudaStream_t s) {
     if (a.f16) {
-        if (head_dim == 128) return launch_fwd_impl<128, true>(q, k, v, a, grid, s);
-        return launch_fwd_impl<64, true>(q, k, v, a, grid, s);
+        if (head_dim == 128) return launch_fwd_impl<128, true>(q, k, v, o, a, grid, s);
+        return launch_fwd_impl<64, true>(q, k, v, o, a, grid, s);
     }
-    if (head_dim == 128) return launch_fwd_impl<128, false>(q, k, v, a, grid, s);
-    return launch_fwd_impl<64, false>(q, k, v, a, grid, s);
+    if (head_dim == 128) return launch_fwd_impl<128, false>(q, k, v, o, a, grid, s);
+    return launch_fwd_impl<64, false>(q, k, v, o, a, grid, s);
 }
 
 }  // namespace usp

@@ -107,10 +107,11 @@ extern "C" usp_status usp_attn_fwd_varlen_noalloc(const void* q, const void* k, 
     sa.items = (WorkItem*)(ws + w.items);
     if (launch_schedule(sa, s) != cudaSuccess) return USP_ERR_CUDA;
 
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mo;
     if (!make_activation_map(&mq, q, total_tokens, hq, head_dim, 0) ||
         !make_activation_map(&mk, k, total_tokens, hkv, head_dim, 0) ||
-        !make_activation_map(&mv, v, total_tokens, hkv, head_dim, 0))
+        !make_activation_map(&mv, v, total_tokens, hkv, head_dim, 0) ||
+        !make_activation_map(&mo, o, total_tokens, hq, head_dim, 0))
         return USP_ERR_CUDA;
     FwdArgs fa{};
     fa.cu = cu_seqlens;
@@ -123,7 +124,7 @@ extern "C" usp_status usp_attn_fwd_varlen_noalloc(const void* q, const void* k, 
     fa.group = hq / hkv;
     fa.causal = sa.causal;
     fa.scale_log2 = (softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)head_dim)) * 1.4426950408889634f;
-    if (launch_attn_fwd(head_dim, mq, mk, mv, fa, w.max_items, s) != cudaSuccess) return USP_ERR_CUDA;
+    if (launch_attn_fwd(head_dim, mq, mk, mv, mo, fa, w.max_items, s) != cudaSuccess) return USP_ERR_CUDA;
     // device-side outcome (USP_OK, USP_ERR_DEVICE_CHECK or USP_ERR_TIMEOUT) for the caller
     if (status && cudaMemcpyAsync(status, &hdr->status, sizeof(int32_t), cudaMemcpyDeviceToDevice, s) != cudaSuccess)
         return USP_ERR_CUDA;

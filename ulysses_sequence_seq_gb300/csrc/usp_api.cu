@@ -152,10 +152,11 @@ usp_status attn_fwd_impl(const void* q, const void* k, const void* v, void* o, f
     sa.items = (WorkItem*)(ws + w.items);
     if (launch_schedule(sa, s) != cudaSuccess) return USP_ERR_CUDA;
 
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mo;
     if (!make_activation_map(&mq, q, total_tokens, hq, head_dim, token_major) ||
         !make_activation_map(&mk, k, total_tokens, hkv, head_dim, token_major) ||
-        !make_activation_map(&mv, v, total_tokens, hkv, head_dim, token_major))
+        !make_activation_map(&mv, v, total_tokens, hkv, head_dim, token_major) ||
+        !make_activation_map(&mo, o, total_tokens, hq, head_dim, token_major))
         return USP_ERR_CUDA;
     FwdArgs fa{};
     fa.cu = cu_seqlens;
@@ -170,7 +171,7 @@ usp_status attn_fwd_impl(const void* q, const void* k, const void* v, void* o, f
     fa.causal = sa.causal;
     fa.token_major = token_major;
     fa.scale_log2 = resolve_scale(softmax_scale, head_dim) * 1.4426950408889634f;
-    if (launch_attn_fwd(head_dim, mq, mk, mv, fa, w.max_items, s) != cudaSuccess) return USP_ERR_CUDA;
+    if (launch_attn_fwd(head_dim, mq, mk, mv, mo, fa, w.max_items, s) != cudaSuccess) return USP_ERR_CUDA;
     return USP_OK;
 }
 
