@@ -4,13 +4,18 @@
 // no materialised score matrix; congresoia365 article, "El Desafío del
 // Entrenamiento de Secuencias Largas", and HF guide "Configurar" on packed samples).
 //
-// One CTA takes one work item: a query head and two 128-row query tiles of one
-// sample. Warp roles (384 threads, warps 10-11 idle):
+// A work item is a query head and two 128-row query tiles of one sample. CTAs are
+// persistent (one per SM): each takes its first item by index and the rest from a
+// counter, in schedule order, so the next item's Q, K, V loads and first Q.K^T overlap
+// the softmax of the current one's last blocks and its output.
+// Warp roles (384 threads, warps 10-11 idle):
 //   warps 0-3  softmax group for query tile 0 (thread = one query row = one TMEM lane)
 //   warps 4-7  softmax group for query tile 1
 //   warp  8    TMA producer: Q tiles once, then K/V blocks into a 2-stage ring
 //   warp  9    MMA issuer (one thread) and TMEM owner
 // Tensor memory (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [384,384+D).
+// A whole output tile leaves through a 64-column shared-memory panel of its own, one TMA
+// store per 64 columns; a sample's ragged last tile is written row by row.
 // P (bf16 or fp16, the input type) overwrites the first 64 columns of its S tile and feeds the P.V MMA
 // straight from TMEM. The two tiles ping-pong: while one softmax group works on
 // its S, the tensor core runs the other tile's P.V and next Q.K^T.
@@ -31,12 +36,13 @@ namespace {
 using namespace ptx;
 
 constexpr int kFwdThreads = 384;  // 3 warpgroups: two softmax groups, one for load / MMA (2 warps idle)
-// Register shares (per thread) after setmaxnreg: the load/MMA warpgroup needs few, the
-// softmax groups hold a 128-column score row each. Launched with kLaunchRegs per thread,
+// Register shares (per thread) after setmaxnreg: the softmax groups hold a 128-column score
+// row each; the load/MMA warpgroup keeps the item ring, the block counters and both tiles'
+// barrier phases across the persistent loop. Launched with kLaunchRegs per thread,
 // 128 * (2 * kSoftmaxRegs + kAuxRegs) must not exceed kFwdThreads * kLaunchRegs.
 constexpr int kLaunchRegs = 168;
-constexpr int kSoftmaxRegs = 208;
-constexpr int kAuxRegs = 72;
+constexpr int kSoftmaxRegs = 200;
+constexpr int kAuxRegs = 104;
 static_assert(128 * (2 * kSoftmaxRegs + kAuxRegs) <= kFwdThreads * kLaunchRegs, "register split exceeds the launch pool");
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
@@ -48,15 +54,48 @@ struct FwdSmem {
     static constexpr int kQ1 = kTileBytes;
     static constexpr int kK = 2 * kTileBytes;          // + stage * kTileBytes
     static constexpr int kV = 4 * kTileBytes;          // + stage * kTileBytes
-    static constexpr int kBars = 6 * kTileBytes;
+    static constexpr int kStage = 6 * kTileBytes;      // O staging: one [128][64] panel per tile
+    static constexpr int kBars = kStage + 2 * kTileM * 128;
     // barrier indices
     static constexpr int bQFull = 0, bKFull = 1, bVFull = 3, bKvEmpty = 5, bSFull = 7, bPFull = 9, bODone = 11,
-                         bDrain = 13, kNumBars = 14;
-    static constexpr int kTmemSlot = kBars + 8 * kNumBars;
+                         bDrain = 13, bQEmpty = 14, bItem = 15, kNumBars = 19;   // bItem: 4-slot ring
+    static constexpr int kItemRing = kBars + 8 * kNumBars;   // int[4]: work item of each slot
+    static constexpr int kTmemSlot = kItemRing + 16;
     static constexpr int kAbort = kTmemSlot + 8;
     static constexpr int kBytes = kAbort + 8;
     static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment of the base
 };
+static_assert(FwdSmem<128>::kAlloc <= 232448, "forward shared memory exceeds the per-CTA limit");
+
+// One forward work item: query head h and the query tiles q00, q01 of one sample, with
+// the key/value blocks each tile sees.
+struct FwdItem {
+    int h, s, e, q00, q01, nb0, nb1, nmax, kvh;
+};
+__device__ __forceinline__ FwdItem fwd_item(const FwdArgs& a, int idx) {
+    const WorkItem it = a.items[idx];
+    FwdItem f;
+    f.h = it.head;
+    f.s = a.cu[it.seq];
+    f.e = a.cu[it.seq + 1];
+    f.q00 = f.s + it.tile * kFwdRowsPerItem;
+    f.q01 = f.q00 + kTileM;
+    f.nb0 = kv_blocks_for_query_tile(f.q00, f.s, f.e, a.causal);
+    f.nb1 = kv_blocks_for_query_tile(f.q01, f.s, f.e, a.causal);
+    f.nmax = f.nb0 > f.nb1 ? f.nb0 : f.nb1;
+    f.kvh = f.h / a.group;
+    return f;
+}
+
+// The CTA's j-th work item from the producer's 4-slot ring (false: the wait gave up). No
+// role runs more than two items behind the producer, so a slot is never rewritten while a
+// reader still needs it.
+__device__ __forceinline__ bool fwd_read_item(uint64_t* item_bars, volatile int* ring, int j,
+                                              volatile int* abort_flag, int& idx) {
+    if (!mbar_wait(&item_bars[j & 3], (j >> 2) & 1, abort_flag, kWaitLimitNs)) return false;
+    idx = ring[j & 3];
+    return true;
+}
 
 template <int D, bool F16>
 __global__ void __maxnreg__(kLaunchRegs)
@@ -67,20 +106,14 @@ __global__ void __maxnreg__(kLaunchRegs)
     if ((int)blockIdx.x >= count) return;
     // once any CTA of this launch has timed out, the rest skip their work
     if (*(volatile int*)&a.hdr->status != (int)USP_OK) return;
-    const WorkItem it = a.items[blockIdx.x];
-    const int h = it.head;
-    const int s = a.cu[it.seq], e = a.cu[it.seq + 1];
-    const int q00 = s + it.tile * kFwdRowsPerItem, q01 = q00 + kTileM;
-    const int nb0 = kv_blocks_for_query_tile(q00, s, e, a.causal);
-    const int nb1 = kv_blocks_for_query_tile(q01, s, e, a.causal);
-    const int nmax = nb0 > nb1 ? nb0 : nb1;
-    const int kvh = h / a.group;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint64_t* bars = (uint64_t*)(sm + L::kBars);
     uint32_t* tmem_slot = (uint32_t*)(sm + L::kTmemSlot);
     volatile int* abort_flag = (volatile int*)(sm + L::kAbort);
+    volatile int* item_ring = (volatile int*)(sm + L::kItemRing);
+    uint64_t* item_bars = &bars[L::bItem];
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
@@ -100,6 +133,8 @@ __global__ void __maxnreg__(kLaunchRegs)
             mbar_init(&bars[L::bODone + i], 1);
         }
         mbar_init(&bars[L::bDrain], 1);
+        mbar_init(&bars[L::bQEmpty], 1);
+        for (int i = 0; i < 4; ++i) mbar_init(&bars[L::bItem + i], 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -108,6 +143,9 @@ __global__ void __maxnreg__(kLaunchRegs)
     tc_fence_after();
     const uint32_t tbase = *tmem_slot;
 
+    // Every per-block barrier phase follows a running count across items (the CTA's key/value
+    // blocks for the K/V ring, each tile's blocks for S and P); the per-item ones (Q, O done)
+    // follow the item count j.
     if (warp >= 10) {
         regs_decrease<kAuxRegs>();  // idle warps of the load/MMA warpgroup
     } else if (warp == 8) {
@@ -117,32 +155,57 @@ __global__ void __maxnreg__(kLaunchRegs)
             prefetch_tmap(&tmQ);
             prefetch_tmap(&tmK);
             prefetch_tmap(&tmV);
-            const int ntiles = nb1 > 0 ? 2 : 1;
-            mbar_arrive_expect_tx(&bars[L::bQFull], ntiles * L::kTileBytes);
-            for (int t = 0; t < ntiles; ++t)
-                for (int p = 0; p < L::kPanels; ++p)
-                    tma_load_rows(sm + (t ? L::kQ1 : L::kQ0) + p * (kTileM * 128), &tmQ, &bars[L::bQFull], p * 64,
-                                  t ? q01 : q00, h, a.token_major);
-            int issued = 0;
-            for (int n = 0; n < nmax; ++n) {
-                const int st = n & 1;
-                if (n >= 2 && !mbar_wait(&bars[L::bKvEmpty + st], ((n >> 1) - 1) & 1, abort_flag, kWaitLimitNs))
-                    break;
-                const int row = s + n * kBlockN;
-                mbar_arrive_expect_tx(&bars[L::bKFull + st], L::kTileBytes);
-                for (int p = 0; p < L::kPanels; ++p)
-                    tma_load_rows(sm + L::kK + st * L::kTileBytes + p * (kTileM * 128), &tmK, &bars[L::bKFull + st],
-                                  p * 64, row, kvh, a.token_major);
-                mbar_arrive_expect_tx(&bars[L::bVFull + st], L::kTileBytes);
-                for (int p = 0; p < L::kPanels; ++p)
-                    tma_load_rows(sm + L::kV + st * L::kTileBytes + p * (kTileM * 128), &tmV, &bars[L::bVFull + st],
-                                  p * 64, row, kvh, a.token_major);
-                issued = n + 1;
+            bool ok = true;
+            int gn = 0, q_loads = 0;
+            int next_idx = (int)blockIdx.x;
+            for (int j = 0; ok && next_idx >= 0; ++j) {
+                const int idx = next_idx;
+                next_idx = -1;
+                item_ring[j & 3] = idx;
+                mbar_arrive(&item_bars[j & 3]);   // release: the slot write is visible to its readers
+                if (idx >= count) break;
+                const FwdItem f = fwd_item(a, idx);
+                // the Q buffers are free once the previous item's last Q.K^T has run
+                if (j > 0 && !mbar_wait(&bars[L::bQEmpty], (j - 1) & 1, abort_flag, kWaitLimitNs)) break;
+                const int ntiles = f.nb1 > 0 ? 2 : 1;
+                mbar_arrive_expect_tx(&bars[L::bQFull], ntiles * L::kTileBytes);
+                for (int t = 0; t < ntiles; ++t)
+                    for (int p = 0; p < L::kPanels; ++p)
+                        tma_load_rows(sm + (t ? L::kQ1 : L::kQ0) + p * (kTileM * 128), &tmQ, &bars[L::bQFull], p * 64,
+                                      t ? f.q01 : f.q00, f.h, a.token_major);
+                ++q_loads;
+                for (int n = 0; n < f.nmax; ++n, ++gn) {
+                    const int st = gn & 1;
+                    if (gn >= 2 && !mbar_wait(&bars[L::bKvEmpty + st], ((gn >> 1) - 1) & 1, abort_flag, kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    const int row = f.s + n * kBlockN;
+                    mbar_arrive_expect_tx(&bars[L::bKFull + st], L::kTileBytes);
+                    for (int p = 0; p < L::kPanels; ++p)
+                        tma_load_rows(sm + L::kK + st * L::kTileBytes + p * (kTileM * 128), &tmK, &bars[L::bKFull + st],
+                                      p * 64, row, f.kvh, a.token_major);
+                    mbar_arrive_expect_tx(&bars[L::bVFull + st], L::kTileBytes);
+                    for (int p = 0; p < L::kPanels; ++p)
+                        tma_load_rows(sm + L::kV + st * L::kTileBytes + p * (kTileM * 128), &tmV, &bars[L::bVFull + st],
+                                      p * 64, row, f.kvh, a.token_major);
+                    // two blocks before the end, reserve the next item and pull its Q into L2
+                    if (n == (f.nmax >= 2 ? f.nmax - 2 : 0)) {
+                        next_idx = (int)gridDim.x + atomicAdd(&a.hdr->fwd_next, 1);
+                        if (next_idx < count) {
+                            const FwdItem nf = fwd_item(a, next_idx);
+                            for (int p = 0; p < L::kPanels; ++p) {
+                                tma_prefetch_rows(&tmQ, p * 64, nf.q00, nf.h, a.token_major);
+                                if (nf.nb1 > 0) tma_prefetch_rows(&tmQ, p * 64, nf.q01, nf.h, a.token_major);
+                            }
+                        }
+                    }
+                }
             }
-            // Before the CTA may exit, every copy it issued must have landed. The last
-            // use of each stage is its final phase, so waiting on it is always sound.
-            mbar_wait_drain(&bars[L::bQFull], 0, kDrainLimitNs);
-            for (int n = issued - 2 < 0 ? 0 : issued - 2; n < issued; ++n) {
+            // Before the CTA may exit, every copy it issued must have landed. The last use of
+            // each barrier is its final phase, so waiting on it is always sound.
+            if (q_loads > 0) mbar_wait_drain(&bars[L::bQFull], (q_loads - 1) & 1, kDrainLimitNs);
+            for (int n = gn - 2 < 0 ? 0 : gn - 2; n < gn; ++n) {
                 mbar_wait_drain(&bars[L::bKFull + (n & 1)], (n >> 1) & 1, kDrainLimitNs);
                 mbar_wait_drain(&bars[L::bVFull + (n & 1)], (n >> 1) & 1, kDrainLimitNs);
             }
@@ -162,7 +225,6 @@ __global__ void __maxnreg__(kLaunchRegs)
             const uint64_t dK1 = dK0 + (uint64_t)(L::kTileBytes >> 4);
             const uint64_t dV0 = sdesc_sw128(smem_u32(sm + L::kV), kTileM * 128, 1024);
             const uint64_t dV1 = dV0 + (uint64_t)(L::kTileBytes >> 4);
-            bool ok = mbar_wait(&bars[L::bQFull], 0, abort_flag, kWaitLimitNs);
             auto issue_s = [&](int t, int st) {
                 const uint64_t ad = t ? dQ1 : dQ0, bd = st ? dK1 : dK0;
                 const uint32_t d = tbase + t * 128;
@@ -181,40 +243,60 @@ __global__ void __maxnreg__(kLaunchRegs)
                 for (int k = 0; k < kBlockN / 16; ++k)
                     mma_ts(d, a_t + k * 8, bd + (uint64_t)((k * 2048) >> 4), idO, (acc || k > 0) ? 1u : 0u);
             };
-            if (ok && nmax > 0) {
-                ok = mbar_wait(&bars[L::bKFull], 0, abort_flag, kWaitLimitNs);
-                if (ok) {
+            bool ok = true;
+            int gn = 0, pb0 = 0, pb1 = 0;   // blocks of the CTA, of tile 0, of tile 1 before this item
+            for (int j = 0; ok; ++j) {
+                int idx;
+                if (!fwd_read_item(item_bars, item_ring, j, abort_flag, idx)) break;
+                if (idx >= count) break;
+                const FwdItem f = fwd_item(a, idx);
+                if (!mbar_wait(&bars[L::bQFull], j & 1, abort_flag, kWaitLimitNs)) break;
+                if (f.nmax > 0) {
+                    if (!mbar_wait(&bars[L::bKFull + (gn & 1)], (gn >> 1) & 1, abort_flag, kWaitLimitNs)) break;
                     tc_fence_after();
-                    if (nb0 > 0) issue_s(0, 0);
-                    if (nb1 > 0) issue_s(1, 0);
+                    // The scores regions are free: the previous item's last P.V, which read them,
+                    // was issued before these (tensor-core MMAs run in issue order).
+                    if (f.nb0 > 0) issue_s(0, gn & 1);
+                    if (f.nb1 > 0) issue_s(1, gn & 1);
                 }
-            }
-            for (int n = 0; ok && n < nmax; ++n) {
-                const int st = n & 1;
-                if (!mbar_wait(&bars[L::bVFull + st], (n >> 1) & 1, abort_flag, kWaitLimitNs)) break;
-                bool next_k_ready = false;
-                for (int t = 0; t < 2 && ok; ++t) {
-                    const int nbt = t ? nb1 : nb0;
-                    if (n >= nbt) continue;
-                    if (!mbar_wait(&bars[L::bPFull + t], n & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
-                    tc_fence_after();
-                    issue_pv(t, st, n > 0);
-                    if (n == nbt - 1) {
-                        mma_commit(&bars[L::bODone + t]);
-                    } else {
-                        const int st1 = (n + 1) & 1;
-                        if (!next_k_ready) {
-                            if (!mbar_wait(&bars[L::bKFull + st1], ((n + 1) >> 1) & 1, abort_flag, kWaitLimitNs)) {
-                                ok = false;
-                                break;
-                            }
-                            tc_fence_after();
-                            next_k_ready = true;
+                if (f.nmax <= 1) mma_commit(&bars[L::bQEmpty]);   // no later Q.K^T in this item
+                for (int n = 0; ok && n < f.nmax; ++n) {
+                    const int gb = gn + n, st = gb & 1;
+                    if (!mbar_wait(&bars[L::bVFull + st], (gb >> 1) & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
+                    bool next_k_ready = false;
+                    for (int t = 0; t < 2 && ok; ++t) {
+                        const int nbt = t ? f.nb1 : f.nb0;
+                        if (n >= nbt) continue;
+                        if (!mbar_wait(&bars[L::bPFull + t], ((t ? pb1 : pb0) + n) & 1, abort_flag, kWaitLimitNs)) {
+                            ok = false;
+                            break;
                         }
-                        issue_s(t, st1);
+                        tc_fence_after();
+                        issue_pv(t, st, n > 0);
+                        if (n == nbt - 1) {
+                            mma_commit(&bars[L::bODone + t]);
+                        } else {
+                            const int st1 = (gb + 1) & 1;
+                            if (!next_k_ready) {
+                                if (!mbar_wait(&bars[L::bKFull + st1], ((gb + 1) >> 1) & 1, abort_flag, kWaitLimitNs)) {
+                                    ok = false;
+                                    break;
+                                }
+                                tc_fence_after();
+                                next_k_ready = true;
+                            }
+                            issue_s(t, st1);
+                        }
                     }
+                    if (ok && n == f.nmax - 2) mma_commit(&bars[L::bQEmpty]);   // the item's last Q.K^T is issued
+                    mma_commit(&bars[L::bKvEmpty + st]);
                 }
-                mma_commit(&bars[L::bKvEmpty + st]);
+                if (!ok) break;
+                for (int t = 0; t < 2; ++t)   // a tile with no blocks still completes its per-item phase
+                    if ((t ? f.nb1 : f.nb0) == 0) mma_commit(&bars[L::bODone + t]);
+                gn += f.nmax;
+                pb0 += f.nb0;
+                pb1 += f.nb1;
             }
             // Drain: the tensor pipe must be idle before TMEM is released.
             mma_commit(&bars[L::bDrain]);
@@ -224,135 +306,167 @@ __global__ void __maxnreg__(kLaunchRegs)
         regs_increase<kSoftmaxRegs>();
         // ------------------------------------------------------------------ softmax groups
         const int t = warp >> 2;
-        const int q0 = t ? q01 : q00;
-        const int nbt = t ? nb1 : nb0;
         const int rq = (warp & 3) * 32 + lane;
-        const int i = q0 + rq;  // this thread's query row
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t tS = tbase + lane_off + t * 128;
         const uint32_t tO = tbase + lane_off + 256 + t * 128;
         const float sl2 = a.scale_log2;
-        float m = -INFINITY, l = 0.f;
         bool ok = true;
-        for (int n = 0; n < nbt; ++n) {
-            if (!mbar_wait(&bars[L::bSFull + t], n & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
-            tc_fence_after();
-            uint32_t r0[32], r1[32], r2[32], r3[32];
-            tmem_ld32(tS + 0, r0);
-            tmem_ld32(tS + 32, r1);
-            tmem_ld32(tS + 64, r2);
-            tmem_ld32(tS + 96, r3);
-            tmem_ld_wait();
-            reg_fence(r0);
-            reg_fence(r1);
-            reg_fence(r2);
-            reg_fence(r3);
-            float sv[128];
-#pragma unroll
-            for (int c = 0; c < 32; ++c) {
-                sv[c] = __uint_as_float(r0[c]);
-                sv[32 + c] = __uint_as_float(r1[c]);
-                sv[64 + c] = __uint_as_float(r2[c]);
-                sv[96 + c] = __uint_as_float(r3[c]);
-            }
-            const int kv0 = s + n * kBlockN;
-            const bool need_mask = (a.causal && kv0 + kBlockN - 1 > q0) || (kv0 + kBlockN > e);
-            if (need_mask) {
-                int lim = e - 1 - kv0;  // last visible column of this block
-                if (a.causal && i - kv0 < lim) lim = i - kv0;
-#pragma unroll
-                for (int c = 0; c < 128; ++c)
-                    if (c > lim) sv[c] = -INFINITY;
-            }
-            // row max over 8 independent chains of three-input max (a single two-input chain
-            // would serialise 127 dependent ops)
-            float mx8[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) mx8[j] = sv[j];
-#pragma unroll
-            for (int c = 8; c < 120; c += 16)
-#pragma unroll
-                for (int j = 0; j < 8; ++j) mx8[j] = fmax3(mx8[j], sv[c + j], sv[c + 8 + j]);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) mx8[j] = fmaxf(mx8[j], sv[120 + j]);
-            const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
-            const float m_blk = mx * sl2;
-            if (n == 0) {
-                m = m_blk;
-            } else if (m_blk > m + kRescaleThreshold) {
-                const float f = ex2_approx(m - m_blk);
-                l *= f;
-#pragma unroll 1
-                for (int c = 0; c < D; c += 32) {
-                    uint32_t o[32];
-                    tmem_ld32(tO + c, o);
-                    tmem_ld_wait(o);
-                    uint32_t lo[16], hi[16];
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        lo[j] = __float_as_uint(__uint_as_float(o[j]) * f);
-                        hi[j] = __float_as_uint(__uint_as_float(o[16 + j]) * f);
+        int pb = 0;   // this tile's blocks before the current item
+        for (int j = 0; ok; ++j) {
+            int idx;
+            if (!fwd_read_item(item_bars, item_ring, j, abort_flag, idx)) break;
+            if (idx >= count) break;
+            const FwdItem f = fwd_item(a, idx);
+            const int s = f.s, e = f.e, h = f.h;
+            const int q0 = t ? f.q01 : f.q00;
+            const int nbt = t ? f.nb1 : f.nb0;
+            const int i = q0 + rq;  // this thread's query row
+            float m = -INFINITY, l = 0.f;
+            for (int n = 0; n < nbt; ++n) {
+                if (!mbar_wait(&bars[L::bSFull + t], (pb + n) & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
+                tc_fence_after();
+                uint32_t r0[32], r1[32], r2[32], r3[32];
+                tmem_ld32(tS + 0, r0);
+                tmem_ld32(tS + 32, r1);
+                tmem_ld32(tS + 64, r2);
+                tmem_ld32(tS + 96, r3);
+                tmem_ld_wait();
+                reg_fence(r0);
+                reg_fence(r1);
+                reg_fence(r2);
+                reg_fence(r3);
+                float sv[128];
+    #pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    sv[c] = __uint_as_float(r0[c]);
+                    sv[32 + c] = __uint_as_float(r1[c]);
+                    sv[64 + c] = __uint_as_float(r2[c]);
+                    sv[96 + c] = __uint_as_float(r3[c]);
+                }
+                const int kv0 = s + n * kBlockN;
+                const bool need_mask = (a.causal && kv0 + kBlockN - 1 > q0) || (kv0 + kBlockN > e);
+                if (need_mask) {
+                    int lim = e - 1 - kv0;  // last visible column of this block
+                    if (a.causal && i - kv0 < lim) lim = i - kv0;
+    #pragma unroll
+                    for (int c = 0; c < 128; ++c)
+                        if (c > lim) sv[c] = -INFINITY;
+                }
+                // row max over 8 independent chains of three-input max (a single two-input chain
+                // would serialise 127 dependent ops)
+                float mx8[8];
+    #pragma unroll
+                for (int j = 0; j < 8; ++j) mx8[j] = sv[j];
+    #pragma unroll
+                for (int c = 8; c < 120; c += 16)
+    #pragma unroll
+                    for (int j = 0; j < 8; ++j) mx8[j] = fmax3(mx8[j], sv[c + j], sv[c + 8 + j]);
+    #pragma unroll
+                for (int j = 0; j < 8; ++j) mx8[j] = fmaxf(mx8[j], sv[120 + j]);
+                const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
+                const float m_blk = mx * sl2;
+                if (n == 0) {
+                    m = m_blk;
+                } else if (m_blk > m + kRescaleThreshold) {
+                    const float f = ex2_approx(m - m_blk);
+                    l *= f;
+    #pragma unroll 1
+                    for (int c = 0; c < D; c += 32) {
+                        uint32_t o[32];
+                        tmem_ld32(tO + c, o);
+                        tmem_ld_wait(o);
+                        uint32_t lo[16], hi[16];
+    #pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            lo[j] = __float_as_uint(__uint_as_float(o[j]) * f);
+                            hi[j] = __float_as_uint(__uint_as_float(o[16 + j]) * f);
+                        }
+                        tmem_st16(tO + c, lo);
+                        tmem_st16(tO + c + 16, hi);
                     }
-                    tmem_st16(tO + c, lo);
-                    tmem_st16(tO + c + 16, hi);
+                    m = m_blk;
                 }
-                m = m_blk;
-            }
-            const float mu = (m == -INFINITY) ? 0.f : m;
-            const float2 sl2x2 = make_float2(sl2, sl2), nmu2 = make_float2(-mu, -mu);
-            float2 l4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const float2 x = fma2(make_float2(sv[32 * c + 2 * j], sv[32 * c + 2 * j + 1]), sl2x2, nmu2);
-                    const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-                    l4[j & 3] = add2(l4[j & 3], pp);   // independent partial row sums
-                    pk[j] = pack2<F16>(pp.x, pp.y);
+                const float mu = (m == -INFINITY) ? 0.f : m;
+                const float2 sl2x2 = make_float2(sl2, sl2), nmu2 = make_float2(-mu, -mu);
+                float2 l4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+    #pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t pk[16];
+    #pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float2 x = fma2(make_float2(sv[32 * c + 2 * j], sv[32 * c + 2 * j + 1]), sl2x2, nmu2);
+                        const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                        l4[j & 3] = add2(l4[j & 3], pp);   // independent partial row sums
+                        pk[j] = pack2<F16>(pp.x, pp.y);
+                    }
+                    tmem_st16(tS + 16 * c, pk);
                 }
-                tmem_st16(tS + 16 * c, pk);
+                const float2 lsum = add2(add2(l4[0], l4[1]), add2(l4[2], l4[3]));
+                l += lsum.x + lsum.y;
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[L::bPFull + t]);
+
             }
-            const float2 lsum = add2(add2(l4[0], l4[1]), add2(l4[2], l4[3]));
-            l += lsum.x + lsum.y;
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[L::bPFull + t]);
-        }
-        if (ok && nbt > 0 && mbar_wait(&bars[L::bODone + t], 0, abort_flag, kWaitLimitNs)) {
-            tc_fence_after();
-            const bool valid = i < e;
-            const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
-            if (q0 + kTileM <= e) {
-                // Whole tile: stage O in this tile's Q buffer (its last reader, the final Q.K^T,
-                // completed before the P.V this group just waited for) and write it with TMA
-                // stores, so the rows leave as full lines instead of 16-byte pieces.
-                uint8_t* qt = sm + (t ? L::kQ1 : L::kQ0);
-#pragma unroll 1
-                for (int c = 0; c < D; c += 32) {
+            if (!ok) break;
+            // every tile waits for its per-item phase, also one without blocks
+            if (!mbar_wait(&bars[L::bODone + t], j & 1, abort_flag, kWaitLimitNs)) break;
+            if (nbt > 0 && q0 + kTileM <= e) {
+                // Whole tile: O leaves through this tile's 64-column staging panel, 64 columns
+                // per round, each round one TMA store (full lines instead of 16-byte pieces 256
+                // bytes apart); the second round is packed into registers first.
+                tc_fence_after();
+                const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+                uint8_t* stage = sm + L::kStage + t * (kTileM * 128);
+                uint32_t held[32 * (D / 64 - 1) + 1];   // columns 64..D-1, two per word (none for D = 64)
+                static_assert(D == 64 || D == 128, "the epilogue holds at most one extra 64-column panel");
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
                     uint32_t o[32];
-                    tmem_ld32(tO + c, o);
+                    tmem_ld32(tO + 32 * c, o);
                     tmem_ld_wait(o);
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        const int col = c + 8 * q;   // [128 rows][D] as D/64 panels of [128][64], 128-byte swizzle
-                        *(uint4*)(qt + (col / 64) * (kTileM * 128) + sw128_offset(rq, (uint32_t)((col % 64) * 2))) =
-                            make_uint4(pack2<F16>(__uint_as_float(o[8 * q]) * inv_l, __uint_as_float(o[8 * q + 1]) * inv_l),
-                                       pack2<F16>(__uint_as_float(o[8 * q + 2]) * inv_l, __uint_as_float(o[8 * q + 3]) * inv_l),
-                                       pack2<F16>(__uint_as_float(o[8 * q + 4]) * inv_l, __uint_as_float(o[8 * q + 5]) * inv_l),
-                                       pack2<F16>(__uint_as_float(o[8 * q + 6]) * inv_l, __uint_as_float(o[8 * q + 7]) * inv_l));
+                        const uint32_t p0 = pack2<F16>(__uint_as_float(o[8 * q]) * inv_l, __uint_as_float(o[8 * q + 1]) * inv_l);
+                        const uint32_t p1 = pack2<F16>(__uint_as_float(o[8 * q + 2]) * inv_l, __uint_as_float(o[8 * q + 3]) * inv_l);
+                        const uint32_t p2 = pack2<F16>(__uint_as_float(o[8 * q + 4]) * inv_l, __uint_as_float(o[8 * q + 5]) * inv_l);
+                        const uint32_t p3 = pack2<F16>(__uint_as_float(o[8 * q + 6]) * inv_l, __uint_as_float(o[8 * q + 7]) * inv_l);
+                        const int col = 32 * c + 8 * q;   // first of the 8 columns in this 16-byte chunk
+                        if (col < 64) {
+                            *(uint4*)(stage + sw128_offset(rq, (uint32_t)(col * 2))) = make_uint4(p0, p1, p2, p3);
+                        } else if (D > 64) {
+                            const int hi = (col - 64) / 2;
+                            held[hi] = p0;
+                            held[hi + 1] = p1;
+                            held[hi + 2] = p2;
+                            held[hi + 3] = p3;
+                        }
                     }
                 }
-                fence_proxy_async_smem();
-                named_bar_sync(1 + t, 128);
-                if (rq == 0) {
-                    for (int p = 0; p < L::kPanels; ++p)
-                        tma_store_rows(&tmO, qt + p * (kTileM * 128), p * 64, q0, h, a.token_major);
-                    bulk_commit_group();
+#pragma unroll 1
+                for (int round = 0; round < D / 64; ++round) {
+                    if (round > 0) {   // columns 64..127 into the panel the first store has released
+#pragma unroll
+                        for (int jj = 0; jj < 8; ++jj)
+                            *(uint4*)(stage + sw128_offset(rq, (uint32_t)(jj * 16))) =
+                                make_uint4(held[4 * jj], held[4 * jj + 1], held[4 * jj + 2], held[4 * jj + 3]);
+                    }
+                    fence_proxy_async_smem();
+                    named_bar_sync(1 + t, 128);
+                    if (rq == 0) {
+                        tma_store_rows(&tmO, stage, round * 64, q0, h, a.token_major);
+                        bulk_commit_group();
+                        bulk_wait_group_read<0>();
+                    }
+                    named_bar_sync(1 + t, 128);
                 }
-                if (rq == 0) bulk_wait_group_read<0>();   // the buffer is read before the CTA ends
-            } else {   // a sample's ragged last tile: row by row, rows past the end skipped
+                a.lse[(int64_t)h * a.T + i] = (m + __log2f(l)) * 0.69314718055994530942f;
+            } else if (nbt > 0) {   // a sample's ragged last tile: row by row, rows past the end skipped
+                tc_fence_after();
+                const bool valid = i < e;
+                const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
                 uint16_t* orow = a.o + act_row(h, i, a.T, a.hq, a.token_major) * D;
 #pragma unroll 1
                 for (int c = 0; c < D; c += 32) {
@@ -361,18 +475,20 @@ __global__ void __maxnreg__(kLaunchRegs)
                     tmem_ld_wait(o);
                     uint32_t pk[16];
 #pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        pk[j] = pack2<F16>(__uint_as_float(o[2 * j]) * inv_l, __uint_as_float(o[2 * j + 1]) * inv_l);
+                    for (int jj = 0; jj < 16; ++jj)
+                        pk[jj] = pack2<F16>(__uint_as_float(o[2 * jj]) * inv_l, __uint_as_float(o[2 * jj + 1]) * inv_l);
                     if (valid) {
                         uint4* dst = (uint4*)(orow + c);
 #pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                        for (int jj = 0; jj < 4; ++jj)
+                            dst[jj] = make_uint4(pk[4 * jj], pk[4 * jj + 1], pk[4 * jj + 2], pk[4 * jj + 3]);
                     }
                 }
+                if (valid) a.lse[(int64_t)h * a.T + i] = (m + __log2f(l)) * 0.69314718055994530942f;
             }
-            if (valid) a.lse[(int64_t)h * a.T + i] = (m + __log2f(l)) * 0.69314718055994530942f;
+            pb += nbt;
         }
+        if (rq == 0) bulk_wait_group<0>();   // the last output stores have landed
     }
 
     __syncwarp();
@@ -393,6 +509,15 @@ cudaError_t launch_fwd_impl(const CUtensorMap& q, const CUtensorMap& k, const CU
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
+    // persistent CTAs, one per SM (the shared-memory footprint allows no more)
+    static int sms = 0;
+    if (sms == 0) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+    }
+    if (grid > sms) grid = sms;
     attn_fwd_kernel<D, F16><<<grid, kFwdThreads, L::kAlloc, s>>>(q, k, v, o, a);
     return cudaGetLastError();
 }

@@ -43,6 +43,7 @@ struct WsHeader {
     int bwd_count;
     int max_cost;
     int bwd_next;  // backward work items handed out past the first one of each CTA
+    int fwd_next;  // the same for the forward
 };
 
 struct WsLayout {
