@@ -68,6 +68,21 @@ def test_fwd_ragged_packed_edges(causal, D):
     check_fwd(q, k, v, w.cu_seqlens(), causal)
 
 
+def test_fwd_runs_of_single_tile_items():
+    """Many short samples, ordered rank by rank across 32 heads: long runs of work items
+    whose second query tile has no blocks, so the persistent CTAs' second softmax group
+    sits out item after item while the first keeps going; 300-token samples add items
+    with both tiles and a ragged tile."""
+    needs_gpu()
+    lengths = [100] * 40 + [300] * 20 + [129] * 10
+    w = custom_workload("runs", lengths, sp=1, hq=32, hkv=8, head_dim=128, index=16)
+    q, k, v, _ = make(w)
+    cu = w.cu_seqlens()
+    p, o1, l1 = check_fwd(q, k, v, cu, True, heads=[0, 13, 31])
+    o2, l2, _ = p.forward()
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16)) and torch.equal(l1, l2)
+
+
 def test_fwd_empty_samples():
     needs_gpu()
     w = custom_workload("empty", [0, 100, 0, 0, 156, 0], sp=1, hq=2, hkv=2, head_dim=128, index=12)

@@ -378,8 +378,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             nl_next = q_ok ? -__ldg(a.lse + (int64_t)h * a.T + q) * 1.4426950408889634f : -INFINITY;
             nd_next = q_ok ? -__ldg(a.delta + (int64_t)h * a.T + q) : 0.f;
         };
+        // The half's four warps leave their loops together: a warp that gave up on a bounded
+        // wait skips ahead to the next vote (group_any) instead of leaving at once, so that no
+        // warp is left waiting at one of the half's barriers for warps that have gone.
         int idx = count;
         if (!read_item(item_bars, item_ring, 0, abort_flag, idx)) ok = false;
+        ok = !group_any(1 + grp, 128, !ok);
         if (ok && idx < count) fetch_row_stats(bwd_item(a, idx), 0);
         for (int j = 0; ok && idx < count; ++j) {
             const BwdItem w = bwd_item(a, idx);
@@ -387,7 +391,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const bool kv_ok = kv < w.e;
             for (int k = 0; k < w.nsteps; ++k, ++gk) {
                 const int q0 = w.q0(k);
-                named_bar_sync(1 + grp, 128);
+                if (group_any(1 + grp, 128, !ok)) {   // also: the previous step's reads of the row stats are done
+                    ok = false;
+                    break;
+                }
                 if (r < kHalfCols) {
                     lse_g[r] = nl_next;
                     delta_g[r] = nd_next;
@@ -398,7 +405,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 // last key tile; there query column c (of 128) is visible to key row r iff c >= r
                 const bool mask_blk = (a.causal && q0 == w.kv0) || (w.kv0 + kBlockN > w.e);
                 const int vis_from = (a.causal && q0 == w.kv0) ? r - grp * kHalfCols : -1;
-                if (!mbar_wait(&bars[L::bSFull + grp], gk & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
+                if (!mbar_wait(&bars[L::bSFull + grp], gk & 1, abort_flag, kWaitLimitNs)) { ok = false; continue; }
                 tc_fence_after();
                 // P for this row's query columns as packed bf16 pairs: the values the dV MMA
                 // consumes, kept (half the registers of fp32) for dS
@@ -436,7 +443,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 if (lane == 0) mbar_arrive(&bars[L::bPFull + grp]);
 
                 // dP^T of this half; its commit also covers the previous block's reads of the dS buffer
-                if (!mbar_wait(&bars[L::bDpFull + grp], gk & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
+                if (!mbar_wait(&bars[L::bDpFull + grp], gk & 1, abort_flag, kWaitLimitNs)) { ok = false; continue; }
                 tc_fence_after();
                 uint8_t* panel = sm + L::kDS + grp * (kBlockN * 128);
 #pragma unroll
@@ -472,13 +479,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars[L::bDsFull + grp]);
             }
-            if (!ok) break;
             // the next item, and its first step's row statistics, before this item's epilogue
             int idx_next = count;
-            if (!read_item(item_bars, item_ring, j + 1, abort_flag, idx_next)) ok = false;
+            if (ok && !read_item(item_bars, item_ring, j + 1, abort_flag, idx_next)) ok = false;
             if (ok && idx_next < count) fetch_row_stats(bwd_item(a, idx_next), 0);
             idx = idx_next;
-            if (!ok || !mbar_wait(&bars[L::bAccFull], j & 1, abort_flag, kWaitLimitNs)) break;
+            if (ok) ok = mbar_wait(&bars[L::bAccFull], j & 1, abort_flag, kWaitLimitNs);
+            if (group_any(1 + grp, 128, !ok)) break;
             tc_fence_after();
             // half A writes dV, half B writes dK; TMEM is handed back to the next item's MMAs as
             // soon as the last chunk has been read, before the global stores finish

@@ -58,7 +58,8 @@ struct FwdSmem {
     static constexpr int kBars = kStage + 2 * kTileM * 128;
     // barrier indices
     static constexpr int bQFull = 0, bKFull = 1, bVFull = 3, bKvEmpty = 5, bSFull = 7, bPFull = 9, bODone = 11,
-                         bDrain = 13, bQEmpty = 14, bItem = 15, kNumBars = 19;   // bItem: 4-slot ring
+                         bDrain = 13, bQEmpty = 14, bItem = 15, bItemFree = 19, kNumBars = 23;
+    // bItem / bItemFree: published / read by every reader, one of each per slot of the 4-slot item ring
     static constexpr int kItemRing = kBars + 8 * kNumBars;   // int[4]: work item of each slot
     static constexpr int kTmemSlot = kItemRing + 16;
     static constexpr int kAbort = kTmemSlot + 8;
@@ -87,9 +88,10 @@ __device__ __forceinline__ FwdItem fwd_item(const FwdArgs& a, int idx) {
     return f;
 }
 
-// The CTA's j-th work item from the producer's 4-slot ring (false: the wait gave up). No
-// role runs more than two items behind the producer, so a slot is never rewritten while a
-// reader still needs it.
+// The CTA's j-th work item from the producer's 4-slot ring (false: the wait gave up). Each
+// reader then arrives on the slot's free barrier (the MMA thread and each softmax warp);
+// the producer rewrites a slot only once all of them have, because a softmax group whose
+// tile has no blocks in a run of items is not held back by the MMAs and may lag.
 __device__ __forceinline__ bool fwd_read_item(uint64_t* item_bars, volatile int* ring, int j,
                                               volatile int* abort_flag, int& idx) {
     if (!mbar_wait(&item_bars[j & 3], (j >> 2) & 1, abort_flag, kWaitLimitNs)) return false;
@@ -114,6 +116,7 @@ __global__ void __maxnreg__(kLaunchRegs)
     volatile int* abort_flag = (volatile int*)(sm + L::kAbort);
     volatile int* item_ring = (volatile int*)(sm + L::kItemRing);
     uint64_t* item_bars = &bars[L::bItem];
+    uint64_t* item_free = &bars[L::bItemFree];
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
@@ -134,7 +137,10 @@ __global__ void __maxnreg__(kLaunchRegs)
         }
         mbar_init(&bars[L::bDrain], 1);
         mbar_init(&bars[L::bQEmpty], 1);
-        for (int i = 0; i < 4; ++i) mbar_init(&bars[L::bItem + i], 1);
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(&bars[L::bItem + i], 1);
+            mbar_init(&bars[L::bItemFree + i], 1 + 8);   // the MMA thread and the 8 softmax warps
+        }
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -144,8 +150,10 @@ __global__ void __maxnreg__(kLaunchRegs)
     const uint32_t tbase = *tmem_slot;
 
     // Every per-block barrier phase follows a running count across items (the CTA's key/value
-    // blocks for the K/V ring, each tile's blocks for S and P); the per-item ones (Q, O done)
-    // follow the item count j.
+    // blocks for the K/V ring, each tile's blocks for S and P); Q's follow the item count j,
+    // and a tile's O-done the count of items in which that tile has blocks. Each phase of
+    // these barriers needs its waiter to have passed the one before, so a waiter is never
+    // two phases behind and parities cannot alias.
     if (warp >= 10) {
         regs_decrease<kAuxRegs>();  // idle warps of the load/MMA warpgroup
     } else if (warp == 8) {
@@ -161,6 +169,8 @@ __global__ void __maxnreg__(kLaunchRegs)
             for (int j = 0; ok && next_idx >= 0; ++j) {
                 const int idx = next_idx;
                 next_idx = -1;
+                // every reader has taken the item this slot held four items ago
+                if (j >= 4 && !mbar_wait(&item_free[j & 3], ((j >> 2) - 1) & 1, abort_flag, kWaitLimitNs)) break;
                 item_ring[j & 3] = idx;
                 mbar_arrive(&item_bars[j & 3]);   // release: the slot write is visible to its readers
                 if (idx >= count) break;
@@ -248,6 +258,7 @@ __global__ void __maxnreg__(kLaunchRegs)
             for (int j = 0; ok; ++j) {
                 int idx;
                 if (!fwd_read_item(item_bars, item_ring, j, abort_flag, idx)) break;
+                mbar_arrive(&item_free[j & 3]);
                 if (idx >= count) break;
                 const FwdItem f = fwd_item(a, idx);
                 if (!mbar_wait(&bars[L::bQFull], j & 1, abort_flag, kWaitLimitNs)) break;
@@ -292,8 +303,6 @@ __global__ void __maxnreg__(kLaunchRegs)
                     mma_commit(&bars[L::bKvEmpty + st]);
                 }
                 if (!ok) break;
-                for (int t = 0; t < 2; ++t)   // a tile with no blocks still completes its per-item phase
-                    if ((t ? f.nb1 : f.nb0) == 0) mma_commit(&bars[L::bODone + t]);
                 gn += f.nmax;
                 pb0 += f.nb0;
                 pb1 += f.nb1;
@@ -311,16 +320,17 @@ __global__ void __maxnreg__(kLaunchRegs)
         const uint32_t tS = tbase + lane_off + t * 128;
         const uint32_t tO = tbase + lane_off + 256 + t * 128;
         const float sl2 = a.scale_log2;
-        bool ok = true;
         int pb = 0;   // this tile's blocks before the current item
-        for (int j = 0; ok; ++j) {
-            int idx;
-            if (!fwd_read_item(item_bars, item_ring, j, abort_flag, idx)) break;
-            if (idx >= count) break;
-            const FwdItem f = fwd_item(a, idx);
+        int od = 0;   // items before the current one in which this tile has blocks
+        for (int j = 0;; ++j) {
+            int idx = count;
+            bool ok = fwd_read_item(item_bars, item_ring, j, abort_flag, idx);
+            __syncwarp();
+            if (ok && lane == 0) mbar_arrive(&item_free[j & 3]);
+            const FwdItem f = fwd_item(a, ok && idx < count ? idx : 0);
             const int s = f.s, e = f.e, h = f.h;
             const int q0 = t ? f.q01 : f.q00;
-            const int nbt = t ? f.nb1 : f.nb0;
+            const int nbt = (ok && idx < count) ? (t ? f.nb1 : f.nb0) : 0;
             const int i = q0 + rq;  // this thread's query row
             float m = -INFINITY, l = 0.f;
             for (int n = 0; n < nbt; ++n) {
@@ -410,9 +420,11 @@ __global__ void __maxnreg__(kLaunchRegs)
                 if (lane == 0) mbar_arrive(&bars[L::bPFull + t]);
 
             }
-            if (!ok) break;
-            // every tile waits for its per-item phase, also one without blocks
-            if (!mbar_wait(&bars[L::bODone + t], j & 1, abort_flag, kWaitLimitNs)) break;
+            if (ok && nbt > 0) ok = mbar_wait(&bars[L::bODone + t], od & 1, abort_flag, kWaitLimitNs);
+            // The group's warps leave together (a warp that gave up on a wait must not leave the
+            // others at the epilogue's barriers); the ring's end marker ends every warp's loop.
+            if (group_any(1 + t, 128, !ok) || idx >= count) break;
+            if (nbt > 0) ++od;
             if (nbt > 0 && q0 + kTileM <= e) {
                 // Whole tile: O leaves through this tile's 64-column staging panel, 64 columns
                 // per round, each round one TMA store (full lines instead of 16-byte pieces 256

@@ -392,6 +392,19 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
 __device__ __forceinline__ void named_bar_arrive(int id, int nthreads) {
     asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
+// Named barrier that also ORs `pred` over its `nthreads` threads: every participant returns
+// the same answer. Warps of a group that must leave a loop together (for example after one
+// of them gave up on a bounded wait) vote with it, so that none is left waiting at a later
+// barrier of the group for warps that have already left.
+__device__ __forceinline__ bool group_any(int id, int nthreads, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
 
 }  // namespace ptx
 }  // namespace usp
