@@ -118,6 +118,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     const __grid_constant__ CUtensorMap tmDQ, const __grid_constant__ CUtensorMap tmDK,
                     const __grid_constant__ CUtensorMap tmDV, const BwdArgs a) {
     using L = BwdSmem<D>;
+    pdl_wait();   // the work list, Delta and the zeroed dQ accumulator come from the kernels before
     const int count = a.hdr->bwd_count;
     if ((int)blockIdx.x >= count) return;
     // once any CTA of this launch has timed out, the rest skip their work
@@ -410,32 +411,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 // P for this row's query columns as packed bf16 pairs: the values the dV MMA
                 // consumes, kept (half the registers of fp32) for dS
                 uint32_t pkall[kHalfCols / 2];
+                static_assert(kHalfCols == 64, "the P pass loads the half's two 32-column chunks at once");
+                {
+                    uint32_t sr[2][32];
+                    tmem_ld32(tS, sr[0]);
+                    tmem_ld32(tS + 32, sr[1]);
+                    tmem_ld_wait(sr[0]);
+                    reg_fence(sr[1]);
 #pragma unroll
-                for (int c = 0; c < kHalfCols / 32; ++c) {
-                    uint32_t sr[32];
-                    tmem_ld32(tS + 32 * c, sr);
-                    float4 nl4[8];
+                    for (int c = 0; c < 2; ++c) {
 #pragma unroll
-                    for (int jj = 0; jj < 8; ++jj) nl4[jj] = *(const float4*)(lse_g + 32 * c + 4 * jj);
-                    tmem_ld_wait(sr);
-#pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) {
-                        const int c0 = 32 * c + 2 * jj;
-                        const float4 q4 = nl4[jj >> 1];
-                        const float2 nl = (jj & 1) ? make_float2(q4.z, q4.w) : make_float2(q4.x, q4.y);
-                        const float2 x = fma2(make_float2(__uint_as_float(sr[2 * jj]), __uint_as_float(sr[2 * jj + 1])),
-                                              make_float2(sl2, sl2), nl);
-                        float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-                        if (mask_blk) {
-                            if (!kv_ok || c0 < vis_from) pp.x = 0.f;
-                            if (!kv_ok || c0 + 1 < vis_from) pp.y = 0.f;
+                        for (int jj = 0; jj < 16; ++jj) {
+                            const int c0 = 32 * c + 2 * jj;
+                            const float2 nl = *(const float2*)(lse_g + c0);
+                            const float2 x = fma2(make_float2(__uint_as_float(sr[c][2 * jj]), __uint_as_float(sr[c][2 * jj + 1])),
+                                                  make_float2(sl2, sl2), nl);
+                            float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                            if (mask_blk) {
+                                if (!kv_ok || c0 < vis_from) pp.x = 0.f;
+                                if (!kv_ok || c0 + 1 < vis_from) pp.y = 0.f;
+                            }
+                            pkall[16 * c + jj] = pack2<F16>(pp.x, pp.y);
                         }
-                        pkall[16 * c + jj] = pack2<F16>(pp.x, pp.y);
-                    }
-                    uint32_t pk[16];
+                        uint32_t pk[16];
 #pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) pk[jj] = pkall[16 * c + jj];
-                    tmem_st16(tS + 16 * c, pk);
+                        for (int jj = 0; jj < 16; ++jj) pk[jj] = pkall[16 * c + jj];
+                        tmem_st16(tS + 16 * c, pk);
+                    }
                 }
                 tmem_st_wait();
                 tc_fence_before();
@@ -638,6 +640,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (lane == 0) bulk_wait_group<0>();
     }
 
+    pdl_trigger();   // this CTA has no more items: dq_convert may start launching
     __syncwarp();
     tc_fence_before();
     __syncthreads();
@@ -652,6 +655,7 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint16_t* __restric
                                                        float* __restrict__ delta, float* __restrict__ dq_acc, int64_t T,
                                                        int H, int token_major, int dq_token_major) {
     constexpr int TPR = D / 8;   // threads per row, 8 elements (16 bytes) each
+    pdl_trigger();   // the scheduler after this kernel needs none of its output
     const int h = blockIdx.y;
     const int sub = threadIdx.x % TPR;
     constexpr int64_t kRowsPerCta = 256 / TPR;
@@ -690,6 +694,7 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint16_t* __restric
 template <int D4, bool F16>
 __global__ void __launch_bounds__(256) dq_convert_kernel(const float4* __restrict__ src, uint2* __restrict__ dst,
                                                          int64_t T, int H, int token_major) {
+    pdl_wait();   // the accumulator is final once the backward kernel has completed
     const int h = blockIdx.y;
     const float4* s_head = src + (int64_t)h * T * D4;
     const int64_t n = T * D4;
@@ -737,8 +742,8 @@ cudaError_t launch_bwd_impl(const CUtensorMap& q, const CUtensorMap& k, const CU
         if (e != cudaSuccess) return e;
     }
     if (grid > sms) grid = sms;
-    attn_bwd_kernel<D, F16><<<grid, kBwdThreads, L::kAlloc, s>>>(q, k, v, dout, dq, dk, dv, a);
-    return cudaGetLastError();
+    return launch_kernel(attn_bwd_kernel<D, F16>, dim3(grid), dim3(kBwdThreads), (size_t)L::kAlloc, s, true, q, k, v,
+                         dout, dq, dk, dv, a);
 }
 
 // CTAs for `work_items` units at `per_cta` units each, capped so that all `ys` rows of the
@@ -787,15 +792,10 @@ cudaError_t launch_dq_convert(const float* dq_acc, void* dq, int64_t T, int hq, 
     const dim3 grid(grid_for(T * D4, 256, hq), hq);
     const float4* src = (const float4*)dq_acc;
     uint2* dst = (uint2*)dq;
-    if (D4 == 32 && f16)
-        dq_convert_kernel<32, true><<<grid, 256, 0, s>>>(src, dst, T, hq, token_major);
-    else if (D4 == 32)
-        dq_convert_kernel<32, false><<<grid, 256, 0, s>>>(src, dst, T, hq, token_major);
-    else if (f16)
-        dq_convert_kernel<16, true><<<grid, 256, 0, s>>>(src, dst, T, hq, token_major);
-    else
-        dq_convert_kernel<16, false><<<grid, 256, 0, s>>>(src, dst, T, hq, token_major);
-    return cudaGetLastError();
+    // launched right after the backward kernel, whose completion it waits for on the device
+    auto kernel = D4 == 32 ? (f16 ? dq_convert_kernel<32, true> : dq_convert_kernel<32, false>)
+                           : (f16 ? dq_convert_kernel<16, true> : dq_convert_kernel<16, false>);
+    return launch_kernel(kernel, grid, dim3(256), 0, s, true, src, dst, T, hq, token_major);
 }
 
 cudaError_t launch_debug_timeout(WsHeader* hdr, uint64_t limit_ns, cudaStream_t s) {

@@ -104,6 +104,7 @@ __global__ void __maxnreg__(kLaunchRegs)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO, const FwdArgs a) {
     using L = FwdSmem<D>;
+    pdl_wait();   // the work list and the header come from the scheduler launched just before
     const int count = a.hdr->fwd_count;
     if ((int)blockIdx.x >= count) return;
     // once any CTA of this launch has timed out, the rest skip their work
@@ -530,8 +531,8 @@ cudaError_t launch_fwd_impl(const CUtensorMap& q, const CUtensorMap& k, const CU
         if (e != cudaSuccess) return e;
     }
     if (grid > sms) grid = sms;
-    attn_fwd_kernel<D, F16><<<grid, kFwdThreads, L::kAlloc, s>>>(q, k, v, o, a);
-    return cudaGetLastError();
+    return launch_kernel(attn_fwd_kernel<D, F16>, dim3(grid), dim3(kFwdThreads), (size_t)L::kAlloc, s, true, q, k, v,
+                         o, a);
 }
 
 }  // namespace

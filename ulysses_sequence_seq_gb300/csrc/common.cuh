@@ -4,6 +4,8 @@
 #include <cstddef>
 #include <cstdint>
 
+#include <cuda_runtime.h>
+
 #include "usp.h"
 
 namespace usp {
@@ -86,6 +88,25 @@ inline WsLayout ws_layout(int64_t T, int num_seqs, int hq, int hkv, int D, int b
     if (bwd) off = align256(off + sizeof(float) * (size_t)hq * (size_t)T * (size_t)D);
     w.total = off;
     return w;
+}
+
+// Launches `kernel` on stream s; with `programmatic` the launch may overlap the end of the
+// previous kernel in the stream, and the kernel must call pdl_wait() before it reads
+// anything that kernel (or one before it) wrote.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                          bool programmatic, Args... args) {
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = programmatic ? &attr : nullptr;
+    cfg.numAttrs = programmatic ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
 }  // namespace usp

@@ -86,8 +86,7 @@ extern "C" usp_status usp_attn_fwd_varlen_noalloc(const void* q, const void* k, 
     void* scratch = nullptr;
     if (scratch_on_current_device(&scratch) != cudaSuccess) return USP_ERR_CUDA;
     uint8_t* ws = (uint8_t*)scratch;
-    WsHeader* hdr = (WsHeader*)ws;
-    if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return USP_ERR_CUDA;
+    WsHeader* hdr = (WsHeader*)ws;   // written by the scheduler: status, item count, item counter
 
     SchedArgs sa{};
     sa.cu = cu_seqlens;
@@ -105,7 +104,7 @@ extern "C" usp_status usp_attn_fwd_varlen_noalloc(const void* q, const void* k, 
     sa.sbase = (int*)(ws + w.sbase);
     sa.head_major_from = head_major_from_tokens(hkv, head_dim, sa.bwd);
     sa.items = (WorkItem*)(ws + w.items);
-    if (launch_schedule(sa, s) != cudaSuccess) return USP_ERR_CUDA;
+    if (launch_schedule(sa, s, false) != cudaSuccess) return USP_ERR_CUDA;
 
     CUtensorMap mq, mk, mv, mo;
     if (!make_activation_map(&mq, q, total_tokens, hq, head_dim, 0) ||

@@ -392,6 +392,14 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
 __device__ __forceinline__ void named_bar_arrive(int id, int nthreads) {
     asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
+// Programmatic dependent launch. A kernel launched with programmatic stream serialization
+// may start while the kernel before it in the stream is still running: pdl_wait() blocks
+// until that kernel has completed and its memory writes are visible (in a kernel launched
+// without the attribute it returns at once). pdl_trigger() lets such a dependent launch as
+// soon as every CTA of this kernel has triggered or exited, instead of at its completion.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Named barrier that also ORs `pred` over its `nthreads` threads: every participant returns
 // the same answer. Warps of a group that must leave a loop together (for example after one
 // of them gave up on a bounded wait) vote with it, so that none is left waiting at a later

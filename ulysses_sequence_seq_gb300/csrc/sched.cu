@@ -11,6 +11,7 @@
 #include <cuda_runtime.h>
 
 #include "common.cuh"
+#include "ptx.cuh"
 #include "sched.cuh"
 #include "tiles.cuh"
 
@@ -76,7 +77,9 @@ __device__ __forceinline__ void fail_schedule(const SchedArgs& a) {
     else a.hdr->fwd_count = 0;
 }
 
-__global__ void __launch_bounds__(1024) schedule_kernel(SchedArgs a) {
+// The whole work list and the call's header: its status, the item count and the counter
+// the persistent attention CTAs take their items from (zeroed here).
+__device__ void schedule_body(const SchedArgs& a) {
     extern __shared__ int hist_smem[];
     __shared__ int bad;
     __shared__ int warp_sums[32];
@@ -144,15 +147,30 @@ __global__ void __launch_bounds__(1024) schedule_kernel(SchedArgs a) {
     }
     if (tid == 0) {
         a.hdr->status = USP_OK;
-        if (a.bwd) a.hdr->bwd_count = ntiles * a.heads;
-        else a.hdr->fwd_count = ntiles * a.heads;
+        a.hdr->max_cost = 0;
+        if (a.bwd) {
+            a.hdr->bwd_count = ntiles * a.heads;
+            a.hdr->bwd_next = 0;
+        } else {
+            a.hdr->fwd_count = ntiles * a.heads;
+            a.hdr->fwd_next = 0;
+        }
     }
 }
 
-cudaError_t launch_schedule(const SchedArgs& a, cudaStream_t s) {
+__global__ void __launch_bounds__(1024) schedule_kernel(SchedArgs a) {
+    // the attention kernel after this one may be launched now; it waits for this kernel to
+    // complete before it reads the work list
+    ptx::pdl_trigger();
+    schedule_body(a);
+    // launched after bwd_prep, this kernel may have started before that one finished: it
+    // completes only once bwd_prep has, so the attention kernel's wait covers both
+    ptx::pdl_wait();
+}
+
+cudaError_t launch_schedule(const SchedArgs& a, cudaStream_t s, bool after_prep) {
     const size_t smem = a.hist_len <= kSchedSmemHist ? sizeof(int) * (size_t)a.hist_len : 0;
-    schedule_kernel<<<1, 1024, smem, s>>>(a);
-    return cudaGetLastError();
+    return launch_kernel(schedule_kernel, dim3(1), dim3(1024), smem, s, after_prep, a);
 }
 
 }  // namespace usp

@@ -25,7 +25,9 @@ struct SchedArgs {
     WorkItem* items;
 };
 
-cudaError_t launch_schedule(const SchedArgs& a, cudaStream_t s);
+// Writes the work list and the header (status, item count, a zeroed item counter). With
+// after_prep the launch may overlap the bwd_prep kernel launched just before it on s.
+cudaError_t launch_schedule(const SchedArgs& a, cudaStream_t s, bool after_prep);
 
 // Sample length from which work items are ordered head by head: the backward always (its
 // persistent CTAs follow the list order closely), the forward once a sample's keys and

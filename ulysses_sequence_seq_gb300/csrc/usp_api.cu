@@ -131,8 +131,7 @@ usp_status attn_fwd_impl(const void* q, const void* k, const void* v, void* o, f
     const WsLayout w = ws_layout(total_tokens, num_seqs, hq, hkv, head_dim, 0);
     if (ws_bytes < w.total) return USP_ERR_WORKSPACE;
     uint8_t* ws = (uint8_t*)workspace;
-    WsHeader* hdr = (WsHeader*)ws;
-    if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return USP_ERR_CUDA;
+    WsHeader* hdr = (WsHeader*)ws;   // written by the scheduler: status, item count, item counter
 
     SchedArgs sa{};
     sa.cu = cu_seqlens;
@@ -150,7 +149,7 @@ usp_status attn_fwd_impl(const void* q, const void* k, const void* v, void* o, f
     sa.sbase = (int*)(ws + w.sbase);
     sa.head_major_from = head_major_from_tokens(hkv, head_dim, sa.bwd);
     sa.items = (WorkItem*)(ws + w.items);
-    if (launch_schedule(sa, s) != cudaSuccess) return USP_ERR_CUDA;
+    if (launch_schedule(sa, s, false) != cudaSuccess) return USP_ERR_CUDA;
 
     CUtensorMap mq, mk, mv, mo;
     if (!make_activation_map(&mq, q, total_tokens, hq, head_dim, token_major) ||
@@ -194,8 +193,7 @@ usp_status attn_bwd_impl(const void* q, const void* k, const void* v, const void
     const WsLayout w = ws_layout(total_tokens, num_seqs, hq, hkv, head_dim, 1);
     if (ws_bytes < w.total) return USP_ERR_WORKSPACE;
     uint8_t* ws = (uint8_t*)workspace;
-    WsHeader* hdr = (WsHeader*)ws;
-    if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return USP_ERR_CUDA;
+    WsHeader* hdr = (WsHeader*)ws;   // written by the scheduler: status, item count, item counter
     const bool fp32_grads = grad_dt == USP_FP32;
     float* delta = (float*)(ws + w.delta);
     // fp32 gradients accumulate straight into the caller's dq (in its layout); bf16 ones go
@@ -224,7 +222,7 @@ usp_status attn_bwd_impl(const void* q, const void* k, const void* v, const void
     sa.sbase = (int*)(ws + w.sbase);
     sa.head_major_from = head_major_from_tokens(hkv, head_dim, sa.bwd);
     sa.items = (WorkItem*)(ws + w.items);
-    if (launch_schedule(sa, s) != cudaSuccess) return USP_ERR_CUDA;
+    if (launch_schedule(sa, s, true) != cudaSuccess) return USP_ERR_CUDA;
 
     CUtensorMap mq, mk, mv, mdo, mdq, mdk, mdv;
     if (!make_activation_map(&mq, q, total_tokens, hq, head_dim, token_major) ||
