@@ -61,8 +61,8 @@ struct BwdSmem {
     static constexpr int kQ = 2 * kTileBytes;        // + stage * kTileBytes
     static constexpr int kDO = 4 * kTileBytes;
     static constexpr int kDS = 5 * kTileBytes;       // [128 key rows][128 query cols] bf16, two 64-col panels
-    static constexpr int kStage = kDS + kTileM * kBlockN * 2;   // dQ staging: 4 warps x 2 chunks
-    static constexpr int kLse = kStage + 4 * 2 * kDqChunkBytes;  // fp32[2][64]: -lse (log2 units), one half each
+    static constexpr int kStage = kDS + kTileM * kBlockN * 2;   // dQ staging: one chunk per warp
+    static constexpr int kLse = kStage + 4 * kDqChunkBytes;     // fp32[2][64]: -lse (log2 units), one half each
     static constexpr int kDelta = kLse + 512;                   // fp32[2][64]: -Delta
     static constexpr int kBars = kDelta + 512;
     static constexpr int bKvFull = 0, bQFull = 1, bQEmpty = 3, bDoFull = 5, bDoEmpty = 6, bSFull = 7, bPFull = 9,
@@ -584,13 +584,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     } else if (warp < kDqWarp0 + 4) {
         // ------------------------------------------------------------------ dQ group (query rows)
         // Each warp owns 32 query rows of the tile: per 32-column chunk it loads 32 x 32 fp32
-        // from TMEM, writes them to one of its two staging buffers in the 128-byte swizzle the
-        // dQ tensor map expects, and one lane hands the box to the TMA unit, which adds it to
-        // the accumulator at L2. Query rows past the sample end carry exact zeros (their P is
+        // from TMEM, writes them to its staging buffer in the 128-byte swizzle the dQ tensor
+        // map expects, and one lane hands the box to the TMA unit, which adds it to the
+        // accumulator at L2. Query rows past the sample end carry exact zeros (their P is
         // zero), so whole boxes can be added; rows past the tensor end are skipped by the TMA.
+        // One buffer per warp, so at most one reduction per warp is in flight: measured
+        // faster than two (the TMA unit also serves the next blocks' Q and dO loads).
         const int w4 = warp - kDqWarp0;
         const uint32_t tDQ = tbase + ((uint32_t)(w4 * 32) << 16) + 128;
-        uint8_t* stage = sm + L::kStage + w4 * (2 * kDqChunkBytes);
+        uint8_t* stage = sm + L::kStage + w4 * kDqChunkBytes;
         if (lane == 0) prefetch_tmap(&tmDQ);
         bool ok = true;
         int gk = 0;
@@ -619,9 +621,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&bars[L::bDqEmpty]);
                     }
-                    uint8_t* buf = stage + (ci & 1) * kDqChunkBytes;
-                    // the reduction that last used this buffer (two chunks ago) must have read it
-                    if (lane == 0) bulk_wait_group_read<1>();
+                    uint8_t* buf = stage;
+                    // the previous chunk's reduction must have read the buffer
+                    if (lane == 0) bulk_wait_group_read<0>();
                     __syncwarp();
 #pragma unroll
                     for (int jj = 0; jj < 8; ++jj)   // row `lane`, 16-byte chunk jj, XOR-swizzled by row
