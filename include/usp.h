@@ -26,7 +26,10 @@
  *     usp_attn_workspace_size().
  *   - Pointers are device pointers, 16-byte aligned. `stream` is a cudaStream_t
  *     (NULL = legacy default stream). Calls are asynchronous on `stream`; the
- *     return value reports host-side validation and launch errors only.
+ *     return value reports host-side validation and launch errors only. The
+ *     first kernel of a call starts after all earlier work on `stream`; the
+ *     call's later kernels are launched as programmatic dependents of the one
+ *     before (they may start early and wait on the device for its results).
  *     Errors found on the device (malformed cu_seqlens, a wait that timed out)
  *     are written to the workspace status word; read it with
  *     usp_get_device_status().
@@ -117,7 +120,8 @@ usp_status usp_head_to_seq_kv_grad(const void* in, void* out, int sp, int64_t to
  * these sizes (bwd != 0: for usp_attn_bwd_varlen, which also needs per-row
  * Delta and, for bf16 gradients, an fp32 dQ accumulator). The workspace holds
  * a status word, the varlen work list and those buffers; it may be reused
- * across calls on the same stream.
+ * across calls on the same stream and needs no initialisation: every call
+ * writes each part of it before reading it.
  */
 size_t usp_attn_workspace_size(int64_t total_tokens, int num_seqs, int hq, int hkv, int head_dim, int bwd);
 
@@ -241,7 +245,7 @@ usp_status usp_get_device_status(const void* workspace, void* stream);
  *   (cudaGetSymbolAddress, with that device current), which may load the
  *   library's device code; make that first call before any stream capture.
  *   Sharing: every call uses the same array, which keeps the previous call's
- *   contents (each call clears the parts that must start at zero). Calls whose
+ *   contents (each call writes the parts it reads first). Calls whose
  *   kernels could overlap on the GPU (two streams, or two host threads without
  *   ordering) race on it; the caller must serialise them.
  * Errors: as usp_attn_fwd_varlen, and USP_ERR_WORKSPACE when the work list for
