@@ -24,7 +24,9 @@ struct FwdArgs {
     int f16;            // 16-bit inputs and outputs are fp16 (else bf16)
 };
 
-// o: the output map (make_activation_map over o) for whole-tile stores.
+// o: the output map (make_activation_map over o) for whole-tile stores. grid: the work-item
+// upper bound; min(grid, SM count) persistent CTAs are launched, as a programmatic
+// dependent of the scheduler launched just before on s.
 cudaError_t launch_attn_fwd(int head_dim, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                             const CUtensorMap& o, const FwdArgs& a, int grid, cudaStream_t s);
 
@@ -51,7 +53,7 @@ struct BwdArgs {
 };
 
 // dk, dv: 16-bit gradient maps (make_activation_map) for whole-tile stores; not read for
-// fp32 gradients.
+// fp32 gradients. grid: as for launch_attn_fwd.
 cudaError_t launch_attn_bwd(int head_dim, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                             const CUtensorMap& dout, const CUtensorMap& dq, const CUtensorMap& dk, const CUtensorMap& dv,
                             const BwdArgs& a, int grid, cudaStream_t s);
@@ -64,7 +66,7 @@ cudaError_t launch_bwd_prep(const void* o, const void* dout, float* delta, float
                             int head_dim, int token_major, int dq_token_major, int f16, cudaStream_t s);
 
 // dq (16-bit, head-major or token-major) = the head-major fp32 accumulator rounded to bf16,
-// or to fp16 when f16.
+// or to fp16 when f16. Launched as a programmatic dependent of the backward kernel.
 cudaError_t launch_dq_convert(const float* dq_acc, void* dq, int64_t T, int hq, int head_dim, int token_major,
                               int f16, cudaStream_t s);
 
