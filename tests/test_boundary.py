@@ -115,3 +115,13 @@ def test_kv_swap_validation():
     assert g(A, B, 4, 64, 3, 128, _lib.USP_FP32, None) == _lib.USP_ERR_INVALID_ARG
     assert g(A, B, 8, 64, 2, 128, _lib.USP_FP16, None) == _lib.USP_ERR_UNSUPPORTED   # fp16 sums
     assert g(0, B, 8, 64, 2, 128, _lib.USP_FP32, None) == _lib.USP_ERR_INVALID_ARG
+
+
+def test_binding_refuses_host_and_strided_tensors():
+    """The Python binding hands only dense device buffers to the C ABI."""
+    torch = pytest.importorskip("torch")
+    with pytest.raises(ValueError, match="contiguous"):
+        _lib._ptr(torch.zeros(8, 8).t())
+    with pytest.raises(ValueError, match="CUDA"):
+        _lib._ptr(torch.zeros(8))
+    assert _lib._ptr(A) == A and _lib._ptr(None) is None

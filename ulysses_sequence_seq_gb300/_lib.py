@@ -113,10 +113,17 @@ def _check(fn: str, code: int):
 
 
 def _ptr(x):
+    """Device address of a tensor (or an integer address as given). The kernels index
+    every buffer as the dense layout the call documents, so a strided view or a host
+    tensor is refused here rather than handed over."""
     if x is None:
         return None
     if isinstance(x, int):
         return x
+    if not x.is_contiguous():
+        raise ValueError("usp: expected a contiguous tensor (the kernels assume the dense layout)")
+    if not x.is_cuda:
+        raise ValueError("usp: expected a CUDA tensor")
     return x.data_ptr()
 
 
