@@ -124,6 +124,10 @@ def _ptr(x):
         raise ValueError("usp: expected a contiguous tensor (the kernels assume the dense layout)")
     if not x.is_cuda:
         raise ValueError("usp: expected a CUDA tensor")
+    import torch
+    cur = torch.cuda.current_device()
+    if x.device.index != cur:   # the call launches on the current device and its stream
+        raise ValueError(f"usp: tensor on cuda:{x.device.index}, but the current device is cuda:{cur}")
     return x.data_ptr()
 
 
