@@ -125,3 +125,23 @@ def test_binding_refuses_host_and_strided_tensors():
     with pytest.raises(ValueError, match="CUDA"):
         _lib._ptr(torch.zeros(8))
     assert _lib._ptr(A) == A and _lib._ptr(None) is None
+
+
+def _declared_params():
+    """Parameter count of every usp_* declaration in the public header."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    out = {}
+    for m in re.finditer(r"\b(usp_\w+)\s*\(([^)]*)\)\s*;", text):
+        args = m.group(2).strip()
+        out[m.group(1)] = 0 if args in ("", "void") else len(args.split(","))
+    return out
+
+
+def test_binding_argument_lists_match_the_header():
+    """Each ctypes argument list has as many entries as the C declaration has parameters."""
+    L = _lib.load()
+    decl = _declared_params()
+    assert set(decl) == set(_lib.EXPORTED)
+    for name, n in decl.items():
+        argtypes = getattr(L, name).argtypes
+        assert argtypes is not None and len(argtypes) == n, (name, n, argtypes and len(argtypes))
