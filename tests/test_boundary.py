@@ -127,21 +127,25 @@ def test_binding_refuses_host_and_strided_tensors():
     assert _lib._ptr(A) == A and _lib._ptr(None) is None
 
 
-def _declared_params():
-    """Parameter count of every usp_* declaration in the public header."""
+def _declarations():
+    """Return type and parameter count of every usp_* declaration in the public header."""
     text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
     out = {}
-    for m in re.finditer(r"\b(usp_\w+)\s*\(([^)]*)\)\s*;", text):
-        args = m.group(2).strip()
-        out[m.group(1)] = 0 if args in ("", "void") else len(args.split(","))
+    for m in re.finditer(r"(usp_status|size_t|const char\*)\s+(usp_\w+)\s*\(([^)]*)\)\s*;", text):
+        args = m.group(3).strip()
+        out[m.group(2)] = (m.group(1), 0 if args in ("", "void") else len(args.split(",")))
     return out
 
 
 def test_binding_argument_lists_match_the_header():
-    """Each ctypes argument list has as many entries as the C declaration has parameters."""
+    """Each ctypes argument list has as many entries as the C declaration has parameters,
+    and each return type is the declared one."""
+    import ctypes
     L = _lib.load()
-    decl = _declared_params()
+    decl = _declarations()
     assert set(decl) == set(_lib.EXPORTED)
-    for name, n in decl.items():
-        argtypes = getattr(L, name).argtypes
-        assert argtypes is not None and len(argtypes) == n, (name, n, argtypes and len(argtypes))
+    restypes = {"usp_status": ctypes.c_int, "size_t": ctypes.c_size_t, "const char*": ctypes.c_char_p}
+    for name, (ret, n) in decl.items():
+        fn = getattr(L, name)
+        assert fn.argtypes is not None and len(fn.argtypes) == n, (name, n, fn.argtypes and len(fn.argtypes))
+        assert fn.restype is restypes[ret], (name, ret, fn.restype)
