@@ -35,6 +35,9 @@
  *     usp_get_device_status().
  *   - No exception crosses the ABI. Calls are thread-safe as long as concurrent
  *     calls use distinct workspaces.
+ *   - One device per process: the first attention call sets the kernels' shared-
+ *     memory limit and reads the SM count on the then-current device; attention
+ *     calls on another device of the same process are not supported.
  */
 #ifndef USP_H_
 #define USP_H_
