@@ -1,15 +1,19 @@
 """Benchmark of the Ulysses sequence-parallel hot path on GB300.
 
-One step = the whole per-layer attention path for all sp simulated ranks of one
-GPU: seq->head swap of Q, K, V; causal packed attention forward; head->seq of O;
-seq->head of dO; attention backward; head->seq of dQ, dK, dV. By default the swaps
-are fused into the attention kernels (usp_ulysses_attn_fwd / _bwd read and write the
-seq-sharded layout); --unfused runs them as separate re-layout kernels. The metric
-is algorithmic attention TFLOP/s (4*D FLOPs per allowed (query, key) pair per query
-head forward, 10*D backward), plus the stand-alone re-layout kernels' GB/s against HBM.
+One step = one rank's share of a Ulysses layer's attention: causal, packed-sample
+attention forward and backward over all T tokens for the rank's hq/sp query heads,
+read from and written to the token-major [T][hq/sp][D] buffers that the
+sequence -> heads exchange delivers (usp_ulysses_attn_fwd / _bwd, layout swaps fused
+into the kernels). The headline workload is the 262,144-token single sequence (32
+heads, D = 128, sp = 8: 4 heads per rank). The metric is algorithmic attention
+TFLOP/s: 4*D FLOPs per allowed (query, key) pair per query head forward, 10*D
+backward. The same line also carries the all-ranks launch of the headline workload,
+one rank's slice of the other >= 32k-token workloads, the stand-alone re-layout
+kernels' GB/s against HBM, the end-to-end figure through the public API with host
+copies, and the float64 oracle timed on the host cores.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl usp|reference]
-       [--workload llama|tiny|packed|gqa|long]
+       [--workload long|packed|gqa|llama|tiny] [--extras packed,gqa]
 Under torchrun (N > 1) every rank runs the same per-GPU workload on its own GPU
 (weak scaling, no data-path collective); rank 0 prints one JSON line.
 """
@@ -61,15 +65,13 @@ def bwd_traffic(w, fused):
     return entry[1] if digest == entry[0] else None
 
 
-def workload_desc(w):
+def workload_desc(w, rank_slice=False):
     kind = "packed" if w.num_seqs > 1 else "single sequence"
+    if rank_slice:
+        return (f"{w.name}: one rank's slice, {w.hq} query / {w.hkv} key-value heads over all {w.total_tokens} "
+                f"tokens ({kind}, {w.num_seqs} samples), D={w.head_dim}, causal, N(0,1), fwd+bwd")
     return (f"{w.name}: {w.total_tokens} tokens ({kind}, {w.num_seqs} samples), sp={w.sp}, hq={w.hq}, "
             f"hkv={w.hkv}, D={w.head_dim}, causal, bf16 N(0,1), fwd+bwd, all sp ranks' heads in one launch")
-
-
-def attention_flops(w):
-    pairs = w.allowed_pairs()
-    return 4.0 * w.head_dim * pairs * w.hq, 10.0 * w.head_dim * pairs * w.hq
 
 
 class ClockSampler:
@@ -163,6 +165,7 @@ def run_reference(args, w):
     if rank != 0:
         return
     from oracle.build import build_oracle
+    from ulysses_sequence_seq_gb300.synth import rank_slice
     build_oracle()
     tokens = args.ref_tokens
     for _ in range(args.warmup):
@@ -179,19 +182,102 @@ def run_reference(args, w):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": workload_desc(w), "sample": sample},
+            "config": {"workload": workload_desc(rank_slice(w), True), "sample": sample},
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
+def attn_flops(w):
+    """(forward, backward) algorithmic FLOPs of one call over all of w's query heads."""
+    pairs = w.allowed_pairs()
+    return 4.0 * w.head_dim * pairs * w.hq, 10.0 * w.head_dim * pairs * w.hq
+
+
+class AttnCase:
+    """Device buffers of one fused attention step (token-major q, k, v, dO in; o, lse,
+    dq, dk, dv out) and its CUDA-event timing."""
+
+    def __init__(self, w, usp, torch, dev, act_dtype, grad_code, host_bits=True, seed=0):
+        self.w, self.usp, self.torch = w, usp, torch
+        T, H, HKV, D = w.total_tokens, w.hq, w.hkv, w.head_dim
+        self.grad_code = grad_code
+        if host_bits:
+            from ulysses_sequence_seq_gb300.synth import seq_sharded_bits
+            import numpy as np
+
+            def pinned(t):
+                bits = np.ascontiguousarray(seq_sharded_bits(w, t, dtype="f16" if act_dtype == torch.float16
+                                                             else "bf16"))
+                return torch.from_numpy(bits.view(np.int16)).view(act_dtype).reshape(T, -1, D).pin_memory()
+            self.host = {t: pinned(t) for t in ("q", "k", "v", "do")}
+            self.x = {t: h.to(dev) for t, h in self.host.items()}
+        else:   # timing-only inputs drawn on the device: N(0, 1) from a seeded generator
+            g = torch.Generator(device=dev)
+            g.manual_seed(seed)
+            self.host = None
+            self.x = {t: torch.randn(T, HKV if t in ("k", "v") else H, D, generator=g, device=dev,
+                                     dtype=torch.float32).to(act_dtype) for t in ("q", "k", "v", "do")}
+        self.cu = torch.from_numpy(w.cu_seqlens()).to(dev)
+        self.layer = usp.UlyssesAttention(T, w.num_seqs, H, HKV, D, w.sp, causal=w.causal, device=dev,
+                                          fused=True, dtype=act_dtype)
+
+    def fwd(self):
+        L, x = self.layer, self.x
+        self.usp.ulysses_attn_fwd(x["q"], x["k"], x["v"], L.o_seq, L.lse, self.cu, L.B, L.T, L.sp, L.hq, L.hkv, L.D,
+                                  L.scale, L.causal, L.ws, L.ws_bytes)
+
+    def bwd(self):
+        L, x = self.layer, self.x
+        self.usp.ulysses_attn_bwd(x["q"], x["k"], x["v"], L.o_seq, L.lse, x["do"], L.dq_seq, L.dk_seq, L.dv_seq,
+                                  self.grad_code, self.cu, L.B, L.T, L.sp, L.hq, L.hkv, L.D, L.scale, L.causal,
+                                  L.ws, L.ws_bytes)
+
+    def time(self, steps, warmup, flush, stream):
+        """Mean forward, backward and step milliseconds over `steps` timed steps (L2 flushed
+        before each, outside the events) after `warmup` untimed ones."""
+        torch = self.torch
+        for _ in range(warmup):
+            self.fwd()
+            self.bwd()
+        torch.cuda.synchronize()
+        st = self.layer.device_status()
+        if st != self.usp.USP_OK:
+            raise RuntimeError(f"device status {self.usp.status_string(st)} after warm-up")
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+        for e in evs:
+            flush.zero_()
+            e[0].record(stream)
+            self.fwd()
+            e[1].record(stream)
+            self.bwd()
+            e[2].record(stream)
+        torch.cuda.synchronize()
+        st = self.layer.device_status()
+        if st != self.usp.USP_OK:
+            raise RuntimeError(f"device status {self.usp.status_string(st)} after timing")
+        fwd = [e[0].elapsed_time(e[1]) for e in evs]
+        bwd = [e[1].elapsed_time(e[2]) for e in evs]
+        return {"fwd_ms": statistics.mean(fwd), "bwd_ms": statistics.mean(bwd),
+                "step_ms_total": sum(f + b for f, b in zip(fwd, bwd)), "steps": steps}
+
+
+def rates(w, t, peak_burst, peak_sust):
+    fl_f, fl_b = attn_flops(w)
+    f = fl_f / (t["fwd_ms"] * 1e-3) / 1e12
+    b = fl_b / (t["bwd_ms"] * 1e-3) / 1e12
+    fb = (fl_f + fl_b) / ((t["fwd_ms"] + t["bwd_ms"]) * 1e-3) / 1e12
+    return {"fwd_tflops": f, "bwd_tflops": b, "fwd_bwd_tflops": fb, "fwd_ms": t["fwd_ms"], "bwd_ms": t["bwd_ms"],
+            "frac_of_sustained": fb / peak_sust, "frac_of_burst": fb / peak_burst,
+            "bwd_frac_of_sustained": b / peak_sust}
+
+
 def run_usp(args, w):
-    import numpy as np
     import torch
 
     import ulysses_sequence_seq_gb300 as usp
-    from ulysses_sequence_seq_gb300.synth import packed_labels, seq_sharded_bits
+    from ulysses_sequence_seq_gb300.synth import WORKLOADS, packed_labels, rank_slice
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -204,124 +290,152 @@ def run_usp(args, w):
 
     usp.load()
     dev = torch.device("cuda", local_rank)
-    T, H, HKV, D, sp = w.total_tokens, w.hq, w.hkv, w.head_dim, w.sp
-
     f16 = args.dtype == "f16"
-    if f16 and args.unfused:
-        raise SystemExit("fp16 activations run on the fused path only")
     act_dtype = torch.float16 if f16 else torch.bfloat16
     grad_code = usp.USP_FP16 if f16 else usp.USP_BF16
-
-    def to_host_pinned(bits):
-        t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(act_dtype)
-        return t.pin_memory()
-
-    hq_, hk_, hv_, hdo_ = (to_host_pinned(seq_sharded_bits(w, t, dtype=args.dtype)) for t in ("q", "k", "v", "do"))
-    xq, xk, xv, xdo = (t.to(dev) for t in (hq_, hk_, hv_, hdo_))
-    cu = torch.from_numpy(w.cu_seqlens()).to(dev)
-    fused = not args.unfused
-    layer = usp.UlyssesAttention(T, w.num_seqs, H, HKV, D, sp, causal=True, device=dev, fused=fused, dtype=act_dtype)
+    peaks, peak_src = load_peaks()
+    peak_burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    peak_sust = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)   # > L2 (129 MB)
     stream = torch.cuda.current_stream(dev)
 
-    # events: 0 start | 1 after the seq->head swaps (unfused) | 2 after the forward |
-    #         3 after the O / dO swaps (unfused) | 4 after the backward | 5 end
-    def step(ev=None):
-        if ev is None:
-            layer.forward(xq, xk, xv, cu)
-            layer.backward(xdo, cu)
-            return
-        ev[0].record(stream)
-        if fused:
-            ev[1].record(stream)
-            usp.ulysses_attn_fwd(xq, xk, xv, layer.o_seq, layer.lse, cu, layer.B, T, sp, H, HKV, D, layer.scale,
-                                 True, layer.ws, layer.ws_bytes)
-            ev[2].record(stream)
-            ev[3].record(stream)
-            usp.ulysses_attn_bwd(xq, xk, xv, layer.o_seq, layer.lse, xdo, layer.dq_seq, layer.dk_seq, layer.dv_seq,
-                                 grad_code, cu, layer.B, T, sp, H, HKV, D, layer.scale, True, layer.ws,
-                                 layer.ws_bytes)
-            ev[4].record(stream)
-            ev[5].record(stream)
-            return
-        usp.seq_to_head(xq, layer.q_h, sp)
-        usp.seq_to_head(xk, layer.k_h, sp)
-        usp.seq_to_head(xv, layer.v_h, sp)
-        ev[1].record(stream)
-        usp.attn_fwd_varlen(layer.q_h, layer.k_h, layer.v_h, layer.o_h, layer.lse, cu, layer.B, T, H, HKV, D,
-                            layer.scale, True, layer.ws, layer.ws_bytes)
-        ev[2].record(stream)
-        usp.head_to_seq(layer.o_h, layer.o_seq, sp)
-        usp.seq_to_head(xdo, layer.do_h, sp)
-        ev[3].record(stream)
-        usp.attn_bwd_varlen(layer.q_h, layer.k_h, layer.v_h, layer.o_h, layer.lse, layer.do_h, layer.dq_h,
-                            layer.dk_h, layer.dv_h, usp.USP_BF16, cu, layer.B, T, H, HKV, D, layer.scale, True,
-                            layer.ws, layer.ws_bytes)
-        ev[4].record(stream)
-        usp.head_to_seq(layer.dq_h, layer.dq_seq, sp)
-        usp.head_to_seq(layer.dk_h, layer.dk_seq, sp)
-        usp.head_to_seq(layer.dv_h, layer.dv_seq, sp)
-        ev[5].record(stream)
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    if layer.device_status() != usp.USP_OK:
-        raise RuntimeError(f"device status {usp.status_string(layer.device_status())} after warm-up")
-
+    # ---- headline: one rank's slice (hq/sp heads over all T tokens, what one GPU computes
+    # under Ulysses once the exchange has delivered its heads), timed in the fused path
+    ws_ = rank_slice(w)
+    main = AttnCase(ws_, usp, torch, dev, act_dtype, grad_code)
     clocks = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
     if clocks:
         clocks.start()
         time.sleep(0.3)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    for i in range(args.steps):
-        flush.zero_()                          # evict L2 between timed steps (outside the events)
-        step(evs[i])
+    t_main = main.time(args.steps, args.warmup, flush, stream)
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
     ck = clocks.stop() if clocks else None
-    if layer.device_status() != usp.USP_OK:
-        raise RuntimeError(f"device status {usp.status_string(layer.device_status())} after timing")
-
-    step_ms = [e[0].elapsed_time(e[5]) for e in evs]
-    fwd_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    bwd_ms = [e[3].elapsed_time(e[4]) for e in evs]
-    total_ms = max_over_ranks(sum(step_ms), dist, dev)
+    total_ms = max_over_ranks(t_main["step_ms_total"], dist, dev)
     ms_per_step = total_ms / args.steps
-    fwd_fl, bwd_fl = attention_flops(w)
-    value = (fwd_fl + bwd_fl) * world / (ms_per_step * 1e-3) / 1e12
+    fl_f, fl_b = attn_flops(ws_)
+    value = (fl_f + fl_b) * world / (ms_per_step * 1e-3) / 1e12
+    main_rates = rates(ws_, t_main, peak_burst, peak_sust)
 
-    # ---- the stand-alone layout swaps (usp_seq_to_head / usp_head_to_seq) on this workload's
-    # eight tensors, L2 flushed before each: the metric's re-layout GB/s against HBM
-    rel_bufs = [(xq, H), (xk, HKV), (xv, HKV), (xdo, H)]
+    # ---- end to end through the public API on the same slice: pinned host inputs in,
+    # results back to host, every copy inside the timed region
+    layer = main.layer
+    out_host = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                for t in (layer.o_seq, layer.dq_seq, layer.dk_seq, layer.dv_seq)]
+    h2d = sum(t.numel() * t.element_size() for t in main.host.values())
+    d2h = sum(t.numel() * t.element_size() for t in out_host)
+    h2d_stream = torch.cuda.Stream(dev)
+    d2h_stream = torch.cuda.Stream(dev)
+    hq_, hk_, hv_, hdo_ = (main.host[t] for t in ("q", "k", "v", "do"))
+
+    def e2e_step():
+        # Q, K, V come in first on a copy stream, dO arrives while the forward runs, O goes
+        # out while the backward runs, the gradients after it
+        h2d_stream.wait_stream(stream)
+        with torch.cuda.stream(h2d_stream):
+            dq_, dk_, dv_ = (t.to(dev, non_blocking=True) for t in (hq_, hk_, hv_))
+            qkv_in = torch.cuda.Event()
+            qkv_in.record(h2d_stream)
+            ddo_ = hdo_.to(dev, non_blocking=True)
+            do_in = torch.cuda.Event()
+            do_in.record(h2d_stream)
+        for t in (dq_, dk_, dv_, ddo_):
+            t.record_stream(stream)
+        stream.wait_event(qkv_in)
+        o = layer.forward(dq_, dk_, dv_, main.cu)
+        d2h_stream.wait_stream(stream)
+        with torch.cuda.stream(d2h_stream):
+            out_host[0].copy_(o, non_blocking=True)
+        stream.wait_event(do_in)
+        g = layer.backward(ddo_, main.cu)
+        for dst, src in zip(out_host[1:], g):
+            dst.copy_(src, non_blocking=True)
+        stream.wait_stream(d2h_stream)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_ms = []
+    for _ in range(args.e2e_steps):
+        flush.zero_()
+        e0.record(stream)
+        e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms.append(e0.elapsed_time(e1))
+    e2e_value = (fl_f + fl_b) * world / (statistics.mean(e2e_ms) * 1e-3) / 1e12
+    main_host = main.host
+    del main, layer, out_host
+    torch.cuda.empty_cache()
+
+    # ---- secondary: all sp ranks' heads of the workload in one launch (timing-only inputs
+    # drawn on the device)
+    all_ranks = None
+    if args.all_ranks_steps > 0:
+        case = AttnCase(w, usp, torch, dev, act_dtype, grad_code, host_bits=False, seed=1000 * w.index)
+        t = case.time(args.all_ranks_steps, 2, flush, stream)
+        all_ranks = dict(rates(w, t, peak_burst, peak_sust), heads=w.hq, kv_heads=w.hkv,
+                         steps=args.all_ranks_steps)
+        del case
+        torch.cuda.empty_cache()
+
+    # ---- the other workloads of size >= 32k tokens, one rank's slice each
+    extras = {}
+    for name in args.extras.split(",") if args.extras else []:
+        if name == w.name or name not in WORKLOADS:
+            continue
+        xw = rank_slice(WORKLOADS[name])
+        case = AttnCase(xw, usp, torch, dev, act_dtype, grad_code)
+        t = case.time(args.steps, args.warmup, flush, stream)
+        extras[name] = dict(rates(xw, t, peak_burst, peak_sust), workload=workload_desc(xw, True),
+                            allowed_pairs_per_head=xw.allowed_pairs())
+        del case
+        torch.cuda.empty_cache()
+
+    # ---- the stand-alone layout swaps (usp_seq_to_head / usp_head_to_seq) on the full
+    # workload's Q, K, V, dO (all heads), L2 flushed before each batch
+    T, H, HKV, D, sp = w.total_tokens, w.hq, w.hkv, w.head_dim, w.sp
+    rel_in = {hh: torch.empty(T * hh * D, dtype=torch.bfloat16, device=dev) for hh in {H, HKV}}
     rel_tmp = {hh: torch.empty(T * hh * D, dtype=torch.bfloat16, device=dev) for hh in {H, HKV}}
     rel_back = {hh: torch.empty(T * hh * D, dtype=torch.bfloat16, device=dev) for hh in {H, HKV}}
+    for t_ in rel_in.values():
+        t_.view(torch.int16).random_(-32768, 32767)
+    heads4 = [H, HKV, HKV, H]
     rel_ms = []
     r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     for it in range(args.steps + 1):
         tot = 0.0
-        for to_head in (True, False):          # a layer swaps Q, K, V (and dO) together
+        for to_head in (True, False):
             flush.zero_()
             r0.record(stream)
-            for x, hh in rel_bufs:
+            for hh in heads4:
                 if to_head:
-                    usp.seq_to_head(x, rel_tmp[hh].view(sp, hh // sp, T, D), sp)
+                    usp.seq_to_head(rel_in[hh].view(sp, T // sp, hh, D), rel_tmp[hh].view(sp, hh // sp, T, D), sp)
                 else:
                     usp.head_to_seq(rel_tmp[hh].view(sp, hh // sp, T, D), rel_back[hh].view(sp, T // sp, hh, D), sp)
             r1.record(stream)
             r1.synchronize()
             tot += r0.elapsed_time(r1)
-        if it > 0:                             # the first pass is a warm-up
+        if it > 0:
             rel_ms.append(tot)
-    relayout_bytes = sum(2 * 2 * T * hh * D for _, hh in rel_bufs) * 2   # read + write, both directions
+    for hh in rel_in:
+        if not torch.equal(rel_back[hh], rel_in[hh]):
+            raise RuntimeError("re-layout round trip is not the identity")
+    relayout_bytes = sum(2 * 2 * T * hh * D for hh in heads4) * 2
+    rel_gbs = relayout_bytes / (statistics.mean(rel_ms) * 1e-3) / 1e9
+    del rel_in, rel_tmp, rel_back
+    torch.cuda.empty_cache()
 
-    # ---- sample and loss bookkeeping on the device: cu_seqlens -> position_ids ->
-    # cu_seqlens (padded to 2x the samples), label shift with per-rank good-token counts,
-    # weighted loss over the sp ranks; L2 flushed before each pass
+    # ---- sample and loss bookkeeping on the device (cu_seqlens -> position_ids ->
+    # cu_seqlens padded to 2x the samples, label shift with per-rank good tokens, weighted
+    # loss over the sp ranks), L2 flushed before each pass
+    cu = torch.from_numpy(w.cu_seqlens()).to(dev)
     max_seqs = 2 * w.num_seqs
     pos_d = torch.empty(T, dtype=torch.int64, device=dev)
     cu_pad = torch.empty(max_seqs + 1, dtype=torch.int32, device=dev)
@@ -349,66 +463,11 @@ def run_usp(args, w):
         raise RuntimeError("position_ids -> cu_seqlens failed on the bench workload")
     book_bytes = 8 * T + 8 * T + 16 * T     # write ids; read ids; read labels + write shifted
 
-    # ---- end to end through the public API: pinned host inputs in, results back to host
-    out_host = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-                for t in (layer.o_seq, layer.dq_seq, layer.dk_seq, layer.dv_seq)]
-    h2d = sum(t.numel() * t.element_size() for t in (hq_, hk_, hv_, hdo_))
-    d2h = sum(t.numel() * t.element_size() for t in out_host)
-
-    h2d_stream = torch.cuda.Stream(dev)
-    d2h_stream = torch.cuda.Stream(dev)
-
-    def e2e_step():
-        # Every copy of the step is inside the timed region; they overlap the compute they do
-        # not feed: Q, K, V come in first on a copy stream, dO arrives while the forward runs,
-        # and O goes out while the backward runs.
-        h2d_stream.wait_stream(stream)
-        with torch.cuda.stream(h2d_stream):
-            dq_, dk_, dv_ = (t.to(dev, non_blocking=True) for t in (hq_, hk_, hv_))
-            qkv_in = torch.cuda.Event()
-            qkv_in.record(h2d_stream)
-            ddo_ = hdo_.to(dev, non_blocking=True)
-            do_in = torch.cuda.Event()
-            do_in.record(h2d_stream)
-        for t in (dq_, dk_, dv_, ddo_):
-            t.record_stream(stream)
-        stream.wait_event(qkv_in)
-        o = layer.forward(dq_, dk_, dv_, cu)
-        d2h_stream.wait_stream(stream)
-        with torch.cuda.stream(d2h_stream):
-            out_host[0].copy_(o, non_blocking=True)
-        stream.wait_event(do_in)
-        g = layer.backward(ddo_, cu)
-        for dst, src in zip(out_host[1:], g):
-            dst.copy_(src, non_blocking=True)
-        stream.wait_stream(d2h_stream)
-
-    for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e2e_ms = []
-    for _ in range(args.steps):
-        flush.zero_()
-        e0.record(stream)
-        e2e_step()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        e2e_ms.append(e0.elapsed_time(e1))
-    e2e_value = (fwd_fl + bwd_fl) * world / (statistics.mean(e2e_ms) * 1e-3) / 1e12
-
     if rank != 0:
         if dist:
             dist.destroy_process_group()
         return
 
-    peaks, peak_src = load_peaks()
-    bwd_mean = statistics.mean(bwd_ms)
-    fwd_mean = statistics.mean(fwd_ms)
-    bwd_tflops = bwd_fl / (bwd_mean * 1e-3) / 1e12
-    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    rel_gbs = relayout_bytes / (statistics.mean(rel_ms) * 1e-3) / 1e9
-    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         from oracle.build import build_oracle
@@ -419,38 +478,46 @@ def run_usp(args, w):
         cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                "sample": f"{nh} query heads, causal fwd+bwd over the first {L} tokens of sample 0 "
                          f"({dt:.1f} s of float64 C oracle work)"}
-    # fused: schedule + attn_fwd | bwd_prep + schedule + attn_bwd + dq_convert;
-    # unfused adds the eight re-layout launches
-    launches_per_step = 6 if fused else 14
+    del main_host
+    # per fused step: schedule + attn_fwd | bwd_prep + schedule + attn_bwd + dq_convert
+    launches_per_step = 6
+    bwd_tflops = main_rates["bwd_tflops"]
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": args.dtype, "data": "synthetic",
-        "config": {"workload": workload_desc(w), "seq_len": T, "heads": H, "kv_heads": HKV, "head_dim": D,
-                   "sp": sp, "parallelism": f"replicas x{world} (sp={sp} simulated per GPU)",
-                   "path": "fused layout swaps (usp_ulysses_attn_fwd/bwd)" if fused else
-                           "separate re-layout kernels around usp_attn_fwd/bwd_varlen",
+        "config": {"workload": workload_desc(ws_, True), "seq_len": ws_.total_tokens, "heads": ws_.hq,
+                   "kv_heads": ws_.hkv, "head_dim": ws_.head_dim, "sp": w.sp,
+                   "allowed_pairs_per_head": ws_.allowed_pairs(),
+                   "parallelism": f"replicas x{world}: each GPU runs one rank's slice of sp={w.sp} Ulysses",
+                   "path": "fused layout swaps (usp_ulysses_attn_fwd/bwd) on the token-major [T][hq/sp][D] buffers",
                    "l2": "flushed between timed steps (512 MB write outside the events)",
-                   "fwd_ms": fwd_mean, "bwd_ms": bwd_mean,
-                   "fwd_tflops": fwd_fl / (fwd_mean * 1e-3) / 1e12, "bwd_tflops": bwd_tflops},
+                   **{k: main_rates[k] for k in ("fwd_ms", "bwd_ms", "fwd_tflops", "bwd_tflops")}},
+        "fwd_bwd_frac_of_sustained_bf16": main_rates["frac_of_sustained"],
+        "fwd_bwd_frac_of_burst_bf16": main_rates["frac_of_burst"],
         "roofline": {"bound": "tensor",
-                     "kernel": ("usp_ulysses_attn_bwd" if fused else "usp_attn_bwd_varlen") +
-                               " call: attn_bwd_kernel + bwd_prep + schedule + dq_convert",
-                     "achieved": bwd_tflops, "peak": peak, "unit": "TFLOP/s", "frac": bwd_tflops / peak,
-                     "peak_source": f"{peak_src} bf16 burst", "traffic": bwd_traffic(w, fused),
+                     "kernel": "usp_ulysses_attn_bwd call: attn_bwd_kernel + bwd_prep + schedule + dq_convert",
+                     "achieved": bwd_tflops, "peak": peak_sust, "unit": "TFLOP/s", "frac": bwd_tflops / peak_sust,
+                     "peak_source": f"{peak_src} bf16 sustained (the timed region runs for seconds)",
+                     "peak_burst": peak_burst, "frac_of_burst": bwd_tflops / peak_burst,
+                     "traffic": bwd_traffic(ws_, True),
                      "traffic_of": "attn_bwd_kernel, DRAM read+write bytes per launch (ncu)"},
+        "all_ranks_one_launch": all_ranks,
+        "extras": extras,
         "relayout": {"achieved_gbs": rel_gbs, "peak_gbs": hbm, "frac": rel_gbs / hbm,
                      "peak_source": f"{peak_src} hbm copy", "bytes": relayout_bytes,
-                     "what": "usp_seq_to_head on Q, K, V, dO back to back, then usp_head_to_seq on the four; "
-                             "L2 flushed before each batch",
+                     "tensor_bytes": 2 * T * H * D,
+                     "what": f"usp_seq_to_head on Q, K, V, dO of all {H} heads back to back, then usp_head_to_seq "
+                             "on the four; L2 flushed before each batch; round trip checked",
                      "ms": statistics.mean(rel_ms)},
         "sp_bookkeeping": {"ms": statistics.mean(book_ms), "bytes": book_bytes,
                            "achieved_gbs": book_bytes / (statistics.mean(book_ms) * 1e-3) / 1e9,
                            "what": "usp_cu_seqlens_to_position_ids, usp_position_ids_to_cu_seqlens (padded), "
                                    "usp_shift_labels (+ good tokens per rank), usp_sp_weighted_loss; "
-                                   "7 launches, L2 flushed before each pass; latency-bound at this T"},
+                                   "7 launches, L2 flushed before each pass"},
         "cpu_baseline": cpu,
-        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": args.e2e_steps},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": ck,
     }
@@ -465,11 +532,16 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="usp", choices=["usp", "reference"])
-    ap.add_argument("--workload", default="llama", choices=["tiny", "llama", "packed", "gqa", "long"])
+    ap.add_argument("--workload", default="long", choices=["tiny", "llama", "packed", "gqa", "long"],
+                    help="the headline workload (timed on one rank's slice)")
+    ap.add_argument("--extras", default="packed,gqa",
+                    help="comma-separated workloads also timed (one rank's slice each); '' for none")
+    ap.add_argument("--all-ranks-steps", type=int, default=3,
+                    help="timed steps of the all-ranks launch of the headline workload (0 skips it)")
+    ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--ref-tokens", type=int, default=2048)
     ap.add_argument("--cpu-tokens", type=int, default=4096)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--unfused", action="store_true", help="time separate re-layout kernels around the attention")
     ap.add_argument("--dtype", default="bf16", choices=["bf16", "f16"],
                     help="activation type (fp32 accumulation and softmax either way)")
     args = ap.parse_args()

@@ -35,9 +35,9 @@
  *     usp_get_device_status().
  *   - No exception crosses the ABI. Calls are thread-safe as long as concurrent
  *     calls use distinct workspaces.
- *   - One device per process: the first attention call sets the kernels' shared-
- *     memory limit and reads the SM count on the then-current device; attention
- *     calls on another device of the same process are not supported.
+ *   - Every call launches on the device current on the calling thread. The
+ *     kernels' shared-memory limits and the SM count are set up once per device
+ *     (under a lock), so one process may drive several devices.
  */
 #ifndef USP_H_
 #define USP_H_
@@ -245,15 +245,18 @@ usp_status usp_get_device_status(const void* workspace, void* stream);
  *   USP_ERR_DEVICE_CHECK (malformed cu_seqlens; no output written) or
  *   USP_ERR_TIMEOUT.
  *   Set-up: the first call on each device looks up the array's device address
- *   (cudaGetSymbolAddress, with that device current), which may load the
- *   library's device code; make that first call before any stream capture.
+ *   (cudaGetSymbolAddress, with that device current) and sets the forward
+ *   kernel's shared-memory limit there, which may load the library's device
+ *   code; make that first call before any stream capture. Each device has its
+ *   own array.
  *   Sharing: every call uses the same array, which keeps the previous call's
  *   contents (each call writes the parts it reads first). Calls whose
  *   kernels could overlap on the GPU (two streams, or two host threads without
  *   ordering) race on it; the caller must serialise them.
- * Errors: as usp_attn_fwd_varlen, and USP_ERR_WORKSPACE when the work list for
- *   these sizes does not fit the 1 MiB array (roughly hq * (T/256 + num_seqs)
- *   above 60000 items), or total_tokens > 2^30; no kernel is launched then.
+ * Errors: as usp_attn_fwd_varlen (the same host-side size checks), and
+ *   USP_ERR_WORKSPACE when total_tokens > 2^30 or the work list for these sizes
+ *   does not fit the 1 MiB array (roughly hq * (T/256 + num_seqs) above 60000
+ *   items); no kernel is launched then.
  */
 usp_status usp_attn_fwd_varlen_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
                                        const int32_t* cu_seqlens, int num_seqs, int64_t total_tokens, int hq,

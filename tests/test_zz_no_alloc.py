@@ -65,3 +65,24 @@ def test_noalloc_reports_bad_cu_seqlens_and_rejects_oversize():
     with pytest.raises(usp.UspError) as e:
         _lib.attn_fwd_varlen_noalloc(p.q, p.k, p.v, o, lse, p.cu, 1, 1 << 22, 512, 512, 128, 0.0, True)
     assert e.value.code == _lib.USP_ERR_WORKSPACE
+
+
+def test_noalloc_host_checks_match_the_workspace_entry_point():
+    """Sizes the workspace entry point refuses on the host are refused here too, before any
+    launch (no scheduler run with a truncated work-list size), and more than 2^30 tokens is
+    a scratch-size refusal. Only host checks run: every pointer is a dummy aligned address."""
+    needs_gpu()
+    fake = 1 << 20
+    lib = _lib.load()
+    stream = torch.cuda.current_stream().cuda_stream
+    # hq * (T / 128 + num_seqs + 1) beyond what the work list can index
+    rc = lib.usp_attn_fwd_varlen_noalloc(fake, fake, fake, fake, fake, fake, 1, 1 << 28, 1 << 14, 1, 128, 0.0, 1,
+                                         None, stream)
+    assert rc == _lib.USP_ERR_UNSUPPORTED
+    rc_ws = lib.usp_attn_fwd_varlen(fake, fake, fake, fake, fake, fake, 1, 1 << 28, 1 << 14, 1, 128, 0.0, 1,
+                                    fake, 1 << 40, stream)
+    assert rc_ws == rc
+    # more than 2^30 tokens: beyond the static array whatever the heads
+    rc = lib.usp_attn_fwd_varlen_noalloc(fake, fake, fake, fake, fake, fake, 1, (1 << 30) + 8, 1, 1, 128, 0.0, 1,
+                                         None, stream)
+    assert rc == _lib.USP_ERR_WORKSPACE

@@ -728,21 +728,10 @@ cudaError_t launch_bwd_impl(const CUtensorMap& q, const CUtensorMap& k, const CU
                             const CUtensorMap& dq, const CUtensorMap& dk, const CUtensorMap& dv, const BwdArgs& a,
                             int grid, cudaStream_t s) {
     using L = BwdSmem<D>;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e =
-            cudaFuncSetAttribute(attn_bwd_kernel<D, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
     // persistent CTAs, one per SM (the shared-memory footprint allows no more)
-    static int sms = 0;
-    if (sms == 0) {
-        int dev = 0;
-        cudaError_t e = cudaGetDevice(&dev);
-        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return e;
-    }
+    int sms = 0;
+    const cudaError_t e = persistent_setup(attn_bwd_kernel<D, F16>, (size_t)L::kAlloc, &sms);
+    if (e != cudaSuccess) return e;
     if (grid > sms) grid = sms;
     return launch_kernel(attn_bwd_kernel<D, F16>, dim3(grid), dim3(kBwdThreads), (size_t)L::kAlloc, s, true, q, k, v,
                          dout, dq, dk, dv, a);
@@ -752,7 +741,8 @@ cudaError_t launch_bwd_impl(const CUtensorMap& q, const CUtensorMap& k, const CU
 // grid together keep about 16 CTAs per SM.
 int grid_for(int64_t work_items, int per_cta, int ys = 1) {
     int64_t g = (work_items + per_cta - 1) / per_cta;
-    const int64_t cap = (152 * 16 + ys - 1) / ys;
+    const int sms = device_sm_count();
+    const int64_t cap = ((sms > 0 ? sms : 148) * 16 + ys - 1) / ys;
     if (g > cap) g = cap;
     if (g < 1) g = 1;
     return (int)g;

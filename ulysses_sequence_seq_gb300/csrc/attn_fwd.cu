@@ -515,21 +515,10 @@ template <int D, bool F16>
 cudaError_t launch_fwd_impl(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& o,
                             const FwdArgs& a, int grid, cudaStream_t s) {
     using L = FwdSmem<D>;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e =
-            cudaFuncSetAttribute(attn_fwd_kernel<D, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
     // persistent CTAs, one per SM (the shared-memory footprint allows no more)
-    static int sms = 0;
-    if (sms == 0) {
-        int dev = 0;
-        cudaError_t e = cudaGetDevice(&dev);
-        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return e;
-    }
+    int sms = 0;
+    const cudaError_t e = persistent_setup(attn_fwd_kernel<D, F16>, (size_t)L::kAlloc, &sms);
+    if (e != cudaSuccess) return e;
     if (grid > sms) grid = sms;
     return launch_kernel(attn_fwd_kernel<D, F16>, dim3(grid), dim3(kFwdThreads), (size_t)L::kAlloc, s, true, q, k, v,
                          o, a);

@@ -3,6 +3,8 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cmath>
+#include <mutex>
 
 #include <cuda_runtime.h>
 
@@ -60,6 +62,22 @@ __host__ __device__ __forceinline__ int64_t act_row(int h, int64_t t, int64_t T,
     return token_major ? t * H + h : (int64_t)h * T + t;
 }
 
+// Host-side checks shared by every attention entry point: sizes, head counts and the
+// limits of the work-list indexing (item counts and offsets stay within int).
+inline usp_status check_attn_sizes(int64_t T, int num_seqs, int hq, int hkv, int D, const int32_t* cu) {
+    if (T < 0 || hq < 1 || hkv < 1 || hq % hkv != 0) return USP_ERR_INVALID_ARG;
+    if (T > 0 && (num_seqs < 1 || !cu)) return USP_ERR_INVALID_ARG;
+    if (T > (int64_t)2147483647 - 2 * kFwdRowsPerItem || num_seqs > (1 << 24)) return USP_ERR_UNSUPPORTED;
+    if (D != 64 && D != 128) return USP_ERR_UNSUPPORTED;
+    if ((int64_t)hq * (T / kTileM + num_seqs + 1) > (int64_t)2147483647 / 2) return USP_ERR_UNSUPPORTED;
+    return USP_OK;
+}
+
+// softmax_scale <= 0 selects 1/sqrt(D).
+inline float resolve_softmax_scale(float softmax_scale, int D) {
+    return softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)D);
+}
+
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 inline int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -88,6 +106,47 @@ inline WsLayout ws_layout(int64_t T, int num_seqs, int hq, int hkv, int D, int b
     if (bwd) off = align256(off + sizeof(float) * (size_t)hq * (size_t)T * (size_t)D);
     w.total = off;
     return w;
+}
+
+constexpr int kMaxDevices = 64;
+
+// SM count of the current device, read once per device (thread-safe); 0 if it cannot be read.
+inline int device_sm_count() {
+    static std::mutex mu;
+    static int sms[kMaxDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    if (sms[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        sms[dev] = n;
+    }
+    return sms[dev];
+}
+
+// One-time set-up of a persistent kernel on the current device: raises its dynamic shared-
+// memory limit to `smem` (once per device and kernel, under a lock, so concurrent first calls
+// from several host threads and calls on several devices of one process are safe) and
+// returns the device's SM count in *sms.
+template <typename... KArgs>
+cudaError_t persistent_setup(void (*kernel)(KArgs...), size_t smem, int* sms) {
+    static std::mutex mu;
+    static bool done[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!done[dev]) {
+            e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return e;
+            done[dev] = true;
+        }
+    }
+    *sms = device_sm_count();
+    return *sms > 0 ? cudaSuccess : cudaErrorInvalidDevice;
 }
 
 // Launches `kernel` on stream s; with `programmatic` the launch may overlap the end of the

@@ -30,7 +30,6 @@ namespace usp {
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = size_t(1) << 20;
-constexpr int kMaxDevices = 64;
 
 // In host code this name is only a host-side stand-in for the device object; its
 // device address must be obtained with cudaGetSymbolAddress on each device.
@@ -66,10 +65,8 @@ extern "C" usp_status usp_attn_fwd_varlen_noalloc(const void* q, const void* k, 
                                                   const int32_t* cu_seqlens, int num_seqs, int64_t total_tokens,
                                                   int hq, int hkv, int head_dim, float softmax_scale, int causal,
                                                   int32_t* status, void* stream) {
-    if (total_tokens < 0 || hq < 1 || hkv < 1 || hq % hkv != 0) return USP_ERR_INVALID_ARG;
-    if (total_tokens > 0 && (num_seqs < 1 || !cu_seqlens)) return USP_ERR_INVALID_ARG;
-    if (head_dim != 64 && head_dim != 128) return USP_ERR_UNSUPPORTED;
-    if (num_seqs > (1 << 24) || total_tokens > (int64_t)(1 << 30)) return USP_ERR_UNSUPPORTED;
+    const usp_status st = check_attn_sizes(total_tokens, num_seqs, hq, hkv, head_dim, cu_seqlens);
+    if (st != USP_OK) return st;
     if (status && ((uintptr_t)status & 3)) return USP_ERR_INVALID_ARG;
     cudaStream_t s = (cudaStream_t)stream;
     if (total_tokens == 0) {
@@ -80,6 +77,7 @@ extern "C" usp_status usp_attn_fwd_varlen_noalloc(const void* q, const void* k, 
     const uintptr_t mis = (uintptr_t)q | (uintptr_t)k | (uintptr_t)v | (uintptr_t)o | (uintptr_t)lse;
     if (mis & 15) return USP_ERR_INVALID_ARG;
     // the scratch holds the forward's work list: it bounds tokens, samples and heads together
+    if (total_tokens > ((int64_t)1 << 30)) return USP_ERR_WORKSPACE;
     const WsLayout w = ws_layout(total_tokens, num_seqs, hq, hkv, head_dim, 0);
     if (w.total > kNoAllocScratchBytes) return USP_ERR_WORKSPACE;
 
@@ -122,7 +120,7 @@ extern "C" usp_status usp_attn_fwd_varlen_noalloc(const void* q, const void* k, 
     fa.hq = hq;
     fa.group = hq / hkv;
     fa.causal = sa.causal;
-    fa.scale_log2 = (softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)head_dim)) * 1.4426950408889634f;
+    fa.scale_log2 = resolve_softmax_scale(softmax_scale, head_dim) * 1.4426950408889634f;
     if (launch_attn_fwd(head_dim, mq, mk, mv, mo, fa, w.max_items, s) != cudaSuccess) return USP_ERR_CUDA;
     // device-side outcome (USP_OK, USP_ERR_DEVICE_CHECK or USP_ERR_TIMEOUT) for the caller
     if (status && cudaMemcpyAsync(status, &hdr->status, sizeof(int32_t), cudaMemcpyDeviceToDevice, s) != cudaSuccess)

@@ -129,16 +129,8 @@ __global__ void __launch_bounds__(256) sum_replicas_kernel(const uint4* __restri
 }
 
 int num_sms_cached() {
-    static int sms = 0;
-    if (sms == 0) {
-        int dev = 0, n = 0;
-        if (cudaGetDevice(&dev) == cudaSuccess &&
-            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
-            sms = n;
-        else
-            return 148;
-    }
-    return sms;
+    const int sms = device_sm_count();
+    return sms > 0 ? sms : 148;
 }
 
 // rep > 1: seq -> head with every seq-sharded head copied to rep consecutive

@@ -17,6 +17,7 @@
 
 #include <cstdint>
 
+#include "common.cuh"
 #include "usp.h"
 
 namespace usp {
@@ -216,7 +217,8 @@ bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0;
 
 int grid_1d(int64_t n) {
     const int64_t want = (n + kThreads - 1) / kThreads;
-    const int64_t cap = 152 * 8;  // 8 CTAs of 256 threads per SM; grid-stride beyond
+    const int sms = device_sm_count();
+    const int64_t cap = (int64_t)(sms > 0 ? sms : 148) * 8;  // 8 CTAs of 256 threads per SM; grid-stride beyond
     return (int)(want < 1 ? 1 : (want < cap ? want : cap));
 }
 

@@ -36,25 +36,12 @@ EncodeTiledFn encode_fn() {
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }
 
-usp_status check_common(int64_t T, int num_seqs, int hq, int hkv, int D, const int32_t* cu) {
-    if (T < 0 || hq < 1 || hkv < 1 || hq % hkv != 0) return USP_ERR_INVALID_ARG;
-    if (T > 0 && (num_seqs < 1 || !cu)) return USP_ERR_INVALID_ARG;
-    if (T > (int64_t)INT_MAX - 2 * kFwdRowsPerItem || num_seqs > (1 << 24)) return USP_ERR_UNSUPPORTED;
-    if (D != 64 && D != 128) return USP_ERR_UNSUPPORTED;
-    if ((int64_t)hq * (T / kTileM + num_seqs + 1) > (int64_t)INT_MAX / 2) return USP_ERR_UNSUPPORTED;
-    return USP_OK;
-}
-
 // T == 0: nothing to compute and the data pointers may be NULL (empty tensors); the
 // status word of a workspace, if one is given, is reset to USP_OK.
 usp_status reset_status_if_any(void* workspace, size_t ws_bytes, cudaStream_t s) {
     if (!workspace || ws_bytes < sizeof(WsHeader)) return USP_OK;
     if (!aligned16(workspace)) return USP_ERR_INVALID_ARG;
     return cudaMemsetAsync(workspace, 0, sizeof(WsHeader), s) == cudaSuccess ? USP_OK : USP_ERR_CUDA;
-}
-
-float resolve_scale(float softmax_scale, int D) {
-    return softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt((float)D);
 }
 
 }  // namespace
@@ -121,7 +108,7 @@ usp_status attn_fwd_impl(const void* q, const void* k, const void* v, void* o, f
                          int num_seqs, int64_t total_tokens, int hq, int hkv, int head_dim, float softmax_scale,
                          int causal, void* workspace, size_t ws_bytes, cudaStream_t s, int token_major,
                          usp_dtype dt = USP_BF16) {
-    usp_status st = check_common(total_tokens, num_seqs, hq, hkv, head_dim, cu_seqlens);
+    usp_status st = check_attn_sizes(total_tokens, num_seqs, hq, hkv, head_dim, cu_seqlens);
     if (st != USP_OK) return st;
     if (dt != USP_BF16 && dt != USP_FP16) return dt == USP_FP32 ? USP_ERR_UNSUPPORTED : USP_ERR_INVALID_ARG;
     if (total_tokens == 0) return reset_status_if_any(workspace, ws_bytes, s);
@@ -169,7 +156,7 @@ usp_status attn_fwd_impl(const void* q, const void* k, const void* v, void* o, f
     fa.group = hq / hkv;
     fa.causal = sa.causal;
     fa.token_major = token_major;
-    fa.scale_log2 = resolve_scale(softmax_scale, head_dim) * 1.4426950408889634f;
+    fa.scale_log2 = resolve_softmax_scale(softmax_scale, head_dim) * 1.4426950408889634f;
     if (launch_attn_fwd(head_dim, mq, mk, mv, mo, fa, w.max_items, s) != cudaSuccess) return USP_ERR_CUDA;
     return USP_OK;
 }
@@ -179,7 +166,7 @@ usp_status attn_bwd_impl(const void* q, const void* k, const void* v, const void
                          int num_seqs, int64_t total_tokens, int hq, int hkv, int head_dim, float softmax_scale,
                          int causal, void* workspace, size_t ws_bytes, cudaStream_t s, int token_major,
                          usp_dtype dt = USP_BF16) {
-    usp_status st = check_common(total_tokens, num_seqs, hq, hkv, head_dim, cu_seqlens);
+    usp_status st = check_attn_sizes(total_tokens, num_seqs, hq, hkv, head_dim, cu_seqlens);
     if (st != USP_OK) return st;
     if (dt != USP_BF16 && dt != USP_FP16) return dt == USP_FP32 ? USP_ERR_UNSUPPORTED : USP_ERR_INVALID_ARG;
     // gradients in the inputs' 16-bit type or in fp32
@@ -257,7 +244,7 @@ usp_status attn_bwd_impl(const void* q, const void* k, const void* v, const void
     ba.dq_token_major = dq_token_major;
     ba.group = hq / hkv;
     ba.causal = sa.causal;
-    ba.scale = resolve_scale(softmax_scale, head_dim);
+    ba.scale = resolve_softmax_scale(softmax_scale, head_dim);
     ba.scale_log2 = ba.scale * 1.4426950408889634f;
     if (launch_attn_bwd(head_dim, mq, mk, mv, mdo, mdq, mdk, mdv, ba, w.max_items, s) != cudaSuccess)
         return USP_ERR_CUDA;

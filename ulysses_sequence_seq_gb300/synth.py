@@ -196,3 +196,13 @@ def index_pattern_bits(T: int, H: int, D: int) -> np.ndarray:
     """A seq-sharded [T][H][D] uint16 array whose values encode their own position
     (used to check permutations exhaustively). Values are ((t*H + h)*D + d) mod 2^16."""
     return (np.arange(T * H * D, dtype=np.int64) % 65536).astype(np.uint16).reshape(T, H, D)
+
+
+# ----------------------------------------------------------------------------- one rank's slice
+def rank_slice(w: Workload) -> Workload:
+    """Rank 0's share of ``w`` after the sequence -> heads exchange: all T tokens of its
+    hq/sp query heads and max(1, hkv/sp) key/value heads (heads 0.. of ``w``, so the same
+    draws), as a one-rank workload. Stacking what every peer sends it, in rank order, gives
+    the token-major [T][hq/sp][D] buffer the fused attention reads."""
+    from dataclasses import replace
+    return replace(w, hq=w.hq // w.sp, hkv=max(1, w.hkv // w.sp), sp=1)
