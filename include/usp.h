@@ -121,7 +121,7 @@ usp_status usp_head_to_seq_kv_grad(const void* in, void* out, int sp, int64_t to
 /*
  * usp_attn_workspace_size -- bytes of workspace the attention calls need for
  * these sizes (bwd != 0: for usp_attn_bwd_varlen, which also needs per-row
- * Delta and, for bf16 gradients, an fp32 dQ accumulator). The workspace holds
+ * Delta, an fp32 dQ accumulator and the fp16 copies of q, k, v and d_o). The workspace holds
  * a status word, the varlen work list and those buffers; it may be reused
  * across calls on the same stream and needs no initialisation: every call
  * writes each part of it before reading it.
@@ -141,6 +141,11 @@ size_t usp_attn_workspace_size(int64_t total_tokens, int num_seqs, int hq, int h
  *   lse_i = log sum_{allowed j} exp(s_ij);  o_i = sum_j exp(s_ij - lse_i) v_j.
  *   q   : bf16 [hq][T][head_dim]        k, v : bf16 [hkv][T][head_dim]
  *   o   : bf16 [hq][T][head_dim]        lse  : fp32 [hq][T] (natural log, includes scale)
+ *   o_res : NULL, or bf16 [hq][T][head_dim]: the rounding residual of o, o_res =
+ *         round(O - o) for the fp32 result O, so that o + o_res carries O to about 16
+ *         significant bits. Passed on to the backward it makes Delta = dO . O exact to
+ *         that precision instead of to bf16's 8 bits (a bf16 O alone puts an error of
+ *         the order of the 2e-2 gradient tolerance into dS on short samples).
  *   cu_seqlens : device int32 [num_seqs + 1], cu[0] = 0, non-decreasing, cu[num_seqs] = T.
  *   Query head h reads key/value head h / (hq / hkv).
  *   softmax_scale <= 0 selects 1/sqrt(head_dim).
@@ -151,7 +156,7 @@ size_t usp_attn_workspace_size(int64_t total_tokens, int num_seqs, int hq, int h
  *   detected on the device: the status word becomes USP_ERR_DEVICE_CHECK and
  *   no output is written. T == 0 is a no-op (the buffers may then be NULL).
  */
-usp_status usp_attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+usp_status usp_attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, void* o_res, float* lse,
                                const int32_t* cu_seqlens, int num_seqs, int64_t total_tokens, int hq,
                                int hkv, int head_dim, float softmax_scale, int causal, void* workspace,
                                size_t ws_bytes, void* stream);
@@ -164,12 +169,17 @@ usp_status usp_attn_fwd_varlen(const void* q, const void* k, const void* v, void
  *   dS_ij = P_ij (dP_ij - Delta_i); dq_i = scale sum_j dS_ij k_j;
  *   dk_j = scale sum_i dS_ij q_i; dv_j = sum_i P_ij dO_i, where dk and dv of a
  *   key/value head sum over the hq/hkv query heads that read it.
- *   q, k, v, o, d_o : bf16 as in the forward; lse : fp32 [hq][T] from the forward.
+ *   q, k, v, o, d_o : bf16 as in the forward; lse : fp32 [hq][T] from the forward;
+ *   o_res : NULL or the forward's o_res (Delta is then taken from o + o_res).
  *   dq : [hq][T][head_dim], dk, dv : [hkv][T][head_dim] of grad_dt (USP_BF16 or USP_FP32).
+ *   Precision: the call first copies q, k, v and d_o into the workspace as fp16, each
+ *   scaled by a power of two per key/value group so that its largest magnitude lies in
+ *   [8, 16); the products then round P and dS to fp16 (11 significant bits) and the
+ *   results are scaled back exactly. Values must stay below 2^40 in magnitude.
  * Errors: as usp_attn_fwd_varlen; USP_ERR_UNSUPPORTED for grad_dt = USP_FP16.
  */
 usp_status usp_attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
-                               const float* lse, const void* d_o, void* dq, void* dk, void* dv,
+                               const void* o_res, const float* lse, const void* d_o, void* dq, void* dk, void* dv,
                                usp_dtype grad_dt, const int32_t* cu_seqlens, int num_seqs,
                                int64_t total_tokens, int hq, int hkv, int head_dim, float softmax_scale,
                                int causal, void* workspace, size_t ws_bytes, void* stream);
@@ -186,6 +196,7 @@ usp_status usp_attn_bwd_varlen(const void* q, const void* k, const void* v, cons
  *   one, whatever sp is.
  *   q   : dt [sp][T/sp][hq][D]        k, v : dt [sp][T/sp][hkv][D]
  *   o   : dt [sp][T/sp][hq][D]        lse  : fp32 [hq][T] (as usp_attn_fwd_varlen)
+ *   o_res : NULL or dt [sp][T/sp][hq][D], the rounding residual of o (as usp_attn_fwd_varlen)
  *   dt  : USP_BF16 or USP_FP16, the type of q, k, v and o. Scores, softmax and the
  *         accumulators are fp32 either way; P is rounded to dt before the P.V MMA,
  *         whose operands must share a type. USP_FP32 returns USP_ERR_UNSUPPORTED.
@@ -195,7 +206,7 @@ usp_status usp_attn_bwd_varlen(const void* q, const void* k, const void* v, cons
  *   sp % hkv is zero. hkv < sp with sp % hkv == 0 is the replicated key/value case of
  *   usp_seq_to_head_kv: the kernels read each shared head in place.
  */
-usp_status usp_ulysses_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+usp_status usp_ulysses_attn_fwd(const void* q, const void* k, const void* v, void* o, void* o_res, float* lse,
                                 const int32_t* cu_seqlens, int num_seqs, int64_t total_tokens, int sp, int hq,
                                 int hkv, int head_dim, float softmax_scale, int causal, usp_dtype dt,
                                 void* workspace, size_t ws_bytes, void* stream);
@@ -206,13 +217,14 @@ usp_status usp_ulysses_attn_fwd(const void* q, const void* k, const void* v, voi
  * usp_attn_bwd_varlen (on the head-sharded q, k, v, o), then usp_head_to_seq on the
  * three gradients.
  *   q, o, d_o : dt [sp][T/sp][hq][D]; k, v : dt [sp][T/sp][hkv][D]; lse : fp32 [hq][T];
- *   dt USP_BF16 or USP_FP16 (P and dS are rounded to dt before their MMAs).
+ *   o_res : NULL or the forward's o_res; dt USP_BF16 or USP_FP16 (the products run on the
+ *   scaled fp16 copies of usp_attn_bwd_varlen either way).
  *   dq : [sp][T/sp][hq][D], dk, dv : [sp][T/sp][hkv][D] of grad_dt: dt or USP_FP32.
  *   The workspace is that of usp_attn_bwd_varlen for the same sizes.
  * Errors: as usp_attn_bwd_varlen, and the sp rules of usp_ulysses_attn_fwd.
  */
 usp_status usp_ulysses_attn_bwd(const void* q, const void* k, const void* v, const void* o,
-                                const float* lse, const void* d_o, void* dq, void* dk, void* dv,
+                                const void* o_res, const float* lse, const void* d_o, void* dq, void* dk, void* dv,
                                 usp_dtype grad_dt, const int32_t* cu_seqlens, int num_seqs, int64_t total_tokens,
                                 int sp, int hq, int hkv, int head_dim, float softmax_scale, int causal,
                                 usp_dtype dt, void* workspace, size_t ws_bytes, void* stream);

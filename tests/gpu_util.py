@@ -61,11 +61,14 @@ class Problem:
                             usp.attn_workspace_size(self.T, self.B, self.hq, self.hkv, self.D, True))
         self.ws = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8, device="cuda")
 
-    def forward(self):
+    def forward(self, residual=True):
+        """O, LSE and the device status; the rounding residual of O is kept in self.o_res
+        (None with residual=False) and handed to the next backward."""
         o = torch.full((self.hq, self.T, self.D), float("nan"), dtype=torch.bfloat16, device="cuda")
         lse = torch.full((self.hq, self.T), float("nan"), dtype=torch.float32, device="cuda")
+        self.o_res = torch.full_like(o, float("nan")) if residual else None
         usp.attn_fwd_varlen(self.q, self.k, self.v, o, lse, self.cu, self.B, self.T, self.hq, self.hkv, self.D,
-                            0.0, self.causal, self.ws, self.ws_bytes)
+                            0.0, self.causal, self.ws, self.ws_bytes, o_res=self.o_res)
         status = usp.get_device_status(self.ws)
         return o, lse, status
 
@@ -75,7 +78,8 @@ class Problem:
         dk = torch.full((self.hkv, self.T, self.D), float("nan"), dtype=grad_dtype, device="cuda")
         dv = torch.full((self.hkv, self.T, self.D), float("nan"), dtype=grad_dtype, device="cuda")
         usp.attn_bwd_varlen(self.q, self.k, self.v, o, lse, self.do, dq, dk, dv, gd, self.cu, self.B, self.T,
-                            self.hq, self.hkv, self.D, 0.0, self.causal, self.ws, self.ws_bytes)
+                            self.hq, self.hkv, self.D, 0.0, self.causal, self.ws, self.ws_bytes,
+                            o_res=getattr(self, "o_res", None))
         status = usp.get_device_status(self.ws)
         return dq, dk, dv, status
 

@@ -64,13 +64,14 @@ def test_head_divisibility_matches_worked_example():
     assert accepted == [1, 2, 4, 8, 16, 32]
 
 
-def fwd(q=A, k=A, v=A, o=B, lse=B, cu=A, nseq=1, T=256, hq=4, hkv=4, D=128, ws=A, wsb=1 << 40):
-    return _lib.load().usp_attn_fwd_varlen(q, k, v, o, lse, cu, nseq, T, hq, hkv, D, 0.0, 1, ws, wsb, None)
+def fwd(q=A, k=A, v=A, o=B, o_res=None, lse=B, cu=A, nseq=1, T=256, hq=4, hkv=4, D=128, ws=A, wsb=1 << 40):
+    return _lib.load().usp_attn_fwd_varlen(q, k, v, o, o_res, lse, cu, nseq, T, hq, hkv, D, 0.0, 1, ws, wsb, None)
 
 
 def test_attn_fwd_validation():
     assert fwd(q=0) == _lib.USP_ERR_INVALID_ARG
     assert fwd(o=MIS) == _lib.USP_ERR_INVALID_ARG
+    assert fwd(o_res=MIS) == _lib.USP_ERR_INVALID_ARG
     assert fwd(hq=6, hkv=4) == _lib.USP_ERR_INVALID_ARG
     assert fwd(nseq=0) == _lib.USP_ERR_INVALID_ARG
     assert fwd(cu=0) == _lib.USP_ERR_INVALID_ARG
@@ -82,13 +83,15 @@ def test_attn_fwd_validation():
 def test_attn_bwd_validation():
     L = _lib.load()
 
-    def bwd(gdt=_lib.USP_FP32, dq=B, D=128, wsb=1 << 40, hq=4, hkv=2):
-        return L.usp_attn_bwd_varlen(A, A, A, A, A, A, dq, B, B, gdt, A, 1, 256, hq, hkv, D, 0.0, 1, A, wsb, None)
+    def bwd(gdt=_lib.USP_FP32, dq=B, D=128, wsb=1 << 40, hq=4, hkv=2, o_res=None):
+        return L.usp_attn_bwd_varlen(A, A, A, A, o_res, A, A, dq, B, B, gdt, A, 1, 256, hq, hkv, D, 0.0, 1, A, wsb,
+                                     None)
 
     assert bwd(gdt=_lib.USP_FP16) == _lib.USP_ERR_UNSUPPORTED
     assert bwd(gdt=7) == _lib.USP_ERR_INVALID_ARG
     assert bwd(dq=0) == _lib.USP_ERR_INVALID_ARG
     assert bwd(dq=MIS) == _lib.USP_ERR_INVALID_ARG
+    assert bwd(o_res=MIS) == _lib.USP_ERR_INVALID_ARG
     assert bwd(D=32) == _lib.USP_ERR_UNSUPPORTED
     assert bwd(hq=3) == _lib.USP_ERR_INVALID_ARG
     assert bwd(wsb=100) == _lib.USP_ERR_WORKSPACE

@@ -66,21 +66,40 @@ def test_bwd_ragged_packed_edges_gqa(causal, D):
 
 def test_bwd_many_short_samples():
     """Several thousand short work items over 152 persistent CTAs (each runs many items
-    back to back), with ragged key tiles in every 300- and 129-token sample. Queries and
-    output gradients are halved (exact in bf16): with N(0,1) inputs the short causal
-    samples give gradients up to about 7, where the bf16 rounding of P and dS alone (a
-    float64 simulation of those two roundings on this input) comes to 0.021 in dK;
-    halving both scales dS, and with it that error, by four in dK and two in dQ and dV."""
+    back to back), with ragged key tiles in every 300- and 129-token sample, on plain
+    N(0, 1) inputs: the short causal samples give gradients up to about 7, where bf16 P
+    and dS (8 significant bits) and a Delta taken from the bf16 output alone would each
+    put about 0.015 into dK (a float64 simulation of those roundings on this input)."""
     needs_gpu()
     lengths = [100] * 40 + [300] * 20 + [129] * 10
     w = custom_workload("runs", lengths, sp=1, hq=32, hkv=8, head_dim=128, index=16)
+    check_bwd(*make(w), w.cu_seqlens(), True, q_heads=[0, 13], kv_heads=[0, 7])
+
+
+def test_bwd_shortest_legal_samples_gqa():
+    """Packed samples of the shortest lengths the packed workload allows (128 to 300
+    tokens, multiples of 8), GQA 4:1, N(0, 1), every head checked in full."""
+    needs_gpu()
+    rng = np.random.default_rng(31)
+    lengths = [int(x) for x in rng.integers(16, 38, size=24) * 8]
+    w = custom_workload("shortest", lengths, sp=1, hq=8, hkv=2, head_dim=128, index=18)
+    check_bwd(*make(w), w.cu_seqlens(), True)
+
+
+def test_bwd_without_residual_still_runs():
+    """The residual is optional: without it Delta comes from the bf16 output alone (looser;
+    checked here only against the 16-bit rounding bound on a long-sample input)."""
+    needs_gpu()
+    w = custom_workload("nores", [700, 324], sp=1, hq=4, hkv=4, head_dim=128, index=19)
     q, k, v, do = make(w)
-
-    def halve(bits):   # bf16 bits of x/2: the exponent drops by one, the mantissa is unchanged
-        return ((((bits.astype(np.uint32) << 16).view(np.float32) * np.float32(0.5)).view(np.uint32)) >> 16).astype(
-            np.uint16)
-
-    check_bwd(halve(q), k, v, halve(do), w.cu_seqlens(), True, q_heads=[0, 13], kv_heads=[0, 7])
+    p = Problem(q, k, v, w.cu_seqlens(), True, do_bits=do)
+    o, lse, st = p.forward(residual=False)
+    assert st == 0
+    dq, dk, dv, st = p.backward(o, lse)
+    assert st == 0
+    rq, rk, rv = oracle.attn_bwd(q, k, v, do, w.cu_seqlens())
+    for g, r in ((dq, rq), (dk, rk), (dv, rv)):
+        assert np.abs(f64(g) - r).max() <= G_TOL
 
 
 def test_bwd_llama_all_heads_launch():

@@ -1,9 +1,12 @@
 """GPU parity of the fused Ulysses steps (layout swaps inside the attention kernels):
 seq-sharded q, k, v, dO in; seq-sharded o, dq, dk, dv out.
 
-Checked against the float64 oracle (O within 1e-2, LSE within 1e-3, fp32 gradients within
-2e-2, as the unfused tests) and against the unfused path: the forward output must be
-bit-identical, since only the rows the kernel reads and writes differ.
+Checked against the float64 oracle (the computed O -- output plus rounding residual --
+within 1e-2 and the bf16 output within 1e-2 plus its half-ulp, LSE within 1e-3, fp32
+gradients within 2e-2, as the unfused tests) and against the unfused path: the forward
+output must be bit-identical, since only the rows the kernel reads and writes differ.
+The packed, long and gqa workloads run here in the configuration the benchmark times:
+one rank's slice of heads, token-major buffers.
 """
 import numpy as np
 import pytest
@@ -12,7 +15,8 @@ import torch
 import oracle
 import ulysses_sequence_seq_gb300 as usp
 from tests.gpu_util import dev_bf16, f64, host_bits, needs_gpu, sample_rows
-from ulysses_sequence_seq_gb300.synth import WORKLOADS, custom_workload, head_sharded_bits, seq_sharded_bits
+from ulysses_sequence_seq_gb300.synth import (WORKLOADS, custom_workload, head_sharded_bits, rank_slice,
+                                              seq_sharded_bits)
 
 pytestmark = pytest.mark.gpu
 
@@ -37,6 +41,7 @@ class Fused:
 
     def run(self):
         o = self.layer.forward(self.dq, self.dk, self.dv, self.cu).clone()
+        self.o_res = self.layer.o_res_seq.clone()
         lse = self.layer.lse.clone()
         g = [t.clone() for t in self.layer.backward(self.ddo, self.cu)]
         torch.cuda.synchronize()
@@ -53,7 +58,9 @@ def check(w, q_heads=None, rows=None, kv_heads=None, k_rows=None, grad_dtype=tor
     hs = list(range(w.hq)) if q_heads is None else list(q_heads)
     rs = np.arange(T) if rows is None else np.asarray(rows)
     o_h = f64(o).reshape(T, w.hq, w.head_dim).transpose(1, 0, 2)        # [H][T][D]
-    assert np.abs(o_h[hs][:, rs] - ro).max() <= O_TOL
+    r_h = f64(f.o_res).reshape(T, w.hq, w.head_dim).transpose(1, 0, 2)
+    assert np.abs(o_h[hs][:, rs] + r_h[hs][:, rs] - ro).max() <= O_TOL
+    assert (np.abs(o_h[hs][:, rs] - ro) <= O_TOL + np.abs(ro) * 2.0 ** -8).all()
     assert np.abs(f64(lse)[hs][:, rs] - rl).max() <= LSE_TOL
     rq, rk, rv = oracle.attn_bwd(q, k, v, do, f.cu_host, causal=w.causal, q_heads=q_heads, q_rows=rows,
                                  kv_heads=kv_heads, k_rows=k_rows)
@@ -111,6 +118,37 @@ def test_fused_gqa_sampled():
     ends = [int(x) for x in cu[1:]]
     check(w, q_heads=[0, 13], rows=sample_rows(cu, 24, seed=19), kv_heads=[3],
           k_rows=sorted({r for e in ends for r in (e - 1, e - 129)}))
+
+
+def test_fused_packed_rank_slice_sampled():
+    """The packed workload as the benchmark runs it: one rank's 4 heads over all 65536
+    tokens in the token-major layout, sampled rows and key rows at every sample end."""
+    needs_gpu()
+    w = rank_slice(WORKLOADS["packed"])
+    cu = w.cu_seqlens()
+    ends = [int(x) for x in cu[1:]]
+    check(w, q_heads=[1, 3], rows=sample_rows(cu, 48, seed=21), kv_heads=[2],
+          k_rows=sorted({r for e in ends for r in (e - 1, e - 2, e - 129)} | {0, 127, 128}))
+
+
+def test_fused_long_rank_slice_sampled():
+    """The headline workload as the benchmark runs it: one rank's 4 heads over the
+    262144-token sequence, token-major."""
+    needs_gpu()
+    w = rank_slice(WORKLOADS["long"])
+    T = w.total_tokens
+    rows = np.array([0, 1, 127, 128, 4095, 65536, 200003, T - 129, T - 1], dtype=np.int64)
+    k_rows = np.array([T - 300, T - 129, T - 128, T - 2, T - 1], dtype=np.int64)
+    check(w, q_heads=[0], rows=rows, kv_heads=[0], k_rows=k_rows)
+
+
+def test_fused_shortest_samples_gqa():
+    """Packed samples of 128 to 300 tokens, GQA 4:1, N(0, 1), sp = 2, all heads in full."""
+    needs_gpu()
+    rng = np.random.default_rng(33)
+    lengths = [int(x) for x in rng.integers(16, 38, size=16) * 8]
+    w = custom_workload("fused_short", lengths, sp=2, hq=8, hkv=2, head_dim=128, index=20)
+    check(w)
 
 
 def test_fused_rejects_sp_violations():

@@ -79,7 +79,7 @@ def test_noalloc_host_checks_match_the_workspace_entry_point():
     rc = lib.usp_attn_fwd_varlen_noalloc(fake, fake, fake, fake, fake, fake, 1, 1 << 28, 1 << 14, 1, 128, 0.0, 1,
                                          None, stream)
     assert rc == _lib.USP_ERR_UNSUPPORTED
-    rc_ws = lib.usp_attn_fwd_varlen(fake, fake, fake, fake, fake, fake, 1, 1 << 28, 1 << 14, 1, 128, 0.0, 1,
+    rc_ws = lib.usp_attn_fwd_varlen(fake, fake, fake, fake, None, fake, fake, 1, 1 << 28, 1 << 14, 1, 128, 0.0, 1,
                                     fake, 1 << 40, stream)
     assert rc_ws == rc
     # more than 2^30 tokens: beyond the static array whatever the heads

@@ -42,7 +42,8 @@ class UlyssesAttention:
 
     Buffers are allocated once for a fixed (T, num_seqs, hq, hkv, D, sp) and reused.
     ``forward`` takes seq-sharded bf16 tensors ([sp][T/sp][H][D] or [T][H][D]) and
-    returns the seq-sharded output; ``backward`` takes the seq-sharded output
+    returns the seq-sharded output (it also keeps the output's rounding residual, from
+    which the backward takes Delta = dO . O); ``backward`` takes the seq-sharded output
     gradient and returns seq-sharded dQ, dK, dV. With ``fused=True`` (the default)
     the layout swaps happen inside the attention kernels; with ``fused=False`` they
     run as separate re-layout kernels around head-sharded attention.
@@ -73,6 +74,7 @@ class UlyssesAttention:
             self.k_h = torch.empty(hk, T, D, dtype=bf, device=device)
             self.v_h = torch.empty(hk, T, D, dtype=bf, device=device)
             self.o_h = torch.empty(hq, T, D, dtype=bf, device=device)
+            self.o_res_h = torch.empty(hq, T, D, dtype=bf, device=device)
             self.do_h = torch.empty(hq, T, D, dtype=bf, device=device)
             gd = self.grad_dtype
             self.dq_h = torch.empty(hq, T, D, dtype=gd, device=device)
@@ -80,6 +82,8 @@ class UlyssesAttention:
             self.dv_h = torch.empty(hk, T, D, dtype=gd, device=device)
         self.lse = torch.empty(hq, T, dtype=torch.float32, device=device)
         self.o_seq = torch.empty(T, hq, D, dtype=bf, device=device)
+        # the rounding residual of the output, kept for the backward's Delta = dO . O
+        self.o_res_seq = torch.empty(T, hq, D, dtype=bf, device=device) if fused else None
         gd = self.grad_dtype
         self.dq_seq = torch.empty(T, hq, D, dtype=gd, device=device)
         self.dk_seq = torch.empty(T, hkv, D, dtype=gd, device=device)
@@ -93,14 +97,15 @@ class UlyssesAttention:
         sp = self.sp
         if self.fused:
             ulysses_attn_fwd(xq, xk, xv, self.o_seq, self.lse, cu_seqlens, self.B, self.T, sp, self.hq, self.hkv,
-                             self.D, self.scale, self.causal, self.ws, self.ws_bytes, stream)
+                             self.D, self.scale, self.causal, self.ws, self.ws_bytes, stream, o_res=self.o_res_seq)
             self._saved = (xq, xk, xv)
             return self.o_seq
         seq_to_head(xq, self.q_h, sp, stream)
         seq_to_head_kv(xk, self.k_h, sp, stream)
         seq_to_head_kv(xv, self.v_h, sp, stream)
         attn_fwd_varlen(self.q_h, self.k_h, self.v_h, self.o_h, self.lse, cu_seqlens, self.B, self.T, self.hq,
-                        self.hkv_h, self.D, self.scale, self.causal, self.ws, self.ws_bytes, stream)
+                        self.hkv_h, self.D, self.scale, self.causal, self.ws, self.ws_bytes, stream,
+                        o_res=self.o_res_h)
         head_to_seq(self.o_h, self.o_seq, sp, stream)
         return self.o_seq
 
@@ -114,12 +119,12 @@ class UlyssesAttention:
             xq, xk, xv = self._saved
             ulysses_attn_bwd(xq, xk, xv, self.o_seq, self.lse, d_out, self.dq_seq, self.dk_seq, self.dv_seq, gdt,
                              cu_seqlens, self.B, self.T, sp, self.hq, self.hkv, self.D, self.scale, self.causal,
-                             self.ws, self.ws_bytes, stream)
+                             self.ws, self.ws_bytes, stream, o_res=self.o_res_seq)
             return self.dq_seq, self.dk_seq, self.dv_seq
         seq_to_head(d_out, self.do_h, sp, stream)
         attn_bwd_varlen(self.q_h, self.k_h, self.v_h, self.o_h, self.lse, self.do_h, self.dq_h, self.dk_h,
                         self.dv_h, gdt, cu_seqlens, self.B, self.T, self.hq, self.hkv_h, self.D, self.scale,
-                        self.causal, self.ws, self.ws_bytes, stream)
+                        self.causal, self.ws, self.ws_bytes, stream, o_res=self.o_res_h)
         head_to_seq(self.dq_h, self.dq_seq, sp, stream)
         head_to_seq_kv_grad(self.dk_h, self.dk_seq, sp, self.hkv, stream)
         head_to_seq_kv_grad(self.dv_h, self.dv_seq, sp, self.hkv, stream)

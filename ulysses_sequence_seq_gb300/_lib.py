@@ -76,15 +76,15 @@ def load(build_if_missing: bool = True):
     L.usp_head_to_seq.argtypes = [P, P, I, I64, I, I, I, P]
     L.usp_attn_workspace_size.argtypes = [I64, I, I, I, I, I]
     L.usp_attn_workspace_size.restype = Z
-    L.usp_attn_fwd_varlen.argtypes = [P, P, P, P, P, P, I, I64, I, I, I, F, I, P, Z, P]
-    L.usp_attn_bwd_varlen.argtypes = [P, P, P, P, P, P, P, P, P, I, P, I, I64, I, I, I, F, I, P, Z, P]
+    L.usp_attn_fwd_varlen.argtypes = [P, P, P, P, P, P, P, I, I64, I, I, I, F, I, P, Z, P]
+    L.usp_attn_bwd_varlen.argtypes = [P, P, P, P, P, P, P, P, P, P, I, P, I, I64, I, I, I, F, I, P, Z, P]
     L.usp_get_device_status.argtypes = [P, P]
     L.usp_status_string.argtypes = [I]
     L.usp_status_string.restype = ctypes.c_char_p
     L.usp_debug_wait_timeout.argtypes = [P, Z, ctypes.c_uint64, P]
     L.usp_attn_fwd_varlen_noalloc.argtypes = [P, P, P, P, P, P, I, I64, I, I, I, F, I, P, P]
-    L.usp_ulysses_attn_fwd.argtypes = [P, P, P, P, P, P, I, I64, I, I, I, I, F, I, I, P, Z, P]
-    L.usp_ulysses_attn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I, P, I, I64, I, I, I, I, F, I, I, P, Z, P]
+    L.usp_ulysses_attn_fwd.argtypes = [P, P, P, P, P, P, P, I, I64, I, I, I, I, F, I, I, P, Z, P]
+    L.usp_ulysses_attn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, I, P, I, I64, I, I, I, I, F, I, I, P, Z, P]
     L.usp_seq_to_head_kv.argtypes = [P, P, I, I64, I, I, I, P]
     L.usp_head_to_seq_kv_grad.argtypes = [P, P, I, I64, I, I, I, P]
     L.usp_position_ids_workspace_size.argtypes = [I64]
@@ -199,41 +199,46 @@ def attn_workspace_size(total_tokens: int, num_seqs: int, hq: int, hkv: int, hea
 
 
 def attn_fwd_varlen(q, k, v, o, lse, cu_seqlens, num_seqs: int, total_tokens: int, hq: int, hkv: int,
-                    head_dim: int, softmax_scale: float, causal: bool, workspace, ws_bytes: int, stream=None):
+                    head_dim: int, softmax_scale: float, causal: bool, workspace, ws_bytes: int, stream=None,
+                    o_res=None):
+    """Head-major forward; `o_res` (optional, like `o`) receives the rounding residual of o."""
     _check("usp_attn_fwd_varlen", load().usp_attn_fwd_varlen(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(cu_seqlens), int(num_seqs), int(total_tokens),
-        int(hq), int(hkv), int(head_dim), float(softmax_scale), int(bool(causal)), _ptr(workspace),
-        int(ws_bytes), _stream(stream)))
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(o_res), _ptr(lse), _ptr(cu_seqlens), int(num_seqs),
+        int(total_tokens), int(hq), int(hkv), int(head_dim), float(softmax_scale), int(bool(causal)),
+        _ptr(workspace), int(ws_bytes), _stream(stream)))
 
 
 def attn_bwd_varlen(q, k, v, o, lse, d_o, dq, dk, dv, grad_dt: int, cu_seqlens, num_seqs: int,
                     total_tokens: int, hq: int, hkv: int, head_dim: int, softmax_scale: float, causal: bool,
-                    workspace, ws_bytes: int, stream=None):
+                    workspace, ws_bytes: int, stream=None, o_res=None):
+    """Head-major backward; pass the forward's `o_res` to take Delta from o + o_res."""
     _check("usp_attn_bwd_varlen", load().usp_attn_bwd_varlen(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(d_o), _ptr(dq), _ptr(dk), _ptr(dv), int(grad_dt),
-        _ptr(cu_seqlens), int(num_seqs), int(total_tokens), int(hq), int(hkv), int(head_dim),
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(o_res), _ptr(lse), _ptr(d_o), _ptr(dq), _ptr(dk), _ptr(dv),
+        int(grad_dt), _ptr(cu_seqlens), int(num_seqs), int(total_tokens), int(hq), int(hkv), int(head_dim),
         float(softmax_scale), int(bool(causal)), _ptr(workspace), int(ws_bytes), _stream(stream)))
 
 
 def ulysses_attn_fwd(q, k, v, o, lse, cu_seqlens, num_seqs: int, total_tokens: int, sp: int, hq: int, hkv: int,
-                     head_dim: int, softmax_scale: float, causal: bool, workspace, ws_bytes: int, stream=None):
-    """Fused forward on the seq-sharded layout: q, k, v, o are [sp][T/sp][H][D], bf16 or
-    fp16 (taken from q)."""
+                     head_dim: int, softmax_scale: float, causal: bool, workspace, ws_bytes: int, stream=None,
+                     o_res=None):
+    """Fused forward on the seq-sharded layout: q, k, v, o (and o_res) are [sp][T/sp][H][D],
+    bf16 or fp16 (taken from q)."""
     _check("usp_ulysses_attn_fwd", load().usp_ulysses_attn_fwd(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(cu_seqlens), int(num_seqs), int(total_tokens), int(sp),
-        int(hq), int(hkv), int(head_dim), float(softmax_scale), int(bool(causal)), _input_dtype(q), _ptr(workspace),
-        int(ws_bytes), _stream(stream)))
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(o_res), _ptr(lse), _ptr(cu_seqlens), int(num_seqs),
+        int(total_tokens), int(sp), int(hq), int(hkv), int(head_dim), float(softmax_scale), int(bool(causal)),
+        _input_dtype(q), _ptr(workspace), int(ws_bytes), _stream(stream)))
 
 
 def ulysses_attn_bwd(q, k, v, o, lse, d_o, dq, dk, dv, grad_dt: int, cu_seqlens, num_seqs: int, total_tokens: int,
                      sp: int, hq: int, hkv: int, head_dim: int, softmax_scale: float, causal: bool, workspace,
-                     ws_bytes: int, stream=None):
+                     ws_bytes: int, stream=None, o_res=None):
     """Fused backward on the seq-sharded layout: every activation and gradient is [sp][T/sp][H][D];
     activations bf16 or fp16 (taken from q), gradients of grad_dt (that type or fp32)."""
     _check("usp_ulysses_attn_bwd", load().usp_ulysses_attn_bwd(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(d_o), _ptr(dq), _ptr(dk), _ptr(dv), int(grad_dt),
-        _ptr(cu_seqlens), int(num_seqs), int(total_tokens), int(sp), int(hq), int(hkv), int(head_dim),
-        float(softmax_scale), int(bool(causal)), _input_dtype(q), _ptr(workspace), int(ws_bytes), _stream(stream)))
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(o_res), _ptr(lse), _ptr(d_o), _ptr(dq), _ptr(dk), _ptr(dv),
+        int(grad_dt), _ptr(cu_seqlens), int(num_seqs), int(total_tokens), int(sp), int(hq), int(hkv),
+        int(head_dim), float(softmax_scale), int(bool(causal)), _input_dtype(q), _ptr(workspace), int(ws_bytes),
+        _stream(stream)))
 
 
 def attn_fwd_varlen_noalloc(q, k, v, o, lse, cu_seqlens, num_seqs: int, total_tokens: int, hq: int, hkv: int,

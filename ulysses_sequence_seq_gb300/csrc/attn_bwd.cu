@@ -34,6 +34,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <cmath>
+
 #include "attn.cuh"
 #include "common.cuh"
 #include "ptx.cuh"
@@ -97,6 +99,31 @@ __device__ __forceinline__ BwdItem bwd_item(const BwdArgs& a, int idx) {
     b.nq = query_blocks_in_sample(b.s, b.e) - b.i0;
     b.nsteps = b.nq * a.group;
     return b;
+}
+
+// Scale factors of one key/value group's fp16 operands (see BwdArgs): the products run on
+// q' = q 2^eq, k' = k 2^ek, v' = v 2^ev, dO' = dO 2^edo, and dS is rounded as dS 2^(ev+edo+ds_exp).
+struct GroupScale {
+    float sl2;      // scale * log2(e) * 2^-(eq+ek): turns the scaled S' into log2 units
+    float sc;       // scale * 2^ds_exp: the factor of dS
+    float dsc;      // 2^(ev+edo) * sc: Delta on the scale of dP', times the factor of dS
+    float dv_un;    // 2^-edo: dV' -> dV
+    float dk_un;    // 2^-(ev+edo+ds_exp+eq): dK' -> dK
+    float dq_un;    // 2^-(ev+edo+ds_exp+ek): dQ' -> dQ
+};
+__device__ __forceinline__ GroupScale group_scale(const BwdArgs& a, int g) {
+    const int eq = range_exponent(__ldg(a.amax + kAmaxQ * a.hkv + g));
+    const int ek = range_exponent(__ldg(a.amax + kAmaxK * a.hkv + g));
+    const int ev = range_exponent(__ldg(a.amax + kAmaxV * a.hkv + g));
+    const int edo = range_exponent(__ldg(a.amax + kAmaxDO * a.hkv + g));
+    GroupScale r;
+    r.sl2 = a.scale_log2 * exp2i(-(eq + ek));
+    r.sc = a.scale * exp2i(a.ds_exp);
+    r.dsc = exp2i(ev + edo) * r.sc;
+    r.dv_un = exp2i(-edo);
+    r.dk_un = exp2i(-(ev + edo + a.ds_exp + eq));
+    r.dq_un = exp2i(-(ev + edo + a.ds_exp + ek));
+    return r;
 }
 
 // The CTA's j-th work item, published by the producer in a 4-slot ring; false when the
@@ -203,7 +230,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     mbar_arrive_expect_tx(&bars[L::bQFull + st], L::kTileBytes);
                     for (int p = 0; p < L::kPanels; ++p)
                         tma_load_rows(sm + L::kQ + st * L::kTileBytes + p * (kTileM * 128), &tmQ,
-                                      &bars[L::bQFull + st], p * 64, q0, h, a.token_major);
+                                      &bars[L::bQFull + st], p * 64, q0, h, 0);
                     ++q_total;
                     // the single dO buffer is free once both halves' dV and dP of the previous block are done
                     if (gk >= 1 && !mbar_wait(&bars[L::bDoEmpty], (gk - 1) & 1, abort_flag, kWaitLimitNs)) {
@@ -212,8 +239,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     }
                     mbar_arrive_expect_tx(&bars[L::bDoFull], L::kTileBytes);
                     for (int p = 0; p < L::kPanels; ++p)
-                        tma_load_rows(sm + L::kDO + p * (kTileM * 128), &tmDO, &bars[L::bDoFull], p * 64, q0, h,
-                                      a.token_major);
+                        tma_load_rows(sm + L::kDO + p * (kTileM * 128), &tmDO, &bars[L::bDoFull], p * 64, q0, h, 0);
                     ++do_total;
                     if (k == 0) {  // K, V once the previous item's last MMA has read them
                         if (j > 0 && !mbar_wait(&bars[L::bKvEmpty], (j - 1) & 1, abort_flag, kWaitLimitNs)) {
@@ -223,9 +249,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         mbar_arrive_expect_tx(&bars[L::bKvFull], 2 * L::kTileBytes);
                         for (int p = 0; p < L::kPanels; ++p) {
                             tma_load_rows(sm + L::kK + p * (kTileM * 128), &tmK, &bars[L::bKvFull], p * 64, w.kv0,
-                                          w.g, a.token_major);
+                                          w.g, 0);
                             tma_load_rows(sm + L::kV + p * (kTileM * 128), &tmV, &bars[L::bKvFull], p * 64, w.kv0,
-                                          w.g, a.token_major);
+                                          w.g, 0);
                         }
                         ++kv_total;
                     }
@@ -236,8 +262,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         if (next_idx < count) {
                             const BwdItem nw = bwd_item(a, next_idx);
                             for (int p = 0; p < L::kPanels; ++p) {
-                                tma_prefetch_rows(&tmK, p * 64, nw.kv0, nw.g, a.token_major);
-                                tma_prefetch_rows(&tmV, p * 64, nw.kv0, nw.g, a.token_major);
+                                tma_prefetch_rows(&tmK, p * 64, nw.kv0, nw.g, 0);
+                                tma_prefetch_rows(&tmV, p * 64, nw.kv0, nw.g, 0);
                             }
                         }
                     }
@@ -363,8 +389,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t tS = tbase + lane_off + grp * kHalfCols;
         float* lse_g = lse_s + grp * kHalfCols;
         float* delta_g = delta_s + grp * kHalfCols;
-        const float sl2 = a.scale_log2;
-        const float sc = a.scale;
         bool ok = true;
         int gk = 0;
         // This half's query rows of a step, negated: -lse (log2 units) and -Delta; rows outside
@@ -372,12 +396,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // (the first step of the next item before this item's epilogue), so that their
         // global-memory latency stays off the critical path.
         float nl_next = -INFINITY, nd_next = 0.f;
-        auto fetch_row_stats = [&](const BwdItem& it, int k) {
+        auto fetch_row_stats = [&](const BwdItem& it, int k, float dsc) {
             const int h = it.g * G + k / it.nq;
             const int q = it.q0(k) + grp * kHalfCols + r;
             const bool q_ok = r < kHalfCols && q < it.e;
             nl_next = q_ok ? -__ldg(a.lse + (int64_t)h * a.T + q) * 1.4426950408889634f : -INFINITY;
-            nd_next = q_ok ? -__ldg(a.delta + (int64_t)h * a.T + q) : 0.f;
+            nd_next = q_ok ? -__ldg(a.delta + (int64_t)h * a.T + q) * dsc : 0.f;   // -Delta' * sc
         };
         // The half's four warps leave their loops together: a warp that gave up on a bounded
         // wait skips ahead to the next vote (group_any) instead of leaving at once, so that no
@@ -385,9 +409,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         int idx = count;
         if (!read_item(item_bars, item_ring, 0, abort_flag, idx)) ok = false;
         ok = !group_any(1 + grp, 128, !ok);
-        if (ok && idx < count) fetch_row_stats(bwd_item(a, idx), 0);
+        if (ok && idx < count) {
+            const BwdItem w0 = bwd_item(a, idx);
+            fetch_row_stats(w0, 0, group_scale(a, w0.g).dsc);
+        }
         for (int j = 0; ok && idx < count; ++j) {
             const BwdItem w = bwd_item(a, idx);
+            float sl2, sc, dsc;
+            {
+                const GroupScale gs = group_scale(a, w.g);
+                sl2 = gs.sl2;
+                sc = gs.sc;
+                dsc = gs.dsc;
+            }
             const int kv = w.kv0 + r;
             const bool kv_ok = kv < w.e;
             for (int k = 0; k < w.nsteps; ++k, ++gk) {
@@ -401,7 +435,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     delta_g[r] = nd_next;
                 }
                 named_bar_sync(1 + grp, 128);
-                if (k + 1 < w.nsteps) fetch_row_stats(w, k + 1);
+                if (k + 1 < w.nsteps) fetch_row_stats(w, k + 1, dsc);
                 // element masks are only needed on the diagonal block and on the sample's ragged
                 // last key tile; there query column c (of 128) is visible to key row r iff c >= r
                 const bool mask_blk = (a.causal && q0 == w.kv0) || (w.kv0 + kBlockN > w.e);
@@ -456,17 +490,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
                     for (int jj = 0; jj < 8; ++jj) nd4[jj] = *(const float4*)(delta_g + 32 * c + 4 * jj);
                     tmem_ld_wait(dr);
+                    // dS = P * ((dP' - Delta') sc): the bracket in fp32 (one fma with -Delta' sc
+                    // from shared memory), rounded to fp16, then multiplied by the fp16 P the dV
+                    // MMA consumed (|(dP' - Delta') sc| <= 2^15 by the choice of ds_exp)
                     uint32_t pk[16];
 #pragma unroll
                     for (int jj = 0; jj < 16; ++jj) {
                         const float4 d4 = nd4[jj >> 1];
                         const float2 nd = (jj & 1) ? make_float2(d4.z, d4.w) : make_float2(d4.x, d4.y);
-                        const float2 d =
-                            add2(make_float2(__uint_as_float(dr[2 * jj]), __uint_as_float(dr[2 * jj + 1])), nd);
-                        const uint32_t pb = pkall[16 * c + jj];
-                        const float2 psc = mul2(unpack2<F16>(pb), make_float2(sc, sc));
-                        const float2 ds = mul2(psc, d);
-                        pk[jj] = pack2<F16>(ds.x, ds.y);
+                        const float2 d = fma2(make_float2(__uint_as_float(dr[2 * jj]), __uint_as_float(dr[2 * jj + 1])),
+                                              make_float2(sc, sc), nd);
+                        pk[jj] = hmul2(pack2<true>(d.x, d.y), pkall[16 * c + jj]);
                     }
                     // row r of the [key][query] dS operand (read K-major by dK, MN-major by dQ)
 #pragma unroll
@@ -484,7 +518,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             // the next item, and its first step's row statistics, before this item's epilogue
             int idx_next = count;
             if (ok && !read_item(item_bars, item_ring, j + 1, abort_flag, idx_next)) ok = false;
-            if (ok && idx_next < count) fetch_row_stats(bwd_item(a, idx_next), 0);
+            if (ok && idx_next < count) {
+                const BwdItem wn = bwd_item(a, idx_next);
+                fetch_row_stats(wn, 0, group_scale(a, wn.g).dsc);
+            }
             idx = idx_next;
             if (ok) ok = mbar_wait(&bars[L::bAccFull], j & 1, abort_flag, kWaitLimitNs);
             if (group_any(1 + grp, 128, !ok)) break;
@@ -492,6 +529,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             // half A writes dV, half B writes dK; TMEM is handed back to the next item's MMAs as
             // soon as the last chunk has been read, before the global stores finish
             const uint32_t src = tbase + lane_off + (grp ? 384 : 256);
+            const float un = grp ? group_scale(a, w.g).dk_un : group_scale(a, w.g).dv_un;   // exact powers of two
+            const bool of16 = a.out_f16 != 0;
+            auto pk_out = [&](float x0, float x1) { return of16 ? pack2<true>(x0 * un, x1 * un) : pack2<false>(x0 * un, x1 * un); };
             if (!a.grad_fp32 && w.kv0 + kBlockN <= w.e) {
                 // Whole 16-bit tile: each half stages its accumulator through its own 64-column
                 // dS panel, 64 columns per round, and writes each round with one TMA store, so
@@ -514,10 +554,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     }
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        const uint32_t p0 = pack2<F16>(__uint_as_float(o[8 * q]), __uint_as_float(o[8 * q + 1]));
-                        const uint32_t p1 = pack2<F16>(__uint_as_float(o[8 * q + 2]), __uint_as_float(o[8 * q + 3]));
-                        const uint32_t p2 = pack2<F16>(__uint_as_float(o[8 * q + 4]), __uint_as_float(o[8 * q + 5]));
-                        const uint32_t p3 = pack2<F16>(__uint_as_float(o[8 * q + 6]), __uint_as_float(o[8 * q + 7]));
+                        const uint32_t p0 = pk_out(__uint_as_float(o[8 * q]), __uint_as_float(o[8 * q + 1]));
+                        const uint32_t p1 = pk_out(__uint_as_float(o[8 * q + 2]), __uint_as_float(o[8 * q + 3]));
+                        const uint32_t p2 = pk_out(__uint_as_float(o[8 * q + 4]), __uint_as_float(o[8 * q + 5]));
+                        const uint32_t p3 = pk_out(__uint_as_float(o[8 * q + 6]), __uint_as_float(o[8 * q + 7]));
                         const int col = 32 * c + 8 * q;   // first of the 8 columns in this 16-byte chunk
                         if (col < 64) {
                             *(uint4*)(panel + sw128_offset(r, (uint32_t)(col * 2))) = make_uint4(p0, p1, p2, p3);
@@ -567,16 +607,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     float4* dst = (float4*)((float*)dst_base + row * D + c);
 #pragma unroll
                     for (int jj = 0; jj < 8; ++jj)
-                        dst[jj] = make_float4(__uint_as_float(o[4 * jj]), __uint_as_float(o[4 * jj + 1]),
-                                              __uint_as_float(o[4 * jj + 2]), __uint_as_float(o[4 * jj + 3]));
+                        dst[jj] = make_float4(__uint_as_float(o[4 * jj]) * un, __uint_as_float(o[4 * jj + 1]) * un,
+                                              __uint_as_float(o[4 * jj + 2]) * un, __uint_as_float(o[4 * jj + 3]) * un);
                 } else {
                     uint4* dst = (uint4*)((uint16_t*)dst_base + row * D + c);
 #pragma unroll
                     for (int jj = 0; jj < 4; ++jj)
-                        dst[jj] = make_uint4(pack2<F16>(__uint_as_float(o[8 * jj]), __uint_as_float(o[8 * jj + 1])),
-                                             pack2<F16>(__uint_as_float(o[8 * jj + 2]), __uint_as_float(o[8 * jj + 3])),
-                                             pack2<F16>(__uint_as_float(o[8 * jj + 4]), __uint_as_float(o[8 * jj + 5])),
-                                             pack2<F16>(__uint_as_float(o[8 * jj + 6]), __uint_as_float(o[8 * jj + 7])));
+                        dst[jj] = make_uint4(pk_out(__uint_as_float(o[8 * jj]), __uint_as_float(o[8 * jj + 1])),
+                                             pk_out(__uint_as_float(o[8 * jj + 2]), __uint_as_float(o[8 * jj + 3])),
+                                             pk_out(__uint_as_float(o[8 * jj + 4]), __uint_as_float(o[8 * jj + 5])),
+                                             pk_out(__uint_as_float(o[8 * jj + 6]), __uint_as_float(o[8 * jj + 7])));
                 }
             }
         }
@@ -632,7 +672,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_reduce_add_rows(&tmDQ, buf, c, qrow0, h, a.dq_token_major);
+                        tma_reduce_add_rows(&tmDQ, buf, c, qrow0, h, 0);
                         bulk_commit_group();
                     }
                     if (ci + 1 < D / 32) tmem_ld_wait(v[(ci + 1) & 1]);
@@ -650,16 +690,47 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (threadIdx.x == 0 && *abort_flag) atomicCAS(&a.hdr->status, (int)USP_OK, (int)USP_ERR_TIMEOUT);
 }
 
-// Delta_i = dO_i . O_i in fp32, and zero row i of the dQ accumulator. TPR threads per row,
-// each owning 8 consecutive elements (one 16-byte vector of 16-bit values).
+// Largest magnitude of the 8 16-bit values of v.
+template <bool F16>
+__device__ __forceinline__ float amax8(uint4 v) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    float m = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float2 x = unpack2<F16>(w[j]);
+        m = fmax3(m, fabsf(x.x), fabsf(x.y));
+    }
+    return m;
+}
+
+// Block-wide max of `m` (every thread of the 256 calls it), then one atomicMax on the float
+// bits, which order like the values for non-negative floats.
+__device__ __forceinline__ void block_amax(float m, uint32_t* dst, float* red) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    __syncthreads();   // `red` may still be read from the previous call
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float b = red[0];
+        for (int i = 1; i < 8; ++i) b = fmaxf(b, red[i]);
+        atomicMax(dst, __float_as_uint(b));
+    }
+}
+
+// Delta_i = dO_i . (O_i + O_res_i) in fp32, zero row i of the dQ accumulator, and the largest
+// magnitudes of q, dO (of query head blockIdx.y) and of k, v (of key/value head blockIdx.y,
+// when there is one). TPR threads per row, each owning 8 consecutive elements (16 bytes).
 template <int D, bool F16>
-__global__ void __launch_bounds__(256) bwd_prep_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
-                                                       float* __restrict__ delta, float* __restrict__ dq_acc, int64_t T,
-                                                       int H, int token_major, int dq_token_major) {
+__global__ void __launch_bounds__(256) bwd_stats_kernel(const BwdStatsArgs a) {
     constexpr int TPR = D / 8;   // threads per row, 8 elements (16 bytes) each
-    pdl_trigger();   // the scheduler after this kernel needs none of its output
+    pdl_trigger();   // the next kernel waits for this one's completion before it reads anything
+    __shared__ float red[8];
     const int h = blockIdx.y;
     const int sub = threadIdx.x % TPR;
+    const int64_t T = a.T;
+    const bool kv_head = h < a.hkv;
+    float mq = 0.f, mdo = 0.f, mk = 0.f, mv = 0.f;
     constexpr int64_t kRowsPerCta = 256 / TPR;
     // the loop bound is uniform across the CTA so that every lane reaches the shuffles
     for (int64_t base = (int64_t)blockIdx.x * kRowsPerCta; base < T; base += (int64_t)gridDim.x * kRowsPerCta) {
@@ -667,44 +738,113 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint16_t* __restric
         const bool valid = t < T;
         float acc = 0.f;
         if (valid) {
-            const int64_t arow = act_row(h, t, T, H, token_major);
-            const uint4 ov = __ldg((const uint4*)(o + arow * D) + sub);
-            const uint4 dv = __ldg((const uint4*)(dout + arow * D) + sub);
+            const int64_t arow = act_row(h, t, T, a.hq, a.token_major);
+            const uint4 ov = __ldg((const uint4*)(a.o + arow * D) + sub);
+            const uint4 dv = __ldg((const uint4*)(a.dout + arow * D) + sub);
+            const uint4 qv = __ldg((const uint4*)(a.q + arow * D) + sub);
+            const uint4 rv = a.o_res ? __ldg((const uint4*)(a.o_res + arow * D) + sub) : make_uint4(0, 0, 0, 0);
             const uint32_t o2[4] = {ov.x, ov.y, ov.z, ov.w};
+            const uint32_t r2[4] = {rv.x, rv.y, rv.z, rv.w};
             const uint32_t d2[4] = {dv.x, dv.y, dv.z, dv.w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const float2 x = unpack2<F16>(o2[j]);
+                const float2 xr = unpack2<F16>(r2[j]);
                 const float2 y = unpack2<F16>(d2[j]);
-                acc = fmaf(x.x, y.x, acc);
-                acc = fmaf(x.y, y.y, acc);
+                acc = fmaf(x.x + xr.x, y.x, acc);
+                acc = fmaf(x.y + xr.y, y.y, acc);
+            }
+            mq = fmaxf(mq, amax8<F16>(qv));
+            mdo = fmaxf(mdo, amax8<F16>(dv));
+            if (kv_head) {
+                const int64_t krow = act_row(h, t, T, a.hkv, a.token_major);
+                mk = fmaxf(mk, amax8<F16>(__ldg((const uint4*)(a.k + krow * D) + sub)));
+                mv = fmaxf(mv, amax8<F16>(__ldg((const uint4*)(a.v + krow * D) + sub)));
             }
         }
 #pragma unroll
         for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
         if (valid) {
-            if (sub == 0) delta[(int64_t)h * T + t] = acc;
-            float4* z = (float4*)(dq_acc + act_row(h, t, T, H, dq_token_major) * D) + 2 * sub;
+            if (sub == 0) a.delta[(int64_t)h * T + t] = acc;
+            float4* z = (float4*)(a.dq_acc + ((int64_t)h * T + t) * D) + 2 * sub;
             z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
             z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
     }
+    const int g = h / a.group;
+    block_amax(mq, a.amax + kAmaxQ * a.hkv + g, red);
+    block_amax(mdo, a.amax + kAmaxDO * a.hkv + g, red);
+    if (kv_head) {   // uniform over the CTA
+        block_amax(mk, a.amax + kAmaxK * a.hkv + h, red);
+        block_amax(mv, a.amax + kAmaxV * a.hkv + h, red);
+    }
 }
 
-// fp32 head-major accumulator -> 16-bit dq (head-major or token-major); D4 (= D / 4, a
-// power of two) threads per row, 4 elements each
-template <int D4, bool F16>
-__global__ void __launch_bounds__(256) dq_convert_kernel(const float4* __restrict__ src, uint2* __restrict__ dst,
-                                                         int64_t T, int H, int token_major) {
+// The fp16 operand copies: tensor blockIdx.z (q, k, v, dO), head blockIdx.y, scaled by
+// 2^range_exponent(amax of its key/value group) and written head-major. 8 elements per thread.
+template <int D, bool F16>
+__global__ void __launch_bounds__(256) bwd_convert_kernel(const BwdConvertArgs a) {
+    constexpr int TPR = D / 8;
+    pdl_wait();   // amax is final once the stats kernel has completed
+    pdl_trigger();
+    const int tz = blockIdx.z;
+    const bool kv = tz == kAmaxK || tz == kAmaxV;
+    const int H = kv ? a.hkv : a.hq;
+    const int h = blockIdx.y;
+    if (h >= H) return;
+    const int g = kv ? h : h / a.group;
+    const float sc = exp2i(range_exponent(__ldg(a.amax + tz * a.hkv + g)));
+    // constant indices keep the parameter arrays out of local memory
+    const uint16_t* src = tz == 0 ? a.src[0] : tz == 1 ? a.src[1] : tz == 2 ? a.src[2] : a.src[3];
+    uint16_t* dst = (tz == 0 ? a.dst[0] : tz == 1 ? a.dst[1] : tz == 2 ? a.dst[2] : a.dst[3]) + (int64_t)h * a.T * D;
+    const int sub = threadIdx.x % TPR;
+    constexpr int64_t kRowsPerCta = 256 / TPR;
+    for (int64_t t = (int64_t)blockIdx.x * kRowsPerCta + threadIdx.x / TPR; t < a.T;
+         t += (int64_t)gridDim.x * kRowsPerCta) {
+        const uint4 x = __ldg((const uint4*)(src + act_row(h, t, a.T, H, a.token_major) * D) + sub);
+        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+        uint32_t r[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float2 f = unpack2<F16>(w[j]);
+            r[j] = pack2<true>(f.x * sc, f.y * sc);
+        }
+        ((uint4*)(dst + t * D))[sub] = make_uint4(r[0], r[1], r[2], r[3]);
+    }
+}
+
+// The head-major fp32 accumulator, which holds dQ' = dQ 2^(ev+edo+ds_exp+ek) of each head's
+// key/value group, scaled back and written as dq (bf16, fp16 or fp32; head-major or
+// token-major). D4 (= D / 4, a power of two) threads per row, 4 elements each.
+struct DqConvertArgs {
+    const float4* src;
+    void* dst;
+    const uint32_t* amax;
+    int64_t T;
+    int H, hkv, group, token_major, out_dt, ds_exp;
+};
+template <int D4>
+__global__ void __launch_bounds__(256) dq_convert_kernel(const DqConvertArgs a) {
     pdl_wait();   // the accumulator is final once the backward kernel has completed
     const int h = blockIdx.y;
-    const float4* s_head = src + (int64_t)h * T * D4;
-    const int64_t n = T * D4;
+    const int g = h / a.group;
+    const int ek = range_exponent(__ldg(a.amax + kAmaxK * a.hkv + g));
+    const int ev = range_exponent(__ldg(a.amax + kAmaxV * a.hkv + g));
+    const int edo = range_exponent(__ldg(a.amax + kAmaxDO * a.hkv + g));
+    const float un = exp2i(-(ev + edo + a.ds_exp + ek));   // exact power of two
+    const float4* s_head = a.src + (int64_t)h * a.T * D4;
+    const int64_t n = a.T * D4;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t t = i / D4;
         const int c = (int)(i % D4);
         const float4 v = s_head[i];
-        dst[act_row(h, t, T, H, token_major) * D4 + c] = make_uint2(pack2<F16>(v.x, v.y), pack2<F16>(v.z, v.w));
+        const int64_t o = act_row(h, t, a.T, a.H, a.token_major) * D4 + c;
+        if (a.out_dt == USP_FP32)
+            ((float4*)a.dst)[o] = make_float4(v.x * un, v.y * un, v.z * un, v.w * un);
+        else if (a.out_dt == USP_FP16)
+            ((uint2*)a.dst)[o] = make_uint2(pack2<true>(v.x * un, v.y * un), pack2<true>(v.z * un, v.w * un));
+        else
+            ((uint2*)a.dst)[o] = make_uint2(pack2<false>(v.x * un, v.y * un), pack2<false>(v.z * un, v.w * un));
     }
 }
 
@@ -723,18 +863,18 @@ __global__ void debug_timeout_kernel(WsHeader* hdr, uint64_t limit_ns) {
     }
 }
 
-template <int D, bool F16>
+template <int D>
 cudaError_t launch_bwd_impl(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& dout,
                             const CUtensorMap& dq, const CUtensorMap& dk, const CUtensorMap& dv, const BwdArgs& a,
                             int grid, cudaStream_t s) {
     using L = BwdSmem<D>;
     // persistent CTAs, one per SM (the shared-memory footprint allows no more)
     int sms = 0;
-    const cudaError_t e = persistent_setup(attn_bwd_kernel<D, F16>, (size_t)L::kAlloc, &sms);
+    const cudaError_t e = persistent_setup<attn_bwd_kernel<D, true>>((size_t)L::kAlloc, &sms);
     if (e != cudaSuccess) return e;
     if (grid > sms) grid = sms;
-    return launch_kernel(attn_bwd_kernel<D, F16>, dim3(grid), dim3(kBwdThreads), (size_t)L::kAlloc, s, true, q, k, v,
-                         dout, dq, dk, dv, a);
+    return launch_kernel(attn_bwd_kernel<D, true>, dim3(grid), dim3(kBwdThreads), (size_t)L::kAlloc, s, true, q, k,
+                         v, dout, dq, dk, dv, a);
 }
 
 // CTAs for `work_items` units at `per_cta` units each, capped so that all `ys` rows of the
@@ -750,44 +890,51 @@ int grid_for(int64_t work_items, int per_cta, int ys = 1) {
 
 }  // namespace
 
+int ds_exponent(int head_dim, float scale) {
+    // bound on |dS| for operands below 16: 2 * D * 16 * 16 * scale
+    const double bound = 512.0 * (double)head_dim * (double)scale;
+    int e = (int)std::floor(std::log2(32768.0 / bound));
+    return e < -24 ? -24 : (e > 24 ? 24 : e);
+}
+
 cudaError_t launch_attn_bwd(int head_dim, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                             const CUtensorMap& dout, const CUtensorMap& dq, const CUtensorMap& dk, const CUtensorMap& dv,
                             const BwdArgs& a, int grid, cudaStream_t s) {
-    if (a.f16) {
-        if (head_dim == 128) return launch_bwd_impl<128, true>(q, k, v, dout, dq, dk, dv, a, grid, s);
-        return launch_bwd_impl<64, true>(q, k, v, dout, dq, dk, dv, a, grid, s);
-    }
-    if (head_dim == 128) return launch_bwd_impl<128, false>(q, k, v, dout, dq, dk, dv, a, grid, s);
-    return launch_bwd_impl<64, false>(q, k, v, dout, dq, dk, dv, a, grid, s);
+    if (head_dim == 128) return launch_bwd_impl<128>(q, k, v, dout, dq, dk, dv, a, grid, s);
+    return launch_bwd_impl<64>(q, k, v, dout, dq, dk, dv, a, grid, s);
 }
 
-cudaError_t launch_bwd_prep(const void* o, const void* dout, float* delta, float* dq_acc, int64_t T, int hq,
-                            int head_dim, int token_major, int dq_token_major, int f16, cudaStream_t s) {
+cudaError_t launch_bwd_stats(int head_dim, const BwdStatsArgs& a, cudaStream_t s) {
     const int tpr = head_dim / 8;
-    const dim3 grid(grid_for(T, 256 / tpr, hq), hq);
-    const uint16_t* o16 = (const uint16_t*)o;
-    const uint16_t* d16 = (const uint16_t*)dout;
-    if (head_dim == 128 && f16)
-        bwd_prep_kernel<128, true><<<grid, 256, 0, s>>>(o16, d16, delta, dq_acc, T, hq, token_major, dq_token_major);
+    const dim3 grid(grid_for(a.T, 256 / tpr, a.hq), a.hq);
+    if (head_dim == 128 && a.f16)
+        bwd_stats_kernel<128, true><<<grid, 256, 0, s>>>(a);
     else if (head_dim == 128)
-        bwd_prep_kernel<128, false><<<grid, 256, 0, s>>>(o16, d16, delta, dq_acc, T, hq, token_major, dq_token_major);
-    else if (f16)
-        bwd_prep_kernel<64, true><<<grid, 256, 0, s>>>(o16, d16, delta, dq_acc, T, hq, token_major, dq_token_major);
+        bwd_stats_kernel<128, false><<<grid, 256, 0, s>>>(a);
+    else if (a.f16)
+        bwd_stats_kernel<64, true><<<grid, 256, 0, s>>>(a);
     else
-        bwd_prep_kernel<64, false><<<grid, 256, 0, s>>>(o16, d16, delta, dq_acc, T, hq, token_major, dq_token_major);
+        bwd_stats_kernel<64, false><<<grid, 256, 0, s>>>(a);
     return cudaGetLastError();
 }
 
-cudaError_t launch_dq_convert(const float* dq_acc, void* dq, int64_t T, int hq, int head_dim, int token_major,
-                              int f16, cudaStream_t s) {
+cudaError_t launch_bwd_convert(int head_dim, const BwdConvertArgs& a, cudaStream_t s) {
+    const int tpr = head_dim / 8;
+    const int hmax = a.hq > a.hkv ? a.hq : a.hkv;
+    const dim3 grid(grid_for(a.T, 256 / tpr, 2 * a.hq + 2 * a.hkv), hmax, 4);
+    auto kernel = head_dim == 128 ? (a.f16 ? bwd_convert_kernel<128, true> : bwd_convert_kernel<128, false>)
+                                  : (a.f16 ? bwd_convert_kernel<64, true> : bwd_convert_kernel<64, false>);
+    return launch_kernel(kernel, grid, dim3(256), 0, s, true, a);
+}
+
+cudaError_t launch_dq_convert(const float* dq_acc, void* dq, const uint32_t* amax, int64_t T, int hq, int hkv,
+                              int head_dim, int token_major, int out_dt, int ds_exp, cudaStream_t s) {
     const int D4 = head_dim / 4;
     const dim3 grid(grid_for(T * D4, 256, hq), hq);
-    const float4* src = (const float4*)dq_acc;
-    uint2* dst = (uint2*)dq;
+    DqConvertArgs a{(const float4*)dq_acc, dq, amax, T, hq, hkv, hq / hkv, token_major, out_dt, ds_exp};
     // launched right after the backward kernel, whose completion it waits for on the device
-    auto kernel = D4 == 32 ? (f16 ? dq_convert_kernel<32, true> : dq_convert_kernel<32, false>)
-                           : (f16 ? dq_convert_kernel<16, true> : dq_convert_kernel<16, false>);
-    return launch_kernel(kernel, grid, dim3(256), 0, s, true, src, dst, T, hq, token_major);
+    auto kernel = D4 == 32 ? dq_convert_kernel<32> : dq_convert_kernel<16>;
+    return launch_kernel(kernel, grid, dim3(256), 0, s, true, a);
 }
 
 cudaError_t launch_debug_timeout(WsHeader* hdr, uint64_t limit_ns, cudaStream_t s) {

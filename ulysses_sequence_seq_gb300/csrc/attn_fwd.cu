@@ -15,7 +15,9 @@
 //   warp  9    MMA issuer (one thread) and TMEM owner
 // Tensor memory (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [384,384+D).
 // A whole output tile leaves through a 64-column shared-memory panel of its own, one TMA
-// store per 64 columns; a sample's ragged last tile is written row by row.
+// store per 64 columns; a sample's ragged last tile is written row by row. On request the
+// rounding residual of O (the fp32 result minus its 16-bit rounding) leaves the same way,
+// so that the backward can take Delta = dO . O from O to about 16 significant bits.
 // P (bf16 or fp16, the input type) overwrites the first 64 columns of its S tile and feeds the P.V MMA
 // straight from TMEM. The two tiles ping-pong: while one softmax group works on
 // its S, the tensor core runs the other tile's P.V and next Q.K^T.
@@ -102,7 +104,8 @@ __device__ __forceinline__ bool fwd_read_item(uint64_t* item_bars, volatile int*
 template <int D, bool F16>
 __global__ void __maxnreg__(kLaunchRegs)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO, const FwdArgs a) {
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                    const __grid_constant__ CUtensorMap tmOres, const FwdArgs a) {
     using L = FwdSmem<D>;
     pdl_wait();   // the work list and the header come from the scheduler launched just before
     const int count = a.hdr->fwd_count;
@@ -475,26 +478,72 @@ __global__ void __maxnreg__(kLaunchRegs)
                     }
                     named_bar_sync(1 + t, 128);
                 }
+                if (a.o_res) {
+                    // The rounding residual O - round16(O) in two more rounds through the same
+                    // panel, reading O from TMEM again: it stays there until this group's next
+                    // P.V, which the MMA thread issues only after the group's next P.
+#pragma unroll 1
+                    for (int round = 0; round < D / 64; ++round) {
+#pragma unroll
+                        for (int c = 0; c < 2; ++c) {
+                            uint32_t o[32];
+                            tmem_ld32(tO + round * 64 + 32 * c, o);
+                            tmem_ld_wait(o);
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                uint32_t r4[4];
+#pragma unroll
+                                for (int u = 0; u < 4; ++u) {
+                                    const float x0 = __uint_as_float(o[8 * q + 2 * u]) * inv_l;
+                                    const float x1 = __uint_as_float(o[8 * q + 2 * u + 1]) * inv_l;
+                                    const float2 hv = unpack2<F16>(pack2<F16>(x0, x1));
+                                    r4[u] = pack2<F16>(x0 - hv.x, x1 - hv.y);
+                                }
+                                *(uint4*)(stage + sw128_offset(rq, (uint32_t)((32 * c + 8 * q) * 2))) =
+                                    make_uint4(r4[0], r4[1], r4[2], r4[3]);
+                            }
+                        }
+                        fence_proxy_async_smem();
+                        named_bar_sync(1 + t, 128);
+                        if (rq == 0) {
+                            tma_store_rows(&tmOres, stage, round * 64, q0, h, a.token_major);
+                            bulk_commit_group();
+                            bulk_wait_group_read<0>();
+                        }
+                        named_bar_sync(1 + t, 128);
+                    }
+                }
                 a.lse[(int64_t)h * a.T + i] = (m + __log2f(l)) * 0.69314718055994530942f;
             } else if (nbt > 0) {   // a sample's ragged last tile: row by row, rows past the end skipped
                 tc_fence_after();
                 const bool valid = i < e;
                 const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
-                uint16_t* orow = a.o + act_row(h, i, a.T, a.hq, a.token_major) * D;
+                const int64_t orow_off = act_row(h, i, a.T, a.hq, a.token_major) * D;
+                uint16_t* orow = a.o + orow_off;
 #pragma unroll 1
                 for (int c = 0; c < D; c += 32) {
                     uint32_t o[32];
                     tmem_ld32(tO + c, o);
                     tmem_ld_wait(o);
-                    uint32_t pk[16];
+                    uint32_t pk[16], rk[16];
 #pragma unroll
-                    for (int jj = 0; jj < 16; ++jj)
-                        pk[jj] = pack2<F16>(__uint_as_float(o[2 * jj]) * inv_l, __uint_as_float(o[2 * jj + 1]) * inv_l);
+                    for (int jj = 0; jj < 16; ++jj) {
+                        const float x0 = __uint_as_float(o[2 * jj]) * inv_l, x1 = __uint_as_float(o[2 * jj + 1]) * inv_l;
+                        pk[jj] = pack2<F16>(x0, x1);
+                        const float2 hv = unpack2<F16>(pk[jj]);
+                        rk[jj] = pack2<F16>(x0 - hv.x, x1 - hv.y);
+                    }
                     if (valid) {
                         uint4* dst = (uint4*)(orow + c);
 #pragma unroll
                         for (int jj = 0; jj < 4; ++jj)
                             dst[jj] = make_uint4(pk[4 * jj], pk[4 * jj + 1], pk[4 * jj + 2], pk[4 * jj + 3]);
+                        if (a.o_res) {
+                            uint4* rdst = (uint4*)(a.o_res + orow_off + c);
+#pragma unroll
+                            for (int jj = 0; jj < 4; ++jj)
+                                rdst[jj] = make_uint4(rk[4 * jj], rk[4 * jj + 1], rk[4 * jj + 2], rk[4 * jj + 3]);
+                        }
                     }
                 }
                 if (valid) a.lse[(int64_t)h * a.T + i] = (m + __log2f(l)) * 0.69314718055994530942f;
@@ -513,27 +562,28 @@ __global__ void __maxnreg__(kLaunchRegs)
 
 template <int D, bool F16>
 cudaError_t launch_fwd_impl(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& o,
-                            const FwdArgs& a, int grid, cudaStream_t s) {
+                            const CUtensorMap& ores, const FwdArgs& a, int grid, cudaStream_t s) {
     using L = FwdSmem<D>;
     // persistent CTAs, one per SM (the shared-memory footprint allows no more)
     int sms = 0;
-    const cudaError_t e = persistent_setup(attn_fwd_kernel<D, F16>, (size_t)L::kAlloc, &sms);
+    const cudaError_t e = persistent_setup<attn_fwd_kernel<D, F16>>((size_t)L::kAlloc, &sms);
     if (e != cudaSuccess) return e;
     if (grid > sms) grid = sms;
     return launch_kernel(attn_fwd_kernel<D, F16>, dim3(grid), dim3(kFwdThreads), (size_t)L::kAlloc, s, true, q, k, v,
-                         o, a);
+                         o, ores, a);
 }
 
 }  // namespace
 
 cudaError_t launch_attn_fwd(int head_dim, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                            const CUtensorMap& o, const FwdArgs& a, int grid, cudaStream_t s) {
+                            const CUtensorMap& o, const CUtensorMap& o_res, const FwdArgs& a, int grid,
+                            cudaStream_t s) {
     if (a.f16) {
-        if (head_dim == 128) return launch_fwd_impl<128, true>(q, k, v, o, a, grid, s);
-        return launch_fwd_impl<64, true>(q, k, v, o, a, grid, s);
+        if (head_dim == 128) return launch_fwd_impl<128, true>(q, k, v, o, o_res, a, grid, s);
+        return launch_fwd_impl<64, true>(q, k, v, o, o_res, a, grid, s);
     }
-    if (head_dim == 128) return launch_fwd_impl<128, false>(q, k, v, o, a, grid, s);
-    return launch_fwd_impl<64, false>(q, k, v, o, a, grid, s);
+    if (head_dim == 128) return launch_fwd_impl<128, false>(q, k, v, o, o_res, a, grid, s);
+    return launch_fwd_impl<64, false>(q, k, v, o, o_res, a, grid, s);
 }
 
 }  // namespace usp

@@ -41,6 +41,8 @@ struct WorkItem {
 //   items            WorkItem[max_items]
 //   delta            fp32[hq][T]       backward only: Delta_i = dO_i . O_i
 //   dq_acc           fp32[hq][T][D]    backward only: dQ accumulator
+//   amax             u32[4][hkv]       backward only: largest |q|, |k|, |v|, |dO| per key/value group
+//   q16, k16, v16, do16                backward only: scaled fp16 operand copies, head-major
 struct WsHeader {
     int status;
     int fwd_count;
@@ -51,7 +53,7 @@ struct WsHeader {
 };
 
 struct WsLayout {
-    size_t hist, prefix, sbase, items, delta, dq_acc, total;
+    size_t hist, prefix, sbase, items, delta, dq_acc, amax, q16, k16, v16, do16, total;
     int hist_len;
     int max_items;
 };
@@ -104,6 +106,17 @@ inline WsLayout ws_layout(int64_t T, int num_seqs, int hq, int hkv, int D, int b
     if (bwd) off = align256(off + sizeof(float) * (size_t)hq * (size_t)T);
     w.dq_acc = off;
     if (bwd) off = align256(off + sizeof(float) * (size_t)hq * (size_t)T * (size_t)D);
+    const size_t qbytes = 2 * (size_t)hq * (size_t)T * (size_t)D, kvbytes = 2 * (size_t)hkv * (size_t)T * (size_t)D;
+    w.amax = off;
+    if (bwd) off = align256(off + sizeof(uint32_t) * 4 * (size_t)hkv);
+    w.q16 = off;
+    if (bwd) off = align256(off + qbytes);
+    w.k16 = off;
+    if (bwd) off = align256(off + kvbytes);
+    w.v16 = off;
+    if (bwd) off = align256(off + kvbytes);
+    w.do16 = off;
+    if (bwd) off = align256(off + qbytes);
     w.total = off;
     return w;
 }
@@ -125,12 +138,12 @@ inline int device_sm_count() {
     return sms[dev];
 }
 
-// One-time set-up of a persistent kernel on the current device: raises its dynamic shared-
-// memory limit to `smem` (once per device and kernel, under a lock, so concurrent first calls
-// from several host threads and calls on several devices of one process are safe) and
-// returns the device's SM count in *sms.
-template <typename... KArgs>
-cudaError_t persistent_setup(void (*kernel)(KArgs...), size_t smem, int* sms) {
+// One-time set-up of a persistent kernel on the current device: raises the dynamic shared-
+// memory limit of `Kernel` to `smem` (once per device and kernel -- the flags are per template
+// instance, so per kernel -- under a lock, so concurrent first calls from several host threads
+// and calls on several devices of one process are safe) and returns the device's SM count in *sms.
+template <auto Kernel>
+cudaError_t persistent_setup(size_t smem, int* sms) {
     static std::mutex mu;
     static bool done[kMaxDevices] = {};
     int dev = 0;
@@ -140,7 +153,7 @@ cudaError_t persistent_setup(void (*kernel)(KArgs...), size_t smem, int* sms) {
     {
         std::lock_guard<std::mutex> lock(mu);
         if (!done[dev]) {
-            e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             if (e != cudaSuccess) return e;
             done[dev] = true;
         }

@@ -104,7 +104,7 @@ extern "C" usp_status usp_attn_fwd_varlen_noalloc(const void* q, const void* k, 
     sa.items = (WorkItem*)(ws + w.items);
     if (launch_schedule(sa, s, false) != cudaSuccess) return USP_ERR_CUDA;
 
-    CUtensorMap mq, mk, mv, mo;
+    CUtensorMap mq, mk, mv, mo;   // o doubles as the (unused) residual map: fa.o_res is NULL
     if (!make_activation_map(&mq, q, total_tokens, hq, head_dim, 0) ||
         !make_activation_map(&mk, k, total_tokens, hkv, head_dim, 0) ||
         !make_activation_map(&mv, v, total_tokens, hkv, head_dim, 0) ||
@@ -121,7 +121,7 @@ extern "C" usp_status usp_attn_fwd_varlen_noalloc(const void* q, const void* k, 
     fa.group = hq / hkv;
     fa.causal = sa.causal;
     fa.scale_log2 = resolve_softmax_scale(softmax_scale, head_dim) * 1.4426950408889634f;
-    if (launch_attn_fwd(head_dim, mq, mk, mv, mo, fa, w.max_items, s) != cudaSuccess) return USP_ERR_CUDA;
+    if (launch_attn_fwd(head_dim, mq, mk, mv, mo, mo, fa, w.max_items, s) != cudaSuccess) return USP_ERR_CUDA;
     // device-side outcome (USP_OK, USP_ERR_DEVICE_CHECK or USP_ERR_TIMEOUT) for the caller
     if (status && cudaMemcpyAsync(status, &hdr->status, sizeof(int32_t), cudaMemcpyDeviceToDevice, s) != cudaSuccess)
         return USP_ERR_CUDA;

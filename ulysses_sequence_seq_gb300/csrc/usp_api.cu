@@ -104,7 +104,8 @@ extern "C" size_t usp_attn_workspace_size(int64_t total_tokens, int num_seqs, in
 namespace usp {
 namespace {
 
-usp_status attn_fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* cu_seqlens,
+usp_status attn_fwd_impl(const void* q, const void* k, const void* v, void* o, void* o_res, float* lse,
+                         const int32_t* cu_seqlens,
                          int num_seqs, int64_t total_tokens, int hq, int hkv, int head_dim, float softmax_scale,
                          int causal, void* workspace, size_t ws_bytes, cudaStream_t s, int token_major,
                          usp_dtype dt = USP_BF16) {
@@ -113,7 +114,8 @@ usp_status attn_fwd_impl(const void* q, const void* k, const void* v, void* o, f
     if (dt != USP_BF16 && dt != USP_FP16) return dt == USP_FP32 ? USP_ERR_UNSUPPORTED : USP_ERR_INVALID_ARG;
     if (total_tokens == 0) return reset_status_if_any(workspace, ws_bytes, s);
     if (!q || !k || !v || !o || !lse || !workspace) return USP_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(workspace))
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(workspace) ||
+        !aligned16(o_res))
         return USP_ERR_INVALID_ARG;
     const WsLayout w = ws_layout(total_tokens, num_seqs, hq, hkv, head_dim, 0);
     if (ws_bytes < w.total) return USP_ERR_WORKSPACE;
@@ -138,17 +140,19 @@ usp_status attn_fwd_impl(const void* q, const void* k, const void* v, void* o, f
     sa.items = (WorkItem*)(ws + w.items);
     if (launch_schedule(sa, s, false) != cudaSuccess) return USP_ERR_CUDA;
 
-    CUtensorMap mq, mk, mv, mo;
+    CUtensorMap mq, mk, mv, mo, mores;
     if (!make_activation_map(&mq, q, total_tokens, hq, head_dim, token_major) ||
         !make_activation_map(&mk, k, total_tokens, hkv, head_dim, token_major) ||
         !make_activation_map(&mv, v, total_tokens, hkv, head_dim, token_major) ||
-        !make_activation_map(&mo, o, total_tokens, hq, head_dim, token_major))
+        !make_activation_map(&mo, o, total_tokens, hq, head_dim, token_major) ||
+        !make_activation_map(&mores, o_res ? o_res : o, total_tokens, hq, head_dim, token_major))
         return USP_ERR_CUDA;
     FwdArgs fa{};
     fa.cu = cu_seqlens;
     fa.items = sa.items;
     fa.hdr = hdr;
     fa.o = (uint16_t*)o;
+    fa.o_res = (uint16_t*)o_res;
     fa.f16 = dt == USP_FP16 ? 1 : 0;
     fa.lse = lse;
     fa.T = total_tokens;
@@ -157,15 +161,15 @@ usp_status attn_fwd_impl(const void* q, const void* k, const void* v, void* o, f
     fa.causal = sa.causal;
     fa.token_major = token_major;
     fa.scale_log2 = resolve_softmax_scale(softmax_scale, head_dim) * 1.4426950408889634f;
-    if (launch_attn_fwd(head_dim, mq, mk, mv, mo, fa, w.max_items, s) != cudaSuccess) return USP_ERR_CUDA;
+    if (launch_attn_fwd(head_dim, mq, mk, mv, mo, mores, fa, w.max_items, s) != cudaSuccess) return USP_ERR_CUDA;
     return USP_OK;
 }
 
-usp_status attn_bwd_impl(const void* q, const void* k, const void* v, const void* o, const float* lse,
-                         const void* d_o, void* dq, void* dk, void* dv, usp_dtype grad_dt, const int32_t* cu_seqlens,
-                         int num_seqs, int64_t total_tokens, int hq, int hkv, int head_dim, float softmax_scale,
-                         int causal, void* workspace, size_t ws_bytes, cudaStream_t s, int token_major,
-                         usp_dtype dt = USP_BF16) {
+usp_status attn_bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* o_res,
+                         const float* lse, const void* d_o, void* dq, void* dk, void* dv, usp_dtype grad_dt,
+                         const int32_t* cu_seqlens, int num_seqs, int64_t total_tokens, int hq, int hkv, int head_dim,
+                         float softmax_scale, int causal, void* workspace, size_t ws_bytes, cudaStream_t s,
+                         int token_major, usp_dtype dt = USP_BF16) {
     usp_status st = check_attn_sizes(total_tokens, num_seqs, hq, hkv, head_dim, cu_seqlens);
     if (st != USP_OK) return st;
     if (dt != USP_BF16 && dt != USP_FP16) return dt == USP_FP32 ? USP_ERR_UNSUPPORTED : USP_ERR_INVALID_ARG;
@@ -175,7 +179,7 @@ usp_status attn_bwd_impl(const void* q, const void* k, const void* v, const void
     if (total_tokens == 0) return reset_status_if_any(workspace, ws_bytes, s);
     if (!q || !k || !v || !o || !lse || !d_o || !dq || !dk || !dv || !workspace) return USP_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(d_o) ||
-        !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace))
+        !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace) || !aligned16(o_res))
         return USP_ERR_INVALID_ARG;
     const WsLayout w = ws_layout(total_tokens, num_seqs, hq, hkv, head_dim, 1);
     if (ws_bytes < w.total) return USP_ERR_WORKSPACE;
@@ -183,15 +187,53 @@ usp_status attn_bwd_impl(const void* q, const void* k, const void* v, const void
     WsHeader* hdr = (WsHeader*)ws;   // written by the scheduler: status, item count, item counter
     const bool fp32_grads = grad_dt == USP_FP32;
     float* delta = (float*)(ws + w.delta);
-    // fp32 gradients accumulate straight into the caller's dq (in its layout); bf16 ones go
-    // through the head-major workspace accumulator and a final conversion.
-    float* dq_acc = fp32_grads ? (float*)dq : (float*)(ws + w.dq_acc);
-    const int dq_token_major = fp32_grads ? token_major : 0;
-
+    // dQ' accumulates in the head-major workspace accumulator; a final pass scales it back
+    // and writes dq in grad_dt and the caller's layout
+    float* dq_acc = (float*)(ws + w.dq_acc);
     const int f16 = dt == USP_FP16 ? 1 : 0;
-    if (launch_bwd_prep(o, d_o, delta, dq_acc, total_tokens, hq, head_dim, token_major, dq_token_major, f16, s) !=
-        cudaSuccess)
-        return USP_ERR_CUDA;
+    uint32_t* amax = (uint32_t*)(ws + w.amax);
+    uint16_t* q16 = (uint16_t*)(ws + w.q16);
+    uint16_t* k16 = (uint16_t*)(ws + w.k16);
+    uint16_t* v16 = (uint16_t*)(ws + w.v16);
+    uint16_t* do16 = (uint16_t*)(ws + w.do16);
+
+    // Delta, the zeroed dQ accumulator and the per-group magnitudes; then the scaled fp16
+    // operand copies; the scheduler runs alongside them
+    if (cudaMemsetAsync(amax, 0, sizeof(uint32_t) * 4 * (size_t)hkv, s) != cudaSuccess) return USP_ERR_CUDA;
+    BwdStatsArgs sta{};
+    sta.q = (const uint16_t*)q;
+    sta.k = (const uint16_t*)k;
+    sta.v = (const uint16_t*)v;
+    sta.o = (const uint16_t*)o;
+    sta.o_res = (const uint16_t*)o_res;
+    sta.dout = (const uint16_t*)d_o;
+    sta.delta = delta;
+    sta.dq_acc = dq_acc;
+    sta.amax = amax;
+    sta.T = total_tokens;
+    sta.hq = hq;
+    sta.hkv = hkv;
+    sta.group = hq / hkv;
+    sta.token_major = token_major;
+    sta.f16 = f16;
+    if (launch_bwd_stats(head_dim, sta, s) != cudaSuccess) return USP_ERR_CUDA;
+    BwdConvertArgs cva{};
+    cva.src[kAmaxQ] = (const uint16_t*)q;
+    cva.src[kAmaxK] = (const uint16_t*)k;
+    cva.src[kAmaxV] = (const uint16_t*)v;
+    cva.src[kAmaxDO] = (const uint16_t*)d_o;
+    cva.dst[kAmaxQ] = q16;
+    cva.dst[kAmaxK] = k16;
+    cva.dst[kAmaxV] = v16;
+    cva.dst[kAmaxDO] = do16;
+    cva.amax = amax;
+    cva.T = total_tokens;
+    cva.hq = hq;
+    cva.hkv = hkv;
+    cva.group = hq / hkv;
+    cva.token_major = token_major;
+    cva.f16 = f16;
+    if (launch_bwd_convert(head_dim, cva, s) != cudaSuccess) return USP_ERR_CUDA;
 
     SchedArgs sa{};
     sa.cu = cu_seqlens;
@@ -212,11 +254,11 @@ usp_status attn_bwd_impl(const void* q, const void* k, const void* v, const void
     if (launch_schedule(sa, s, true) != cudaSuccess) return USP_ERR_CUDA;
 
     CUtensorMap mq, mk, mv, mdo, mdq, mdk, mdv;
-    if (!make_activation_map(&mq, q, total_tokens, hq, head_dim, token_major) ||
-        !make_activation_map(&mk, k, total_tokens, hkv, head_dim, token_major) ||
-        !make_activation_map(&mv, v, total_tokens, hkv, head_dim, token_major) ||
-        !make_activation_map(&mdo, d_o, total_tokens, hq, head_dim, token_major) ||
-        !make_dq_accum_map(&mdq, dq_acc, total_tokens, hq, head_dim, dq_token_major))
+    if (!make_activation_map(&mq, q16, total_tokens, hq, head_dim, 0) ||
+        !make_activation_map(&mk, k16, total_tokens, hkv, head_dim, 0) ||
+        !make_activation_map(&mv, v16, total_tokens, hkv, head_dim, 0) ||
+        !make_activation_map(&mdo, do16, total_tokens, hq, head_dim, 0) ||
+        !make_dq_accum_map(&mdq, dq_acc, total_tokens, hq, head_dim, 0))
         return USP_ERR_CUDA;
     // 16-bit dK/dV leave as whole tiles through these maps; fp32 gradients are stored by rows
     if (fp32_grads) {
@@ -232,24 +274,25 @@ usp_status attn_bwd_impl(const void* q, const void* k, const void* v, const void
     ba.hdr = hdr;
     ba.lse = lse;
     ba.delta = delta;
+    ba.amax = amax;
     ba.dq_acc = dq_acc;
     ba.dk = dk;
     ba.dv = dv;
     ba.grad_fp32 = fp32_grads ? 1 : 0;
-    ba.f16 = f16;
+    ba.out_f16 = f16;
     ba.T = total_tokens;
     ba.hq = hq;
     ba.hkv = hkv;
     ba.token_major = token_major;
-    ba.dq_token_major = dq_token_major;
     ba.group = hq / hkv;
     ba.causal = sa.causal;
     ba.scale = resolve_softmax_scale(softmax_scale, head_dim);
     ba.scale_log2 = ba.scale * 1.4426950408889634f;
+    ba.ds_exp = ds_exponent(head_dim, ba.scale);
     if (launch_attn_bwd(head_dim, mq, mk, mv, mdo, mdq, mdk, mdv, ba, w.max_items, s) != cudaSuccess)
         return USP_ERR_CUDA;
-    if (!fp32_grads &&
-        launch_dq_convert(dq_acc, dq, total_tokens, hq, head_dim, token_major, f16, s) != cudaSuccess)
+    if (launch_dq_convert(dq_acc, dq, amax, total_tokens, hq, hkv, head_dim, token_major, (int)grad_dt, ba.ds_exp,
+                          s) != cudaSuccess)
         return USP_ERR_CUDA;
     return USP_OK;
 }
@@ -268,43 +311,43 @@ usp_status check_sp(int sp, int64_t total_tokens, int hq, int hkv) {
 }  // namespace
 }  // namespace usp
 
-extern "C" usp_status usp_attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
-                                          const int32_t* cu_seqlens, int num_seqs, int64_t total_tokens, int hq,
-                                          int hkv, int head_dim, float softmax_scale, int causal, void* workspace,
-                                          size_t ws_bytes, void* stream) {
-    return attn_fwd_impl(q, k, v, o, lse, cu_seqlens, num_seqs, total_tokens, hq, hkv, head_dim, softmax_scale,
+extern "C" usp_status usp_attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, void* o_res,
+                                          float* lse, const int32_t* cu_seqlens, int num_seqs, int64_t total_tokens,
+                                          int hq, int hkv, int head_dim, float softmax_scale, int causal,
+                                          void* workspace, size_t ws_bytes, void* stream) {
+    return attn_fwd_impl(q, k, v, o, o_res, lse, cu_seqlens, num_seqs, total_tokens, hq, hkv, head_dim, softmax_scale,
                          causal, workspace, ws_bytes, (cudaStream_t)stream, 0);
 }
 
 extern "C" usp_status usp_attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
-                                          const float* lse, const void* d_o, void* dq, void* dk, void* dv,
-                                          usp_dtype grad_dt, const int32_t* cu_seqlens, int num_seqs,
+                                          const void* o_res, const float* lse, const void* d_o, void* dq, void* dk,
+                                          void* dv, usp_dtype grad_dt, const int32_t* cu_seqlens, int num_seqs,
                                           int64_t total_tokens, int hq, int hkv, int head_dim, float softmax_scale,
                                           int causal, void* workspace, size_t ws_bytes, void* stream) {
-    return attn_bwd_impl(q, k, v, o, lse, d_o, dq, dk, dv, grad_dt, cu_seqlens, num_seqs, total_tokens, hq, hkv,
-                         head_dim, softmax_scale, causal, workspace, ws_bytes, (cudaStream_t)stream, 0);
+    return attn_bwd_impl(q, k, v, o, o_res, lse, d_o, dq, dk, dv, grad_dt, cu_seqlens, num_seqs, total_tokens, hq,
+                         hkv, head_dim, softmax_scale, causal, workspace, ws_bytes, (cudaStream_t)stream, 0);
 }
 
-extern "C" usp_status usp_ulysses_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
-                                           const int32_t* cu_seqlens, int num_seqs, int64_t total_tokens, int sp,
-                                           int hq, int hkv, int head_dim, float softmax_scale, int causal,
+extern "C" usp_status usp_ulysses_attn_fwd(const void* q, const void* k, const void* v, void* o, void* o_res,
+                                           float* lse, const int32_t* cu_seqlens, int num_seqs, int64_t total_tokens,
+                                           int sp, int hq, int hkv, int head_dim, float softmax_scale, int causal,
                                            usp_dtype dt, void* workspace, size_t ws_bytes, void* stream) {
     const usp_status st = check_sp(sp, total_tokens, hq, hkv);
     if (st != USP_OK) return st;
-    return attn_fwd_impl(q, k, v, o, lse, cu_seqlens, num_seqs, total_tokens, hq, hkv, head_dim, softmax_scale,
+    return attn_fwd_impl(q, k, v, o, o_res, lse, cu_seqlens, num_seqs, total_tokens, hq, hkv, head_dim, softmax_scale,
                          causal, workspace, ws_bytes, (cudaStream_t)stream, 1, dt);
 }
 
 extern "C" usp_status usp_ulysses_attn_bwd(const void* q, const void* k, const void* v, const void* o,
-                                           const float* lse, const void* d_o, void* dq, void* dk, void* dv,
-                                           usp_dtype grad_dt, const int32_t* cu_seqlens, int num_seqs,
+                                           const void* o_res, const float* lse, const void* d_o, void* dq, void* dk,
+                                           void* dv, usp_dtype grad_dt, const int32_t* cu_seqlens, int num_seqs,
                                            int64_t total_tokens, int sp, int hq, int hkv, int head_dim,
                                            float softmax_scale, int causal, usp_dtype dt, void* workspace,
                                            size_t ws_bytes, void* stream) {
     const usp_status st = check_sp(sp, total_tokens, hq, hkv);
     if (st != USP_OK) return st;
-    return attn_bwd_impl(q, k, v, o, lse, d_o, dq, dk, dv, grad_dt, cu_seqlens, num_seqs, total_tokens, hq, hkv,
-                         head_dim, softmax_scale, causal, workspace, ws_bytes, (cudaStream_t)stream, 1, dt);
+    return attn_bwd_impl(q, k, v, o, o_res, lse, d_o, dq, dk, dv, grad_dt, cu_seqlens, num_seqs, total_tokens, hq,
+                         hkv, head_dim, softmax_scale, causal, workspace, ws_bytes, (cudaStream_t)stream, 1, dt);
 }
 
 extern "C" usp_status usp_get_device_status(const void* workspace, void* stream) {
