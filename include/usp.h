@@ -119,6 +119,42 @@ usp_status usp_head_to_seq_kv_grad(const void* in, void* out, int sp, int64_t to
                                    usp_dtype dt, void* stream);
 
 /*
+ * usp_a2a_pack / usp_a2a_unpack -- the rank-local halves of Ulysses' all-to-all when the
+ * ranks are real processes (one GPU each) and the exchange itself is a collective that
+ * moves equal contiguous blocks (NCCL all-to-all; torch.distributed all_to_all_single).
+ *   Passage: HF Transformers "Ulysses sequence parallelism" guide, opening paragraph and
+ *   layout figure (each rank holds S = T/sp tokens with all heads before attention and
+ *   all tokens of H/sp heads during it); congresoia365 article, "Cómo Funciona Ulysses",
+ *   steps 3 and 5.
+ *   usp_a2a_pack: in [S][heads][head_dim] (this rank's S = shard_tokens tokens) ->
+ *     out [sp][S][nheads][head_dim], block r to be sent to rank r:
+ *       out[r][s][j] = in[s][r*Hl + head0 + j], Hl = heads/sp, 0 <= head0,
+ *       head0 + nheads <= Hl (a chunk of every rank's heads, so that the exchange of one
+ *       chunk can overlap attention on another).
+ *     After the collective the receive buffer [sp][S][nheads][D] is the token-major
+ *     [T][nheads][D] layout the fused attention calls read (usp_ulysses_attn_fwd with
+ *     sp = 1), and their token-major outputs go back as they are (block r' = the tokens
+ *     of rank r').
+ *   usp_a2a_unpack: in [sp][S][nheads][head_dim] received (block r from rank r) ->
+ *     out [S][heads][head_dim]: out[s][r*Hl + head0 + j] = in[r][s][j]; heads outside the
+ *     chunk are left untouched.
+ *   Fewer key/value heads than ranks (heads < sp, sp % heads == 0; head0 = 0,
+ *     nheads = 1): pack sends each rank the one head its query heads read,
+ *     out[r][s][0] = in[s][r*heads/sp]; unpack receives the replicas' gradients and
+ *     writes out[s][g] = the fp32 sum of in[r][s][0] over the sp/heads ranks r with
+ *     r*heads/sp = g, in rank order, rounded once (dt USP_BF16 or USP_FP32).
+ *   The copies move bits (dt fixes the element size) except for the replica sums.
+ * Errors: USP_ERR_INVALID_ARG (NULL or misaligned pointer, overlapping buffers, sp < 1,
+ *   shard_tokens < 0, heads neither dividing over sp nor dividing it, a head chunk
+ *   outside the rank's heads); USP_ERR_UNSUPPORTED (a row not a multiple of 16 bytes,
+ *   an fp16 replica sum). shard_tokens == 0 is a no-op.
+ */
+usp_status usp_a2a_pack(const void* in, void* out, int sp, int64_t shard_tokens, int heads, int head_dim,
+                        int head0, int nheads, usp_dtype dt, void* stream);
+usp_status usp_a2a_unpack(const void* in, void* out, int sp, int64_t shard_tokens, int heads, int head_dim,
+                          int head0, int nheads, usp_dtype dt, void* stream);
+
+/*
  * usp_attn_workspace_size -- bytes of workspace the attention calls need for
  * these sizes (bwd != 0: for usp_attn_bwd_varlen, which also needs per-row
  * Delta, an fp32 dQ accumulator and the fp16 copies of q, k, v and d_o). The workspace holds

@@ -101,3 +101,68 @@ def head_to_seq_kv_grad(y: np.ndarray, sp: int, hkv: int) -> np.ndarray:
     for r in range(y.shape[0]):
         out[:, r // rep, :] += y[r].astype(np.float64)
     return out
+
+
+# ------------------------------------------------------------------ the exchange between real ranks
+def _rank_heads(H: int, sp: int, head0: int, nheads):
+    """(per-rank heads Hl, chunk size nh, replication) of a rank-local exchange step."""
+    if H % sp == 0:
+        Hl = H // sp
+        nh = Hl - head0 if nheads is None else nheads
+        if head0 < 0 or nh < 1 or head0 + nh > Hl:
+            raise ValueError("head chunk outside the rank's heads")
+        return Hl, nh, 1
+    rep = kv_replication(sp, H)
+    if head0 != 0 or (nheads not in (None, 1)):
+        raise ValueError("replicated heads move whole")
+    return 1, 1, rep
+
+
+def a2a_pack(x_shard: np.ndarray, sp: int, head0: int = 0, nheads=None) -> np.ndarray:
+    """What one rank sends in the sequence -> heads all-to-all, one block per destination.
+
+    x_shard: [S][H][D] bits, this rank's S tokens with all heads. Returns [sp][S][nh][D]
+    whose block r goes to rank r: the rank's tokens of rank r's heads r*Hl + head0 + j
+    (j < nh); with fewer heads than ranks, the one head rank r reads, r*H // sp.
+    """
+    S, H, D = x_shard.shape
+    Hl, nh, rep = _rank_heads(H, sp, head0, nheads)
+    out = np.empty((sp, S, nh, D), dtype=x_shard.dtype)
+    for r in range(sp):
+        for j in range(nh):
+            h = r * H // sp if rep > 1 else r * Hl + head0 + j
+            out[r, :, j, :] = x_shard[:, h, :]
+    return out
+
+
+def exchange_blocks(sends):
+    """The all-to-all itself over ranks given as a list: rank r receives, in rank order,
+    block r of every rank's send buffer (recv_r[r'] = send_{r'}[r])."""
+    sp = len(sends)
+    return [np.stack([sends[src][r] for src in range(sp)]) for r in range(sp)]
+
+
+def a2a_unpack(recv: np.ndarray, sp: int, H: int, head0: int = 0, nheads=None, out=None) -> np.ndarray:
+    """What one rank does with what it receives in the heads -> sequence all-to-all.
+
+    recv: [sp][S][nh][D], block r from rank r: this rank's tokens of rank r's heads.
+    Writes out[s][r*Hl + head0 + j] = recv[r][s][j] into `out` ([S][H][D], created when
+    None). With fewer heads than ranks the blocks are gradients of replicas of one head
+    (rank r's is head r*H // sp) and are summed (float64 result).
+    """
+    _, S, nh_in, D = recv.shape
+    Hl, nh, rep = _rank_heads(H, sp, head0, nheads)
+    if nh_in != nh:
+        raise ValueError("received blocks do not match the head chunk")
+    if rep > 1:
+        if out is None:
+            out = np.zeros((S, H, D), dtype=np.float64)
+        for r in range(sp):
+            out[:, r * H // sp, :] += recv[r, :, 0, :].astype(np.float64)
+        return out
+    if out is None:
+        out = np.zeros((S, H, D), dtype=recv.dtype)
+    for r in range(sp):
+        for j in range(nh):
+            out[:, r * Hl + head0 + j, :] = recv[r, :, j, :]
+    return out

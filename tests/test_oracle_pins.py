@@ -424,3 +424,82 @@ def test_f16_attention_equals_bf16_attention_on_shared_values():
     g1 = oracle.attn_bwd(bf[0], bf[1], bf[2], bf[3], cu)
     g2 = oracle.attn_bwd(hf[0], hf[1], hf[2], hf[3], cu, dtype="f16")
     assert all(np.array_equal(a, b) for a, b in zip(g1, g2))
+
+
+# ====================================================== the exchange between real ranks
+def _exchange_to_heads(x, sp, head0=0, nheads=None):
+    """Every rank packs its shard, the blocks are exchanged; returns each rank's receive
+    buffer as a token-major [T][nh][D] array."""
+    T, H, D = x.shape
+    S = T // sp
+    sends = [relayout.a2a_pack(x[r * S:(r + 1) * S], sp, head0, nheads) for r in range(sp)]
+    return [recv.reshape(T, recv.shape[2], D) for recv in relayout.exchange_blocks(sends)]
+
+
+def test_exchange_layout_figure_worked_example():
+    """The two-GPU layout figure, now as what each rank holds after packing and the
+    all-to-all: rank r's receive buffer is every token of its heads, in token order."""
+    T, H, D, sp = 8, 4, 1, 2
+    x = index_pattern_bits(T, H, D)              # value = t*H + h
+    got_heads = _exchange_to_heads(x, sp)
+    rows = [l.split() for l in open(os.path.join(GOLDEN, "layout_figure_2gpu.txt"))
+            if l.strip() and not l.startswith("#")]
+    for phase, r, t0, t1, h0, h1 in rows:
+        r, t0, t1, h0, h1 = map(int, (r, t0, t1, h0, h1))
+        if phase != "head":
+            continue
+        recv = got_heads[r]
+        assert [int(v) // H for v in recv[:, 0, 0]] == list(range(t0, t1))       # token order
+        assert {int(v) % H for v in recv.ravel()} == set(range(h0, h1))
+    # back: every rank sends its token-major result in sp blocks of S tokens and unpacks
+    S = T // sp
+    back = relayout.exchange_blocks([g.reshape(sp, S, -1, D) for g in got_heads])
+    for r in range(sp):
+        assert np.array_equal(relayout.a2a_unpack(back[r], sp, H), x[r * S:(r + 1) * S])
+
+
+def test_exchange_pure_python_loops():
+    """From the step description: rank r receives, from each source rank in order, the
+    source's tokens of rank r's heads."""
+    T, H, D, sp = 12, 6, 2, 3
+    S, Hl = T // sp, H // sp
+    x = index_pattern_bits(T, H, D)
+    got = _exchange_to_heads(x, sp)
+    for r in range(sp):
+        for src in range(sp):
+            for s in range(S):
+                for hl in range(Hl):
+                    for d in range(D):
+                        assert got[r][src * S + s, hl, d] == x[src * S + s, r * Hl + hl, d]
+
+
+def test_exchange_head_chunks_reassemble():
+    """Exchanging each rank's heads in chunks (to overlap the exchange with attention)
+    gives the same heads as one exchange."""
+    rng = np.random.default_rng(43)
+    T, H, D, sp = 16, 8, 4, 2
+    x = rand_bits(rng, (T, H, D))
+    whole = _exchange_to_heads(x, sp)
+    parts = [_exchange_to_heads(x, sp, head0, 2) for head0 in (0, 2)]
+    for r in range(sp):
+        assert np.array_equal(np.concatenate([p[r] for p in parts], axis=1), whole[r])
+
+
+@pytest.mark.parametrize("hkv,sp", [(2, 4), (1, 2), (2, 8)])
+def test_exchange_replication_adjoint(hkv, sp):
+    """With fewer key/value heads than ranks the exchange replicates; its adjoint -- the
+    gradient's way back -- must sum the replicas: <E x, y> = <x, E^T y>."""
+    rng = np.random.default_rng(hkv * 100 + sp)
+    T, D = 4 * sp, 3
+    S = T // sp
+    xb = f32_to_bf16_bits(rng.standard_normal((T, hkv, D)).astype(np.float32))
+    ex = _exchange_to_heads(xb, sp)                              # rank r: [T][1][D]
+    y = [rng.standard_normal((T, 1, D)) for _ in range(sp)]
+    lhs = sum(float((f64(ex[r]) * y[r]).sum()) for r in range(sp))
+    back = relayout.exchange_blocks([yr.reshape(sp, S, 1, D) for yr in y])
+    grads = [relayout.a2a_unpack(back[r], sp, hkv) for r in range(sp)]
+    rhs = sum(float((f64(xb[r * S:(r + 1) * S]) * grads[r]).sum()) for r in range(sp))
+    assert abs(lhs - rhs) <= 1e-9 * max(1.0, abs(lhs))
+    # and each rank received the head its query heads read (kv_replication's rule)
+    for r in range(sp):
+        assert np.array_equal(ex[r][:, 0], xb[:, r * hkv // sp])

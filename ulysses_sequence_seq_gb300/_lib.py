@@ -44,6 +44,8 @@ EXPORTED = (
     "usp_cu_seqlens_to_position_ids",
     "usp_shift_labels",
     "usp_sp_weighted_loss",
+    "usp_a2a_pack",
+    "usp_a2a_unpack",
 )
 
 
@@ -93,11 +95,13 @@ def load(build_if_missing: bool = True):
     L.usp_cu_seqlens_to_position_ids.argtypes = [P, I, I64, P, P]
     L.usp_shift_labels.argtypes = [P, P, I, I64, I, P, P, P]
     L.usp_sp_weighted_loss.argtypes = [P, P, I, P, P]
+    L.usp_a2a_pack.argtypes = [P, P, I, I64, I, I, I, I, I, P]
+    L.usp_a2a_unpack.argtypes = [P, P, I, I64, I, I, I, I, I, P]
     for name in ("usp_seq_to_head", "usp_head_to_seq", "usp_attn_fwd_varlen", "usp_attn_bwd_varlen",
                  "usp_get_device_status", "usp_debug_wait_timeout", "usp_attn_fwd_varlen_noalloc",
                  "usp_ulysses_attn_fwd", "usp_ulysses_attn_bwd", "usp_position_ids_to_cu_seqlens",
                  "usp_cu_seqlens_to_position_ids", "usp_shift_labels", "usp_sp_weighted_loss",
-                 "usp_seq_to_head_kv", "usp_head_to_seq_kv_grad"):
+                 "usp_seq_to_head_kv", "usp_head_to_seq_kv_grad", "usp_a2a_pack", "usp_a2a_unpack"):
         getattr(L, name).restype = I
     _lib = L
     return _lib
@@ -190,6 +194,27 @@ def head_to_seq_kv_grad(y, out, sp: int, hkv: int, stream=None):
     T = y.numel() // (D * max(sp, hkv))
     _check("usp_head_to_seq_kv_grad", load().usp_head_to_seq_kv_grad(_ptr(y), _ptr(out), int(sp), int(T), int(hkv),
                                                                       int(D), _dtype_code(y), _stream(stream)))
+    return out
+
+
+def a2a_pack(x, out, sp: int, head0: int = 0, nheads: int = 0, stream=None):
+    """x: [S][H][D] this rank's shard -> out: [sp][S][nheads][D], block r for rank r
+    (heads r*H/sp + head0 ..; with H < sp the one head rank r reads). nheads 0: all the
+    rank's heads from head0 (1 when replicated)."""
+    S, H, D = x.shape[-3], x.shape[-2], x.shape[-1]
+    nh = nheads or (H // sp - head0 if H % sp == 0 else 1)
+    _check("usp_a2a_pack", load().usp_a2a_pack(_ptr(x), _ptr(out), int(sp), int(S), int(H), int(D), int(head0),
+                                               int(nh), _dtype_code(x), _stream(stream)))
+    return out
+
+
+def a2a_unpack(recv, out, sp: int, head0: int = 0, nheads: int = 0, stream=None):
+    """recv: [sp][S][nheads][D] (block r from rank r) -> out: [S][H][D], the chunk's heads
+    of every rank written (with H < sp: the replicas' gradients summed)."""
+    S, H, D = out.shape[-3], out.shape[-2], out.shape[-1]
+    nh = nheads or (H // sp - head0 if H % sp == 0 else 1)
+    _check("usp_a2a_unpack", load().usp_a2a_unpack(_ptr(recv), _ptr(out), int(sp), int(S), int(H), int(D),
+                                                   int(head0), int(nh), _dtype_code(out), _stream(stream)))
     return out
 
 
