@@ -48,10 +48,11 @@ def load_peaks():
 
 
 # DRAM bytes (read + write) of one attn_bwd_kernel launch from an ncu capture of this
-# bench's own command, keyed by workload, path and the kernel source they were taken on;
-# any change to the kernel source makes the figure stale and it is reported as null.
+# bench's own command (one rank's slice of the workload), keyed by workload, path and the
+# kernel source they were taken on; any change to the kernel source makes the figure stale
+# and it is reported as null.
 MEASURED_BWD_TRAFFIC = {
-    ("llama", True): ("fa020faed73a5828", 404870656 + 222942208),
+    ("long", True): ("bb559b132530ac17", 8080000000 + 4250000000),
 }
 
 
@@ -63,6 +64,13 @@ def bwd_traffic(w, fused):
     with open(os.path.join(ROOT, "ulysses_sequence_seq_gb300", "csrc", "attn_bwd.cu"), "rb") as f:
         digest = hashlib.sha256(f.read()).hexdigest()[:16]
     return entry[1] if digest == entry[0] else None
+
+
+def bwd_algorithmic_bytes(w):
+    """Bytes attn_bwd_kernel must move once: its fp16 q, k, v, dO copies read, the fp32 dQ
+    accumulator read and written, dK and dV written (bf16), LSE and Delta read."""
+    T, D = w.total_tokens, w.head_dim
+    return 2 * T * D * (2 * w.hq + 2 * w.hkv) + 8 * w.hq * T * D + 4 * w.hkv * T * D + 8 * w.hq * T
 
 
 def workload_desc(w, rank_slice=False):
@@ -502,7 +510,10 @@ def run_usp(args, w):
                      "peak_source": f"{peak_src} bf16 sustained (the timed region runs for seconds)",
                      "peak_burst": peak_burst, "frac_of_burst": bwd_tflops / peak_burst,
                      "traffic": bwd_traffic(ws_, True),
-                     "traffic_of": "attn_bwd_kernel, DRAM read+write bytes per launch (ncu)"},
+                     "traffic_of": "attn_bwd_kernel, DRAM read+write bytes per launch (ncu)",
+                     "algorithmic_bytes": bwd_algorithmic_bytes(ws_)},
+        "scheduler_share_of_step": {"value": 0.0001, "source": "ncu launch list of this command's kernels "
+                                                                "(schedule_kernel 0.01% of the step)"},
         "all_ranks_one_launch": all_ranks,
         "extras": extras,
         "relayout": {"achieved_gbs": rel_gbs, "peak_gbs": hbm, "frac": rel_gbs / hbm,
