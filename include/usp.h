@@ -154,6 +154,49 @@ usp_status usp_a2a_pack(const void* in, void* out, int sp, int64_t shard_tokens,
 usp_status usp_a2a_unpack(const void* in, void* out, int sp, int64_t shard_tokens, int heads, int head_dim,
                           int head0, int nheads, usp_dtype dt, void* stream);
 
+/* ------------------------------------------------------------------------------
+ * Ring-attention steps. In ring attention every rank keeps a chunk of the queries
+ * while the key/value chunks travel around the ring; each step attends the local
+ * queries to the visiting chunk and the partial results are combined through their
+ * log-sum-exp (ColossalAI sequence parallelism tutorial, the ring-attention plugin
+ * set-up and its closing comparison of Ulysses and ring attention). With equal chunks
+ * of one sequence (packed samples split evenly, the same chunk-local cu_seqlens for
+ * every chunk), the causal mask on global positions makes a step unmasked for an
+ * earlier key chunk, causal for the query chunk's own keys and empty for a later one:
+ * one attention call (causal 0 or 1) of this library, or none. The calls below do the
+ * rest of a step; the Python class RingAttention chains them.
+ * ------------------------------------------------------------------------------ */
+
+/*
+ * usp_lse_merge -- o_acc, lse_acc <- the softmax over the union of the keys seen so far
+ * and a new disjoint key set, from each side's normalised output and log-sum-exp:
+ *   lse = log(e^lse_acc + e^lse_part),
+ *   o_acc = e^(lse_acc - lse) o_acc + e^(lse_part - lse) (o_part + o_part_res).
+ *   A side with lse = -inf contributes nothing (both -inf: o 0, lse -inf).
+ *   o_acc : fp32, o_part / o_part_res : dt (USP_BF16 or USP_FP16; o_part_res may be
+ *   NULL), all [T][heads][head_dim] when token_major, else [heads][T][head_dim];
+ *   lse_acc, lse_part : fp32 [heads][T] (natural log). init != 0: o_acc and lse_acc
+ *   are set to the part (their contents are not read).
+ * Errors: USP_ERR_INVALID_ARG (NULL or misaligned pointer, T < 0, heads < 1, head_dim
+ *   not 64 or 128, dt not 16-bit). T == 0 is a no-op.
+ */
+usp_status usp_lse_merge(float* o_acc, float* lse_acc, const void* o_part, const void* o_part_res,
+                         const float* lse_part, int64_t total_tokens, int heads, int head_dim, int token_major,
+                         usp_dtype dt, int init, void* stream);
+
+/*
+ * usp_o_finalize -- o = round(o_acc) and o_res = round(o_acc - o) in dt (bf16 or fp16),
+ * element by element (`elements` a multiple of 4; o_res may be NULL): the merged output
+ * in the form the backward calls take (o and its rounding residual).
+ */
+usp_status usp_o_finalize(const float* o_acc, void* o, void* o_res, int64_t elements, usp_dtype dt, void* stream);
+
+/*
+ * usp_accumulate_f32 -- acc += part over `elements` fp32 values (a multiple of 4): sums
+ * the gradient shares of the ring steps.
+ */
+usp_status usp_accumulate_f32(float* acc, const float* part, int64_t elements, void* stream);
+
 /*
  * usp_attn_workspace_size -- bytes of workspace the attention calls need for
  * these sizes (bwd != 0: for usp_attn_bwd_varlen, which also needs per-row

@@ -503,3 +503,88 @@ def test_exchange_replication_adjoint(hkv, sp):
     # and each rank received the head its query heads read (kv_replication's rule)
     for r in range(sp):
         assert np.array_equal(ex[r][:, 0], xb[:, r * hkv // sp])
+
+
+# ======================================================= ring-attention steps and merges
+from oracle import ring  # noqa: E402
+
+
+def _ring_inputs(seed, T=96, hq=4, hkv=2, D=16):
+    rng = np.random.default_rng(seed)
+    return (rand_bits(rng, (hq, T, D)), rand_bits(rng, (hkv, T, D)), rand_bits(rng, (hkv, T, D)),
+            rand_bits(rng, (hq, T, D)))
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("order", ["forward", "reverse"])
+def test_ring_merged_chunks_equal_full_attention(causal, order):
+    """Attending one query chunk to each key chunk of the sequence and merging the partial
+    results through their log-sum-exp gives full attention (softmax over a disjoint union),
+    checked against the C oracle (itself pinned to torch SDPA), in either ring order."""
+    q, k, v, _ = _ring_inputs(51)
+    T, nc = q.shape[1], 4
+    L = T // nc
+    ro, rl = oracle.attn_fwd(q, k, v, np.array([0, T], dtype=np.int32), causal=causal)
+    for qc in range(nc):
+        o = np.zeros((q.shape[0], L, q.shape[2]))
+        lse = np.full((q.shape[0], L), -np.inf)
+        chunks = range(nc) if order == "forward" else reversed(range(nc))
+        for kc in chunks:
+            po, pl = ring.chunk_attn_fwd(q[:, qc * L:(qc + 1) * L], k[:, kc * L:(kc + 1) * L],
+                                         v[:, kc * L:(kc + 1) * L], qc * L, kc * L, causal)
+            o, lse = ring.lse_merge(o, lse, po, pl)
+        assert np.allclose(o, ro[:, qc * L:(qc + 1) * L], rtol=0, atol=1e-12)
+        assert np.allclose(lse, rl[:, qc * L:(qc + 1) * L], rtol=0, atol=1e-12)
+
+
+def test_ring_step_mask_on_global_positions():
+    """A key chunk wholly after the query chunk contributes nothing (lse -inf, O 0); one
+    wholly before it is unmasked attention; the diagonal chunk is causal attention."""
+    q, k, v, _ = _ring_inputs(52, T=32)
+    a, b = slice(0, 16), slice(16, 32)
+    o, lse = ring.chunk_attn_fwd(q[:, a], k[:, b], v[:, b], 0, 16, True)
+    assert np.isneginf(lse).all() and (o == 0).all()
+    o1, l1 = ring.chunk_attn_fwd(q[:, b], k[:, a], v[:, a], 16, 0, True)
+    o2, l2 = ring.chunk_attn_fwd(q[:, b], k[:, a], v[:, a], 16, 0, False)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+    o3, l3 = ring.chunk_attn_fwd(q[:, b], k[:, b], v[:, b], 16, 16, True)
+    r3, rl3 = oracle.attn_fwd(q[:, b], k[:, b], v[:, b], np.array([0, 16], dtype=np.int32), causal=True)
+    assert np.allclose(o3, r3, rtol=0, atol=1e-12) and np.allclose(l3, rl3, rtol=0, atol=1e-12)
+
+
+def test_ring_lse_merge_identities():
+    rng = np.random.default_rng(53)
+    o, lse = rng.standard_normal((2, 5, 3)), rng.standard_normal((2, 5))
+    z, zl = np.zeros_like(o), np.full_like(lse, -np.inf)
+    mo, ml = ring.lse_merge(o, lse, z, zl)
+    assert np.array_equal(mo, o) and np.array_equal(ml, lse)
+    o2, l2 = rng.standard_normal((2, 5, 3)), rng.standard_normal((2, 5))
+    a, al = ring.lse_merge(o, lse, o2, l2)
+    b, bl = ring.lse_merge(o2, l2, o, lse)
+    assert np.allclose(a, b, rtol=0, atol=1e-14) and np.allclose(al, bl, rtol=0, atol=1e-14)
+    eo, el = ring.lse_merge(z, zl, z, zl)
+    assert (eo == 0).all() and np.isneginf(el).all()
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_ring_step_gradients_sum_to_full_gradients(causal):
+    """Each step's gradient share, taken with the final output and log-sum-exp, summed over
+    the ring equals the full gradient of the C oracle (itself pinned to torch autograd)."""
+    q, k, v, do = _ring_inputs(54)
+    T, nc = q.shape[1], 3 if q.shape[1] % 3 == 0 else 4
+    L = T // nc
+    cu = np.array([0, T], dtype=np.int32)
+    ro, rl = oracle.attn_fwd(q, k, v, cu, causal=causal)
+    rq, rk, rv = oracle.attn_bwd(q, k, v, do, cu, causal=causal)
+    dq, dk, dv = np.zeros(rq.shape), np.zeros(rk.shape), np.zeros(rv.shape)
+    for qc in range(nc):
+        qs = slice(qc * L, (qc + 1) * L)
+        for kc in range(nc):
+            ks = slice(kc * L, (kc + 1) * L)
+            a, b, c = ring.chunk_attn_bwd(q[:, qs], k[:, ks], v[:, ks], do[:, qs], ro[:, qs], rl[:, qs],
+                                          qc * L, kc * L, causal)
+            dq[:, qs] += a
+            dk[:, ks] += b
+            dv[:, ks] += c
+    for got, want in ((dq, rq), (dk, rk), (dv, rv)):
+        assert np.allclose(got, want, rtol=0, atol=1e-10)

@@ -46,6 +46,9 @@ EXPORTED = (
     "usp_sp_weighted_loss",
     "usp_a2a_pack",
     "usp_a2a_unpack",
+    "usp_lse_merge",
+    "usp_o_finalize",
+    "usp_accumulate_f32",
 )
 
 
@@ -97,11 +100,15 @@ def load(build_if_missing: bool = True):
     L.usp_sp_weighted_loss.argtypes = [P, P, I, P, P]
     L.usp_a2a_pack.argtypes = [P, P, I, I64, I, I, I, I, I, P]
     L.usp_a2a_unpack.argtypes = [P, P, I, I64, I, I, I, I, I, P]
+    L.usp_lse_merge.argtypes = [P, P, P, P, P, I64, I, I, I, I, I, P]
+    L.usp_o_finalize.argtypes = [P, P, P, I64, I, P]
+    L.usp_accumulate_f32.argtypes = [P, P, I64, P]
     for name in ("usp_seq_to_head", "usp_head_to_seq", "usp_attn_fwd_varlen", "usp_attn_bwd_varlen",
                  "usp_get_device_status", "usp_debug_wait_timeout", "usp_attn_fwd_varlen_noalloc",
                  "usp_ulysses_attn_fwd", "usp_ulysses_attn_bwd", "usp_position_ids_to_cu_seqlens",
                  "usp_cu_seqlens_to_position_ids", "usp_shift_labels", "usp_sp_weighted_loss",
-                 "usp_seq_to_head_kv", "usp_head_to_seq_kv_grad", "usp_a2a_pack", "usp_a2a_unpack"):
+                 "usp_seq_to_head_kv", "usp_head_to_seq_kv_grad", "usp_a2a_pack", "usp_a2a_unpack", "usp_lse_merge", "usp_o_finalize",
+                 "usp_accumulate_f32"):
         getattr(L, name).restype = I
     _lib = L
     return _lib
@@ -216,6 +223,27 @@ def a2a_unpack(recv, out, sp: int, head0: int = 0, nheads: int = 0, stream=None)
     _check("usp_a2a_unpack", load().usp_a2a_unpack(_ptr(recv), _ptr(out), int(sp), int(S), int(H), int(D),
                                                    int(head0), int(nh), _dtype_code(out), _stream(stream)))
     return out
+
+
+def lse_merge(o_acc, lse_acc, o_part, lse_part, o_part_res=None, token_major=True, init=False, stream=None):
+    """o_acc (fp32), lse_acc <- merged with a partial result over disjoint keys (usp_lse_merge).
+    o_*: [T][H][D] (token_major) or [H][T][D]; lse_*: [H][T]."""
+    H, T = lse_acc.shape
+    _check("usp_lse_merge", load().usp_lse_merge(
+        _ptr(o_acc), _ptr(lse_acc), _ptr(o_part), _ptr(o_part_res), _ptr(lse_part), int(T), int(H),
+        int(o_part.shape[-1]), int(bool(token_major)), _dtype_code(o_part), int(bool(init)), _stream(stream)))
+
+
+def o_finalize(o_acc, o, o_res=None, stream=None):
+    """o (16-bit) = round(o_acc), o_res = round(o_acc - o)."""
+    _check("usp_o_finalize", load().usp_o_finalize(_ptr(o_acc), _ptr(o), _ptr(o_res), int(o_acc.numel()),
+                                                   _dtype_code(o), _stream(stream)))
+
+
+def accumulate_f32(acc, part, stream=None):
+    """acc += part (fp32)."""
+    _check("usp_accumulate_f32", load().usp_accumulate_f32(_ptr(acc), _ptr(part), int(acc.numel()),
+                                                           _stream(stream)))
 
 
 def attn_workspace_size(total_tokens: int, num_seqs: int, hq: int, hkv: int, head_dim: int, bwd: bool) -> int:

@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libusp.so")
-SOURCES = ["relayout.cu", "sched.cu", "attn_fwd.cu", "attn_bwd.cu", "usp_api.cu", "noalloc.cu", "sp_loss.cu", "a2a.cu"]
+SOURCES = ["relayout.cu", "sched.cu", "attn_fwd.cu", "attn_bwd.cu", "usp_api.cu", "noalloc.cu", "sp_loss.cu", "a2a.cu", "ring.cu"]
 
 # Kernels that rebalance registers between warpgroups with setmaxnreg: the increase waits
 # until the decreases have returned enough of the registers the CTA was launched with, so
