@@ -163,8 +163,9 @@ __global__ void __launch_bounds__(1024) schedule_kernel(SchedArgs a) {
     // complete before it reads the work list
     ptx::pdl_trigger();
     schedule_body(a);
-    // launched after bwd_prep, this kernel may have started before that one finished: it
-    // completes only once bwd_prep has, so the attention kernel's wait covers both
+    // launched after the backward's operand conversion, this kernel may have started before
+    // that one finished: it completes only once the conversion has (which itself waited for
+    // the stats kernel), so the attention kernel's wait covers all of them
     ptx::pdl_wait();
 }
 

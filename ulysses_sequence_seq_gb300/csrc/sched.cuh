@@ -26,7 +26,8 @@ struct SchedArgs {
 };
 
 // Writes the work list and the header (status, item count, a zeroed item counter). With
-// after_prep the launch may overlap the bwd_prep kernel launched just before it on s.
+// after_prep the launch may overlap the backward's operand-conversion kernel launched just
+// before it on s.
 cudaError_t launch_schedule(const SchedArgs& a, cudaStream_t s, bool after_prep);
 
 // Sample length from which work items are ordered head by head: the backward always (its
