@@ -71,13 +71,15 @@ def check_launch_registers(ptxas_log: str) -> None:
                                f"split needs {need}")
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
+def build(force: bool = False, verbose: bool = False, defines=()) -> str:
+    """Compile every translation unit and link libusp.so. `defines` adds preprocessor
+    symbols (e.g. USP_TIMELINE for the backward's optional clock64 timeline)."""
     if not force and up_to_date():
         return LIB
     os.makedirs(OUT_DIR, exist_ok=True)
     cc = nvcc()
     common = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC,
-                     "-Xptxas", "-v"]
+                     "-Xptxas", "-v"] + ["-D" + d for d in defines]
 
     def compile_one(src):
         obj = os.path.join(OUT_DIR, src.replace(".cu", ".o"))

@@ -79,6 +79,25 @@ struct BwdSmem {
 static_assert(BwdSmem<128>::kAlloc <= 232448, "backward shared memory exceeds the per-CTA limit");
 static_assert(BwdSmem<128>::kStage % 1024 == 0, "dQ staging must keep the 128-byte swizzle atoms aligned");
 
+// Optional clock64 timeline of the first kTlSteps steps of every CTA (compile with
+// -DUSP_TIMELINE; the default build has none of it). Events: MMA thread 0-4 (both halves'
+// P ready, both halves' dS ready, dQ issued), compute half h 5+5h..8+5h (S ready, P
+// stored, dP ready, dS stored), dQ drain 14-15 (dQ ready, TMEM released), MMA thread 16
+// (dO arrived), producer 17-18 (dO load issued, Q load issued). Read back with
+// usp_debug_timeline.
+#ifdef USP_TIMELINE
+constexpr int kTlSteps = 48, kTlEvents = 20, kTlCtas = 160;
+static __device__ long long g_timeline[kTlCtas][kTlSteps][kTlEvents];
+#define USP_TL(step, ev)                                                                        \
+    do {                                                                                        \
+        if ((step) < kTlSteps && blockIdx.x < kTlCtas) g_timeline[blockIdx.x][(step)][(ev)] = clock64(); \
+    } while (0)
+#else
+#define USP_TL(step, ev) \
+    do {                 \
+    } while (0)
+#endif
+
 // One backward work item: a key/value tile of one sample and one key/value head, and the
 // query blocks (of every query head of its GQA group) that see it.
 struct BwdItem {
@@ -228,6 +247,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         break;
                     }
                     mbar_arrive_expect_tx(&bars[L::bQFull + st], L::kTileBytes);
+                    USP_TL(gk, 18);
                     for (int p = 0; p < L::kPanels; ++p)
                         tma_load_rows(sm + L::kQ + st * L::kTileBytes + p * (kTileM * 128), &tmQ,
                                       &bars[L::bQFull + st], p * 64, q0, h, 0);
@@ -238,9 +258,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         break;
                     }
                     mbar_arrive_expect_tx(&bars[L::bDoFull], L::kTileBytes);
+                    USP_TL(gk, 17);
                     for (int p = 0; p < L::kPanels; ++p)
                         tma_load_rows(sm + L::kDO + p * (kTileM * 128), &tmDO, &bars[L::bDoFull], p * 64, q0, h, 0);
                     ++do_total;
+                    // The CTAs walk the same query blocks in near lockstep, so a block's first
+                    // load goes to DRAM for all of them; pull Q and dO two steps ahead into L2
+                    // (the next item's first two steps are pulled when it is reserved, below).
+                    if (k + 2 < w.nsteps) {
+                        const int k2 = k + 2, h2 = w.g * G + k2 / w.nq, q2 = w.q0(k2);
+                        for (int p = 0; p < L::kPanels; ++p) {
+                            tma_prefetch_rows(&tmQ, p * 64, q2, h2, 0);
+                            tma_prefetch_rows(&tmDO, p * 64, q2, h2, 0);
+                        }
+                    }
                     if (k == 0) {  // K, V once the previous item's last MMA has read them
                         if (j > 0 && !mbar_wait(&bars[L::bKvEmpty], (j - 1) & 1, abort_flag, kWaitLimitNs)) {
                             ok = false;
@@ -264,6 +295,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                             for (int p = 0; p < L::kPanels; ++p) {
                                 tma_prefetch_rows(&tmK, p * 64, nw.kv0, nw.g, 0);
                                 tma_prefetch_rows(&tmV, p * 64, nw.kv0, nw.g, 0);
+                                for (int k2 = 0; k2 < 2 && k2 < nw.nsteps; ++k2) {
+                                    tma_prefetch_rows(&tmQ, p * 64, nw.q0(k2), nw.g * G + k2 / nw.nq, 0);
+                                    tma_prefetch_rows(&tmDO, p * 64, nw.q0(k2), nw.g * G + k2 / nw.nq, 0);
+                                }
                             }
                         }
                     }
@@ -327,8 +362,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 for (int k = 0; ok && k < nsteps; ++k, ++gk) {
                     const int st = gk & 1;
                     if (!mbar_wait(&bars[L::bDoFull], gk & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
+                    USP_TL(gk, 16);
                     for (int hf = 0; ok && hf < 2; ++hf) {
                         if (!mbar_wait(&bars[L::bPFull + hf], gk & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
+                        USP_TL(gk, hf);
                         tc_fence_after();
 #pragma unroll
                         for (int kk = 0; kk < kHalfCols / 16; ++kk)  // dV += P^T . dO over this half's queries
@@ -342,6 +379,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     mma_commit(&bars[L::bDoEmpty]);
                     for (int hf = 0; ok && hf < 2; ++hf) {
                         if (!mbar_wait(&bars[L::bDsFull + hf], gk & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
+                        USP_TL(gk, 2 + hf);
                         tc_fence_after();
                         if (k + 1 < nsteps) {  // S^T of the next block first: it heads this half's next step
                             const int st1 = st ^ 1;
@@ -372,6 +410,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         mma_ss(tDQ, dDS_mn + (uint64_t)((kk * 2048) >> 4), dK_mn + (uint64_t)((kk * 2048) >> 4), idDq,
                                kk > 0 ? 1u : 0u);
                     mma_commit(&bars[L::bDqFull]);
+                    USP_TL(gk, 4);
                 }
                 if (!ok) break;
                 mma_commit(&bars[L::bKvEmpty]);   // K and V have been read for the last time
@@ -441,6 +480,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 const bool mask_blk = (a.causal && q0 == w.kv0) || (w.kv0 + kBlockN > w.e);
                 const int vis_from = (a.causal && q0 == w.kv0) ? r - grp * kHalfCols : -1;
                 if (!mbar_wait(&bars[L::bSFull + grp], gk & 1, abort_flag, kWaitLimitNs)) { ok = false; continue; }
+                if ((warp & 3) == 0 && lane == 0) USP_TL(gk, 5 + 5 * grp);
                 tc_fence_after();
                 // P for this row's query columns as packed bf16 pairs: the values the dV MMA
                 // consumes, kept (half the registers of fp32) for dS
@@ -477,9 +517,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars[L::bPFull + grp]);
+                if ((warp & 3) == 0 && lane == 0) USP_TL(gk, 6 + 5 * grp);
 
                 // dP^T of this half; its commit also covers the previous block's reads of the dS buffer
                 if (!mbar_wait(&bars[L::bDpFull + grp], gk & 1, abort_flag, kWaitLimitNs)) { ok = false; continue; }
+                if ((warp & 3) == 0 && lane == 0) USP_TL(gk, 7 + 5 * grp);
                 tc_fence_after();
                 uint8_t* panel = sm + L::kDS + grp * (kBlockN * 128);
 #pragma unroll
@@ -514,6 +556,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars[L::bDsFull + grp]);
+                if ((warp & 3) == 0 && lane == 0) USP_TL(gk, 8 + 5 * grp);
             }
             // the next item, and its first step's row statistics, before this item's epilogue
             int idx_next = count;
@@ -645,6 +688,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 const int h = w.g * G + k / w.nq;
                 const int qrow0 = w.q0(k) + w4 * 32;   // first query row of this warp
                 if (!mbar_wait(&bars[L::bDqFull], gk & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
+                if (w4 == 0 && lane == 0) USP_TL(gk, 14);
                 tc_fence_after();
                 // chunk c+1 is read from TMEM while chunk c is staged
                 uint32_t v[2][32];
@@ -660,6 +704,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&bars[L::bDqEmpty]);
+                        if (w4 == 0 && lane == 0) USP_TL(gk, 15);
                     }
                     uint8_t* buf = stage;
                     // the previous chunk's reduction must have read the buffer
@@ -936,6 +981,14 @@ cudaError_t launch_dq_convert(const float* dq_acc, void* dq, const uint32_t* ama
     auto kernel = D4 == 32 ? dq_convert_kernel<32> : dq_convert_kernel<16>;
     return launch_kernel(kernel, grid, dim3(256), 0, s, true, a);
 }
+
+#ifdef USP_TIMELINE
+// The backward's timeline (kTlCtas x kTlSteps x kTlEvents clock64 values) into host memory.
+extern "C" int usp_debug_timeline(void* host_dst, size_t bytes) {
+    if (bytes < sizeof(g_timeline)) return (int)USP_ERR_INVALID_ARG;
+    return cudaMemcpyFromSymbol(host_dst, g_timeline, sizeof(g_timeline)) == cudaSuccess ? 0 : (int)USP_ERR_CUDA;
+}
+#endif
 
 cudaError_t launch_debug_timeout(WsHeader* hdr, uint64_t limit_ns, cudaStream_t s) {
     debug_timeout_kernel<<<1, 32, 0, s>>>(hdr, limit_ns);

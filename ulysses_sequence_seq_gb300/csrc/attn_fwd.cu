@@ -203,6 +203,14 @@ __global__ void __maxnreg__(kLaunchRegs)
                     for (int p = 0; p < L::kPanels; ++p)
                         tma_load_rows(sm + L::kV + st * L::kTileBytes + p * (kTileM * 128), &tmV, &bars[L::bVFull + st],
                                       p * 64, row, f.kvh, a.token_major);
+                    // The CTAs walk the same key/value blocks in near lockstep, so a block's first
+                    // load goes to DRAM for all of them: pull K and V two blocks ahead into L2.
+                    if (n + 2 < f.nmax) {
+                        for (int p = 0; p < L::kPanels; ++p) {
+                            tma_prefetch_rows(&tmK, p * 64, row + 2 * kBlockN, f.kvh, a.token_major);
+                            tma_prefetch_rows(&tmV, p * 64, row + 2 * kBlockN, f.kvh, a.token_major);
+                        }
+                    }
                     // two blocks before the end, reserve the next item and pull its Q into L2
                     if (n == (f.nmax >= 2 ? f.nmax - 2 : 0)) {
                         next_idx = (int)gridDim.x + atomicAdd(&a.hdr->fwd_next, 1);
