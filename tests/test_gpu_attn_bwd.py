@@ -153,3 +153,31 @@ def test_bwd_key_gradients_sum_to_zero_per_sample():
     g = f64(dk)
     for b in range(3):
         assert np.abs(g[:, cu[b]:cu[b + 1]].sum(axis=1)).max() < 1e-1
+
+
+@pytest.mark.parametrize("stds", [(1.0, 1.0, 1.0, 1e-6), (1.0, 1.0, 300.0, 1.0), (20.0, 0.05, 1.0, 3e-5)])
+def test_bwd_scaled_operands_keep_precision_at_any_magnitude(stds):
+    """The backward rounds its operands to fp16 after scaling each key/value group by a power
+    of two, so gradients keep ~fp16 relative precision whatever the magnitudes: output
+    gradients of a real loss (1e-6, far below fp16's normal range), large values (300),
+    small keys. Checked relative to each gradient's largest magnitude (the 2e-2 gate is
+    stated for N(0, 1) inputs)."""
+    needs_gpu()
+    sq, sk, sv, sd = stds
+    w = custom_workload("scaled", [300, 129, 600], sp=1, hq=4, hkv=2, head_dim=128, index=29)
+    from ulysses_sequence_seq_gb300.synth import head_bits
+    def scaled(t, heads, std):
+        return np.stack([head_bits(w, t, h, std=std) for h in heads])
+    q, k, v, do = (scaled("q", range(4), sq), scaled("k", range(2), sk), scaled("v", range(2), sv),
+                   scaled("do", range(4), sd))
+    p = Problem(q, k, v, w.cu_seqlens(), True, do_bits=do)
+    o, lse, st = p.forward()
+    assert st == 0
+    dq, dk, dv, st = p.backward(o, lse)
+    assert st == 0
+    rq, rk, rv = oracle.attn_bwd(q, k, v, do, w.cu_seqlens())
+    for name, g, r in (("dQ", dq, rq), ("dK", dk, rk), ("dV", dv, rv)):
+        scale = np.abs(r).max()
+        assert scale > 0
+        err = np.abs(f64(g) - r).max() / scale
+        assert err <= 5e-3, f"{name}: error {err:.2e} of the largest magnitude {scale:.2e}"
