@@ -27,9 +27,10 @@ struct FwdArgs {
 };
 
 // o, o_res: the output maps (make_activation_map over o and o_res; o_res is not read when
-// a.o_res is NULL) for whole-tile stores. grid: the work-item upper bound; min(grid, SM
-// count) persistent CTAs are launched, as a programmatic dependent of the scheduler
-// launched just before on s.
+// a.o_res is NULL) for whole-tile stores; k: boxes of fwd_k_box_rows(head_dim) rows.
+// grid: the work-item upper bound; persistent CTAs (one per SM; pairs of them for head_dim
+// 128, as many as can be resident) are launched, as a programmatic dependent of the
+// scheduler launched just before on s.
 cudaError_t launch_attn_fwd(int head_dim, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                             const CUtensorMap& o, const CUtensorMap& o_res, const FwdArgs& a, int grid,
                             cudaStream_t s);
@@ -126,8 +127,11 @@ cudaError_t launch_dq_convert(const float* dq_acc, void* dq, const uint32_t* ama
                               int head_dim, int token_major, int out_dt, int ds_exp, cudaStream_t s);
 
 // TMA tensor map over a 16-bit activation (bf16 or fp16: the copy moves bytes), head-major [heads][T][D] or token-major
-// [T][heads][D]: boxes of 64 columns x 128 rows of one head, 128-byte swizzle.
-bool make_activation_map(CUtensorMap* map, const void* base, int64_t T, int heads, int D, int token_major);
+// [T][heads][D]: boxes of 64 columns x box_rows rows of one head, 128-byte swizzle.
+bool make_activation_map(CUtensorMap* map, const void* base, int64_t T, int heads, int D, int token_major,
+                         int box_rows = kTileM);
+// Rows of the forward's K boxes: a CTA pair (head_dim 128) loads half of each key block per CTA.
+inline int fwd_k_box_rows(int head_dim) { return head_dim == 128 ? kBlockN / 2 : kBlockN; }
 // fp32 dQ accumulator ([heads][T][D] or [T][heads][D]) in 32-column x 32-row boxes with the
 // 128-byte swizzle, the target of the backward's bulk tensor reductions.
 bool make_dq_accum_map(CUtensorMap* map, float* base, int64_t T, int heads, int D, int token_major);

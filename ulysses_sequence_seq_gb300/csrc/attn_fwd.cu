@@ -4,15 +4,26 @@
 // no materialised score matrix; congresoia365 article, "El Desafío del
 // Entrenamiento de Secuencias Largas", and HF guide "Configurar" on packed samples).
 //
-// A work item is a query head and two 128-row query tiles of one sample. CTAs are
-// persistent (one per SM): each takes its first item by index and the rest from a
-// counter, in schedule order, so the next item's Q, K, V loads and first Q.K^T overlap
-// the softmax of the current one's last blocks and its output.
-// Warp roles (384 threads, warps 10-11 idle):
+// Two forms of one kernel, persistent and warp-specialised:
+//  * head_dim 128 -- a pair of CTAs (a cluster of two, one per SM) shares every MMA
+//    (tcgen05 cta_group::2, M = 256): each CTA holds 128 query rows of each of its two
+//    256-row tiles and only half of each key/value block's operands (64 of its 128 keys of
+//    K, 64 of the 128 columns of V). With one CTA per tile, each SM would take in 64 KB of K
+//    and V per block and its MMAs would read both operands of every Q.K^T from its own
+//    shared memory; that traffic, not the tensor core, set the pace. The pair halves both.
+//    A work item is 512 query rows; the leader (rank 0) takes the items, issues the MMAs and
+//    counts both CTAs' loads on its barriers; the halved operands leave room for a 4-stage
+//    key/value ring.
+//  * head_dim 64 -- one CTA per SM, two 128-row query tiles (256 rows) per item, a
+//    2-stage ring.
+// Pairs (or CTAs) take their first item by index and the rest from a counter, in schedule
+// order, so the next item's Q, K, V loads and first Q.K^T overlap the softmax of the
+// current one's last blocks and its output.
+// Warp roles (384 threads per CTA, warps 10-11 idle):
 //   warps 0-3  softmax group for query tile 0 (thread = one query row = one TMEM lane)
 //   warps 4-7  softmax group for query tile 1
-//   warp  8    TMA producer: Q tiles once, then K/V blocks into a 2-stage ring
-//   warp  9    MMA issuer (one thread) and TMEM owner
+//   warp  8    TMA producer: Q tiles once, then K/V blocks (or this CTA's halves) into the ring
+//   warp  9    MMA issuer (one thread; the pair's leader only) and TMEM owner
 // Tensor memory (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [384,384+D).
 // A whole output tile leaves through a 64-column shared-memory panel of its own, one TMA
 // store per 64 columns; a sample's ragged last tile is written row by row. On request the
@@ -47,71 +58,175 @@ constexpr int kSoftmaxRegs = 200;
 constexpr int kAuxRegs = 104;
 static_assert(128 * (2 * kSoftmaxRegs + kAuxRegs) <= kFwdThreads * kLaunchRegs, "register split exceeds the launch pool");
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr uint16_t kPairMask = 0x3;        // both CTAs of a pair
 
-template <int D>
+template <int D, bool PAIR>
 struct FwdSmem {
+    static_assert(!PAIR || D == 128, "the pair splits V into two 64-column panels");
     static constexpr int kPanels = D / 64;
-    static constexpr int kTileBytes = kTileM * D * 2;  // one 128-row tile of 16-bit elements
+    static constexpr int kTileBytes = kTileM * D * 2;          // one 128-row tile of 16-bit elements
+    static constexpr int kStages = PAIR ? 4 : 2;               // key/value ring depth
+    static constexpr int kKRows = PAIR ? kBlockN / 2 : kBlockN;   // keys of a block whose K this CTA holds
+    static constexpr int kKPanel = kKRows * 128;               // one 64-column panel of them
+    static constexpr int kKBytes = kKPanel * kPanels;
+    static constexpr int kVPanels = PAIR ? kPanels / 2 : kPanels;   // 64-column panels of V this CTA holds
+    static constexpr int kVBytes = kBlockN * 128 * kVPanels;
     static constexpr int kQ0 = 0;
     static constexpr int kQ1 = kTileBytes;
-    static constexpr int kK = 2 * kTileBytes;          // + stage * kTileBytes
-    static constexpr int kV = 4 * kTileBytes;          // + stage * kTileBytes
-    static constexpr int kStage = 6 * kTileBytes;      // O staging: one [128][64] panel per tile
+    static constexpr int kK = 2 * kTileBytes;                  // + stage * kKBytes
+    static constexpr int kV = kK + kStages * kKBytes;          // + stage * kVBytes
+    static constexpr int kStage = kV + kStages * kVBytes;      // O staging: one [128][64] panel per tile
     static constexpr int kBars = kStage + 2 * kTileM * 128;
     // barrier indices
-    static constexpr int bQFull = 0, bKFull = 1, bVFull = 3, bKvEmpty = 5, bSFull = 7, bPFull = 9, bODone = 11,
-                         bDrain = 13, bQEmpty = 14, bItem = 15, bItemFree = 19, kNumBars = 23;
+    static constexpr int bQFull = 0, bKFull = 1, bVFull = bKFull + kStages, bKvEmpty = bVFull + kStages,
+                         bSFull = bKvEmpty + kStages, bPFull = bSFull + 2, bODone = bPFull + 2, bDrain = bODone + 2,
+                         bQEmpty = bDrain + 1, bItem = bQEmpty + 1, bItemFree = bItem + 4, kNumBars = bItemFree + 4;
     // bItem / bItemFree: published / read by every reader, one of each per slot of the 4-slot item ring
     static constexpr int kItemRing = kBars + 8 * kNumBars;   // int[4]: work item of each slot
     static constexpr int kTmemSlot = kItemRing + 16;
     static constexpr int kAbort = kTmemSlot + 8;
     static constexpr int kBytes = kAbort + 8;
     static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment of the base
+    static_assert(kKBytes % 1024 == 0 && kVBytes % 1024 == 0, "ring stages must keep 1024-byte alignment");
 };
-static_assert(FwdSmem<128>::kAlloc <= 232448, "forward shared memory exceeds the per-CTA limit");
+static_assert(FwdSmem<128, true>::kAlloc <= 232448, "forward shared memory exceeds the per-CTA limit");
+static_assert(FwdSmem<64, false>::kAlloc <= 232448, "forward shared memory exceeds the per-CTA limit");
 
-// One forward work item: query head h and the query tiles q00, q01 of one sample, with
-// the key/value blocks each tile sees.
+// Optional clock64 timeline of the first kTlSteps key/value blocks of every CTA (compile with
+// -DUSP_TIMELINE; the default build has none of it). Events by the CTA's running block count:
+// MMA thread 15 (block started), 0 (V ready), 1-2 (tile 0 / 1 P ready), 3-4 (tile 0 / 1 next S
+// issued); softmax
+// group t 5+4t (S ready), 6+4t (row max done), 8+4t (P stored), 7+4t (P-ready arrival made);
+// producer 13-14 (K / V load issued). Read back with usp_debug_fwd_timeline.
+#ifdef USP_TIMELINE
+constexpr int kFTlSteps = 48, kFTlEvents = 16, kFTlCtas = 160;
+static __device__ long long g_fwd_timeline[kFTlCtas][kFTlSteps][kFTlEvents];
+#define USP_FTL(step, ev)                                                                            \
+    do {                                                                                             \
+        if ((step) < kFTlSteps && blockIdx.x < kFTlCtas) g_fwd_timeline[blockIdx.x][(step)][(ev)] = clock64(); \
+    } while (0)
+#else
+#define USP_FTL(step, ev) \
+    do {                  \
+    } while (0)
+#endif
+
+// Query rows of one forward work item (a multiple of both tiles' 128 rows).
+template <bool PAIR>
+__host__ __device__ constexpr int fwd_item_rows() {
+    return PAIR ? 4 * kTileM : 2 * kTileM;
+}
+
+// One forward work item as this CTA sees it: query head h of the sample [s, e); this CTA's
+// rows of query tiles 0 and 1 start at q00 and q01, and the tiles take nb0 and nb1 key/value
+// blocks. In a pair, tile t is the 256 rows from base + 256 t (the leader holds the first 128,
+// the peer the rest), and its block count is the pair's, so both CTAs walk the same blocks
+// (a row that sees none of a block's keys has them all masked).
 struct FwdItem {
     int h, s, e, q00, q01, nb0, nb1, nmax, kvh;
 };
-__device__ __forceinline__ FwdItem fwd_item(const FwdArgs& a, int idx) {
+template <bool PAIR>
+__device__ __forceinline__ FwdItem fwd_item(const FwdArgs& a, int idx, uint32_t rank) {
     const WorkItem it = a.items[idx];
     FwdItem f;
     f.h = it.head;
     f.s = a.cu[it.seq];
     f.e = a.cu[it.seq + 1];
-    f.q00 = f.s + it.tile * kFwdRowsPerItem;
-    f.q01 = f.q00 + kTileM;
-    f.nb0 = kv_blocks_for_query_tile(f.q00, f.s, f.e, a.causal);
-    f.nb1 = kv_blocks_for_query_tile(f.q01, f.s, f.e, a.causal);
+    const int base = f.s + it.tile * fwd_item_rows<PAIR>();
+    if constexpr (PAIR) {
+        f.q00 = base + (int)rank * kTileM;
+        f.q01 = f.q00 + 2 * kTileM;
+        const int a0 = kv_blocks_for_query_tile(base, f.s, f.e, a.causal);
+        const int a1 = kv_blocks_for_query_tile(base + kTileM, f.s, f.e, a.causal);
+        const int b0 = kv_blocks_for_query_tile(base + 2 * kTileM, f.s, f.e, a.causal);
+        const int b1 = kv_blocks_for_query_tile(base + 3 * kTileM, f.s, f.e, a.causal);
+        f.nb0 = a0 > a1 ? a0 : a1;
+        f.nb1 = b0 > b1 ? b0 : b1;
+    } else {
+        f.q00 = base;
+        f.q01 = base + kTileM;
+        f.nb0 = kv_blocks_for_query_tile(f.q00, f.s, f.e, a.causal);
+        f.nb1 = kv_blocks_for_query_tile(f.q01, f.s, f.e, a.causal);
+    }
     f.nmax = f.nb0 > f.nb1 ? f.nb0 : f.nb1;
     f.kvh = f.h / a.group;
     return f;
 }
 
-// The CTA's j-th work item from the producer's 4-slot ring (false: the wait gave up). Each
-// reader then arrives on the slot's free barrier (the MMA thread and each softmax warp);
-// the producer rewrites a slot only once all of them have, because a softmax group whose
-// tile has no blocks in a run of items is not held back by the MMAs and may lag.
+// Bounded wait on a per-block barrier. In a pair the other CTA's arrivals on it are MMA
+// commits (for data the waiter reads through tcgen05 after tcgen05.fence::after_thread_sync)
+// and P-ready signals (for P in tensor memory), so a CTA-scope acquire is enough.
+template <bool PAIR>
+__device__ __forceinline__ bool fwait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+    return mbar_wait(bar, parity, abort_flag, kWaitLimitNs);
+}
+// Signal the barrier at `bar`'s offset in the pair's leader (this CTA's own otherwise).
+template <bool PAIR>
+__device__ __forceinline__ void arrive_leader(uint64_t* bar, uint32_t rank) {
+    if (PAIR && rank != 0)
+        mbar_arrive_remote_signal(mapa_shared(smem_u32(bar), 0));
+    else
+        mbar_arrive(bar);
+}
+// Release an item slot on the leader's free barrier: at cluster scope, since the leader then
+// rewrites the slot in this CTA's shared memory with a generic store.
+template <bool PAIR>
+__device__ __forceinline__ void release_item_slot(uint64_t* bar, uint32_t rank) {
+    if (PAIR && rank != 0)
+        mbar_arrive_remote(mapa_shared(smem_u32(bar), 0));
+    else
+        mbar_arrive(bar);
+}
+// MMA commit to the barrier at `bar`'s offset in every CTA that waits on it.
+template <bool PAIR>
+__device__ __forceinline__ void commit_all(uint64_t* bar) {
+    if constexpr (PAIR)
+        mma_commit_pair_multicast(bar, kPairMask);
+    else
+        mma_commit(bar);
+}
+
+// The j-th work item from this CTA's 4-slot ring (false: the wait gave up), which the
+// producer (in a pair, the leader's, in both CTAs) writes. Each reader then frees the slot on
+// the leader's free barrier; the slot is rewritten only once every reader has, because a
+// softmax group whose tile has no blocks in a run of items is not held back by the MMAs and
+// may lag.
+template <bool PAIR>
 __device__ __forceinline__ bool fwd_read_item(uint64_t* item_bars, volatile int* ring, int j,
                                               volatile int* abort_flag, int& idx) {
-    if (!mbar_wait(&item_bars[j & 3], (j >> 2) & 1, abort_flag, kWaitLimitNs)) return false;
+    // the slot was written by the leader's producer, in a pair with a remote generic store
+    const bool got = PAIR ? mbar_wait_cluster(&item_bars[j & 3], (j >> 2) & 1, abort_flag, kWaitLimitNs)
+                          : mbar_wait(&item_bars[j & 3], (j >> 2) & 1, abort_flag, kWaitLimitNs);
+    if (!got) return false;
     idx = ring[j & 3];
     return true;
 }
+// Readers of an item slot: the MMA thread and the 8 softmax warps; in a pair the leader's
+// MMA thread, both CTAs' softmax warps and the peer's producer.
+template <bool PAIR>
+__host__ __device__ constexpr int fwd_slot_readers() {
+    return PAIR ? 1 + 2 * 8 + 1 : 1 + 8;
+}
 
-template <int D, bool F16>
+template <int D, bool F16, bool PAIR>
 __global__ void __maxnreg__(kLaunchRegs)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                     const __grid_constant__ CUtensorMap tmOres, const FwdArgs a) {
-    using L = FwdSmem<D>;
+    using L = FwdSmem<D, PAIR>;
+    constexpr int S = L::kStages;
     pdl_wait();   // the work list and the header come from the scheduler launched just before
     const int count = a.hdr->fwd_count;
-    if ((int)blockIdx.x >= count) return;
-    // once any CTA of this launch has timed out, the rest skip their work
-    if (*(volatile int*)&a.hdr->status != (int)USP_OK) return;
+    const uint32_t rank = PAIR ? cluster_ctarank() : 0;
+    const int unit = PAIR ? (int)blockIdx.x >> 1 : (int)blockIdx.x;   // this pair (or CTA)
+    const int units = PAIR ? (int)gridDim.x >> 1 : (int)gridDim.x;
+    // the same answer in both CTAs of a pair (the count is final): they take the same path
+    if (unit >= count) return;
+    if constexpr (!PAIR) {
+        // once any CTA of this launch has timed out, the rest skip their work (a pair's leader
+        // checks before each item and ends both CTAs' work through the item ring)
+        if (*(volatile int*)&a.hdr->status != (int)USP_OK) return;
+    }
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -126,24 +241,31 @@ __global__ void __maxnreg__(kLaunchRegs)
     const int lane = threadIdx.x % 32;
 
     if (warp == 9) {
-        tmem_alloc(tmem_slot, 512);
-        tmem_relinquish();
+        if constexpr (PAIR) {
+            tmem_alloc_pair(tmem_slot, 512);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(tmem_slot, 512);
+            tmem_relinquish();
+        }
     }
     if (threadIdx.x == 0) {
         mbar_init(&bars[L::bQFull], 1);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < S; ++i) {
             mbar_init(&bars[L::bKFull + i], 1);
             mbar_init(&bars[L::bVFull + i], 1);
-            mbar_init(&bars[L::bKvEmpty + i], 1);
+            mbar_init(&bars[L::bKvEmpty + i], 1);   // the releasing softmax thread
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(&bars[L::bSFull + i], 1);
-            mbar_init(&bars[L::bPFull + i], 4);
+            mbar_init(&bars[L::bPFull + i], PAIR ? 8 : 4);   // the tile's softmax warps (of both CTAs)
             mbar_init(&bars[L::bODone + i], 1);
         }
         mbar_init(&bars[L::bDrain], 1);
         mbar_init(&bars[L::bQEmpty], 1);
         for (int i = 0; i < 4; ++i) {
             mbar_init(&bars[L::bItem + i], 1);
-            mbar_init(&bars[L::bItemFree + i], 1 + 8);   // the MMA thread and the 8 softmax warps
+            mbar_init(&bars[L::bItemFree + i], fwd_slot_readers<PAIR>());
         }
         *abort_flag = 0;
         fence_barrier_init();
@@ -152,12 +274,14 @@ __global__ void __maxnreg__(kLaunchRegs)
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = *tmem_slot;
+    // the peer's barriers are initialised before any remote arrival or copy reaches them
+    if constexpr (PAIR) cluster_sync_all();
 
-    // Every per-block barrier phase follows a running count across items (the CTA's key/value
-    // blocks for the K/V ring, each tile's blocks for S and P); Q's follow the item count j,
-    // and a tile's O-done the count of items in which that tile has blocks. Each phase of
-    // these barriers needs its waiter to have passed the one before, so a waiter is never
-    // two phases behind and parities cannot alias.
+    // Every per-block barrier phase follows a running count across items (the key/value
+    // blocks for the ring, each tile's blocks for S and P); Q's follow the item count j, and a
+    // tile's O-done the count of items in which that tile has blocks. Each phase of these
+    // barriers needs its waiter to have passed the one before, so a waiter is never two
+    // phases behind and parities cannot alias.
     if (warp >= 10) {
         regs_decrease<kAuxRegs>();  // idle warps of the load/MMA warpgroup
     } else if (warp == 8) {
@@ -167,141 +291,189 @@ __global__ void __maxnreg__(kLaunchRegs)
             prefetch_tmap(&tmQ);
             prefetch_tmap(&tmK);
             prefetch_tmap(&tmV);
+            // a load completes on the leader's barrier in a pair, on this CTA's otherwise
+            auto load = [&](void* dst, const CUtensorMap* map, uint64_t* bar, int x, int row, int h) {
+                if constexpr (PAIR)
+                    tma_load_rows_pair(dst, map, mapa_shared(smem_u32(bar), 0), x, row, h, a.token_major);
+                else
+                    tma_load_rows(dst, map, bar, x, row, h, a.token_major);
+            };
+            const bool leader = rank == 0;
             bool ok = true;
             int gn = 0, q_loads = 0;
-            int next_idx = (int)blockIdx.x;
-            for (int j = 0; ok && next_idx >= 0; ++j) {
-                const int idx = next_idx;
-                next_idx = -1;
-                // every reader has taken the item this slot held four items ago
-                if (j >= 4 && !mbar_wait(&item_free[j & 3], ((j >> 2) - 1) & 1, abort_flag, kWaitLimitNs)) break;
-                item_ring[j & 3] = idx;
-                mbar_arrive(&item_bars[j & 3]);   // release: the slot write is visible to its readers
+            int next_idx = unit;
+            for (int j = 0; ok; ++j) {
+                int idx;
+                if (leader) {
+                    idx = next_idx;
+                    next_idx = -1;
+                    // once any CTA of this launch has timed out, the rest end their work
+                    if (PAIR && *(volatile int*)&a.hdr->status != (int)USP_OK) idx = count;
+                    // every reader has taken the item this slot held four items ago
+                    if (j >= 4 && !(PAIR ? mbar_wait_cluster(&item_free[j & 3], ((j >> 2) - 1) & 1, abort_flag,
+                                                             kWaitLimitNs)
+                                         : mbar_wait(&item_free[j & 3], ((j >> 2) - 1) & 1, abort_flag,
+                                                     kWaitLimitNs)))
+                        break;
+                    item_ring[j & 3] = idx;
+                    mbar_arrive(&item_bars[j & 3]);   // release: the slot write is visible to its readers
+                    if constexpr (PAIR) {
+                        st_cluster_u32(mapa_shared(smem_u32((const void*)&item_ring[j & 3]), 1), (uint32_t)idx);
+                        mbar_arrive_remote(mapa_shared(smem_u32(&item_bars[j & 3]), 1));
+                    }
+                } else {
+                    if (!fwd_read_item<PAIR>(item_bars, item_ring, j, abort_flag, idx)) break;
+                    release_item_slot<PAIR>(&item_free[j & 3], rank);
+                }
                 if (idx >= count) break;
-                const FwdItem f = fwd_item(a, idx);
+                const FwdItem f = fwd_item<PAIR>(a, idx, rank);
                 // the Q buffers are free once the previous item's last Q.K^T has run
-                if (j > 0 && !mbar_wait(&bars[L::bQEmpty], (j - 1) & 1, abort_flag, kWaitLimitNs)) break;
+                if (j > 0 && !fwait<PAIR>(&bars[L::bQEmpty], (j - 1) & 1, abort_flag)) break;
                 const int ntiles = f.nb1 > 0 ? 2 : 1;
-                mbar_arrive_expect_tx(&bars[L::bQFull], ntiles * L::kTileBytes);
+                if (leader) mbar_arrive_expect_tx(&bars[L::bQFull], (PAIR ? 2 : 1) * ntiles * L::kTileBytes);
                 for (int t = 0; t < ntiles; ++t)
                     for (int p = 0; p < L::kPanels; ++p)
-                        tma_load_rows(sm + (t ? L::kQ1 : L::kQ0) + p * (kTileM * 128), &tmQ, &bars[L::bQFull], p * 64,
-                                      t ? f.q01 : f.q00, f.h, a.token_major);
+                        load(sm + (t ? L::kQ1 : L::kQ0) + p * (kTileM * 128), &tmQ, &bars[L::bQFull], p * 64,
+                             t ? f.q01 : f.q00, f.h);
                 ++q_loads;
                 for (int n = 0; n < f.nmax; ++n, ++gn) {
-                    const int st = gn & 1;
-                    if (gn >= 2 && !mbar_wait(&bars[L::bKvEmpty + st], ((gn >> 1) - 1) & 1, abort_flag, kWaitLimitNs)) {
+                    const int st = gn % S;
+                    if (gn >= S && !fwait<PAIR>(&bars[L::bKvEmpty + st], ((gn / S) - 1) & 1, abort_flag)) {
                         ok = false;
                         break;
                     }
                     const int row = f.s + n * kBlockN;
-                    mbar_arrive_expect_tx(&bars[L::bKFull + st], L::kTileBytes);
+                    const int krow = row + (int)rank * L::kKRows;   // this CTA's keys of the block
+                    const int vcol = (int)rank * 64 * L::kVPanels;  // and its columns of V
+                    if (leader) {
+                        mbar_arrive_expect_tx(&bars[L::bKFull + st], (PAIR ? 2 : 1) * L::kKBytes);
+                        mbar_arrive_expect_tx(&bars[L::bVFull + st], (PAIR ? 2 : 1) * L::kVBytes);
+                    }
+                    USP_FTL(gn, 13);
                     for (int p = 0; p < L::kPanels; ++p)
-                        tma_load_rows(sm + L::kK + st * L::kTileBytes + p * (kTileM * 128), &tmK, &bars[L::bKFull + st],
-                                      p * 64, row, f.kvh, a.token_major);
-                    mbar_arrive_expect_tx(&bars[L::bVFull + st], L::kTileBytes);
-                    for (int p = 0; p < L::kPanels; ++p)
-                        tma_load_rows(sm + L::kV + st * L::kTileBytes + p * (kTileM * 128), &tmV, &bars[L::bVFull + st],
-                                      p * 64, row, f.kvh, a.token_major);
+                        load(sm + L::kK + st * L::kKBytes + p * L::kKPanel, &tmK, &bars[L::bKFull + st], p * 64, krow,
+                             f.kvh);
+                    USP_FTL(gn, 14);
+                    for (int p = 0; p < L::kVPanels; ++p)
+                        load(sm + L::kV + st * L::kVBytes + p * (kBlockN * 128), &tmV, &bars[L::bVFull + st],
+                             vcol + p * 64, row, f.kvh);
                     // The CTAs walk the same key/value blocks in near lockstep, so a block's first
-                    // load goes to DRAM for all of them: pull K and V two blocks ahead into L2.
+                    // load goes to DRAM for all of them: pull this CTA's share two blocks ahead into L2.
                     if (n + 2 < f.nmax) {
-                        for (int p = 0; p < L::kPanels; ++p) {
-                            tma_prefetch_rows(&tmK, p * 64, row + 2 * kBlockN, f.kvh, a.token_major);
-                            tma_prefetch_rows(&tmV, p * 64, row + 2 * kBlockN, f.kvh, a.token_major);
-                        }
+                        for (int p = 0; p < L::kPanels; ++p)
+                            tma_prefetch_rows(&tmK, p * 64, krow + 2 * kBlockN, f.kvh, a.token_major);
+                        for (int p = 0; p < L::kVPanels; ++p)
+                            tma_prefetch_rows(&tmV, vcol + p * 64, row + 2 * kBlockN, f.kvh, a.token_major);
                     }
                     // two blocks before the end, reserve the next item and pull its Q into L2
-                    if (n == (f.nmax >= 2 ? f.nmax - 2 : 0)) {
-                        next_idx = (int)gridDim.x + atomicAdd(&a.hdr->fwd_next, 1);
+                    if (leader && n == (f.nmax >= 2 ? f.nmax - 2 : 0)) {
+                        next_idx = units + atomicAdd(&a.hdr->fwd_next, 1);
                         if (next_idx < count) {
-                            const FwdItem nf = fwd_item(a, next_idx);
-                            for (int p = 0; p < L::kPanels; ++p) {
-                                tma_prefetch_rows(&tmQ, p * 64, nf.q00, nf.h, a.token_major);
-                                if (nf.nb1 > 0) tma_prefetch_rows(&tmQ, p * 64, nf.q01, nf.h, a.token_major);
-                            }
+                            const WorkItem nit = a.items[next_idx];
+                            const int nbase = a.cu[nit.seq] + nit.tile * fwd_item_rows<PAIR>();
+                            const int nend = a.cu[nit.seq + 1];
+                            for (int r = 0; r < fwd_item_rows<PAIR>() && nbase + r < nend; r += kTileM)
+                                for (int p = 0; p < L::kPanels; ++p)
+                                    tma_prefetch_rows(&tmQ, p * 64, nbase + r, nit.head, a.token_major);
                         }
                     }
                 }
+                // (every item has blocks: its first tile starts inside its sample; kept for safety)
+                if (leader && ok && next_idx < 0) next_idx = units + atomicAdd(&a.hdr->fwd_next, 1);
             }
-            // Before the CTA may exit, every copy it issued must have landed. The last use of
-            // each barrier is its final phase, so waiting on it is always sound.
-            if (q_loads > 0) mbar_wait_drain(&bars[L::bQFull], (q_loads - 1) & 1, kDrainLimitNs);
-            for (int n = gn - 2 < 0 ? 0 : gn - 2; n < gn; ++n) {
-                mbar_wait_drain(&bars[L::bKFull + (n & 1)], (n >> 1) & 1, kDrainLimitNs);
-                mbar_wait_drain(&bars[L::bVFull + (n & 1)], (n >> 1) & 1, kDrainLimitNs);
+            // Before the CTAs may exit, every copy must have landed. In a pair all of them
+            // complete on the leader's barriers (the CTAs leave together, after both have
+            // finished). The last use of each barrier is its final phase, so waiting on it is
+            // always sound.
+            if (leader) {
+                if (q_loads > 0) mbar_wait_drain(&bars[L::bQFull], (q_loads - 1) & 1, kDrainLimitNs);
+                for (int n = gn - S < 0 ? 0 : gn - S; n < gn; ++n) {
+                    mbar_wait_drain(&bars[L::bKFull + n % S], (n / S) & 1, kDrainLimitNs);
+                    mbar_wait_drain(&bars[L::bVFull + n % S], (n / S) & 1, kDrainLimitNs);
+                }
             }
         }
     } else if (warp == 9) {
         regs_decrease<kAuxRegs>();
         // ------------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idS = idesc_16b_f32(kTileM, kBlockN, false, false, F16);  // Q.K^T: both K-major
-            constexpr uint32_t idO = idesc_16b_f32(kTileM, D, false, true, F16);         // P.V: V is MN-major
+        if (lane == 0 && rank == 0) {
+            constexpr int M = PAIR ? 2 * kTileM : kTileM;
+            constexpr uint32_t idS = idesc_16b_f32(M, kBlockN, false, false, F16);  // Q.K^T: both K-major
+            constexpr uint32_t idO = idesc_16b_f32(M, D, false, true, F16);         // P.V: V is MN-major
             // The 64-bit shared-memory descriptors are built once; a K step only adds a constant
             // to the start-address field (addresses stay below 2^18, so the field never carries).
             // Rebuilding them per MMA made the issuing thread, not the tensor core, the limit.
             const uint64_t dQ0 = sdesc_sw128(smem_u32(sm + L::kQ0), 0, 1024);
             const uint64_t dQ1 = sdesc_sw128(smem_u32(sm + L::kQ1), 0, 1024);
             const uint64_t dK0 = sdesc_sw128(smem_u32(sm + L::kK), 0, 1024);
-            const uint64_t dK1 = dK0 + (uint64_t)(L::kTileBytes >> 4);
-            const uint64_t dV0 = sdesc_sw128(smem_u32(sm + L::kV), kTileM * 128, 1024);
-            const uint64_t dV1 = dV0 + (uint64_t)(L::kTileBytes >> 4);
+            const uint64_t dV0 = sdesc_sw128(smem_u32(sm + L::kV), kBlockN * 128, 1024);
             auto issue_s = [&](int t, int st) {
-                const uint64_t ad = t ? dQ1 : dQ0, bd = st ? dK1 : dK0;
+                const uint64_t ad = t ? dQ1 : dQ0, bd = dK0 + (uint64_t)((st * L::kKBytes) >> 4);
                 const uint32_t d = tbase + t * 128;
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
-                    constexpr uint32_t kPanel = kTileM * 128;
-                    const uint64_t off = (uint64_t)((((k / 4) * kPanel) + (k % 4) * 32) >> 4);
-                    mma_ss(d, ad + off, bd + off, idS, k > 0);
+                    const uint64_t aoff = (uint64_t)((((k / 4) * (kTileM * 128)) + (k % 4) * 32) >> 4);
+                    const uint64_t boff = (uint64_t)((((k / 4) * L::kKPanel) + (k % 4) * 32) >> 4);
+                    if constexpr (PAIR)
+                        mma_ss_pair(d, ad + aoff, bd + boff, idS, k > 0);
+                    else
+                        mma_ss(d, ad + aoff, bd + boff, idS, k > 0);
                 }
-                mma_commit(&bars[L::bSFull + t]);
+                commit_all<PAIR>(&bars[L::bSFull + t]);
             };
             auto issue_pv = [&](int t, int st, bool acc) {
-                const uint64_t bd = st ? dV1 : dV0;
+                const uint64_t bd = dV0 + (uint64_t)((st * L::kVBytes) >> 4);
                 const uint32_t d = tbase + 256 + t * 128, a_t = tbase + t * 128;
 #pragma unroll
-                for (int k = 0; k < kBlockN / 16; ++k)
-                    mma_ts(d, a_t + k * 8, bd + (uint64_t)((k * 2048) >> 4), idO, (acc || k > 0) ? 1u : 0u);
+                for (int k = 0; k < kBlockN / 16; ++k) {
+                    if constexpr (PAIR)
+                        mma_ts_pair(d, a_t + k * 8, bd + (uint64_t)((k * 2048) >> 4), idO, (acc || k > 0) ? 1u : 0u);
+                    else
+                        mma_ts(d, a_t + k * 8, bd + (uint64_t)((k * 2048) >> 4), idO, (acc || k > 0) ? 1u : 0u);
+                }
             };
+            // This thread commits only the S-ready and O-done signals: the softmax releases the
+            // ring stages and Q (a commit right behind another one holds the issuing thread until
+            // the first has been delivered, which left the tensor pipe idle before each P.V).
             bool ok = true;
-            int gn = 0, pb0 = 0, pb1 = 0;   // blocks of the CTA, of tile 0, of tile 1 before this item
+            int gn = 0, pb0 = 0, pb1 = 0;   // blocks of the ring, of tile 0, of tile 1 before this item
             for (int j = 0; ok; ++j) {
                 int idx;
-                if (!fwd_read_item(item_bars, item_ring, j, abort_flag, idx)) break;
+                if (!fwd_read_item<PAIR>(item_bars, item_ring, j, abort_flag, idx)) break;
                 mbar_arrive(&item_free[j & 3]);
                 if (idx >= count) break;
-                const FwdItem f = fwd_item(a, idx);
-                if (!mbar_wait(&bars[L::bQFull], j & 1, abort_flag, kWaitLimitNs)) break;
+                const FwdItem f = fwd_item<PAIR>(a, idx, 0);
+                if (!fwait<PAIR>(&bars[L::bQFull], j & 1, abort_flag)) break;
                 if (f.nmax > 0) {
-                    if (!mbar_wait(&bars[L::bKFull + (gn & 1)], (gn >> 1) & 1, abort_flag, kWaitLimitNs)) break;
+                    if (!fwait<PAIR>(&bars[L::bKFull + gn % S], (gn / S) & 1, abort_flag)) break;
                     tc_fence_after();
                     // The scores regions are free: the previous item's last P.V, which read them,
                     // was issued before these (tensor-core MMAs run in issue order).
-                    if (f.nb0 > 0) issue_s(0, gn & 1);
-                    if (f.nb1 > 0) issue_s(1, gn & 1);
+                    if (f.nb0 > 0) issue_s(0, gn % S);
+                    if (f.nb1 > 0) issue_s(1, gn % S);
                 }
-                if (f.nmax <= 1) mma_commit(&bars[L::bQEmpty]);   // no later Q.K^T in this item
                 for (int n = 0; ok && n < f.nmax; ++n) {
-                    const int gb = gn + n, st = gb & 1;
-                    if (!mbar_wait(&bars[L::bVFull + st], (gb >> 1) & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
+                    const int gb = gn + n, st = gb % S;
+                    USP_FTL(gb, 15);
+                    if (!fwait<PAIR>(&bars[L::bVFull + st], (gb / S) & 1, abort_flag)) { ok = false; break; }
+                    USP_FTL(gb, 0);
                     bool next_k_ready = false;
                     for (int t = 0; t < 2 && ok; ++t) {
                         const int nbt = t ? f.nb1 : f.nb0;
                         if (n >= nbt) continue;
-                        if (!mbar_wait(&bars[L::bPFull + t], ((t ? pb1 : pb0) + n) & 1, abort_flag, kWaitLimitNs)) {
+                        if (!fwait<PAIR>(&bars[L::bPFull + t], ((t ? pb1 : pb0) + n) & 1, abort_flag)) {
                             ok = false;
                             break;
                         }
+                        USP_FTL(gb, 1 + t);
                         tc_fence_after();
                         issue_pv(t, st, n > 0);
                         if (n == nbt - 1) {
-                            mma_commit(&bars[L::bODone + t]);
+                            commit_all<PAIR>(&bars[L::bODone + t]);
                         } else {
-                            const int st1 = (gb + 1) & 1;
+                            const int st1 = (gb + 1) % S;
                             if (!next_k_ready) {
-                                if (!mbar_wait(&bars[L::bKFull + st1], ((gb + 1) >> 1) & 1, abort_flag, kWaitLimitNs)) {
+                                if (!fwait<PAIR>(&bars[L::bKFull + st1], ((gb + 1) / S) & 1, abort_flag)) {
                                     ok = false;
                                     break;
                                 }
@@ -309,10 +481,9 @@ __global__ void __maxnreg__(kLaunchRegs)
                                 next_k_ready = true;
                             }
                             issue_s(t, st1);
+                            USP_FTL(gb, 3 + t);
                         }
                     }
-                    if (ok && n == f.nmax - 2) mma_commit(&bars[L::bQEmpty]);   // the item's last Q.K^T is issued
-                    mma_commit(&bars[L::bKvEmpty + st]);
                 }
                 if (!ok) break;
                 gn += f.nmax;
@@ -320,7 +491,7 @@ __global__ void __maxnreg__(kLaunchRegs)
                 pb1 += f.nb1;
             }
             // Drain: the tensor pipe must be idle before TMEM is released.
-            mma_commit(&bars[L::bDrain]);
+            commit_all<PAIR>(&bars[L::bDrain]);
             mbar_wait_drain(&bars[L::bDrain], 0, kDrainLimitNs);
         }
     } else {
@@ -334,19 +505,31 @@ __global__ void __maxnreg__(kLaunchRegs)
         const float sl2 = a.scale_log2;
         int pb = 0;   // this tile's blocks before the current item
         int od = 0;   // items before the current one in which this tile has blocks
+        int gq = 0;   // ring blocks before the current item
         for (int j = 0;; ++j) {
             int idx = count;
-            bool ok = fwd_read_item(item_bars, item_ring, j, abort_flag, idx);
+            bool ok = fwd_read_item<PAIR>(item_bars, item_ring, j, abort_flag, idx);
             __syncwarp();
-            if (ok && lane == 0) mbar_arrive(&item_free[j & 3]);
-            const FwdItem f = fwd_item(a, ok && idx < count ? idx : 0);
+            if (ok && lane == 0) release_item_slot<PAIR>(&item_free[j & 3], rank);
+            const FwdItem f = fwd_item<PAIR>(a, ok && idx < count ? idx : 0, rank);
             const int s = f.s, e = f.e, h = f.h;
             const int q0 = t ? f.q01 : f.q00;
             const int nbt = (ok && idx < count) ? (t ? f.nb1 : f.nb0) : 0;
             const int i = q0 + rq;  // this thread's query row
+            // The releasing tile has the item's most blocks: tile 1 unless its rows lie past the
+            // sample's end (tile 1's rows follow tile 0's, so nb1 >= nb0 whenever nb1 > 0). The
+            // tensor pipe runs PV0(n), S0(n+1), PV1(n), S1(n+1) in order, so once it has seen S(n)
+            // complete, every MMA reading block n-1 (its Q.K^T and both P.V) has run; its O-done
+            // covers the last block, and its last S completes the item's last Q.K^T.
+            const bool releaser = (t == (f.nb1 > 0 ? 1 : 0)) && rq == 0;
             float m = -INFINITY, l = 0.f;
             for (int n = 0; n < nbt; ++n) {
-                if (!mbar_wait(&bars[L::bSFull + t], (pb + n) & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
+                if (!fwait<PAIR>(&bars[L::bSFull + t], (pb + n) & 1, abort_flag)) { ok = false; break; }
+                if (releaser) {
+                    if (n > 0) mbar_arrive(&bars[L::bKvEmpty + (gq + n - 1) % S]);   // block n-1 is read
+                    if (n == nbt - 1) mbar_arrive(&bars[L::bQEmpty]);               // Q is read
+                }
+                if (rq == 0) USP_FTL(pb + n, 5 + 4 * t);
                 tc_fence_after();
                 uint32_t r0[32], r1[32], r2[32], r3[32];
                 tmem_ld32(tS + 0, r0);
@@ -388,6 +571,7 @@ __global__ void __maxnreg__(kLaunchRegs)
                 for (int j = 0; j < 8; ++j) mx8[j] = fmaxf(mx8[j], sv[120 + j]);
                 const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
                 const float m_blk = mx * sl2;
+                if (rq == 0) USP_FTL(pb + n, 6 + 4 * t);
                 if (n == 0) {
                     m = m_blk;
                 } else if (m_blk > m + kRescaleThreshold) {
@@ -429,10 +613,13 @@ __global__ void __maxnreg__(kLaunchRegs)
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[L::bPFull + t]);
+                if (rq == 0) USP_FTL(pb + n, 8 + 4 * t);
+                if (lane == 0) arrive_leader<PAIR>(&bars[L::bPFull + t], rank);   // P ready for the MMA issuer
+                if (rq == 0) USP_FTL(pb + n, 7 + 4 * t);
 
             }
-            if (ok && nbt > 0) ok = mbar_wait(&bars[L::bODone + t], od & 1, abort_flag, kWaitLimitNs);
+            if (ok && nbt > 0) ok = fwait<PAIR>(&bars[L::bODone + t], od & 1, abort_flag);
+            if (ok && releaser && nbt > 0) mbar_arrive(&bars[L::bKvEmpty + (gq + nbt - 1) % S]);   // the last block
             // The group's warps leave together (a warp that gave up on a wait must not leave the
             // others at the epilogue's barriers); the ring's end marker ends every warp's loop.
             if (group_any(1 + t, 128, !ok) || idx >= count) break;
@@ -557,6 +744,7 @@ __global__ void __maxnreg__(kLaunchRegs)
                 if (valid) a.lse[(int64_t)h * a.T + i] = (m + __log2f(l)) * 0.69314718055994530942f;
             }
             pb += nbt;
+            gq += f.nmax;
         }
         if (rq == 0) bulk_wait_group<0>();   // the last output stores have landed
     }
@@ -564,21 +752,51 @@ __global__ void __maxnreg__(kLaunchRegs)
     __syncwarp();
     tc_fence_before();
     __syncthreads();
-    if (warp == 9) tmem_dealloc(tbase, 512);
+    if constexpr (PAIR) {
+        // neither CTA leaves (or frees tensor memory the pair's MMAs write) while the other may
+        // still copy into it, arrive on its barriers or run MMAs on it
+        cluster_sync_all();
+        if (warp == 9) tmem_dealloc_pair(tbase, 512);
+    } else {
+        if (warp == 9) tmem_dealloc(tbase, 512);
+    }
     if (threadIdx.x == 0 && *abort_flag) atomicCAS(&a.hdr->status, (int)USP_OK, (int)USP_ERR_TIMEOUT);
 }
 
-template <int D, bool F16>
+#ifdef USP_TIMELINE
+}  // namespace
+// The forward's timeline (kFTlCtas x kFTlSteps x kFTlEvents clock64 values) into host memory.
+extern "C" int usp_debug_fwd_timeline(void* host_dst, size_t bytes) {
+    if (bytes < sizeof(g_fwd_timeline)) return (int)USP_ERR_INVALID_ARG;
+    return cudaMemcpyFromSymbol(host_dst, g_fwd_timeline, sizeof(g_fwd_timeline)) == cudaSuccess ? 0
+                                                                                                 : (int)USP_ERR_CUDA;
+}
+namespace {
+#endif
+
+template <int D, bool F16, bool PAIR>
 cudaError_t launch_fwd_impl(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& o,
                             const CUtensorMap& ores, const FwdArgs& a, int grid, cudaStream_t s) {
-    using L = FwdSmem<D>;
-    // persistent CTAs, one per SM (the shared-memory footprint allows no more)
-    int sms = 0;
-    const cudaError_t e = persistent_setup<attn_fwd_kernel<D, F16>>((size_t)L::kAlloc, &sms);
-    if (e != cudaSuccess) return e;
-    if (grid > sms) grid = sms;
-    return launch_kernel(attn_fwd_kernel<D, F16>, dim3(grid), dim3(kFwdThreads), (size_t)L::kAlloc, s, true, q, k, v,
-                         o, ores, a);
+    using L = FwdSmem<D, PAIR>;
+    if constexpr (PAIR) {
+        // persistent pairs, one CTA per SM (the shared-memory footprint allows no more): as
+        // many as can be resident at once
+        int pairs_cap = 0;
+        const cudaError_t e =
+            persistent_cluster_setup<attn_fwd_kernel<D, F16, PAIR>>((size_t)L::kAlloc, kFwdThreads, 2, &pairs_cap);
+        if (e != cudaSuccess) return e;
+        const int pairs = grid < pairs_cap ? grid : pairs_cap;
+        return launch_kernel_cluster(attn_fwd_kernel<D, F16, PAIR>, dim3(2 * pairs), dim3(kFwdThreads),
+                                     (size_t)L::kAlloc, s, true, 2, q, k, v, o, ores, a);
+    } else {
+        // persistent CTAs, one per SM
+        int sms = 0;
+        const cudaError_t e = persistent_setup<attn_fwd_kernel<D, F16, PAIR>>((size_t)L::kAlloc, &sms);
+        if (e != cudaSuccess) return e;
+        if (grid > sms) grid = sms;
+        return launch_kernel(attn_fwd_kernel<D, F16, PAIR>, dim3(grid), dim3(kFwdThreads), (size_t)L::kAlloc, s, true,
+                             q, k, v, o, ores, a);
+    }
 }
 
 }  // namespace
@@ -586,12 +804,14 @@ cudaError_t launch_fwd_impl(const CUtensorMap& q, const CUtensorMap& k, const CU
 cudaError_t launch_attn_fwd(int head_dim, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                             const CUtensorMap& o, const CUtensorMap& o_res, const FwdArgs& a, int grid,
                             cudaStream_t s) {
+    static_assert(fwd_item_rows<true>() == fwd_rows_per_item(128) && fwd_item_rows<false>() == fwd_rows_per_item(64),
+                  "the scheduler's forward items and the kernels' must agree");
     if (a.f16) {
-        if (head_dim == 128) return launch_fwd_impl<128, true>(q, k, v, o, o_res, a, grid, s);
-        return launch_fwd_impl<64, true>(q, k, v, o, o_res, a, grid, s);
+        if (head_dim == 128) return launch_fwd_impl<128, true, true>(q, k, v, o, o_res, a, grid, s);
+        return launch_fwd_impl<64, true, false>(q, k, v, o, o_res, a, grid, s);
     }
-    if (head_dim == 128) return launch_fwd_impl<128, false>(q, k, v, o, o_res, a, grid, s);
-    return launch_fwd_impl<64, false>(q, k, v, o, o_res, a, grid, s);
+    if (head_dim == 128) return launch_fwd_impl<128, false, true>(q, k, v, o, o_res, a, grid, s);
+    return launch_fwd_impl<64, false, false>(q, k, v, o, o_res, a, grid, s);
 }
 
 }  // namespace usp

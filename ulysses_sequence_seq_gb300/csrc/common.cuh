@@ -15,8 +15,11 @@ namespace usp {
 // Rows of one attention tile (tensor-core M) and of one key/value block (N).
 constexpr int kTileM = 128;
 constexpr int kBlockN = 128;
-// The forward gives each CTA two query tiles (256 rows); the backward one key/value tile.
-constexpr int kFwdRowsPerItem = 2 * kTileM;
+// A forward work item is four query tiles (512 rows) for head_dim 128, run by a pair of CTAs
+// sharing each MMA, and two (256 rows) for head_dim 64, run by one CTA; a backward item is
+// one key/value tile.
+__host__ __device__ constexpr int fwd_rows_per_item(int head_dim) { return head_dim == 128 ? 4 * kTileM : 2 * kTileM; }
+constexpr int kFwdRowsMax = 4 * kTileM;
 constexpr int kBwdRowsPerItem = kTileM;
 
 // Wall-clock limit of every bounded wait inside the attention kernels, and of the
@@ -69,7 +72,7 @@ __host__ __device__ __forceinline__ int64_t act_row(int h, int64_t t, int64_t T,
 inline usp_status check_attn_sizes(int64_t T, int num_seqs, int hq, int hkv, int D, const int32_t* cu) {
     if (T < 0 || hq < 1 || hkv < 1 || hq % hkv != 0) return USP_ERR_INVALID_ARG;
     if (T > 0 && (num_seqs < 1 || !cu)) return USP_ERR_INVALID_ARG;
-    if (T > (int64_t)2147483647 - 2 * kFwdRowsPerItem || num_seqs > (1 << 24)) return USP_ERR_UNSUPPORTED;
+    if (T > (int64_t)2147483647 - 2 * kFwdRowsMax || num_seqs > (1 << 24)) return USP_ERR_UNSUPPORTED;
     if (D != 64 && D != 128) return USP_ERR_UNSUPPORTED;
     if ((int64_t)hq * (T / kTileM + num_seqs + 1) > (int64_t)2147483647 / 2) return USP_ERR_UNSUPPORTED;
     return USP_OK;
@@ -86,7 +89,7 @@ inline int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 inline WsLayout ws_layout(int64_t T, int num_seqs, int hq, int hkv, int D, int bwd) {
     WsLayout w{};
-    const int64_t rows_per_item = bwd ? kBwdRowsPerItem : kFwdRowsPerItem;
+    const int64_t rows_per_item = bwd ? kBwdRowsPerItem : fwd_rows_per_item(D);
     const int64_t heads = bwd ? hkv : hq;
     const int64_t tiles = ceil_div64(T, rows_per_item) + num_seqs;
     // costs are counted in key/value blocks (x query heads per kv head for the backward)
@@ -162,6 +165,42 @@ cudaError_t persistent_setup(size_t smem, int* sms) {
     return *sms > 0 ? cudaSuccess : cudaErrorInvalidDevice;
 }
 
+// persistent_setup for a kernel launched in clusters of `cluster_x` CTAs: *units is how many
+// clusters can be resident at once on the device (a cluster's CTAs share one GPC, so an SM
+// count alone can overstate it), computed once per device.
+template <auto Kernel>
+cudaError_t persistent_cluster_setup(size_t smem, int threads, int cluster_x, int* units) {
+    static std::mutex mu;
+    static int clusters[kMaxDevices] = {};
+    int sms = 0;
+    cudaError_t e = persistent_setup<Kernel>(smem, &sms);
+    if (e != cudaSuccess) return e;
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    if (clusters[dev] == 0) {
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = (unsigned)cluster_x;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(sms / cluster_x * cluster_x));
+        cfg.blockDim = dim3((unsigned)threads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        e = cudaOccupancyMaxActiveClusters(&n, Kernel, &cfg);
+        if (e != cudaSuccess) return e;
+        if (n < 1) return cudaErrorInvalidConfiguration;
+        clusters[dev] = n;
+    }
+    *units = clusters[dev];
+    return cudaSuccess;
+}
+
 // Launches `kernel` on stream s; with `programmatic` the launch may overlap the end of the
 // previous kernel in the stream, and the kernel must call pdl_wait() before it reads
 // anything that kernel (or one before it) wrote.
@@ -178,6 +217,27 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
     cfg.stream = s;
     cfg.attrs = programmatic ? &attr : nullptr;
     cfg.numAttrs = programmatic ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+// launch_kernel for clusters of `cluster_x` CTAs along x (gridDim.x a multiple of it).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                  bool programmatic, int cluster_x, Args... args) {
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cluster_x;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = programmatic ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 

@@ -92,6 +92,7 @@ extern "C" usp_status usp_attn_fwd_varlen_noalloc(const void* q, const void* k, 
     sa.T = total_tokens;
     sa.heads = hq;
     sa.bwd = 0;
+    sa.fwd_rows = fwd_rows_per_item(head_dim);
     sa.causal = causal ? 1 : 0;
     sa.group = hq / hkv;
     sa.hist_len = w.hist_len;
@@ -106,7 +107,7 @@ extern "C" usp_status usp_attn_fwd_varlen_noalloc(const void* q, const void* k, 
 
     CUtensorMap mq, mk, mv, mo;   // o doubles as the (unused) residual map: fa.o_res is NULL
     if (!make_activation_map(&mq, q, total_tokens, hq, head_dim, 0) ||
-        !make_activation_map(&mk, k, total_tokens, hkv, head_dim, 0) ||
+        !make_activation_map(&mk, k, total_tokens, hkv, head_dim, 0, fwd_k_box_rows(head_dim)) ||
         !make_activation_map(&mv, v, total_tokens, hkv, head_dim, 0) ||
         !make_activation_map(&mo, o, total_tokens, hq, head_dim, 0))
         return USP_ERR_CUDA;

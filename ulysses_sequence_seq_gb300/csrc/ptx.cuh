@@ -84,6 +84,68 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     }
 }
 
+// ---- thread-block clusters (pairs of CTAs sharing key/value tiles)
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// The shared::cluster address of `saddr` (a shared::cta address of this CTA) in CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+// Arrive on an mbarrier of another CTA of the cluster (release at cluster scope: this
+// thread's earlier writes, to its own or the peer's shared memory, are visible first).
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar_addr) : "memory");
+}
+// Arrive on an mbarrier of another CTA of the cluster with the default (CTA-scope release)
+// semantics: for signals that order no generic memory writes across the CTAs, only tensor-core
+// operations already waited for and fenced (tcgen05.wait + tcgen05.fence::before_thread_sync).
+// A cluster-scope release waits for this thread's earlier writes to become visible cluster-wide,
+// which cost about a thousand cycles per arrival on the per-block path.
+__device__ __forceinline__ void mbar_arrive_remote_signal(uint32_t cluster_bar_addr) {
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar_addr) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// mbar_wait for a barrier that threads of the other CTA of the cluster arrive on (acquire at
+// cluster scope, so their writes before the arrival are visible).
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                                  uint64_t limit_ns) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait_cluster(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > limit_ns) {
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+// Every thread of both CTAs (all threads call it): release this CTA's shared-memory writes
+// and barrier initialisations to the cluster, then wait for the peer's.
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // Wait used while tearing down after an abort: ignores the abort flag (copies and MMAs
 // already in flight always finish in microseconds) but still gives up after limit_ns.
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
@@ -116,6 +178,25 @@ __device__ __forceinline__ void tma_load_rows(void* smem_dst, const CUtensorMap*
         tma_load_3d(smem_dst, map, bar, x, h, t0);
     else
         tma_load_3d(smem_dst, map, bar, x, t0, h);
+}
+
+// The same load for a CTA pair running cta_group::2 MMAs: the box lands in this CTA's shared
+// memory and completes its bytes on `bar_cluster`, a shared::cluster barrier address that may
+// be the peer CTA's (the pair's leader counts both CTAs' bytes on one barrier).
+__device__ __forceinline__ void tma_load_3d_pair(void* smem_dst, const CUtensorMap* map, uint32_t bar_cluster, int x,
+                                                 int y, int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_rows_pair(void* smem_dst, const CUtensorMap* map, uint32_t bar_cluster, int x,
+                                                   int t0, int h, int token_major) {
+    if (token_major)
+        tma_load_3d_pair(smem_dst, map, bar_cluster, x, h, t0);
+    else
+        tma_load_3d_pair(smem_dst, map, bar_cluster, x, t0, h);
 }
 
 // 3-D tiled store of a shared-memory box to global memory (rows past the tensor end are
@@ -215,6 +296,50 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                      smem_u32(bar))
                  : "memory");
+}
+
+// ---- CTA pairs sharing one MMA (tcgen05 with cta_group::2). The pair's leader (cluster rank
+// 0) issues M=256 MMAs: A's rows and the accumulator's lanes are split between the two CTAs
+// (128 each, at the same shared-memory offset / tensor-memory address), and B is split by
+// columns (the first N/2 from the leader's shared memory, the rest from the peer's). Every
+// tcgen05 instruction of such a kernel uses cta_group::2; one warp of each CTA allocates.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void mma_ss_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_ts_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive once on the barrier at `bar`'s offset in every CTA of `cta_mask` when every
+// previously issued tcgen05 op of this thread (on both SMs of the pair) completes.
+__device__ __forceinline__ void mma_commit_pair_multicast(uint64_t* bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"(cta_mask)
+        : "memory");
 }
 
 // Instruction descriptor, kind::f16: bf16 A/B, fp32 D, dense.

@@ -97,7 +97,7 @@ __device__ void schedule_body(const SchedArgs& a) {
         if (tid == 0) fail_schedule(a);
         return;
     }
-    const int rows = a.bwd ? kBwdRowsPerItem : kFwdRowsPerItem;
+    const int rows = a.bwd ? kBwdRowsPerItem : a.fwd_rows;
     // tiles per sample, then their exclusive prefix sum (prefix[num_seqs] = total)
     for (int b = tid; b <= a.num_seqs; b += nthr)
         a.prefix[b] = b < a.num_seqs ? (a.cu[b + 1] - a.cu[b] + rows - 1) / rows : 0;
@@ -132,7 +132,7 @@ __device__ void schedule_body(const SchedArgs& a) {
         const int tile = p - a.prefix[b];
         const int nt = a.prefix[b + 1] - a.prefix[b];
         const int s = a.cu[b], e = a.cu[b + 1];
-        const int cost = a.bwd ? bwd_item_cost(tile, s, e, a.causal, a.group) : fwd_item_cost(tile, s, e, a.causal);
+        const int cost = a.bwd ? bwd_item_cost(tile, s, e, a.causal, a.group) : fwd_item_cost(tile, s, e, a.causal, a.fwd_rows);
         const int rank = a.bwd ? tile : nt - 1 - tile;
         const bool head_major = e - s >= a.head_major_from;
         for (int h = 0; h < a.heads; ++h) {

@@ -12,7 +12,8 @@ struct SchedArgs {
     int num_seqs;
     int64_t T;
     int heads;           // query heads (forward) or key/value heads (backward)
-    int bwd;             // 0: forward items (two 128-row query tiles), 1: backward items (one kv tile)
+    int bwd;             // 0: forward items (fwd_rows query rows), 1: backward items (one kv tile)
+    int fwd_rows;        // fwd_rows_per_item(head_dim) for the forward
     int causal;
     int group;           // query heads per key/value head
     int hist_len;

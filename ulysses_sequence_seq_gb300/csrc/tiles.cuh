@@ -33,10 +33,12 @@ __host__ __device__ __forceinline__ int query_blocks_in_sample(int s, int e) {
     return (e - s + kTileM - 1) / kTileM;
 }
 
-// Scheduling cost of a forward item: KV blocks over its two query tiles.
-__host__ __device__ __forceinline__ int fwd_item_cost(int tile, int s, int e, int causal) {
-    const int q0 = s + tile * kFwdRowsPerItem;
-    return kv_blocks_for_query_tile(q0, s, e, causal) + kv_blocks_for_query_tile(q0 + kTileM, s, e, causal);
+// Scheduling cost of a forward item of `rows` query rows: KV blocks over its query tiles.
+__host__ __device__ __forceinline__ int fwd_item_cost(int tile, int s, int e, int causal, int rows) {
+    const int q0 = s + tile * rows;
+    int c = 0;
+    for (int r = 0; r < rows; r += kTileM) c += kv_blocks_for_query_tile(q0 + r, s, e, causal);
+    return c;
 }
 
 // Scheduling cost of a backward item: query blocks it visits, times query heads per kv head.

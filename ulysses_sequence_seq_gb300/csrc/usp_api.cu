@@ -46,10 +46,11 @@ usp_status reset_status_if_any(void* workspace, size_t ws_bytes, cudaStream_t s)
 
 }  // namespace
 
-// Tensor map over a bf16 activation, 64-column x 128-row boxes of one head, 128-byte
+// Tensor map over a bf16 activation, 64-column x box_rows-row boxes of one head, 128-byte
 // swizzled (the layout the tensor-core descriptors expect). Head-major [heads][T][D] maps
 // are (D, T, heads); token-major [T][heads][D] maps are (D, heads, T), so the strides grow.
-bool make_activation_map(CUtensorMap* map, const void* base, int64_t T, int heads, int D, int token_major) {
+bool make_activation_map(CUtensorMap* map, const void* base, int64_t T, int heads, int D, int token_major,
+                         int box_rows) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
     const cuuint64_t row = (cuuint64_t)D * 2;
@@ -58,11 +59,11 @@ bool make_activation_map(CUtensorMap* map, const void* base, int64_t T, int head
     if (token_major) {
         dims[0] = (cuuint64_t)D; dims[1] = (cuuint64_t)heads; dims[2] = (cuuint64_t)T;
         strides[0] = row; strides[1] = row * (cuuint64_t)heads;
-        box[0] = 64; box[1] = 1; box[2] = (cuuint32_t)kTileM;
+        box[0] = 64; box[1] = 1; box[2] = (cuuint32_t)box_rows;
     } else {
         dims[0] = (cuuint64_t)D; dims[1] = (cuuint64_t)T; dims[2] = (cuuint64_t)heads;
         strides[0] = row; strides[1] = row * (cuuint64_t)T;
-        box[0] = 64; box[1] = (cuuint32_t)kTileM; box[2] = 1;
+        box[0] = 64; box[1] = (cuuint32_t)box_rows; box[2] = 1;
     }
     cuuint32_t es[3] = {1, 1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
@@ -128,6 +129,7 @@ usp_status attn_fwd_impl(const void* q, const void* k, const void* v, void* o, v
     sa.T = total_tokens;
     sa.heads = hq;
     sa.bwd = 0;
+    sa.fwd_rows = fwd_rows_per_item(head_dim);
     sa.causal = causal ? 1 : 0;
     sa.group = hq / hkv;
     sa.hist_len = w.hist_len;
@@ -142,7 +144,7 @@ usp_status attn_fwd_impl(const void* q, const void* k, const void* v, void* o, v
 
     CUtensorMap mq, mk, mv, mo, mores;
     if (!make_activation_map(&mq, q, total_tokens, hq, head_dim, token_major) ||
-        !make_activation_map(&mk, k, total_tokens, hkv, head_dim, token_major) ||
+        !make_activation_map(&mk, k, total_tokens, hkv, head_dim, token_major, fwd_k_box_rows(head_dim)) ||
         !make_activation_map(&mv, v, total_tokens, hkv, head_dim, token_major) ||
         !make_activation_map(&mo, o, total_tokens, hq, head_dim, token_major) ||
         !make_activation_map(&mores, o_res ? o_res : o, total_tokens, hq, head_dim, token_major))
