@@ -78,7 +78,8 @@ struct FwdSmem {
     static constexpr int kStage = kV + kStages * kVBytes;      // O staging: one [128][64] panel per tile
     static constexpr int kBars = kStage + 2 * kTileM * 128;
     // barrier indices
-    static constexpr int bQFull = 0, bKFull = 1, bVFull = bKFull + kStages, bKvEmpty = bVFull + kStages,
+    // bKvFull: a stage's K and V both landed (one barrier, so that the MMA thread checks a block once)
+    static constexpr int bQFull = 0, bKvFull = 1, bKvEmpty = bKvFull + kStages,
                          bSFull = bKvEmpty + kStages, bPFull = bSFull + 2, bODone = bPFull + 2, bDrain = bODone + 2,
                          bQEmpty = bDrain + 1, bItem = bQEmpty + 1, bItemFree = bItem + 4, kNumBars = bItemFree + 4;
     // bItem / bItemFree: published / read by every reader, one of each per slot of the 4-slot item ring
@@ -94,8 +95,7 @@ static_assert(FwdSmem<64, false>::kAlloc <= 232448, "forward shared memory excee
 
 // Optional clock64 timeline of the first kTlSteps key/value blocks of every CTA (compile with
 // -DUSP_TIMELINE; the default build has none of it). Events by the CTA's running block count:
-// MMA thread 15 (block started), 0 (V ready), 1-2 (tile 0 / 1 P ready), 3-4 (tile 0 / 1 next S
-// issued); softmax
+// MMA thread 15 (block started), 1-2 (tile 0 / 1 P ready), 3-4 (tile 0 / 1 next S issued); softmax
 // group t 5+4t (S ready), 6+4t (row max done), 8+4t (P stored), 7+4t (P-ready arrival made);
 // producer 13-14 (K / V load issued). Read back with usp_debug_fwd_timeline.
 #ifdef USP_TIMELINE
@@ -252,8 +252,7 @@ __global__ void __maxnreg__(kLaunchRegs)
     if (threadIdx.x == 0) {
         mbar_init(&bars[L::bQFull], 1);
         for (int i = 0; i < S; ++i) {
-            mbar_init(&bars[L::bKFull + i], 1);
-            mbar_init(&bars[L::bVFull + i], 1);
+            mbar_init(&bars[L::bKvFull + i], 1);
             mbar_init(&bars[L::bKvEmpty + i], 1);   // the releasing softmax thread
         }
         for (int i = 0; i < 2; ++i) {
@@ -346,16 +345,15 @@ __global__ void __maxnreg__(kLaunchRegs)
                     const int krow = row + (int)rank * L::kKRows;   // this CTA's keys of the block
                     const int vcol = (int)rank * 64 * L::kVPanels;  // and its columns of V
                     if (leader) {
-                        mbar_arrive_expect_tx(&bars[L::bKFull + st], (PAIR ? 2 : 1) * L::kKBytes);
-                        mbar_arrive_expect_tx(&bars[L::bVFull + st], (PAIR ? 2 : 1) * L::kVBytes);
+                        mbar_arrive_expect_tx(&bars[L::bKvFull + st], (PAIR ? 2 : 1) * (L::kKBytes + L::kVBytes));
                     }
                     USP_FTL(gn, 13);
                     for (int p = 0; p < L::kPanels; ++p)
-                        load(sm + L::kK + st * L::kKBytes + p * L::kKPanel, &tmK, &bars[L::bKFull + st], p * 64, krow,
+                        load(sm + L::kK + st * L::kKBytes + p * L::kKPanel, &tmK, &bars[L::bKvFull + st], p * 64, krow,
                              f.kvh);
                     USP_FTL(gn, 14);
                     for (int p = 0; p < L::kVPanels; ++p)
-                        load(sm + L::kV + st * L::kVBytes + p * (kBlockN * 128), &tmV, &bars[L::bVFull + st],
+                        load(sm + L::kV + st * L::kVBytes + p * (kBlockN * 128), &tmV, &bars[L::bKvFull + st],
                              vcol + p * 64, row, f.kvh);
                     // The CTAs walk the same key/value blocks in near lockstep, so a block's first
                     // load goes to DRAM for all of them: pull this CTA's share two blocks ahead into L2.
@@ -388,8 +386,7 @@ __global__ void __maxnreg__(kLaunchRegs)
             if (leader) {
                 if (q_loads > 0) mbar_wait_drain(&bars[L::bQFull], (q_loads - 1) & 1, kDrainLimitNs);
                 for (int n = gn - S < 0 ? 0 : gn - S; n < gn; ++n) {
-                    mbar_wait_drain(&bars[L::bKFull + n % S], (n / S) & 1, kDrainLimitNs);
-                    mbar_wait_drain(&bars[L::bVFull + n % S], (n / S) & 1, kDrainLimitNs);
+                    mbar_wait_drain(&bars[L::bKvFull + n % S], (n / S) & 1, kDrainLimitNs);
                 }
             }
         }
@@ -445,43 +442,55 @@ __global__ void __maxnreg__(kLaunchRegs)
                 const FwdItem f = fwd_item<PAIR>(a, idx, 0);
                 if (!fwait<PAIR>(&bars[L::bQFull], j & 1, abort_flag)) break;
                 if (f.nmax > 0) {
-                    if (!fwait<PAIR>(&bars[L::bKFull + gn % S], (gn / S) & 1, abort_flag)) break;
+                    if (!fwait<PAIR>(&bars[L::bKvFull + gn % S], (gn / S) & 1, abort_flag)) break;
                     tc_fence_after();
                     // The scores regions are free: the previous item's last P.V, which read them,
                     // was issued before these (tensor-core MMAs run in issue order).
                     if (f.nb0 > 0) issue_s(0, gn % S);
                     if (f.nb1 > 0) issue_s(1, gn % S);
                 }
+                // The issue queue of the tensor pipe is about one MMA deep, so every wait between
+                // two batches of MMAs leaves the pipe idle for its latency. Per block there are
+                // two such gaps: before tile 0's P.V, where block n+1's K and V (for both next
+                // Q.K^T) are confirmed together with P0, and before tile 1's P.V.
                 for (int n = 0; ok && n < f.nmax; ++n) {
-                    const int gb = gn + n, st = gb % S;
+                    const int gb = gn + n, st = gb % S, st1 = (gb + 1) % S;
+                    const bool more = n + 1 < f.nmax;   // a next Q.K^T reads block n+1
+                    const bool has0 = n < f.nb0, has1 = n < f.nb1;
                     USP_FTL(gb, 15);
-                    if (!fwait<PAIR>(&bars[L::bVFull + st], (gb / S) & 1, abort_flag)) { ok = false; break; }
-                    USP_FTL(gb, 0);
-                    bool next_k_ready = false;
-                    for (int t = 0; t < 2 && ok; ++t) {
-                        const int nbt = t ? f.nb1 : f.nb0;
-                        if (n >= nbt) continue;
-                        if (!fwait<PAIR>(&bars[L::bPFull + t], ((t ? pb1 : pb0) + n) & 1, abort_flag)) {
+                    uint64_t* kv1 = &bars[L::bKvFull + st1];
+                    const uint32_t kv1_par = ((gb + 1) / S) & 1;
+                    if (has0 && more)
+                        ok = mbar_wait2(kv1, kv1_par, &bars[L::bPFull + 0], (pb0 + n) & 1, abort_flag, kWaitLimitNs);
+                    else if (has0)
+                        ok = fwait<PAIR>(&bars[L::bPFull + 0], (pb0 + n) & 1, abort_flag);
+                    else if (more)
+                        ok = fwait<PAIR>(kv1, kv1_par, abort_flag);
+                    if (!ok) break;
+                    USP_FTL(gb, 1);
+                    tc_fence_after();
+                    if (has0) {
+                        issue_pv(0, st, n > 0);
+                        if (n == f.nb0 - 1) {
+                            commit_all<PAIR>(&bars[L::bODone + 0]);
+                        } else {
+                            issue_s(0, st1);
+                            USP_FTL(gb, 3);
+                        }
+                    }
+                    if (has1) {
+                        if (!fwait<PAIR>(&bars[L::bPFull + 1], (pb1 + n) & 1, abort_flag)) {
                             ok = false;
                             break;
                         }
-                        USP_FTL(gb, 1 + t);
+                        USP_FTL(gb, 2);
                         tc_fence_after();
-                        issue_pv(t, st, n > 0);
-                        if (n == nbt - 1) {
-                            commit_all<PAIR>(&bars[L::bODone + t]);
+                        issue_pv(1, st, n > 0);
+                        if (n == f.nb1 - 1) {
+                            commit_all<PAIR>(&bars[L::bODone + 1]);
                         } else {
-                            const int st1 = (gb + 1) % S;
-                            if (!next_k_ready) {
-                                if (!fwait<PAIR>(&bars[L::bKFull + st1], ((gb + 1) / S) & 1, abort_flag)) {
-                                    ok = false;
-                                    break;
-                                }
-                                tc_fence_after();
-                                next_k_ready = true;
-                            }
-                            issue_s(t, st1);
-                            USP_FTL(gb, 3 + t);
+                            issue_s(1, st1);
+                            USP_FTL(gb, 4);
                         }
                     }
                 }

@@ -84,6 +84,24 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     }
 }
 
+// Two bounded waits whose first checks are issued back to back, so that their latencies
+// overlap when both phases are already complete (the common case for a thread that must
+// return to issuing tensor-core work quickly).
+__device__ __forceinline__ bool mbar_wait2(uint64_t* a, uint32_t pa, uint64_t* b, uint32_t pb,
+                                           volatile int* abort_flag, uint64_t limit_ns) {
+    uint32_t ra, rb;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%2], %3;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 q, [%4], %5;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\tselp.u32 %1, 1, 0, q;\n\t}\n"
+        : "=r"(ra), "=r"(rb)
+        : "r"(smem_u32(a)), "r"(pa), "r"(smem_u32(b)), "r"(pb)
+        : "memory");
+    if (ra && rb) return true;
+    return (ra || mbar_wait(a, pa, abort_flag, limit_ns)) && (rb || mbar_wait(b, pb, abort_flag, limit_ns));
+}
+
 // ---- thread-block clusters (pairs of CTAs sharing key/value tiles)
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
