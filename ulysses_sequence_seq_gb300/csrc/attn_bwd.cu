@@ -67,9 +67,10 @@ struct BwdSmem {
     static constexpr int kLse = kStage + 4 * kDqChunkBytes;     // fp32[2][64]: -lse (log2 units), one half each
     static constexpr int kDelta = kLse + 512;                   // fp32[2][64]: -Delta
     static constexpr int kBars = kDelta + 512;
+    // bKvEmpty: the item's last MMA has run (K and V free, dK and dV final); bItem: 4-slot ring
     static constexpr int bKvFull = 0, bQFull = 1, bQEmpty = 3, bDoFull = 5, bDoEmpty = 6, bSFull = 7, bPFull = 9,
-                         bDpFull = 11, bDsFull = 13, bDqFull = 15, bDqEmpty = 16, bAccFull = 17, bDrain = 18,
-                         bKvEmpty = 19, bAccEmpty = 20, bItem = 21, kNumBars = 25;   // bItem: 4-slot ring
+                         bDpFull = 11, bDsFull = 13, bDqFull = 15, bDqEmpty = 16, bDrain = 17, bKvEmpty = 18,
+                         bAccEmpty = 19, bItem = 20, kNumBars = 24;
     static constexpr int kItemRing = kBars + 8 * kNumBars;        // int[4]: work item of each slot
     static constexpr int kTmemSlot = kItemRing + 16;
     static constexpr int kAbort = kTmemSlot + 8;
@@ -193,17 +194,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(&bars[L::bKvFull], 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars[L::bQFull + i], 1);
-            mbar_init(&bars[L::bQEmpty + i], 1);
+            mbar_init(&bars[L::bQEmpty + i], 1);   // released by the dQ group (see there)
             mbar_init(&bars[L::bSFull + i], 1);
             mbar_init(&bars[L::bPFull + i], 4);
             mbar_init(&bars[L::bDpFull + i], 1);
             mbar_init(&bars[L::bDsFull + i], 4);
         }
         mbar_init(&bars[L::bDoFull], 1);
-        mbar_init(&bars[L::bDoEmpty], 1);
+        mbar_init(&bars[L::bDoEmpty], 1);   // released by compute half B (see there)
         mbar_init(&bars[L::bDqFull], 1);
         mbar_init(&bars[L::bDqEmpty], 4);
-        mbar_init(&bars[L::bAccFull], 1);
         mbar_init(&bars[L::bDrain], 1);
         mbar_init(&bars[L::bKvEmpty], 1);
         mbar_init(&bars[L::bAccEmpty], kComputeWarps);
@@ -346,8 +346,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 if (!read_item(item_bars, item_ring, j, abort_flag, idx)) break;
                 if (idx >= count) break;
                 const int nsteps = bwd_item(a, idx).nsteps;
-                if (!mbar_wait(&bars[L::bKvFull], j & 1, abort_flag, kWaitLimitNs)) break;
-                if (!mbar_wait(&bars[L::bQFull + (gk & 1)], (gk >> 1) & 1, abort_flag, kWaitLimitNs)) break;
+                if (!mbar_wait2(&bars[L::bKvFull], j & 1, &bars[L::bQFull + (gk & 1)], (gk >> 1) & 1, abort_flag,
+                                kWaitLimitNs))
+                    break;
                 tc_fence_after();
                 for (int hf = 0; hf < 2; ++hf) {
                     issue_half(tS + hf * kHalfCols, dK_kmaj, dQ_kmaj + (gk & 1) * kStageQ + hf * kHalfRows);
@@ -359,12 +360,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 // next block and dK += dS^T.Q (after dS); dQ = dS.K once both halves wrote dS. The
                 // tensor cores run in issue order, so the commit that releases a half's dP^T also
                 // covers the previous block's dQ and dK reads of the dS buffer that half rewrites.
+                // The issue queue of the tensor pipe is about one MMA deep, so each wait between
+                // two batches leaves the pipe idle for its latency, and so does a commit right
+                // behind another (it holds this thread until the first is delivered): per step
+                // there are four gaps, each waiting on what its batch needs, two barriers at
+                // once where possible, and the dO and Q buffers are released by the warps that
+                // see their last readers complete instead of by commits.
                 for (int k = 0; ok && k < nsteps; ++k, ++gk) {
                     const int st = gk & 1;
-                    if (!mbar_wait(&bars[L::bDoFull], gk & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
+                    const bool next = k + 1 < nsteps;
+                    // gap 1: this step's dO and half A's P^T
+                    if (!mbar_wait2(&bars[L::bDoFull], gk & 1, &bars[L::bPFull + 0], gk & 1, abort_flag,
+                                    kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
                     USP_TL(gk, 16);
                     for (int hf = 0; ok && hf < 2; ++hf) {
-                        if (!mbar_wait(&bars[L::bPFull + hf], gk & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
+                        // gap 2 (half B): its P^T
+                        if (hf == 1 && !mbar_wait(&bars[L::bPFull + 1], gk & 1, abort_flag, kWaitLimitNs)) {
+                            ok = false;
+                            break;
+                        }
                         USP_TL(gk, hf);
                         tc_fence_after();
 #pragma unroll
@@ -376,20 +393,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         mma_commit(&bars[L::bDpFull + hf]);
                     }
                     if (!ok) break;
-                    mma_commit(&bars[L::bDoEmpty]);
                     for (int hf = 0; ok && hf < 2; ++hf) {
-                        if (!mbar_wait(&bars[L::bDsFull + hf], gk & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
+                        // gap 3 (half A): its dS and, for the next S^T, the next block's Q;
+                        // gap 4 (half B): its dS and the dQ accumulator's tensor memory
+                        uint64_t* other = nullptr;
+                        uint32_t other_par = 0;
+                        if (hf == 0 && next) {
+                            other = &bars[L::bQFull + (st ^ 1)];
+                            other_par = ((gk + 1) >> 1) & 1;
+                        } else if (hf == 1 && gk > 0) {
+                            other = &bars[L::bDqEmpty];
+                            other_par = (gk - 1) & 1;
+                        }
+                        const bool got = other ? mbar_wait2(&bars[L::bDsFull + hf], gk & 1, other, other_par, abort_flag,
+                                                            kWaitLimitNs)
+                                               : mbar_wait(&bars[L::bDsFull + hf], gk & 1, abort_flag, kWaitLimitNs);
+                        if (!got) {
+                            ok = false;
+                            break;
+                        }
                         USP_TL(gk, 2 + hf);
                         tc_fence_after();
-                        if (k + 1 < nsteps) {  // S^T of the next block first: it heads this half's next step
-                            const int st1 = st ^ 1;
-                            if (hf == 0 && !mbar_wait(&bars[L::bQFull + st1], ((gk + 1) >> 1) & 1, abort_flag,
-                                                      kWaitLimitNs)) {
-                                ok = false;
-                                break;
-                            }
-                            tc_fence_after();
-                            issue_half(tS + hf * kHalfCols, dK_kmaj, dQ_kmaj + st1 * kStageQ + hf * kHalfRows);
+                        if (next) {  // S^T of the next block first: it heads this half's next step
+                            issue_half(tS + hf * kHalfCols, dK_kmaj, dQ_kmaj + (st ^ 1) * kStageQ + hf * kHalfRows);
                             mma_commit(&bars[L::bSFull + hf]);
                         }
 #pragma unroll
@@ -399,12 +425,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                    idDk, (k > 0 || hf > 0 || kk > 0) ? 1u : 0u);
                     }
                     if (!ok) break;
-                    mma_commit(&bars[L::bQEmpty + st]);
-                    if (gk > 0 && !mbar_wait(&bars[L::bDqEmpty], (gk - 1) & 1, abort_flag, kWaitLimitNs)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < kBlockN / 16; ++kk)  // dQ = dS . K
                         mma_ss(tDQ, dDS_mn + (uint64_t)((kk * 2048) >> 4), dK_mn + (uint64_t)((kk * 2048) >> 4), idDq,
@@ -413,8 +433,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     USP_TL(gk, 4);
                 }
                 if (!ok) break;
-                mma_commit(&bars[L::bKvEmpty]);   // K and V have been read for the last time
-                mma_commit(&bars[L::bAccFull]);   // dK and dV of this item are final
+                mma_commit(&bars[L::bKvEmpty]);   // K and V read for the last time; dK and dV final
             }
             mma_commit(&bars[L::bDrain]);
             mbar_wait_drain(&bars[L::bDrain], 0, kDrainLimitNs);
@@ -522,6 +541,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 // dP^T of this half; its commit also covers the previous block's reads of the dS buffer
                 if (!mbar_wait(&bars[L::bDpFull + grp], gk & 1, abort_flag, kWaitLimitNs)) { ok = false; continue; }
                 if ((warp & 3) == 0 && lane == 0) USP_TL(gk, 7 + 5 * grp);
+                // half B's dP^T is the step's last MMA reading dO (they run in issue order): the
+                // dO buffer is free for the next block
+                if (grp == 1 && r == 0) mbar_arrive(&bars[L::bDoEmpty]);
                 tc_fence_after();
                 uint8_t* panel = sm + L::kDS + grp * (kBlockN * 128);
 #pragma unroll
@@ -566,7 +588,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 fetch_row_stats(wn, 0, group_scale(a, wn.g).dsc);
             }
             idx = idx_next;
-            if (ok) ok = mbar_wait(&bars[L::bAccFull], j & 1, abort_flag, kWaitLimitNs);
+            if (ok) ok = mbar_wait(&bars[L::bKvEmpty], j & 1, abort_flag, kWaitLimitNs);   // dK, dV final
             if (group_any(1 + grp, 128, !ok)) break;
             tc_fence_after();
             // half A writes dV, half B writes dK; TMEM is handed back to the next item's MMAs as
@@ -689,6 +711,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 const int qrow0 = w.q0(k) + w4 * 32;   // first query row of this warp
                 if (!mbar_wait(&bars[L::bDqFull], gk & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
                 if (w4 == 0 && lane == 0) USP_TL(gk, 14);
+                // this dQ follows the step's dK, the last MMA reading its Q block: Q's stage is free
+                if (w4 == 0 && lane == 0) mbar_arrive(&bars[L::bQEmpty + (gk & 1)]);
                 tc_fence_after();
                 // chunk c+1 is read from TMEM while chunk c is staged
                 uint32_t v[2][32];
