@@ -52,7 +52,7 @@ def load_peaks():
 # kernel source they were taken on; any change to the kernel source makes the figure stale
 # and it is reported as null.
 MEASURED_BWD_TRAFFIC = {
-    ("long", True): ("bb559b132530ac17", 8080000000 + 4250000000),
+    ("long", True): ("0f9d85cd63b5da9b", 8073999360 + 4251312128),
 }
 
 
