@@ -73,6 +73,22 @@ def test_fwd_ragged_packed_edges(causal, D):
     check_fwd(q, k, v, w.cu_seqlens(), causal)
 
 
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("D", [64, 128])
+def test_fwd_item_split_edges(causal, D):
+    """Sample lengths around the forward's work-item splits. At head_dim 128 an item is 512
+    query rows run by a pair of CTAs (256-row tiles, each CTA holding 128 rows of each):
+    400 (the second tile's upper 128 rows partly past the end), 512 (exactly one item),
+    513 (a one-row item: its first tile's upper rows and its whole second tile past the
+    end), 640 and 767 (a second item ending in its first tile's upper half), 1024 and 1100.
+    At head_dim 64 the same lengths cross its 256-row items."""
+    needs_gpu()
+    w = custom_workload("split_edges", [400, 512, 513, 640, 767, 1024, 1100], sp=1, hq=4, hkv=2, head_dim=D,
+                        causal=causal, index=33)
+    q, k, v, _ = make(w)
+    check_fwd(q, k, v, w.cu_seqlens(), causal)
+
+
 def test_fwd_runs_of_single_tile_items():
     """Many short samples, ordered rank by rank across 32 heads: long runs of work items
     whose second query tile has no blocks, so the persistent CTAs' second softmax group
