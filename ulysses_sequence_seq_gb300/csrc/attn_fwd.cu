@@ -31,7 +31,11 @@
 // so that the backward can take Delta = dO . O from O to about 16 significant bits.
 // P (bf16 or fp16, the input type) overwrites the first 64 columns of its S tile and feeds the P.V MMA
 // straight from TMEM. The two tiles ping-pong: while one softmax group works on
-// its S, the tensor core runs the other tile's P.V and next Q.K^T.
+// its S, the tensor core runs the other tile's P.V and next Q.K^T (the single MMA thread's
+// issue order keeps them half a period apart). The tensor pipe's issue queue is about one MMA
+// deep, so the MMA thread waits only twice per block (for each tile's P; the next block's K/V
+// is checked in the same gap) and commits only S-ready and O-done: the softmax releases the
+// ring stages and Q.
 // The O rescale is lazy: the running max is only moved when a row's max grows by
 // more than 2^8, which is exact after the final division by the row sum.
 #include <cuda.h>
