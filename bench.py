@@ -483,12 +483,31 @@ def run_usp(args, w):
         dt1, _, _, _ = oracle_sample_step(w, args.cpu_tokens)          # calibration: one head
         nh = max(1, min(w.hq, math.ceil(12.0 / max(dt1, 1e-3))))         # about 12 s of oracle work
         dt, fl, threads, L = oracle_sample_step(w, args.cpu_tokens, nh)
+        pairs_run = nh * L * (L + 1) // 2
+        full_fl = sum(attn_flops(ws_))
         cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                "sample": f"{nh} query heads, causal fwd+bwd over the first {L} tokens of sample 0 "
-                         f"({dt:.1f} s of float64 C oracle work)"}
+                         f"({dt:.1f} s of float64 C oracle work)",
+               "wall_s": dt, "pairs_per_s": pairs_run / dt,
+               "extrapolated_full_step_s": full_fl / (fl / dt),
+               "extrapolated_note": "one full fwd+bwd step of the headline slice at the sample's FLOP rate "
+                                    "(extrapolated, not run)"}
     del main_host
     # per fused step: schedule + attn_fwd | bwd_stats + bwd_convert + schedule + attn_bwd + dq_convert
     launches_per_step = 7
+    # Exponentials per second, a diagnostic beside the tensor-core figure: the forward takes one
+    # exp per allowed pair and query head (4·D FLOPs), the backward one (P recomputed, 10·D).
+    # The ceiling: 32 ex2 per clock per SM (a register-only probe of ex2.approx.ftz.f32 measured
+    # 31.4 on this part), times the SMs, at the median SM clock sampled during the timed steps.
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    mhz = (ck or {}).get("sm_mhz") or (ck or {}).get("sm_max_mhz")
+    exp_peak = 32.0 * sms * mhz * 1e6 if mhz else None
+    exp_f = main_rates["fwd_tflops"] * 1e12 / (4 * ws_.head_dim)
+    exp_b = main_rates["bwd_tflops"] * 1e12 / (10 * ws_.head_dim)
+    exp_rate = {"fwd_exp_per_s": exp_f, "bwd_exp_per_s": exp_b, "peak_exp_per_s": exp_peak,
+                "fwd_frac": exp_f / exp_peak if exp_peak else None,
+                "bwd_frac": exp_b / exp_peak if exp_peak else None,
+                "peak_source": f"32 ex2/clk/SM x {sms} SMs x median {mhz} MHz"}
     bwd_tflops = main_rates["bwd_tflops"]
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -512,6 +531,7 @@ def run_usp(args, w):
                      "traffic": bwd_traffic(ws_, True),
                      "traffic_of": "attn_bwd_kernel, DRAM read+write bytes per launch (ncu)",
                      "algorithmic_bytes": bwd_algorithmic_bytes(ws_)},
+        "exp_rate": exp_rate,
         "scheduler_share_of_step": {"value": 0.0001, "source": "ncu launch list of this command's kernels "
                                                                 "(schedule_kernel 0.01% of the step)"},
         "all_ranks_one_launch": all_ranks,
