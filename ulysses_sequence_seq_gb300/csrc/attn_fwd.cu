@@ -19,11 +19,12 @@
 // Pairs (or CTAs) take their first item by index and the rest from a counter, in schedule
 // order, so the next item's Q, K, V loads and first Q.K^T overlap the softmax of the
 // current one's last blocks and its output.
-// Warp roles (384 threads per CTA, warps 10-11 idle):
+// Warp roles (384 threads per CTA, warp 11 idle):
 //   warps 0-3  softmax group for query tile 0 (thread = one query row = one TMEM lane)
 //   warps 4-7  softmax group for query tile 1
 //   warp  8    TMA producer: Q tiles once, then K/V blocks (or this CTA's halves) into the ring
-//   warp  9    MMA issuer (one thread; the pair's leader only) and TMEM owner
+//   warp  9    MMA issuer of tile 0 (one thread; the pair's leader only) and TMEM owner
+//   warp  10   MMA issuer of tile 1
 // Tensor memory (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [384,384+D).
 // A whole output tile leaves through a 64-column shared-memory panel of its own, one TMA
 // store per 64 columns; a sample's ragged last tile is written row by row. On request the
@@ -31,11 +32,11 @@
 // so that the backward can take Delta = dO . O from O to about 16 significant bits.
 // P (bf16 or fp16, the input type) overwrites the first 64 columns of its S tile and feeds the P.V MMA
 // straight from TMEM. The two tiles ping-pong: while one softmax group works on
-// its S, the tensor core runs the other tile's P.V and next Q.K^T (the single MMA thread's
-// issue order keeps them half a period apart). The tensor pipe's issue queue is about one MMA
-// deep, so the MMA thread waits only twice per block (for each tile's P; the next block's K/V
-// is checked in the same gap) and commits only S-ready and O-done: the softmax releases the
-// ring stages and Q.
+// its S, the tensor core runs the other tile's P.V and next Q.K^T. Each tile has its own MMA
+// thread, so that one thread's waits (for its P and the next K/V block) overlap the other's
+// batch in the tensor pipe, whose issue queue is about one MMA deep; a turn passed between
+// the two threads keeps the tiles half a period apart. The threads commit only S-ready and
+// O-done: each tile's softmax group releases the ring stages and Q its MMAs have read.
 // The O rescale is lazy: the running max is only moved when a row's max grows by
 // more than 2^8, which is exact after the final division by the row sum.
 #include <cuda.h>
@@ -82,10 +83,12 @@ struct FwdSmem {
     static constexpr int kStage = kV + kStages * kVBytes;      // O staging: one [128][64] panel per tile
     static constexpr int kBars = kStage + 2 * kTileM * 128;
     // barrier indices
-    // bKvFull: a stage's K and V both landed (one barrier, so that the MMA thread checks a block once)
+    // bKvFull: a stage's K and V both landed (one barrier, so that an MMA thread checks a block once);
+    // bDrain, bTurn: one per tile's MMA thread
     static constexpr int bQFull = 0, bKvFull = 1, bKvEmpty = bKvFull + kStages,
                          bSFull = bKvEmpty + kStages, bPFull = bSFull + 2, bODone = bPFull + 2, bDrain = bODone + 2,
-                         bQEmpty = bDrain + 1, bItem = bQEmpty + 1, bItemFree = bItem + 4, kNumBars = bItemFree + 4;
+                         bTurn = bDrain + 2, bQEmpty = bTurn + 2, bItem = bQEmpty + 1, bItemFree = bItem + 4,
+                         kNumBars = bItemFree + 4;
     // bItem / bItemFree: published / read by every reader, one of each per slot of the 4-slot item ring
     static constexpr int kItemRing = kBars + 8 * kNumBars;   // int[4]: work item of each slot
     static constexpr int kTmemSlot = kItemRing + 16;
@@ -99,15 +102,20 @@ static_assert(FwdSmem<64, false>::kAlloc <= 232448, "forward shared memory excee
 
 // Optional clock64 timeline of the first kTlSteps key/value blocks of every CTA (compile with
 // -DUSP_TIMELINE; the default build has none of it). Events by the CTA's running block count:
-// MMA thread 15 (block started), 1-2 (tile 0 / 1 P ready), 3-4 (tile 0 / 1 next S issued); softmax
+// MMA threads 15 (tile 0's block started), 1-2 (tile 0 / 1 P ready and turn taken), 3-4 (tile 0 / 1
+// next S issued); softmax
 // group t 5+4t (S ready), 6+4t (row max done), 8+4t (P stored), 7+4t (P-ready arrival made);
 // producer 13-14 (K / V load issued). Read back with usp_debug_fwd_timeline.
 #ifdef USP_TIMELINE
+#ifndef USP_TIMELINE_FIRST
+#define USP_TIMELINE_FIRST 0   // first recorded block (a later window shows the steady state)
+#endif
 constexpr int kFTlSteps = 48, kFTlEvents = 16, kFTlCtas = 160;
 static __device__ long long g_fwd_timeline[kFTlCtas][kFTlSteps][kFTlEvents];
 #define USP_FTL(step, ev)                                                                            \
     do {                                                                                             \
-        if ((step) < kFTlSteps && blockIdx.x < kFTlCtas) g_fwd_timeline[blockIdx.x][(step)][(ev)] = clock64(); \
+        const int s_ = (step) - USP_TIMELINE_FIRST;                                                  \
+        if (s_ >= 0 && s_ < kFTlSteps && blockIdx.x < kFTlCtas) g_fwd_timeline[blockIdx.x][s_][(ev)] = clock64(); \
     } while (0)
 #else
 #define USP_FTL(step, ev) \
@@ -205,11 +213,11 @@ __device__ __forceinline__ bool fwd_read_item(uint64_t* item_bars, volatile int*
     idx = ring[j & 3];
     return true;
 }
-// Readers of an item slot: the MMA thread and the 8 softmax warps; in a pair the leader's
-// MMA thread, both CTAs' softmax warps and the peer's producer.
+// Readers of an item slot: the two MMA threads and the 8 softmax warps; in a pair the
+// leader's MMA threads, both CTAs' softmax warps and the peer's producer.
 template <bool PAIR>
 __host__ __device__ constexpr int fwd_slot_readers() {
-    return PAIR ? 1 + 2 * 8 + 1 : 1 + 8;
+    return PAIR ? 2 + 2 * 8 + 1 : 2 + 8;
 }
 
 template <int D, bool F16, bool PAIR>
@@ -257,15 +265,16 @@ __global__ void __maxnreg__(kLaunchRegs)
         mbar_init(&bars[L::bQFull], 1);
         for (int i = 0; i < S; ++i) {
             mbar_init(&bars[L::bKvFull + i], 1);
-            mbar_init(&bars[L::bKvEmpty + i], 1);   // the releasing softmax thread
+            mbar_init(&bars[L::bKvEmpty + i], 2);   // one releasing softmax thread per tile
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars[L::bSFull + i], 1);
             mbar_init(&bars[L::bPFull + i], PAIR ? 8 : 4);   // the tile's softmax warps (of both CTAs)
             mbar_init(&bars[L::bODone + i], 1);
+            mbar_init(&bars[L::bDrain + i], 1);
+            mbar_init(&bars[L::bTurn + i], 1);
         }
-        mbar_init(&bars[L::bDrain], 1);
-        mbar_init(&bars[L::bQEmpty], 1);
+        mbar_init(&bars[L::bQEmpty], 2);
         for (int i = 0; i < 4; ++i) {
             mbar_init(&bars[L::bItem + i], 1);
             mbar_init(&bars[L::bItemFree + i], fwd_slot_readers<PAIR>());
@@ -285,8 +294,8 @@ __global__ void __maxnreg__(kLaunchRegs)
     // tile's O-done the count of items in which that tile has blocks. Each phase of these
     // barriers needs its waiter to have passed the one before, so a waiter is never two
     // phases behind and parities cannot alias.
-    if (warp >= 10) {
-        regs_decrease<kAuxRegs>();  // idle warps of the load/MMA warpgroup
+    if (warp == 11) {
+        regs_decrease<kAuxRegs>();  // the idle warp of the load/MMA warpgroup
     } else if (warp == 8) {
         regs_decrease<kAuxRegs>();
         // ------------------------------------------------------------------ TMA producer
@@ -394,118 +403,128 @@ __global__ void __maxnreg__(kLaunchRegs)
                 }
             }
         }
-    } else if (warp == 9) {
+    } else if (warp == 9 || warp == 10) {
         regs_decrease<kAuxRegs>();
-        // ------------------------------------------------------------------ MMA issuer
+        // ------------------------------------------------------------------ MMA issuers
+        // One thread per query tile (the pair's leader only): tile t's thread issues its P.V
+        // and Q.K^T. The tensor pipe's issue queue is about one MMA deep, so a thread that
+        // waits between two batches leaves the pipe idle; with two threads, one waits (for its
+        // tile's P, the next K/V block and its turn) while the other's batch runs. The turn
+        // keeps the tiles half a period apart: per item there are 1 + nmax slots (the first
+        // Q.K^T, then one per key/value block), tile 0 goes first in each and hands the turn
+        // to tile 1 shortly before its batch's last MMAs, tile 1 hands it back. A tile with
+        // nothing in a slot passes the turn on at once. Without the turn, two free-running
+        // threads let the tiles fall into phase (both S ready together, both softmax groups
+        // competing, then both batches).
         if (lane == 0 && rank == 0) {
+            const int t = warp - 9;
             constexpr int M = PAIR ? 2 * kTileM : kTileM;
             constexpr uint32_t idS = idesc_16b_f32(M, kBlockN, false, false, F16);  // Q.K^T: both K-major
             constexpr uint32_t idO = idesc_16b_f32(M, D, false, true, F16);         // P.V: V is MN-major
+            // The turn goes to the other tile this many MMAs before a batch ends (measured on the
+            // 262,144-token slice: 1 -> 1560, 2 -> 1548, 3 -> 1545, 4 -> 1534 TFLOP/s).
+            constexpr int kEarly = 1;
             // The 64-bit shared-memory descriptors are built once; a K step only adds a constant
             // to the start-address field (addresses stay below 2^18, so the field never carries).
             // Rebuilding them per MMA made the issuing thread, not the tensor core, the limit.
-            const uint64_t dQ0 = sdesc_sw128(smem_u32(sm + L::kQ0), 0, 1024);
-            const uint64_t dQ1 = sdesc_sw128(smem_u32(sm + L::kQ1), 0, 1024);
+            const uint64_t dQt = sdesc_sw128(smem_u32(sm + (t ? L::kQ1 : L::kQ0)), 0, 1024);
             const uint64_t dK0 = sdesc_sw128(smem_u32(sm + L::kK), 0, 1024);
             const uint64_t dV0 = sdesc_sw128(smem_u32(sm + L::kV), kBlockN * 128, 1024);
-            auto issue_s = [&](int t, int st) {
-                const uint64_t ad = t ? dQ1 : dQ0, bd = dK0 + (uint64_t)((st * L::kKBytes) >> 4);
-                const uint32_t d = tbase + t * 128;
+            const uint32_t tS = tbase + t * 128, tO = tbase + 256 + t * 128;
+            auto pass_turn = [&]() { mbar_arrive(&bars[L::bTurn + (t ^ 1)]); };
+            // Q.K^T of this tile into its S region; `pass` hands the turn on inside the batch
+            auto issue_s = [&](int st, bool pass) {
+                const uint64_t bd = dK0 + (uint64_t)((st * L::kKBytes) >> 4);
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
                     const uint64_t aoff = (uint64_t)((((k / 4) * (kTileM * 128)) + (k % 4) * 32) >> 4);
                     const uint64_t boff = (uint64_t)((((k / 4) * L::kKPanel) + (k % 4) * 32) >> 4);
                     if constexpr (PAIR)
-                        mma_ss_pair(d, ad + aoff, bd + boff, idS, k > 0);
+                        mma_ss_pair(tS, dQt + aoff, bd + boff, idS, k > 0);
                     else
-                        mma_ss(d, ad + aoff, bd + boff, idS, k > 0);
+                        mma_ss(tS, dQt + aoff, bd + boff, idS, k > 0);
+                    if (pass && k == D / 16 - 1 - kEarly) pass_turn();
                 }
                 commit_all<PAIR>(&bars[L::bSFull + t]);
             };
-            auto issue_pv = [&](int t, int st, bool acc) {
+            auto issue_pv = [&](int st, bool acc, bool pass) {
                 const uint64_t bd = dV0 + (uint64_t)((st * L::kVBytes) >> 4);
-                const uint32_t d = tbase + 256 + t * 128, a_t = tbase + t * 128;
 #pragma unroll
                 for (int k = 0; k < kBlockN / 16; ++k) {
                     if constexpr (PAIR)
-                        mma_ts_pair(d, a_t + k * 8, bd + (uint64_t)((k * 2048) >> 4), idO, (acc || k > 0) ? 1u : 0u);
+                        mma_ts_pair(tO, tS + k * 8, bd + (uint64_t)((k * 2048) >> 4), idO, (acc || k > 0) ? 1u : 0u);
                     else
-                        mma_ts(d, a_t + k * 8, bd + (uint64_t)((k * 2048) >> 4), idO, (acc || k > 0) ? 1u : 0u);
+                        mma_ts(tO, tS + k * 8, bd + (uint64_t)((k * 2048) >> 4), idO, (acc || k > 0) ? 1u : 0u);
+                    if (pass && k == kBlockN / 16 - 1 - kEarly) pass_turn();
                 }
             };
-            // This thread commits only the S-ready and O-done signals: the softmax releases the
-            // ring stages and Q (a commit right behind another one holds the issuing thread until
-            // the first has been delivered, which left the tensor pipe idle before each P.V).
+            // This tile's turn for its next slot (tile 0's very first slot needs none).
+            int slots = 0;
+            auto take_turn = [&]() -> bool {
+                if (t == 0) return slots == 0 || fwait<PAIR>(&bars[L::bTurn + 0], (slots - 1) & 1, abort_flag);
+                return fwait<PAIR>(&bars[L::bTurn + 1], slots & 1, abort_flag);
+            };
+            // This thread commits only the S-ready and O-done signals of its tile: the softmax
+            // releases the ring stages and Q (a commit right behind another one holds the
+            // issuing thread until the first has been delivered).
             bool ok = true;
-            int gn = 0, pb0 = 0, pb1 = 0;   // blocks of the ring, of tile 0, of tile 1 before this item
+            int gn = 0, pb = 0;   // blocks of the ring and of this tile before this item
             for (int j = 0; ok; ++j) {
                 int idx;
                 if (!fwd_read_item<PAIR>(item_bars, item_ring, j, abort_flag, idx)) break;
                 mbar_arrive(&item_free[j & 3]);
                 if (idx >= count) break;
                 const FwdItem f = fwd_item<PAIR>(a, idx, 0);
+                const int nbt = t ? f.nb1 : f.nb0;
                 if (!fwait<PAIR>(&bars[L::bQFull], j & 1, abort_flag)) break;
-                if (f.nmax > 0) {
-                    if (!fwait<PAIR>(&bars[L::bKvFull + gn % S], (gn / S) & 1, abort_flag)) break;
+                // slot 0: the first Q.K^T (the S region is free: this thread issued the previous
+                // item's last P.V, which read it, before)
+                if (nbt > 0 && !fwait<PAIR>(&bars[L::bKvFull + gn % S], (gn / S) & 1, abort_flag)) break;
+                if (!take_turn()) break;
+                if (nbt > 0) {
                     tc_fence_after();
-                    // The scores regions are free: the previous item's last P.V, which read them,
-                    // was issued before these (tensor-core MMAs run in issue order).
-                    if (f.nb0 > 0) issue_s(0, gn % S);
-                    if (f.nb1 > 0) issue_s(1, gn % S);
+                    issue_s(gn % S, true);
+                } else {
+                    pass_turn();
                 }
-                // The issue queue of the tensor pipe is about one MMA deep, so every wait between
-                // two batches of MMAs leaves the pipe idle for its latency. Per block there are
-                // two such gaps: before tile 0's P.V, where block n+1's K and V (for both next
-                // Q.K^T) are confirmed together with P0, and before tile 1's P.V.
+                ++slots;
                 for (int n = 0; ok && n < f.nmax; ++n) {
                     const int gb = gn + n, st = gb % S, st1 = (gb + 1) % S;
-                    const bool more = n + 1 < f.nmax;   // a next Q.K^T reads block n+1
-                    const bool has0 = n < f.nb0, has1 = n < f.nb1;
-                    USP_FTL(gb, 15);
-                    uint64_t* kv1 = &bars[L::bKvFull + st1];
-                    const uint32_t kv1_par = ((gb + 1) / S) & 1;
-                    if (has0 && more)
-                        ok = mbar_wait2(kv1, kv1_par, &bars[L::bPFull + 0], (pb0 + n) & 1, abort_flag, kWaitLimitNs);
-                    else if (has0)
-                        ok = fwait<PAIR>(&bars[L::bPFull + 0], (pb0 + n) & 1, abort_flag);
-                    else if (more)
-                        ok = fwait<PAIR>(kv1, kv1_par, abort_flag);
+                    const bool has = n < nbt, more = n + 1 < nbt;   // a next Q.K^T of this tile reads block n+1
+                    const uint32_t pph = (pb + n) & 1;
+                    if (t == 0) USP_FTL(gb, 15);
+                    // this tile's P, the next block's K and V, and this tile's turn (the other
+                    // thread hands it over shortly before its batch ends), tested together
+                    if (has) {
+                        ok = mbar_wait3(&bars[L::bPFull + t], pph, more ? &bars[L::bKvFull + st1] : nullptr,
+                                        ((gb + 1) / S) & 1, t == 0 && slots == 0 ? nullptr : &bars[L::bTurn + t],
+                                        (t == 0 ? slots - 1 : slots) & 1, abort_flag, kWaitLimitNs);
+                    } else {
+                        ok = take_turn();
+                    }
                     if (!ok) break;
-                    USP_FTL(gb, 1);
-                    tc_fence_after();
-                    if (has0) {
-                        issue_pv(0, st, n > 0);
-                        if (n == f.nb0 - 1) {
-                            commit_all<PAIR>(&bars[L::bODone + 0]);
-                        } else {
-                            issue_s(0, st1);
-                            USP_FTL(gb, 3);
-                        }
-                    }
-                    if (has1) {
-                        if (!fwait<PAIR>(&bars[L::bPFull + 1], (pb1 + n) & 1, abort_flag)) {
-                            ok = false;
-                            break;
-                        }
-                        USP_FTL(gb, 2);
+                    USP_FTL(gb, 1 + t);
+                    if (has) {
                         tc_fence_after();
-                        issue_pv(1, st, n > 0);
-                        if (n == f.nb1 - 1) {
-                            commit_all<PAIR>(&bars[L::bODone + 1]);
+                        issue_pv(st, n > 0, !more);
+                        if (more) {
+                            issue_s(st1, true);
+                            USP_FTL(gb, 3 + t);
                         } else {
-                            issue_s(1, st1);
-                            USP_FTL(gb, 4);
+                            commit_all<PAIR>(&bars[L::bODone + t]);
                         }
+                    } else {
+                        pass_turn();
                     }
+                    ++slots;
                 }
                 if (!ok) break;
                 gn += f.nmax;
-                pb0 += f.nb0;
-                pb1 += f.nb1;
+                pb += nbt;
             }
-            // Drain: the tensor pipe must be idle before TMEM is released.
-            commit_all<PAIR>(&bars[L::bDrain]);
-            mbar_wait_drain(&bars[L::bDrain], 0, kDrainLimitNs);
+            // Drain: this thread's MMAs have run before TMEM is released.
+            commit_all<PAIR>(&bars[L::bDrain + t]);
+            mbar_wait_drain(&bars[L::bDrain + t], 0, kDrainLimitNs);
         }
     } else {
         regs_increase<kSoftmaxRegs>();
@@ -529,18 +548,20 @@ __global__ void __maxnreg__(kLaunchRegs)
             const int q0 = t ? f.q01 : f.q00;
             const int nbt = (ok && idx < count) ? (t ? f.nb1 : f.nb0) : 0;
             const int i = q0 + rq;  // this thread's query row
-            // The releasing tile has the item's most blocks: tile 1 unless its rows lie past the
-            // sample's end (tile 1's rows follow tile 0's, so nb1 >= nb0 whenever nb1 > 0). The
-            // tensor pipe runs PV0(n), S0(n+1), PV1(n), S1(n+1) in order, so once it has seen S(n)
-            // complete, every MMA reading block n-1 (its Q.K^T and both P.V) has run; its O-done
-            // covers the last block, and its last S completes the item's last Q.K^T.
-            const bool releaser = (t == (f.nb1 > 0 ? 1 : 0)) && rq == 0;
+            // Each tile releases what its own MMA thread's MMAs read: once the group has seen
+            // S(n) complete, this tile's Q.K^T and P.V of block n-1 have run (one thread's MMAs
+            // run in issue order); its O-done covers its last block, and its last S its Q. A
+            // block or a Q the other tile does not read (tile 0 has fewer blocks when nb0 < nb1,
+            // tile 1 none when its rows lie past the sample's end) is released for both.
+            const bool releaser = rq == 0;
+            const int other_nb = (ok && idx < count) ? (t ? f.nb0 : f.nb1) : 0;
+            auto rel_count = [&](int blk) -> uint32_t { return blk < other_nb ? 1u : 2u; };
             float m = -INFINITY, l = 0.f;
             for (int n = 0; n < nbt; ++n) {
                 if (!fwait<PAIR>(&bars[L::bSFull + t], (pb + n) & 1, abort_flag)) { ok = false; break; }
                 if (releaser) {
-                    if (n > 0) mbar_arrive(&bars[L::bKvEmpty + (gq + n - 1) % S]);   // block n-1 is read
-                    if (n == nbt - 1) mbar_arrive(&bars[L::bQEmpty]);               // Q is read
+                    if (n > 0) mbar_arrive_cnt(&bars[L::bKvEmpty + (gq + n - 1) % S], rel_count(n - 1));   // block n-1
+                    if (n == nbt - 1) mbar_arrive_cnt(&bars[L::bQEmpty], other_nb > 0 ? 1u : 2u);          // Q
                 }
                 if (rq == 0) USP_FTL(pb + n, 5 + 4 * t);
                 tc_fence_after();
@@ -627,12 +648,13 @@ __global__ void __maxnreg__(kLaunchRegs)
                 tc_fence_before();
                 __syncwarp();
                 if (rq == 0) USP_FTL(pb + n, 8 + 4 * t);
-                if (lane == 0) arrive_leader<PAIR>(&bars[L::bPFull + t], rank);   // P ready for the MMA issuer
+                if (lane == 0) arrive_leader<PAIR>(&bars[L::bPFull + t], rank);   // P ready for the tile's MMA thread
                 if (rq == 0) USP_FTL(pb + n, 7 + 4 * t);
 
             }
             if (ok && nbt > 0) ok = fwait<PAIR>(&bars[L::bODone + t], od & 1, abort_flag);
-            if (ok && releaser && nbt > 0) mbar_arrive(&bars[L::bKvEmpty + (gq + nbt - 1) % S]);   // the last block
+            if (ok && releaser && nbt > 0)   // this tile's last block
+                mbar_arrive_cnt(&bars[L::bKvEmpty + (gq + nbt - 1) % S], rel_count(nbt - 1));
             // The group's warps leave together (a warp that gave up on a wait must not leave the
             // others at the epilogue's barriers); the ring's end marker ends every warp's loop.
             if (group_any(1 + t, 128, !ok) || idx >= count) break;

@@ -48,6 +48,11 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// Arrive `count` times at once (for a thread that stands in for another arriver).
+__device__ __forceinline__ void mbar_arrive_cnt(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                  : "memory");
@@ -100,6 +105,44 @@ __device__ __forceinline__ bool mbar_wait2(uint64_t* a, uint32_t pa, uint64_t* b
         : "memory");
     if (ra && rb) return true;
     return (ra || mbar_wait(a, pa, abort_flag, limit_ns)) && (rb || mbar_wait(b, pb, abort_flag, limit_ns));
+}
+
+// Bounded wait for up to three phases (a null barrier counts as complete). The first check
+// tests all three back to back, so that their latencies overlap; after that the thread
+// blocks on the first pending barrier (pass the one expected to complete last first) and
+// re-tests the rest together once it completes.
+__device__ __forceinline__ bool mbar_wait3(uint64_t* a, uint32_t pa, uint64_t* b, uint32_t pb, uint64_t* c,
+                                           uint32_t pc, volatile int* abort_flag, uint64_t limit_ns) {
+    uint32_t ra = a ? 0u : 1u, rb = b ? 0u : 1u, rc = c ? 0u : 1u;
+    uint64_t t0 = 0;
+    while (true) {
+        asm volatile(
+            "{\n\t.reg .pred p, q, r;\n\t"
+            "setp.ne.u32 p, %0, 0;\n\tsetp.ne.u32 q, %1, 0;\n\tsetp.ne.u32 r, %2, 0;\n\t"
+            "@!p mbarrier.test_wait.parity.shared::cta.b64 p, [%3], %4;\n\t"
+            "@!q mbarrier.test_wait.parity.shared::cta.b64 q, [%5], %6;\n\t"
+            "@!r mbarrier.test_wait.parity.shared::cta.b64 r, [%7], %8;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\tselp.u32 %1, 1, 0, q;\n\tselp.u32 %2, 1, 0, r;\n\t}\n"
+            : "+r"(ra), "+r"(rb), "+r"(rc)
+            : "r"(smem_u32(a)), "r"(pa), "r"(smem_u32(b)), "r"(pb), "r"(smem_u32(c)), "r"(pc)
+            : "memory");
+        if (ra && rb && rc) return true;
+        if (!ra) {
+            ra = mbar_try_wait(a, pa) ? 1u : 0u;
+        } else if (!rb) {
+            rb = mbar_try_wait(b, pb) ? 1u : 0u;
+        } else {
+            rc = mbar_try_wait(c, pc) ? 1u : 0u;
+        }
+        if (ra && rb && rc) return true;
+        if (*abort_flag) return false;
+        if (t0 == 0) {
+            t0 = globaltimer_ns();
+        } else if (globaltimer_ns() - t0 > limit_ns) {
+            *abort_flag = 1;
+            return false;
+        }
+    }
 }
 
 // ---- thread-block clusters (pairs of CTAs sharing key/value tiles)
