@@ -498,7 +498,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 // last key tile; there query column c (of 128) is visible to key row r iff c >= r
                 const bool mask_blk = (a.causal && q0 == w.kv0) || (w.kv0 + kBlockN > w.e);
                 const int vis_from = (a.causal && q0 == w.kv0) ? r - grp * kHalfCols : -1;
-                if (!mbar_wait(&bars[L::bSFull + grp], gk & 1, abort_flag, kWaitLimitNs)) { ok = false; continue; }
+                // the warp agrees on every wait's outcome: its tcgen05 loads and stores are collective
+                if (!__all_sync(0xffffffffu, mbar_wait(&bars[L::bSFull + grp], gk & 1, abort_flag, kWaitLimitNs))) {
+                    ok = false;
+                    continue;
+                }
                 if ((warp & 3) == 0 && lane == 0) USP_TL(gk, 5 + 5 * grp);
                 tc_fence_after();
                 // P for this row's query columns as packed bf16 pairs: the values the dV MMA
@@ -539,7 +543,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 if ((warp & 3) == 0 && lane == 0) USP_TL(gk, 6 + 5 * grp);
 
                 // dP^T of this half; its commit also covers the previous block's reads of the dS buffer
-                if (!mbar_wait(&bars[L::bDpFull + grp], gk & 1, abort_flag, kWaitLimitNs)) { ok = false; continue; }
+                if (!__all_sync(0xffffffffu, mbar_wait(&bars[L::bDpFull + grp], gk & 1, abort_flag, kWaitLimitNs))) {
+                    ok = false;
+                    continue;
+                }
                 if ((warp & 3) == 0 && lane == 0) USP_TL(gk, 7 + 5 * grp);
                 // half B's dP^T is the step's last MMA reading dO (they run in issue order): the
                 // dO buffer is free for the next block
@@ -709,7 +716,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             for (int k = 0; k < w.nsteps; ++k, ++gk) {
                 const int h = w.g * G + k / w.nq;
                 const int qrow0 = w.q0(k) + w4 * 32;   // first query row of this warp
-                if (!mbar_wait(&bars[L::bDqFull], gk & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
+                if (!__all_sync(0xffffffffu, mbar_wait(&bars[L::bDqFull], gk & 1, abort_flag, kWaitLimitNs))) {
+                    ok = false;
+                    break;
+                }
                 if (w4 == 0 && lane == 0) USP_TL(gk, 14);
                 // this dQ follows the step's dK, the last MMA reading its Q block: Q's stage is free
                 if (w4 == 0 && lane == 0) mbar_arrive(&bars[L::bQEmpty + (gk & 1)]);

@@ -558,7 +558,11 @@ __global__ void __maxnreg__(kLaunchRegs)
             auto rel_count = [&](int blk) -> uint32_t { return blk < other_nb ? 1u : 2u; };
             float m = -INFINITY, l = 0.f;
             for (int n = 0; n < nbt; ++n) {
-                if (!fwait<PAIR>(&bars[L::bSFull + t], (pb + n) & 1, abort_flag)) { ok = false; break; }
+                // (the warp agrees on the outcome: its tcgen05 loads and stores below are collective)
+                if (!__all_sync(0xffffffffu, fwait<PAIR>(&bars[L::bSFull + t], (pb + n) & 1, abort_flag))) {
+                    ok = false;
+                    break;
+                }
                 if (releaser) {
                     if (n > 0) mbar_arrive_cnt(&bars[L::bKvEmpty + (gq + n - 1) % S], rel_count(n - 1));   // block n-1
                     if (n == nbt - 1) mbar_arrive_cnt(&bars[L::bQEmpty], other_nb > 0 ? 1u : 2u);          // Q
@@ -592,57 +596,70 @@ __global__ void __maxnreg__(kLaunchRegs)
                     for (int c = 0; c < 128; ++c)
                         if (c > lim) sv[c] = -INFINITY;
                 }
-                // row max over 8 independent chains of three-input max (a single two-input chain
-                // would serialise 127 dependent ops)
-                float mx8[8];
+                // the block's row max (log2 units) over 8 independent chains of three-input max (a
+                // single two-input chain would serialise 127 dependent ops)
+                auto block_max = [&]() -> float {
+                    float mx8[8];
     #pragma unroll
-                for (int j = 0; j < 8; ++j) mx8[j] = sv[j];
+                    for (int q = 0; q < 8; ++q) mx8[q] = sv[q];
     #pragma unroll
-                for (int c = 8; c < 120; c += 16)
+                    for (int c = 8; c < 120; c += 16)
     #pragma unroll
-                    for (int j = 0; j < 8; ++j) mx8[j] = fmax3(mx8[j], sv[c + j], sv[c + 8 + j]);
+                        for (int q = 0; q < 8; ++q) mx8[q] = fmax3(mx8[q], sv[c + q], sv[c + 8 + q]);
     #pragma unroll
-                for (int j = 0; j < 8; ++j) mx8[j] = fmaxf(mx8[j], sv[120 + j]);
-                const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
-                const float m_blk = mx * sl2;
+                    for (int q = 0; q < 8; ++q) mx8[q] = fmaxf(mx8[q], sv[120 + q]);
+                    return fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])) * sl2;
+                };
+                // P = exp2(s sl2 - m) into the S columns; returns the partial row sums
+                auto exponentials = [&](float m_used) -> float2 {
+                    const float mu = (m_used == -INFINITY) ? 0.f : m_used;
+                    const float2 sl2x2 = make_float2(sl2, sl2), nmu2 = make_float2(-mu, -mu);
+                    float2 l4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                    make_float2(0.f, 0.f)};
+    #pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t pk[16];
+    #pragma unroll
+                        for (int q = 0; q < 16; ++q) {
+                            const float2 x = fma2(make_float2(sv[32 * c + 2 * q], sv[32 * c + 2 * q + 1]), sl2x2, nmu2);
+                            const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                            l4[q & 3] = add2(l4[q & 3], pp);   // independent partial row sums
+                            pk[q] = pack2<F16>(pp.x, pp.y);
+                        }
+                        tmem_st16(tS + 16 * c, pk);
+                    }
+                    return add2(add2(l4[0], l4[1]), add2(l4[2], l4[3]));
+                };
+                const float m_blk = block_max();
                 if (rq == 0) USP_FTL(pb + n, 6 + 4 * t);
                 if (n == 0) {
                     m = m_blk;
-                } else if (m_blk > m + kRescaleThreshold) {
-                    const float f = ex2_approx(m - m_blk);
-                    l *= f;
+                } else {
+                    // tcgen05.ld / st are warp-collective: when any row of the warp moves its max,
+                    // the whole warp rescales, each row by its own factor (1 for rows that keep
+                    // theirs, which leaves their O bit-identical)
+                    const bool up = m_blk > m + kRescaleThreshold;
+                    if (__any_sync(0xffffffffu, up)) {
+                        const float f = up ? ex2_approx(m - m_blk) : 1.f;
+                        l *= f;
     #pragma unroll 1
-                    for (int c = 0; c < D; c += 32) {
-                        uint32_t o[32];
-                        tmem_ld32(tO + c, o);
-                        tmem_ld_wait(o);
-                        uint32_t lo[16], hi[16];
+                        for (int c = 0; c < D; c += 32) {
+                            uint32_t o[32];
+                            tmem_ld32(tO + c, o);
+                            tmem_ld_wait(o);
+                            uint32_t lo[16], hi[16];
     #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            lo[j] = __float_as_uint(__uint_as_float(o[j]) * f);
-                            hi[j] = __float_as_uint(__uint_as_float(o[16 + j]) * f);
+                            for (int q = 0; q < 16; ++q) {
+                                lo[q] = __float_as_uint(__uint_as_float(o[q]) * f);
+                                hi[q] = __float_as_uint(__uint_as_float(o[16 + q]) * f);
+                            }
+                            tmem_st16(tO + c, lo);
+                            tmem_st16(tO + c + 16, hi);
                         }
-                        tmem_st16(tO + c, lo);
-                        tmem_st16(tO + c + 16, hi);
+                        if (up) m = m_blk;
                     }
-                    m = m_blk;
                 }
-                const float mu = (m == -INFINITY) ? 0.f : m;
-                const float2 sl2x2 = make_float2(sl2, sl2), nmu2 = make_float2(-mu, -mu);
-                float2 l4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-    #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t pk[16];
-    #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const float2 x = fma2(make_float2(sv[32 * c + 2 * j], sv[32 * c + 2 * j + 1]), sl2x2, nmu2);
-                        const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-                        l4[j & 3] = add2(l4[j & 3], pp);   // independent partial row sums
-                        pk[j] = pack2<F16>(pp.x, pp.y);
-                    }
-                    tmem_st16(tS + 16 * c, pk);
-                }
-                const float2 lsum = add2(add2(l4[0], l4[1]), add2(l4[2], l4[3]));
+                const float2 lsum = exponentials(m);
                 l += lsum.x + lsum.y;
                 tmem_st_wait();
                 tc_fence_before();
@@ -652,7 +669,7 @@ __global__ void __maxnreg__(kLaunchRegs)
                 if (rq == 0) USP_FTL(pb + n, 7 + 4 * t);
 
             }
-            if (ok && nbt > 0) ok = fwait<PAIR>(&bars[L::bODone + t], od & 1, abort_flag);
+            if (ok && nbt > 0) ok = __all_sync(0xffffffffu, fwait<PAIR>(&bars[L::bODone + t], od & 1, abort_flag));
             if (ok && releaser && nbt > 0)   // this tile's last block
                 mbar_arrive_cnt(&bars[L::bKvEmpty + (gq + nbt - 1) % S], rel_count(nbt - 1));
             // The group's warps leave together (a warp that gave up on a wait must not leave the
