@@ -52,7 +52,7 @@ def load_peaks():
 # kernel source they were taken on; any change to the kernel source makes the figure stale
 # and it is reported as null.
 MEASURED_BWD_TRAFFIC = {
-    ("long", True): ("0f9d85cd63b5da9b", 8073999360 + 4251312128),
+    ("long", True): ("bbed6de96912f02e", 8073437696 + 4252054272),
 }
 
 
