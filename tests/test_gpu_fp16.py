@@ -20,14 +20,35 @@ def heads_of(x_seq):
     return np.ascontiguousarray(x_seq.reshape(sp * S, H, D).transpose(1, 0, 2))
 
 
-def run_check(w, grad_dtype, q_heads=None, rows=None, kv_heads=None, k_rows=None):
+def growing_scores(w, xq, xk):
+    """A large first component in every query and keys whose first component grows with their
+    position in the sample: causal rows whose block maxima rise by about 8 (log2 units) per
+    key block, so the forward's running max is overtaken by more than 2^8 every block or two."""
+    from ulysses_sequence_seq_gb300.synth import f32_to_f16_bits
+    T, D = w.total_tokens, w.head_dim
+    qf = xq.view(np.float16).astype(np.float32).reshape(T, -1, D)
+    kf = xk.view(np.float16).astype(np.float32).reshape(T, -1, D)
+    qf[:, :, 0] = 4.0
+    cu = w.cu_seqlens()
+    for b in range(len(cu) - 1):
+        kf[cu[b]:cu[b + 1], :, 0] = (0.12 * np.sqrt(D / 128.0) * np.arange(cu[b + 1] - cu[b]))[:, None]
+    return f32_to_f16_bits(qf).reshape(xq.shape), f32_to_f16_bits(kf).reshape(xk.shape)
+
+
+def run_check(w, grad_dtype, q_heads=None, rows=None, kv_heads=None, k_rows=None, grow=False):
+    """grow: the growing-score inputs; dQ is then checked against 2e-2 plus the allowance of
+    gpu_util.dq_key_amplified_bound (what 16-bit dS and Delta leave, scaled by the large keys),
+    the rest at the gates."""
     xs = [seq_sharded_bits(w, t, dtype="f16") for t in ("q", "k", "v", "do")]
+    if grow:
+        xs[0], xs[1] = growing_scores(w, xs[0], xs[1])
     cu_host = w.cu_seqlens()
     layer = usp.UlyssesAttention(w.total_tokens, w.num_seqs, w.hq, w.hkv, w.head_dim, w.sp, causal=w.causal,
                                  grad_dtype=grad_dtype, dtype=torch.float16)
     dq_, dk_, dv_, ddo = (dev_16(x, torch.float16) for x in xs)
     cu = torch.from_numpy(cu_host).cuda()
     o = layer.forward(dq_, dk_, dv_, cu).clone()
+    o_res = layer.o_res_seq.clone()
     lse = layer.lse.clone()
     gq, gk, gv = (t.clone() for t in layer.backward(ddo, cu))
     torch.cuda.synchronize()
@@ -50,6 +71,11 @@ def run_check(w, grad_dtype, q_heads=None, rows=None, kv_heads=None, k_rows=None
            f64(gv).reshape(T, w.hkv, w.head_dim).transpose(1, 0, 2)[kh][:, kr]]
     for name, g, r in zip(("dQ", "dK", "dV"), got, (rq, rk, rv)):
         tol = G_TOL if grad_dtype == torch.float32 else G_TOL + np.abs(r) * 2.0 ** -11
+        if grow and name == "dQ":
+            from tests.gpu_util import dq_key_amplified_bound
+            assert q_heads is None and rows is None and w.hq == w.hkv
+            o_kernel = (f64(o) + f64(o_res)).reshape(T, w.hq, w.head_dim).transpose(1, 0, 2)
+            tol = tol + dq_key_amplified_bound(q, k, v, do, cu_host, o_kernel, dtype="f16")
         assert (np.abs(g - r) <= tol).all(), f"{name} max-abs error {np.abs(g - r).max()}"
 
 
@@ -88,3 +114,12 @@ def test_fp16_rejects_mixed_types():
     zf = torch.zeros(64, 4, 64, dtype=torch.float32, device="cuda")
     with pytest.raises(usp.UspError):    # fp32 activations
         usp.ulysses_attn_fwd(zf, zf, zf, zf, lse, cu, 1, 64, 2, 4, 4, 64, 0.0, True, ws, ws.numel())
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_fp16_growing_scores(D):
+    """Peaked rows whose running max moves often (the forward's rescale path) in fp16, through
+    the forward and the backward (dQ with the large-key allowance)."""
+    needs_gpu()
+    w = custom_workload("grow16", [700, 300, 130], sp=2, hq=2, hkv=2, head_dim=D, index=21)
+    run_check(w, torch.float32, grow=True)
