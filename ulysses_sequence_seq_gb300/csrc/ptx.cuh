@@ -114,6 +114,13 @@ __device__ __forceinline__ bool mbar_wait2(uint64_t* a, uint32_t pa, uint64_t* b
 __device__ __forceinline__ bool mbar_wait3(uint64_t* a, uint32_t pa, uint64_t* b, uint32_t pb, uint64_t* c,
                                            uint32_t pc, volatile int* abort_flag, uint64_t limit_ns) {
     uint32_t ra = a ? 0u : 1u, rb = b ? 0u : 1u, rc = c ? 0u : 1u;
+    // an absent barrier is never tested (its predicate starts true); its address operand is a
+    // present one's
+    uint64_t* any = a ? a : (b ? b : c);
+    if (!any) return true;
+    if (!a) a = any;
+    if (!b) b = any;
+    if (!c) c = any;
     uint64_t t0 = 0;
     while (true) {
         asm volatile(
