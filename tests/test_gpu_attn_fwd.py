@@ -89,16 +89,17 @@ def test_fwd_item_split_edges(causal, D):
     check_fwd(q, k, v, w.cu_seqlens(), causal)
 
 
+@pytest.mark.parametrize("causal", [True, False])
 @pytest.mark.parametrize("D", [64, 128])
-def test_fwd_growing_scores_rescale(D):
+def test_fwd_growing_scores_rescale(causal, D):
     """Scores that grow along the keys: every query has a large first component and key t's
-    first component grows with t, so along a causal row the block maxima rise by about 8
+    first component grows with t, so along a row the block maxima rise by about 8
     (log2 units) per key block and the running max is overtaken by more than 2^8 every one or
     two blocks. That exercises the output rescale and the redone exponentials of such blocks (the
     plain N(0,1) inputs almost never do). Checked in full against the oracle."""
     needs_gpu()
     from ulysses_sequence_seq_gb300.synth import bf16_bits_to_f32, f32_to_bf16_bits
-    w = custom_workload("grow", [700, 300, 130], sp=1, hq=2, hkv=2, head_dim=D, index=19)
+    w = custom_workload("grow", [700, 300, 130], sp=1, hq=2, hkv=2, head_dim=D, causal=causal, index=19)
     q, k, v, _ = make(w)
     qf, kf = bf16_bits_to_f32(q), bf16_bits_to_f32(k)
     qf[:, :, 0] = 4.0
@@ -106,7 +107,7 @@ def test_fwd_growing_scores_rescale(D):
     for b in range(len(cu) - 1):
         qf_pos = np.arange(cu[b + 1] - cu[b], dtype=np.float32)
         kf[:, cu[b]:cu[b + 1], 0] = 0.12 * qf_pos * np.sqrt(D / 128.0)
-    check_fwd(f32_to_bf16_bits(qf), f32_to_bf16_bits(kf), v, cu, True)
+    check_fwd(f32_to_bf16_bits(qf), f32_to_bf16_bits(kf), v, cu, causal)
 
 
 def test_fwd_runs_of_single_tile_items():
