@@ -90,7 +90,7 @@ def dev_16(bits: np.ndarray, dtype) -> torch.Tensor:
     return t.view(dtype).cuda()
 
 
-def dq_key_amplified_bound(q, k, v, do, cu, o_kernel, dtype="bf16"):
+def dq_key_amplified_bound(q, k, v, do, cu, o_kernel, dtype="bf16", causal=True):
     """Per element of dQ [hq][T][D], what the 16-bit arithmetic of the backward can add beyond
     plain rounding when keys are large, both terms scaled by max_j |K_j| (over the row's
     sample, per column) and the softmax scale:
@@ -99,13 +99,14 @@ def dq_key_amplified_bound(q, k, v, do, cu, o_kernel, dtype="bf16"):
         instead of 0 and dQ gains -scale * eps * sum_j P_j K_j;
       * dS's own three roundings to fp16 (P, the bracket dP - Delta, their product), each at
         most 2^-11 relative: 3 * 2^-11 * sum_j |dS_j| for the row.
-    The float64 P, dP and dS come from the oracle's LSE and the same inputs. hq must equal hkv."""
+    The float64 P, dP and dS come from the oracle's LSE and the same inputs; query head h
+    reads key/value head h // (hq / hkv)."""
     import oracle
     dec = (lambda x: np.asarray(x, dtype=np.uint16).view(np.float16).astype(np.float64)) if dtype == "f16" else \
         (lambda x: (np.asarray(x, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64))
     Q, K, V, dO = dec(q), dec(k), dec(v), dec(do)
-    assert Q.shape[0] == K.shape[0]
-    ro, rl = oracle.attn_fwd(q, k, v, cu, causal=True, dtype=dtype)
+    group = Q.shape[0] // K.shape[0]
+    ro, rl = oracle.attn_fwd(q, k, v, cu, causal=causal, dtype=dtype)
     eps = np.einsum("htd,htd->ht", dO, o_kernel - ro)
     sc = 1.0 / np.sqrt(Q.shape[2])
     bound = np.zeros_like(Q)
@@ -114,11 +115,14 @@ def dq_key_amplified_bound(q, k, v, do, cu, o_kernel, dtype="bf16"):
             s0, s1 = int(cu[b]), int(cu[b + 1])
             if s1 == s0:
                 continue
-            S = Q[h, s0:s1] @ K[h, s0:s1].T * sc + np.triu(np.full((s1 - s0, s1 - s0), -np.inf), 1)
+            kh = h // group
+            S = Q[h, s0:s1] @ K[kh, s0:s1].T * sc
+            if causal:
+                S = S + np.triu(np.full((s1 - s0, s1 - s0), -np.inf), 1)
             P = np.exp(S - rl[h, s0:s1, None])
-            dP = dO[h, s0:s1] @ V[h, s0:s1].T
+            dP = dO[h, s0:s1] @ V[kh, s0:s1].T
             dS = P * (dP - (P * dP).sum(axis=1, keepdims=True))
-            kmax = np.abs(K[h, s0:s1]).max(axis=0)
+            kmax = np.abs(K[kh, s0:s1]).max(axis=0)
             per_row = np.abs(eps[h, s0:s1]) + 3 * 2.0 ** -11 * np.abs(dS).sum(axis=1)
             bound[h, s0:s1] = sc * per_row[:, None] * kmax[None, :]
     return bound

@@ -64,8 +64,9 @@ def test_bwd_ragged_packed_edges_gqa(causal, D):
     check_bwd(*make(w), w.cu_seqlens(), causal)
 
 
-@pytest.mark.parametrize("D", [64, 128])
-def test_bwd_growing_scores(D):
+@pytest.mark.parametrize("causal,hq,hkv,D", [(True, 2, 2, 64), (True, 2, 2, 128), (True, 4, 2, 128),
+                                              (False, 2, 2, 128)])
+def test_bwd_growing_scores(causal, hq, hkv, D):
     """Peaked softmax rows with large keys: every query has a large first component and key
     t's first component grows with t up to 84 (the forward's rescale inputs). dK and dV must
     meet the 2e-2 gate. dQ = scale sum_j dS_j K_j carries in addition what 16-bit arithmetic
@@ -77,7 +78,7 @@ def test_bwd_growing_scores(D):
     needs_gpu()
     from tests.gpu_util import dq_key_amplified_bound
     from ulysses_sequence_seq_gb300.synth import bf16_bits_to_f32, f32_to_bf16_bits
-    w = custom_workload("grow", [700, 300, 130], sp=1, hq=2, hkv=2, head_dim=D, index=19)
+    w = custom_workload("grow", [700, 300, 130], sp=1, hq=hq, hkv=hkv, head_dim=D, causal=causal, index=19)
     q, k, v, do = make(w)
     qf, kf = bf16_bits_to_f32(q), bf16_bits_to_f32(k)
     qf[:, :, 0] = 4.0
@@ -85,16 +86,16 @@ def test_bwd_growing_scores(D):
     for b in range(len(cu) - 1):
         kf[:, cu[b]:cu[b + 1], 0] = 0.12 * np.arange(cu[b + 1] - cu[b], dtype=np.float32) * np.sqrt(D / 128.0)
     q, k = f32_to_bf16_bits(qf), f32_to_bf16_bits(kf)
-    p = Problem(q, k, v, cu, True, do_bits=do)
+    p = Problem(q, k, v, cu, causal, do_bits=do)
     o, lse, st = p.forward()
     assert st == 0
     dq, dk, dv, st = p.backward(o, lse, torch.float32)
     assert st == 0
-    rq, rk, rv = oracle.attn_bwd(q, k, v, do, cu, causal=True)
+    rq, rk, rv = oracle.attn_bwd(q, k, v, do, cu, causal=causal)
     for name, g, r in (("dK", dk, rk), ("dV", dv, rv)):
         err = np.abs(f64(g) - r)
         assert (err <= G_TOL).all(), f"{name} max-abs error {err.max()}"
-    bound = G_TOL + dq_key_amplified_bound(q, k, v, do, cu, f64(o) + f64(p.o_res))
+    bound = G_TOL + dq_key_amplified_bound(q, k, v, do, cu, f64(o) + f64(p.o_res), causal=causal)
     err = np.abs(f64(dq) - rq)
     assert (err <= bound).all(), f"dQ error {err.max()} above its allowance (worst excess {(err - bound).max()})"
 

@@ -50,14 +50,16 @@ def test_lse_merge_kernel_matches_oracle(init):
     assert np.abs(got_o - want_o).max() <= 1e-5
 
 
-def _ring(w, sp, grad=True, chunk_cu=None):
+def _ring(w, sp, grad=True, chunk_cu=None, bits=None):
     """Run the ring for every query chunk of `w` split into sp chunks (token-major), in ring
     order (own chunk first, then the chunk arriving from each earlier rank). Returns the
     per-chunk outputs (o + o_res), LSE and the gradients summed over the ring. chunk_cu:
-    the chunk-local cu_seqlens shared by every chunk (default: one sample)."""
+    the chunk-local cu_seqlens shared by every chunk (default: one sample); bits: head-major
+    q, k, v, do to use instead of the workload's draws."""
     T, hq, hkv, D = w.total_tokens, w.hq, w.hkv, w.head_dim
     L = T // sp
-    tm = {t: head_sharded_bits(w, t).transpose(1, 0, 2) for t in ("q", "k", "v", "do")}   # [T][H][D] bits
+    src = bits if bits is not None else {t: head_sharded_bits(w, t) for t in ("q", "k", "v", "do")}
+    tm = {t: src[t].transpose(1, 0, 2) for t in ("q", "k", "v", "do")}   # [T][H][D] bits
     chunk = {t: [dev_bf16(np.ascontiguousarray(tm[t][r * L:(r + 1) * L])) for r in range(sp)] for t in tm}
     ccu = np.array([0, L] if chunk_cu is None else chunk_cu, dtype=np.int32)
     cu = torch.from_numpy(ccu).cuda()
@@ -102,6 +104,36 @@ def test_ring_equals_full_attention(causal_ring):
         assert np.abs(outs[r].transpose(1, 0, 2) - ro[:, sl]).max() <= O_TOL
         assert np.abs(lses[r] - rl[:, sl]).max() <= LSE_TOL
         assert np.abs(dq[r].transpose(1, 0, 2) - rq[:, sl]).max() <= G_TOL
+        assert np.abs(dk[r].transpose(1, 0, 2) - rk[:, sl]).max() <= G_TOL
+        assert np.abs(dv[r].transpose(1, 0, 2) - rv[:, sl]).max() <= G_TOL
+
+
+def test_ring_growing_scores():
+    """Peaked rows whose maxima grow along the sequence (every query's first component 4, key
+    t's 0.03 t): the later chunks' LSEs exceed the earlier ones' by up to ~20, so the merge
+    must weight the chunks' partial outputs by exp(LSE differences) of that size. Forward at
+    1e-2 / 1e-3, dK and dV at 2e-2, dQ at 2e-2 plus the large-key allowance
+    (gpu_util.dq_key_amplified_bound)."""
+    needs_gpu()
+    from tests.gpu_util import dq_key_amplified_bound
+    w = custom_workload("ringgrow", [2560], sp=4, hq=2, hkv=2, head_dim=128, index=29)
+    sp, L = 4, 640
+    b = {t: head_sharded_bits(w, t) for t in ("q", "k", "v", "do")}
+    qf, kf = bf16_bits_to_f32(b["q"]), bf16_bits_to_f32(b["k"])
+    qf[:, :, 0] = 4.0
+    kf[:, :, 0] = 0.03 * np.arange(2560, dtype=np.float32)
+    b["q"], b["k"] = f32_to_bf16_bits(qf), f32_to_bf16_bits(kf)
+    outs, lses, dq, dk, dv = _ring(w, sp, bits=b)
+    cu = w.cu_seqlens()
+    ro, rl = oracle.attn_fwd(b["q"], b["k"], b["v"], cu)
+    rq, rk, rv = oracle.attn_bwd(b["q"], b["k"], b["v"], b["do"], cu)
+    o_kernel = np.concatenate(outs, axis=0).transpose(1, 0, 2)
+    bound = G_TOL + dq_key_amplified_bound(b["q"], b["k"], b["v"], b["do"], cu, o_kernel)
+    for r in range(sp):
+        sl = slice(r * L, (r + 1) * L)
+        assert np.abs(outs[r].transpose(1, 0, 2) - ro[:, sl]).max() <= O_TOL
+        assert np.abs(lses[r] - rl[:, sl]).max() <= LSE_TOL
+        assert (np.abs(dq[r].transpose(1, 0, 2) - rq[:, sl]) <= bound[:, sl]).all()
         assert np.abs(dk[r].transpose(1, 0, 2) - rk[:, sl]).max() <= G_TOL
         assert np.abs(dv[r].transpose(1, 0, 2) - rv[:, sl]).max() <= G_TOL
 
