@@ -175,6 +175,25 @@ def test_bwd_long_rank_slice_sampled():
     check_bwd(*make(w, range(4), range(4)), cu, True, q_heads=[2], q_rows=q_rows, kv_heads=[2], k_rows=k_rows)
 
 
+@pytest.mark.parametrize("hq,hkv,D", [(16, 2, 128), (16, 1, 128), (16, 2, 64)])
+def test_bwd_large_gqa_groups(hq, hkv, D):
+    """Groups of 8 and 16 query heads per key/value head (the forward reads each key/value
+    head for its whole group; the backward sums the group's dK and dV contributions in
+    tensor memory over G times as many query blocks and scales each group's fp16 operands
+    by its own magnitude), over ragged packed samples: forward and backward in full."""
+    needs_gpu()
+    w = custom_workload("gqa_big", [300, 129, 1, 270], sp=1, hq=hq, hkv=hkv, head_dim=D, index=37)
+    q, k, v, do = make(w)
+    cu = w.cu_seqlens()
+    p = Problem(q, k, v, cu, True, do_bits=do)
+    o, lse, st = p.forward()
+    assert st == 0
+    ro, rl = oracle.attn_fwd(q, k, v, cu, causal=True)
+    assert np.abs(f64(o) + f64(p.o_res) - ro).max() <= 1e-2
+    assert np.abs(f64(lse) - rl).max() <= 1e-3
+    check_bwd(q, k, v, do, cu, True)
+
+
 def test_bwd_key_gradients_sum_to_zero_per_sample():
     """Each row of dS sums to zero, so the key gradients of every sample sum to zero (up to
     the bf16 rounding of O inside Delta = dO . O, hence the loose bound)."""
