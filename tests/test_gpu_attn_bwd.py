@@ -194,6 +194,26 @@ def test_bwd_large_gqa_groups(hq, hkv, D):
     check_bwd(q, k, v, do, cu, True)
 
 
+def test_many_tiny_samples_fwd_bwd():
+    """3000 samples of 1 to 8 tokens (a work item per sample and head, every tile ragged, the
+    scheduler's cost histogram at its small end), forward and backward in full; and a single
+    one-token sequence."""
+    needs_gpu()
+    rng = np.random.default_rng(41)
+    lengths = [int(x) for x in rng.integers(1, 9, size=3000)]
+    for lens, hq, hkv, D in ((lengths, 4, 2, 128), ([1], 2, 1, 64)):
+        w = custom_workload("tiny_many", lens, sp=1, hq=hq, hkv=hkv, head_dim=D, index=43)
+        q, k, v, do = make(w)
+        cu = w.cu_seqlens()
+        p = Problem(q, k, v, cu, True, do_bits=do)
+        o, lse, st = p.forward()
+        assert st == 0
+        ro, rl = oracle.attn_fwd(q, k, v, cu, causal=True)
+        assert np.abs(f64(o) + f64(p.o_res) - ro).max() <= 1e-2
+        assert np.abs(f64(lse) - rl).max() <= 1e-3
+        check_bwd(q, k, v, do, cu, True)
+
+
 def test_bwd_key_gradients_sum_to_zero_per_sample():
     """Each row of dS sums to zero, so the key gradients of every sample sum to zero (up to
     the bf16 rounding of O inside Delta = dO . O, hence the loose bound)."""
