@@ -48,7 +48,7 @@ def sample_rows(cu, n_random: int, seed: int = 0, T: int | None = None):
 class Problem:
     """Device buffers for one attention problem in the head-major layout."""
 
-    def __init__(self, q_bits, k_bits, v_bits, cu, causal=True, do_bits=None):
+    def __init__(self, q_bits, k_bits, v_bits, cu, causal=True, do_bits=None, scale=0.0):
         self.q, self.k, self.v = dev_bf16(q_bits), dev_bf16(k_bits), dev_bf16(v_bits)
         self.do = dev_bf16(do_bits) if do_bits is not None else None
         self.cu_host = np.asarray(cu, dtype=np.int32)
@@ -57,6 +57,7 @@ class Problem:
         self.hkv = k_bits.shape[0]
         self.B = len(cu) - 1
         self.causal = causal
+        self.scale = scale   # <= 0: 1/sqrt(D)
         self.ws_bytes = max(usp.attn_workspace_size(self.T, self.B, self.hq, self.hkv, self.D, False),
                             usp.attn_workspace_size(self.T, self.B, self.hq, self.hkv, self.D, True))
         self.ws = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8, device="cuda")
@@ -68,7 +69,7 @@ class Problem:
         lse = torch.full((self.hq, self.T), float("nan"), dtype=torch.float32, device="cuda")
         self.o_res = torch.full_like(o, float("nan")) if residual else None
         usp.attn_fwd_varlen(self.q, self.k, self.v, o, lse, self.cu, self.B, self.T, self.hq, self.hkv, self.D,
-                            0.0, self.causal, self.ws, self.ws_bytes, o_res=self.o_res)
+                            self.scale, self.causal, self.ws, self.ws_bytes, o_res=self.o_res)
         status = usp.get_device_status(self.ws)
         return o, lse, status
 
@@ -78,7 +79,7 @@ class Problem:
         dk = torch.full((self.hkv, self.T, self.D), float("nan"), dtype=grad_dtype, device="cuda")
         dv = torch.full((self.hkv, self.T, self.D), float("nan"), dtype=grad_dtype, device="cuda")
         usp.attn_bwd_varlen(self.q, self.k, self.v, o, lse, self.do, dq, dk, dv, gd, self.cu, self.B, self.T,
-                            self.hq, self.hkv, self.D, 0.0, self.causal, self.ws, self.ws_bytes,
+                            self.hq, self.hkv, self.D, self.scale, self.causal, self.ws, self.ws_bytes,
                             o_res=getattr(self, "o_res", None))
         status = usp.get_device_status(self.ws)
         return dq, dk, dv, status

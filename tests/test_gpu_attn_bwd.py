@@ -214,6 +214,33 @@ def test_many_tiny_samples_fwd_bwd():
         check_bwd(q, k, v, do, cu, True)
 
 
+@pytest.mark.parametrize("scale,D", [(1.0, 128), (0.02, 128), (0.5, 64)])
+def test_softmax_scale_fwd_bwd(scale, D):
+    """A softmax scale other than 1/sqrt(D): sharper (1.0 at head_dim 128 is 11 times the
+    default) and flatter rows, which also move the backward's dS scaling (a power of two
+    chosen from the scale and D). Forward and backward in full against the oracle with the
+    same scale. dQ = scale sum_j dS_j K_j grows with the scale (to ~50 here); gradients are
+    held to 2e-2 or, when larger, to 5e-3 of their largest magnitude, the bound the
+    magnitude test below uses for large gradients."""
+    needs_gpu()
+    w = custom_workload("scale", [300, 129, 1, 270], sp=1, hq=4, hkv=2, head_dim=D, index=47)
+    q, k, v, do = make(w)
+    cu = w.cu_seqlens()
+    p = Problem(q, k, v, cu, True, do_bits=do, scale=scale)
+    o, lse, st = p.forward()
+    assert st == 0
+    ro, rl = oracle.attn_fwd(q, k, v, cu, causal=True, scale=scale)
+    assert np.abs(f64(o) + f64(p.o_res) - ro).max() <= 1e-2
+    assert np.abs(f64(lse) - rl).max() <= 1e-3
+    dq, dk, dv, st = p.backward(o, lse, torch.float32)
+    assert st == 0
+    rq, rk, rv = oracle.attn_bwd(q, k, v, do, cu, causal=True, scale=scale)
+    for name, g, r in (("dQ", dq, rq), ("dK", dk, rk), ("dV", dv, rv)):
+        err = np.abs(f64(g) - r)
+        tol = max(G_TOL, 5e-3 * np.abs(r).max())
+        assert (err <= tol).all(), f"{name} max-abs error {err.max()} (max |ref| {np.abs(r).max()})"
+
+
 def test_bwd_key_gradients_sum_to_zero_per_sample():
     """Each row of dS sums to zero, so the key gradients of every sample sum to zero (up to
     the bf16 rounding of O inside Delta = dO . O, hence the loose bound)."""
