@@ -728,7 +728,7 @@ __global__ void __maxnreg__(kLaunchRegs)
                 if (a.o_res) {
                     // The rounding residual O - round16(O) in two more rounds through the same
                     // panel, reading O from TMEM again: it stays there until this group's next
-                    // P.V, which the MMA thread issues only after the group's next P.
+                    // P.V, which the tile's MMA thread issues only after the group's next P.
 #pragma unroll 1
                     for (int round = 0; round < D / 64; ++round) {
 #pragma unroll
