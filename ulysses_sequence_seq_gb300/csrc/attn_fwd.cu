@@ -422,7 +422,7 @@ __global__ void __maxnreg__(kLaunchRegs)
             constexpr uint32_t idS = idesc_16b_f32(M, kBlockN, false, false, F16);  // Q.K^T: both K-major
             constexpr uint32_t idO = idesc_16b_f32(M, D, false, true, F16);         // P.V: V is MN-major
             // The turn goes to the other tile this many MMAs before a batch ends (measured on the
-            // 262,144-token slice: 1 -> 1560, 2 -> 1548, 3 -> 1545, 4 -> 1534 TFLOP/s).
+            // 262,144-token slice: 0 -> 1516, 1 -> 1548-1560, 2 -> 1548, 3 -> 1545, 4 -> 1534 TFLOP/s).
             constexpr int kEarly = 1;
             // The 64-bit shared-memory descriptors are built once; a K step only adds a constant
             // to the start-address field (addresses stay below 2^18, so the field never carries).
