@@ -10,6 +10,7 @@ import torch
 
 import oracle
 import ulysses_sequence_seq_gb300 as usp
+from ulysses_sequence_seq_gb300 import _lib
 from tests.gpu_util import dev_bf16, f64, needs_gpu
 from ulysses_sequence_seq_gb300.synth import custom_workload, head_sharded_bits
 
@@ -109,3 +110,47 @@ def test_fused_outputs_stay_inside_their_tensors(D):
     rq, rk, rv = oracle.attn_bwd(q, k, v, do, cu_host)
     for g_, r in ((dq, rq), (dk, rk), (dv, rv)):
         assert np.abs(heads(f64(g_)) - r).max() <= 2e-2
+
+
+def test_relayout_and_merge_outputs_stay_inside_their_tensors():
+    """The stand-alone layout swaps (including the replicating key/value swap and its summing
+    gradient), the rank-local halves of the exchange, and the ring-merge kernels, on sizes
+    whose last rows end mid-warp: canaries intact, results as their inverses or oracles give."""
+    needs_gpu()
+    sp, T, H, HKV, D = 4, 4 * 37, 8, 2, 128
+    rng = np.random.default_rng(83)
+    x = torch.from_numpy(rng.integers(-30000, 30000, size=(sp, T // sp, H, D), dtype=np.int16)).cuda().view(torch.bfloat16)
+    bh, h, gh = guarded((sp, H // sp, T, D), torch.bfloat16)
+    usp.seq_to_head(x, h, sp)
+    bs, back, gs = guarded((sp, T // sp, H, D), torch.bfloat16)
+    usp.head_to_seq(h, back, sp)
+    xk = torch.from_numpy(rng.integers(-30000, 30000, size=(sp, T // sp, HKV, D), dtype=np.int16)).cuda().view(torch.bfloat16)
+    bk, hk, gk = guarded((max(sp, HKV), T, D), torch.bfloat16)
+    usp.seq_to_head_kv(xk, hk, sp)
+    bg, gsum, gg = guarded((sp, T // sp, HKV, D), torch.float32)
+    usp.head_to_seq_kv_grad(hk.float(), gsum, sp, HKV)
+    S = T // sp
+    shard = x[0].contiguous()                                           # one rank's [S][H][D]
+    bp, packed, gp = guarded((sp, S, H // sp, D), torch.bfloat16)
+    _lib.a2a_pack(shard, packed, sp)
+    bu, unpacked, gu = guarded((S, H, D), torch.bfloat16)
+    _lib.a2a_unpack(packed, unpacked, sp)
+    o_acc = torch.from_numpy(rng.standard_normal((T, H, D)).astype(np.float32)).cuda()
+    lse_acc = torch.from_numpy(rng.standard_normal((H, T)).astype(np.float32)).cuda()
+    o_part = torch.from_numpy(rng.standard_normal((T, H, D)).astype(np.float32)).cuda().to(torch.bfloat16)
+    lse_part = torch.from_numpy(rng.standard_normal((H, T)).astype(np.float32)).cuda()
+    _lib.lse_merge(o_acc, lse_acc, o_part, lse_part)
+    bo, o16, go = guarded((T, H, D), torch.bfloat16)
+    br, ores, gr = guarded((T, H, D), torch.bfloat16)
+    _lib.o_finalize(o_acc, o16, ores)
+    ba, acc, ga = guarded((T, H, D), torch.float32)
+    acc.zero_()
+    _lib.accumulate_f32(acc, o_acc)
+    torch.cuda.synchronize()
+    for name, buf, g in (("seq_to_head", bh, gh), ("head_to_seq", bs, gs), ("seq_to_head_kv", bk, gk),
+                         ("head_to_seq_kv_grad", bg, gg), ("a2a_pack", bp, gp), ("a2a_unpack", bu, gu),
+                         ("o_finalize o", bo, go), ("o_finalize residual", br, gr), ("accumulate_f32", ba, ga)):
+        assert canaries_intact(buf, g), f"a write left {name}'s output"
+    assert torch.equal(back.view(torch.int16), x.view(torch.int16))   # the swaps are inverse permutations
+    assert torch.equal(acc, o_acc)                                      # 0 + o_acc
+    assert float((o16.float() + ores.float() - o_acc).abs().max()) <= 2.0 ** -14 * float(o_acc.abs().max()) + 1e-30
